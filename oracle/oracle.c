@@ -1,0 +1,311 @@
+/*
+ * Oracle for the PagedAttention decode hot path: a plain, slow, obviously
+ * correct fp64 CPU restatement of what the path computes.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The product path never
+ * calls it, and it shares no code, header, table or helper with the CUDA
+ * library: it has its own element decoders, its own slot arithmetic and its
+ * own loops, written straight from the definitions below.
+ *
+ * Sources (web pages on PagedAttention; cited by title and section):
+ *  [P1] "第4章 PagedAttention：虚拟内存的启示" (vLLM source-reading book):
+ *       §4.3.1 block shape (2, num_blocks, block_size, num_kv_heads,
+ *       head_size), index 0 = K, index 1 = V; §4.4.1 block table;
+ *       §4.4.3 slot mapping (slot = table[pos / B] * B + pos % B);
+ *       §4.5 write-then-read call chain; §4.6 online-softmax recurrence.
+ *  [P3] "PagedAttention: virtual memory for the KV cache" digest:
+ *       "写时复制" paragraph (clone the whole block on write);
+ *       "常见误解" (paging does not change the attention result).
+ *  [P4] CSDN beginner article, §三.1 `page_attention`: gather the valid
+ *       K/V of every block in logical order, softmax(q k^T / sqrt(d)), x V.
+ *  [P5] "PagedAttention原理（下）" lecture, §4.3: COW copies block P into
+ *       a new block Q before the write.
+ *
+ * Precision: inputs are 16-bit (fp16 or bf16) bit patterns, decoded exactly
+ * to double; every sum, max, exp and division is done in double.
+ *
+ * Parity pins for every function here live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+
+/* ---- exact 16-bit float decoders (IEEE 754 binary16, bfloat16) ---- */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double mag;
+    if (expo == 0) {
+        mag = ldexp((double)frac, -24);             /* subnormal: frac * 2^-24 */
+    } else if (expo == 31) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        mag = ldexp((double)(1024 + frac), expo - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32 value. */
+double oracle_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 7) & 0xff;
+    int frac = h & 0x7f;
+    double mag;
+    if (expo == 0) {
+        mag = ldexp((double)frac, -133);            /* subnormal: frac * 2^-126 / 128 */
+    } else if (expo == 255) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        mag = ldexp((double)(128 + frac), expo - 134); /* (1 + f/128) * 2^(e-127) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* Vector form of the two decoders, for tests: out[i] = value of bits[i]. */
+void oracle_decode_elems(const uint16_t *bits, double *out, long long n, int dtype)
+{
+    for (long long i = 0; i < n; ++i)
+        out[i] = dtype == ORACLE_BF16 ? oracle_bf16_to_double(bits[i]) : oracle_f16_to_double(bits[i]);
+}
+
+static double elem(const uint16_t *p, long long i, int dtype)
+{
+    return dtype == ORACLE_BF16 ? oracle_bf16_to_double(p[i]) : oracle_f16_to_double(p[i]);
+}
+
+/* Element (c, b, t, h, d) of a per-layer pool shaped
+ * (2, num_blocks, block_size, num_kv_heads, head_size), row-major [P1 §4.3.1]. */
+static long long pool_index(int c, int b, int t, int h, int d,
+                            int num_blocks, int block_size, int num_kv_heads, int head_size)
+{
+    return ((((long long)c * num_blocks + b) * block_size + t) * num_kv_heads + h)
+               * head_size + d;
+}
+
+/* ---- slot mapping [P1 §4.4.3] ---- */
+
+/* Physical slot of logical token position `pos` of a sequence whose block
+ * table row is `table`: the logical block pos / B is looked up, and the
+ * offset inside it is pos % B. */
+long long oracle_slot(const int32_t *table, int block_size, long long pos)
+{
+    long long logical_block = pos / block_size;
+    long long offset = pos % block_size;
+    return (long long)table[logical_block] * block_size + offset;
+}
+
+/* ---- write path: reshape_and_cache [P1 §4.5 step 1, §4.4.3] ----
+ * For every new token t with slot >= 0: the K row [num_kv_heads][head_size]
+ * goes to pool[0][slot / B][slot % B], the V row to pool[1][...]. Negative
+ * slots are skipped (padding). Returns the number of rows written, or -1 if
+ * a slot lies beyond the pool. */
+int oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *pool,
+                             const int32_t *slot_mapping, int num_tokens,
+                             int num_blocks, int block_size, int num_kv_heads, int head_size)
+{
+    int written = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        long long slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= (long long)num_blocks * block_size)
+            return -1;
+        int b = (int)(slot / block_size);
+        int off = (int)(slot % block_size);
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_size; ++d) {
+                long long src = ((long long)t * num_kv_heads + h) * head_size + d;
+                pool[pool_index(0, b, off, h, d, num_blocks, block_size, num_kv_heads, head_size)] = key[src];
+                pool[pool_index(1, b, off, h, d, num_blocks, block_size, num_kv_heads, head_size)] = value[src];
+            }
+        }
+        ++written;
+    }
+    return written;
+}
+
+/* ---- copy-on-write block copy [P3 写时复制; P5 §4.3] ----
+ * For each (src, dst) pair, in order, and for every layer pool: the whole
+ * physical block (all B slots, K and V, all heads) of src is copied to dst.
+ * Returns 0, or -1 on an out-of-range block id (nothing after it copied). */
+int oracle_copy_blocks(uint16_t *const *pools, int num_layers,
+                       const int32_t *pairs, int num_pairs,
+                       int num_blocks, int block_size, int num_kv_heads, int head_size)
+{
+    for (int i = 0; i < num_pairs; ++i) {
+        int src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return -1;
+        for (int layer = 0; layer < num_layers; ++layer) {
+            uint16_t *pool = pools[layer];
+            for (int c = 0; c < 2; ++c)
+                for (int t = 0; t < block_size; ++t)
+                    for (int h = 0; h < num_kv_heads; ++h)
+                        for (int d = 0; d < head_size; ++d)
+                            pool[pool_index(c, dst, t, h, d, num_blocks, block_size, num_kv_heads, head_size)] =
+                                pool[pool_index(c, src, t, h, d, num_blocks, block_size, num_kv_heads, head_size)];
+        }
+    }
+    return 0;
+}
+
+/* ---- read path: plain attention over a contiguous K/V [P4 §三.1] ----
+ * out[d] = sum_i w_i V[i][d] / sum_i w_i, w_i = exp(x_i - max_j x_j),
+ * x_i = scale * sum_d q[d] K[i][d]. K and V are [L][head_size]. L = 0
+ * gives a zero row (the pages are silent; this is the reading taken). */
+void oracle_attention_contiguous(double *out, const uint16_t *q, const uint16_t *k,
+                                 const uint16_t *v, int seq_len, int head_size,
+                                 double scale, int dtype)
+{
+    for (int d = 0; d < head_size; ++d)
+        out[d] = 0.0;
+    if (seq_len <= 0)
+        return;
+    double *x = (double *)malloc(sizeof(double) * (size_t)seq_len);
+    double mx = -INFINITY;
+    for (int i = 0; i < seq_len; ++i) {
+        double dot = 0.0;
+        for (int d = 0; d < head_size; ++d)
+            dot += elem(q, d, dtype) * elem(k, (long long)i * head_size + d, dtype);
+        x[i] = scale * dot;
+        if (x[i] > mx)
+            mx = x[i];
+    }
+    double denom = 0.0;
+    for (int i = 0; i < seq_len; ++i) {
+        x[i] = exp(x[i] - mx);
+        denom += x[i];
+    }
+    for (int d = 0; d < head_size; ++d) {
+        double acc = 0.0;
+        for (int i = 0; i < seq_len; ++i)
+            acc += x[i] * elem(v, (long long)i * head_size + d, dtype);
+        out[d] = acc / denom;
+    }
+    free(x);
+}
+
+/* ---- read path: paged decode for one (sequence, q-head) [P1 §4.5, §4.4.1] ----
+ * Walk logical tokens 0..L-1; token i lives in physical block
+ * table[i / B] at offset i % B. The q-head maps to kv-head
+ * hq / (num_q_heads / num_kv_heads) (contiguous GQA groups). The K/V rows
+ * are gathered in logical order and handed to the contiguous definition. */
+void oracle_decode_one(double *out, const uint16_t *query, const uint16_t *pool,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *seq_lens, int seq, int q_head,
+                       double scale, int num_q_heads, int num_kv_heads, int head_size,
+                       int num_blocks, int block_size, int dtype)
+{
+    int seq_len = seq_lens[seq];
+    int group = num_q_heads / num_kv_heads;
+    int kv_head = q_head / group;
+    const int32_t *table = block_tables + (long long)seq * max_blocks_per_seq;
+    size_t n = seq_len > 0 ? (size_t)seq_len * head_size : 1;
+    uint16_t *k = (uint16_t *)malloc(sizeof(uint16_t) * n);
+    uint16_t *v = (uint16_t *)malloc(sizeof(uint16_t) * n);
+    for (int i = 0; i < seq_len; ++i) {
+        int b = table[i / block_size];
+        int off = i % block_size;
+        for (int d = 0; d < head_size; ++d) {
+            k[(long long)i * head_size + d] =
+                pool[pool_index(0, b, off, kv_head, d, num_blocks, block_size, num_kv_heads, head_size)];
+            v[(long long)i * head_size + d] =
+                pool[pool_index(1, b, off, kv_head, d, num_blocks, block_size, num_kv_heads, head_size)];
+        }
+    }
+    const uint16_t *q = query + ((long long)seq * num_q_heads + q_head) * head_size;
+    oracle_attention_contiguous(out, q, k, v, seq_len, head_size, scale, dtype);
+    free(k);
+    free(v);
+}
+
+/* Paged decode for a whole batch: out is [num_seqs][num_q_heads][head_size]. */
+void oracle_decode(double *out, const uint16_t *query, const uint16_t *pool,
+                   const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *seq_lens, int num_seqs,
+                   double scale, int num_q_heads, int num_kv_heads, int head_size,
+                   int num_blocks, int block_size, int dtype)
+{
+    for (int s = 0; s < num_seqs; ++s)
+        for (int hq = 0; hq < num_q_heads; ++hq)
+            oracle_decode_one(out + ((long long)s * num_q_heads + hq) * head_size, query, pool,
+                              block_tables, max_blocks_per_seq, seq_lens, s, hq, scale,
+                              num_q_heads, num_kv_heads, head_size, num_blocks, block_size, dtype);
+}
+
+/* Decode for a list of sampled (seq, q_head) pairs: out is [n][head_size]. */
+void oracle_decode_sampled(double *out, const int32_t *seq_ids, const int32_t *q_heads, int n,
+                           const uint16_t *query, const uint16_t *pool,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, double scale, int num_q_heads,
+                           int num_kv_heads, int head_size, int num_blocks, int block_size,
+                           int dtype)
+{
+    for (int i = 0; i < n; ++i)
+        oracle_decode_one(out + (long long)i * head_size, query, pool, block_tables,
+                          max_blocks_per_seq, seq_lens, seq_ids[i], q_heads[i], scale,
+                          num_q_heads, num_kv_heads, head_size, num_blocks, block_size, dtype);
+}
+
+/* ---- the online-softmax recurrence [P1 §4.6] ----
+ * The same attention, computed the way the method streams it: the logical
+ * tokens are cut into consecutive parts of `part_len` tokens; each part
+ * yields its local state (m', s', O' = sum_t exp(x_t - m') V_t); the
+ * running state (m, s, O) absorbs it with
+ *     m_new = max(m, m'),
+ *     s_new = s * exp(m - m_new) + s' * exp(m' - m_new),
+ *     O_new = O * exp(m - m_new) + O' * exp(m' - m_new),
+ * and the result is O / s. This is the merge rule split-K decoding relies
+ * on; it is kept here so that tests can pin it against the two-pass
+ * definition above. */
+void oracle_attention_online(double *out, const uint16_t *q, const uint16_t *k,
+                             const uint16_t *v, int seq_len, int head_size,
+                             double scale, int dtype, int part_len)
+{
+    double m = -INFINITY, s = 0.0;
+    double *o = (double *)calloc((size_t)head_size, sizeof(double));
+    double *op = (double *)calloc((size_t)head_size, sizeof(double));
+    double *x = (double *)malloc(sizeof(double) * (size_t)(part_len > 0 ? part_len : 1));
+    for (int start = 0; start < seq_len; start += part_len) {
+        int end = start + part_len < seq_len ? start + part_len : seq_len;
+        double mp = -INFINITY;
+        for (int i = start; i < end; ++i) {
+            double dot = 0.0;
+            for (int d = 0; d < head_size; ++d)
+                dot += elem(q, d, dtype) * elem(k, (long long)i * head_size + d, dtype);
+            x[i - start] = scale * dot;
+            if (x[i - start] > mp)
+                mp = x[i - start];
+        }
+        double sp = 0.0;
+        for (int d = 0; d < head_size; ++d)
+            op[d] = 0.0;
+        for (int i = start; i < end; ++i) {
+            double p = exp(x[i - start] - mp);
+            sp += p;
+            for (int d = 0; d < head_size; ++d)
+                op[d] += p * elem(v, (long long)i * head_size + d, dtype);
+        }
+        double m_new = m > mp ? m : mp;
+        double a_old = exp(m - m_new); /* exp(-inf) = 0 on the first part */
+        double a_new = exp(mp - m_new);
+        s = s * a_old + sp * a_new;
+        for (int d = 0; d < head_size; ++d)
+            o[d] = o[d] * a_old + op[d] * a_new;
+        m = m_new;
+    }
+    for (int d = 0; d < head_size; ++d)
+        out[d] = seq_len > 0 ? o[d] / s : 0.0;
+    free(o);
+    free(op);
+    free(x);
+}
