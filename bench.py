@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of one PagedAttention decode step on GB300.
+
+A step is one pass of the whole hot path over one batch:
+    pa_copy_blocks (COW pairs, if the workload has any)
+    -> pa_reshape_and_cache (one new token per sequence)
+    -> pa_decode (main kernel + split-K reduce)
+Default workload: the Llama-2-13B layer (64 sequences, 40/40 heads,
+head_dim 128, fp16, lengths uniform in [1, 2048], 9000-block pool).
+
+Prints one JSON line (rank 0). ``value`` is the step's algorithmic HBM bytes
+per second (GB/s); ``seq_steps_per_s`` is sequences decoded per second.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+Under torchrun every rank runs its own replica of the workload (weak
+scaling: sequences are independent, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_120_gb300 import workloads  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------ bytes of a step
+
+def algorithmic_bytes(w, seq_lens, num_pairs: int, num_new_tokens: int) -> dict:
+    """Bytes a step must move at minimum: every valid K/V element once per kv
+    head (padding slots of partial blocks not counted), Q, the output, block
+    table entries and lengths; the new K/V rows read and written; each COW
+    pair's K and V block read and written."""
+    e = 2
+    L = np.asarray(seq_lens, dtype=np.int64)
+    S = len(L)
+    kv = int((2 * L * w.num_kv_heads * w.head_size * e).sum())
+    tables = int((4 * ((L + w.block_size - 1) // w.block_size)).sum())
+    qo = 2 * S * w.num_q_heads * w.head_size * e
+    decode = kv + qo + tables + 4 * S
+    reshape = num_new_tokens * (2 * 2 * w.num_kv_heads * w.head_size * e + 4)
+    copy = num_pairs * 2 * 2 * w.block_size * w.num_kv_heads * w.head_size * e + 8 * num_pairs
+    return dict(decode=decode, kv=kv, reshape=reshape, copy=copy, step=decode + reshape + copy)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy-based)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
+
+
+def traffic_record(workload: str):
+    """DRAM traffic per decode launch from a committed ncu summary, if the
+    summary was taken on the current decode source (its hash matches)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
+    src = os.path.join(ROOT, "paged_kv_cache_120_gb300", "csrc", "pa_kernels.cu")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        if kv.get("source_sha256") != h:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi in the background; samples are filtered to the timed window."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        time.sleep(0.3)
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+                except Exception:
+                    continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in use for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside),
+                "window": "timed region" if inside else "whole run (timed region too short to sample)"}
+
+
+# --------------------------------------------------------------- distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 0, 1
+    import torch.distributed as dist
+    backend = os.environ.get("BENCH_DIST_BACKEND", "nccl")
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), int(os.environ.get("LOCAL_RANK", "0")), dist.get_world_size()
+
+
+def dist_max(value: float, world: int, device=None) -> float:
+    """Max of a host float over ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------ oracle timing
+
+def oracle_sample_time(name, plan, pool_bits, q_bits, budget_s: float, start_seq: int = 0):
+    """Time the oracle's decode on whole sequences (round-robin from
+    start_seq) until about budget_s of CPU time is spent. Returns
+    (seconds, algorithmic bytes covered, sequences, next start)."""
+    import oracle
+    w = workloads.WORKLOADS[name]
+    S = len(plan.seq_lens)
+    done_bytes, n, t = 0, 0, 0.0
+    s = start_seq % S
+    while t < budget_s and n < S:
+        seqs = np.full(w.num_q_heads, s, dtype=np.int32)
+        heads = np.arange(w.num_q_heads, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.decode_sampled(seqs, heads, q_bits, pool_bits, plan.block_tables, plan.seq_lens,
+                              w.scale, w.num_q_heads, w.num_kv_heads, w.head_size, w.num_blocks,
+                              w.block_size, w.dtype)
+        t += time.perf_counter() - t0
+        done_bytes += algorithmic_bytes(w, [plan.seq_lens[s]], 0, 0)["decode"]
+        n += 1
+        s = (s + 1) % S
+    return t, done_bytes, n, s
+
+
+def host_inputs(name, plan, seed):
+    """The oracle's host copies of the step's inputs (bit patterns)."""
+    import torch
+    from paged_kv_cache_120_gb300 import step as stepmod
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
+    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev)
+    to = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    pool_bits, q_bits = to(pool), to(q)
+    del pool
+    return pool_bits, q_bits
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on the host cores."""
+    if rank != 0:
+        return
+    from paged_kv_cache_120_gb300 import step as stepmod
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    plan = stepmod.plan_step(name, args.seed)
+    pool_bits, q_bits = host_inputs(name, plan, args.seed)
+    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    nxt = 0
+    for _ in range(args.warmup):
+        _, _, _, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt)
+    tot_t, tot_b, tot_n = 0.0, 0, 0
+    for _ in range(args.steps):
+        t, b, n, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt)
+        tot_t, tot_b, tot_n = tot_t + t, tot_b + b, tot_n + n
+    gbs = tot_b / tot_t / 1e9
+    sample = (f"{tot_n} whole sequences (all {w.num_q_heads} q heads each) of the {name} batch, "
+              f"about {per_step:.2f} s of oracle time per step")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": workload_config(name, plan),
+            "seq_steps_per_s": tot_n / tot_t,
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "paged-decode attention achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+
+
+def workload_config(name, plan):
+    w = workloads.WORKLOADS[name]
+    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), int((plan.slot_mapping >= 0).sum()))
+    return {"workload": f"{name}: {w.description}", "num_seqs": int(len(plan.seq_lens)),
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "mean_seq_len": float(np.mean(plan.seq_lens)), "cow_pairs": int(len(plan.cow_pairs)),
+            "kv_bytes_per_step": ab["kv"], "step_bytes": ab["step"],
+            "l2": ("inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2, no flush"
+                   % (ab["kv"] / 1e9))}
+
+
+# -------------------------------------------------------------------- ours
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    from paged_kv_cache_120_gb300 import binding, build, step as stepmod
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    seed = args.seed + 1000 * rank
+    plan = stepmod.plan_step(name, seed, args.variant)
+    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev)
+    st = stepmod.DecodeStep(name, plan, pool, q, k, v, dev)
+    n_tokens = int((plan.slot_mapping >= 0).sum())
+    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(3, args.warmup)):
+        st.run()
+    torch.cuda.synchronize(dev)
+    if binding.pa_get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(K):
+        if st.cow_pairs is not None:
+            binding.pa_copy_blocks([st.pool], st.cow_pairs)
+        binding.pa_reshape_and_cache(st.key_new, st.value_new, st.pool, st.slot_mapping)
+        ev[i][0].record(stream)
+        st.decode()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world, dev)
+    if clocks:
+        clocks.stop()
+    t_ms = start.elapsed_time(end)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    t_s = dist_max(t_ms / 1e3, world, dev)
+    dev_err = binding.pa_get_device_error()
+    if dev_err:
+        raise RuntimeError(f"device error word {dev_err} set during the timed region")
+
+    # End to end through the public step API with pinned host buffers.
+    host = {n: t.cpu().pin_memory() for n, t in
+            (("query", st.query), ("key_new", st.key_new), ("value_new", st.value_new),
+             ("slot_mapping", st.slot_mapping), ("block_tables", st.block_tables),
+             ("seq_lens", st.seq_lens))}
+    if st.cow_pairs is not None:
+        host["cow_pairs"] = st.cow_pairs.cpu().pin_memory()
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    for _ in range(3):
+        st.run_host(host, out_host)
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ke = max(1, min(K, 500))
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        st.run_host(host, out_host)
+    e2e_s = time.perf_counter() - t0
+    e2e_s = dist_max(e2e_s, world, dev)
+    dist_barrier(world, dev)
+
+    if rank != 0:
+        return
+    peak, peak_note = measured_peak()
+    dec_ms = statistics.mean(decode_ms)
+    achieved = ab["decode"] / (dec_ms / 1e3) / 1e9
+    value = world * ab["step"] * K / t_s / 1e9
+    seq_steps = world * len(plan.seq_lens) * K / t_s
+    traffic = traffic_record(name)
+
+    # CPU baseline: the oracle, single-threaded, on a bounded sample.
+    pool_bits, q_bits = st.pool.view(torch.int16).cpu().numpy().view(np.uint16), \
+        st.query.view(torch.int16).cpu().numpy().view(np.uint16)
+    ot, ob, on, _ = oracle_sample_time(name, plan, pool_bits, q_bits, args.cpu_budget)
+    del pool_bits
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_s * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
+        "data": "synthetic (seeded N(0,1) values, seeded block placement)",
+        "config": workload_config(name, plan),
+        "seq_steps_per_s": seq_steps,
+        "pct_of_nominal_8TBps": 100.0 * value / NOMINAL_HBM_GBS,
+        "pct_of_measured_peak": 100.0 * value / peak,
+        "decode_only": {"ms": dec_ms, "gbs": achieved, "seq_steps_per_s": len(plan.seq_lens) / (dec_ms / 1e3)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "pa_decode (paged_decode_kernel + paged_decode_reduce_kernel)",
+                     "peak_source": peak_note, "bytes_per_launch": ab["decode"]},
+        "e2e": {"value": world * ab["step"] * ke / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3 / ke},
+        "gpu_launches": st.launches_per_step() * K,
+        "cpu_baseline": {"value": ob / ot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{on} whole sequences x {w.num_q_heads} q heads of the same batch "
+                                   f"({ot:.1f} s, single-threaded fp64 C)"},
+        "clocks": clocks.summary() if clocks else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama13b", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--variant", default="literal", choices=["literal", "fork"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, local_rank, world = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local_rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

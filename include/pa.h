@@ -1,0 +1,246 @@
+/*
+ * pa.h — C ABI of libpa: PagedAttention decode on GB300 (sm_103a).
+ *
+ * Three device operations make up the hot path, plus a host block allocator
+ * that builds their index inputs. Sources are the PagedAttention pages, cited
+ * by title and section:
+ *   [book]    "第4章 PagedAttention：虚拟内存的启示" (vLLM source-reading book)
+ *   [digest]  "PagedAttention: virtual memory for the KV cache" (digest of
+ *             thegustafson.com)
+ *   [codex]   "01 · PagedAttention 与 KV cache 块管理"
+ *   [lecture] "4. PagedAttention原理（下）"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - KV pool: one per layer, a dense row-major array shaped
+ *   (2, num_blocks, block_size, num_kv_heads, head_size); index 0 of the
+ *   first dimension holds K, index 1 holds V; head_size is innermost
+ *   ([book] §4.3.1, §4.3.2). Element type: PA_F16 or PA_BF16.
+ * - Pointers named "device" must point to GPU memory of the current device
+ *   and be 16-byte aligned; the caller owns every buffer. The library never
+ *   allocates device memory.
+ * - Index arrays are int32 ([book] §4.4.1, §4.4.3).
+ * - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream). A return value of PA_OK means the work was
+ *   validated and enqueued. Argument errors are detected on the host before
+ *   any CUDA call and return a negative PA_ERR_* code; pa_last_error()
+ *   returns a message for the calling thread's most recent failure.
+ * - Data-dependent errors (a block id, slot or sequence length outside the
+ *   pool or table) cannot be seen on the host. Kernels never read or write
+ *   outside the buffers because of them: the offending item is skipped (or
+ *   read as zeros) and a bit is set in a per-device error word, which
+ *   pa_get_device_error() returns and clears.
+ * - block_size must be a positive multiple of 16 ([book] §4.3.4: the CUDA
+ *   backends require block_size % 16 == 0).
+ */
+#ifndef PAGED_KV_CACHE_PA_H
+#define PAGED_KV_CACHE_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including CUDA headers (same type). */
+typedef struct CUstream_st *pa_stream_t;
+
+/* Status codes. */
+#define PA_OK                  0
+#define PA_ERR_INVALID_ARG    -1  /* null pointer, bad size, misalignment */
+#define PA_ERR_UNSUPPORTED    -2  /* dtype / head_size / group shape not built */
+#define PA_ERR_CUDA           -3  /* a CUDA runtime or driver call failed */
+#define PA_ERR_WORKSPACE      -4  /* workspace missing or too small */
+#define PA_ERR_OUT_OF_BLOCKS  -5  /* allocator: free list exhausted */
+#define PA_ERR_NOT_FOUND      -6  /* allocator: unknown sequence id */
+
+/* Element types of Q, K, V and the output. */
+#define PA_F16   0
+#define PA_BF16  1
+
+/* Bits of the device error word. */
+#define PA_DEVERR_BLOCK_ID  1   /* a block table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT      2   /* a slot >= num_blocks * block_size */
+#define PA_DEVERR_SEQ_LEN   4   /* a seq_len < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEVERR_PAIR      8   /* a copy pair out of range, or a dst repeated / also a src */
+#define PA_DEVERR_TIMEOUT  16   /* a bounded wait inside a kernel gave up */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pa_version(void);
+
+/* Message for the calling thread's most recent failed call ("" if none).
+ * The string stays valid until that thread's next failing call. */
+const char *pa_last_error(void);
+
+/*
+ * pa_reshape_and_cache — write this step's new K/V rows into their slots.
+ * [book] §4.4.3 (slot_mapping: one physical slot per new token, slot =
+ * block_table[pos / B] * B + pos % B) and §4.5 step 1 (the step's K/V are
+ * written into the cache by slot before attention reads it).
+ *
+ *   key, value    device, [num_tokens][num_kv_heads][head_size], contiguous
+ *   kv_cache      device, the layer's pool (see conventions)
+ *   slot_mapping  device, [num_tokens] int32. Token t goes to
+ *                 kv_cache[0 or 1][slot / block_size][slot % block_size].
+ *                 A negative slot means "skip this token" (padding).
+ *                 A slot >= num_blocks * block_size is skipped and sets
+ *                 PA_DEVERR_SLOT.
+ *   num_tokens    >= 0 (0 is a no-op)
+ *   head_size     num_kv_heads * head_size must be a multiple of 8
+ * Writes are bit copies. Two tokens with the same slot race (last writer
+ * unspecified). Returns PA_OK or a PA_ERR_* code.
+ */
+int pa_reshape_and_cache(const void *key, const void *value, void *kv_cache,
+                         const int32_t *slot_mapping, int num_tokens,
+                         int num_blocks, int block_size, int num_kv_heads,
+                         int head_size, int dtype, pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size — bytes of device workspace pa_decode needs for
+ * this batch shape on the current device (it depends on the device's SM
+ * count). The same arguments must be passed to pa_decode. Writes *bytes.
+ */
+int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                             int head_size, int block_size, int dtype,
+                             size_t *bytes);
+
+/*
+ * pa_decode — one query token per sequence attends over all its cached
+ * tokens through the block table ([book] §4.5 step 2 and the read loop
+ * "for logical_block in used_blocks: phys = block_table[row, logical_block]";
+ * §4.4.1 block table; [digest] "注意力内核为何能正常工作").
+ *
+ *   out            device, [num_seqs][num_q_heads][head_size], dtype
+ *   query          device, [num_seqs][num_q_heads][head_size], dtype
+ *   kv_cache       device, the layer's pool (see conventions)
+ *   block_tables   device, [num_seqs][max_blocks_per_seq] int32; row s,
+ *                  column j = physical block of logical block j of sequence
+ *                  s. Only the first ceil(seq_lens[s] / block_size) entries
+ *                  of a row are read; the rest may hold anything.
+ *   seq_lens       device, [num_seqs] int32: tokens cached for each
+ *                  sequence, this step's token included. 0 gives a zero
+ *                  output row.
+ *   scale          multiplies q.k before the softmax (1/sqrt(head_size) in
+ *                  the pages' pseudo-code)
+ *   num_q_heads, num_kv_heads: num_q_heads % num_kv_heads == 0. Query head
+ *                  hq reads kv head hq / (num_q_heads / num_kv_heads)
+ *                  (contiguous groups: MHA, GQA, MQA). The group size G must
+ *                  be <= 16 or a multiple of 16.
+ *   head_size      64 or 128
+ *   workspace      device, >= pa_decode_workspace_size(...) bytes, 256-byte
+ *                  aligned; scratch for the split-K partial results. Its
+ *                  contents need no initialisation and are not preserved.
+ *                  Calls that share a workspace must not overlap on the GPU.
+ *
+ * Result: out[s][hq] = sum_i softmax_i(scale * q.k_i) v_i over the
+ * seq_lens[s] logical tokens, computed with fp32 dot products, an fp32
+ * online softmax ([book] §4.6), split-K partial states merged with the same
+ * (m, s, O) rule, and one rounding to dtype at the end. For a given device
+ * and batch shape the result does not depend on where the blocks sit in
+ * the pool (bit-identical under any permutation of physical placement).
+ * num_seqs must be <= 4096. Returns PA_OK or a PA_ERR_* code.
+ */
+int pa_decode(void *out, const void *query, const void *kv_cache,
+              const int32_t *block_tables, int max_blocks_per_seq,
+              const int32_t *seq_lens, int num_seqs, float scale,
+              int num_q_heads, int num_kv_heads, int head_size,
+              int num_blocks, int block_size, int dtype,
+              void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks — copy-on-write clones of whole physical blocks
+ * ([digest] "写时复制": a shared block is cloned before a write and the
+ * writer's table retargeted; [lecture] §4.3 steps: allocate Q, copy P into
+ * Q). A block spans every layer ([book] §4.3.1: a "complete block" covers
+ * all layers), so each pair is copied in every given pool.
+ *
+ *   kv_caches      HOST array of num_layers device pointers, one pool each;
+ *                  1 <= num_layers <= 512
+ *   src_dst_pairs  device, [num_pairs][2] int32 (src, dst)
+ * For every pair and layer, kv_cache[c][dst] = kv_cache[c][src] for c in
+ * {0, 1}: all block_size slots, all heads, bit for bit. Preconditions: ids in
+ * [0, num_blocks); no dst appears twice; no dst is also a src. A pair that
+ * breaks them is not copied and sets PA_DEVERR_PAIR; the other pairs are
+ * copied from the pre-call contents. Returns PA_OK or a PA_ERR_* code.
+ */
+int pa_copy_blocks(void *const *kv_caches, int num_layers,
+                   const int32_t *src_dst_pairs, int num_pairs,
+                   int num_blocks, int block_size, int num_kv_heads,
+                   int head_size, int dtype, pa_stream_t stream);
+
+/*
+ * pa_get_device_error — read and clear the current device's error word
+ * (PA_DEVERR_* bits, 0 if none). Synchronises the device first, so every
+ * earlier launch has finished. Returns PA_OK or PA_ERR_CUDA.
+ */
+int pa_get_device_error(int *bits);
+
+/* ------------------------------------------------------------------ */
+/* Host block allocator: builds block tables, slot mappings and COW    */
+/* pairs ([digest] "调度器机制简述" and "写时复制"; [codex] §3, §4.3;   */
+/* [lecture] §4.3). Host memory only; not thread-safe per handle.      */
+/* ------------------------------------------------------------------ */
+
+typedef struct pa_allocator pa_allocator;
+
+/*
+ * Create a pool of num_blocks blocks of block_size tokens. `order` (may be
+ * NULL = 0, 1, ..., num_blocks-1) is the initial free list, head first:
+ * allocation pops the head, so an explicit order reproduces a given
+ * placement and a random permutation gives random non-repeating ids.
+ * Blocks whose count drops to 0 return to the head (LIFO reuse of freed
+ * blocks, [codex] §4.3). Returns NULL on bad arguments (order must list
+ * every block exactly once).
+ */
+pa_allocator *pa_alloc_create(int num_blocks, int block_size, const int32_t *order);
+void pa_alloc_destroy(pa_allocator *a);
+
+int pa_alloc_num_free(const pa_allocator *a);
+/* Reference count of a block (0 = on the free list), or PA_ERR_INVALID_ARG. */
+int pa_alloc_ref_count(const pa_allocator *a, int block);
+
+/* New sequence holding num_tokens tokens: ceil(num_tokens / block_size)
+ * blocks. All-or-nothing: PA_ERR_OUT_OF_BLOCKS leaves the pool unchanged. */
+int pa_alloc_add_seq(pa_allocator *a, int num_tokens, int *seq_id);
+
+/* New sequence sharing every block of `parent` (each block's count + 1),
+ * as parallel sampling or a shared prompt does ([book] §4.7.1). */
+int pa_alloc_fork(pa_allocator *a, int parent, int *child);
+
+/*
+ * Reserve the slot of the sequence's next token (position = its length).
+ * If the last block is full (or there is none), a new block is taken. If the
+ * last block has room but is shared (count > 1), it is copied on write: a
+ * new block Q is taken, *cow_src = old block, *cow_dst = Q, the sequence's
+ * table points at Q, and the old block's count drops by 1 ([lecture] §4.3).
+ * Otherwise *cow_src = *cow_dst = -1. *slot = table[pos / B] * B + pos % B
+ * ([book] §4.4.3). The caller must run pa_copy_blocks on the pair before
+ * writing the token. PA_ERR_OUT_OF_BLOCKS leaves everything unchanged.
+ */
+int pa_alloc_append_token(pa_allocator *a, int seq_id, int32_t *slot,
+                          int32_t *cow_src, int32_t *cow_dst);
+
+/* Release a sequence: its blocks in reverse table order, each count - 1. */
+int pa_alloc_free_seq(pa_allocator *a, int seq_id);
+
+/* Tokens held by a sequence (>= 0), or a PA_ERR_* code. */
+int pa_alloc_seq_len(const pa_allocator *a, int seq_id);
+
+/* Number of blocks in a sequence's table (>= 0), or a PA_ERR_* code. */
+int pa_alloc_seq_num_blocks(const pa_allocator *a, int seq_id);
+
+/* Fill out[n][max_blocks_per_seq] (host, int32) with the tables of the
+ * given sequences, padding each row with -1. PA_ERR_INVALID_ARG if a table
+ * is longer than max_blocks_per_seq. */
+int pa_alloc_block_tables(const pa_allocator *a, const int *seq_ids, int n,
+                          int max_blocks_per_seq, int32_t *out);
+
+/* Fill out[n] (host, int32) with the sequences' lengths. */
+int pa_alloc_seq_lens(const pa_allocator *a, const int *seq_ids, int n, int32_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_CACHE_PA_H */

@@ -1,0 +1,252 @@
+"""Thin ctypes binding of libpa (``include/pa.h``), with the same names.
+
+Argument marshalling only: tensors are turned into pointers and sizes, the
+current torch CUDA stream is passed as ``stream``, and a negative status is
+raised as :class:`PAError` with the library's message. Every step of the
+hot path runs in libpa's kernels; there is no fallback. If the library is
+not built this module raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpa.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = -1
+PA_ERR_UNSUPPORTED = -2
+PA_ERR_CUDA = -3
+PA_ERR_WORKSPACE = -4
+PA_ERR_OUT_OF_BLOCKS = -5
+PA_ERR_NOT_FOUND = -6
+PA_F16 = 0
+PA_BF16 = 1
+PA_DEVERR_BLOCK_ID = 1
+PA_DEVERR_SLOT = 2
+PA_DEVERR_SEQ_LEN = 4
+PA_DEVERR_PAIR = 8
+PA_DEVERR_TIMEOUT = 16
+
+# (name, restype, argtypes) of every exported function, in header order.
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_ip = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = [
+    ("pa_version", _i, []),
+    ("pa_last_error", ctypes.c_char_p, []),
+    ("pa_reshape_and_cache", _i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    ("pa_decode_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    ("pa_decode", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
+    ("pa_get_device_error", _i, [_ip]),
+    ("pa_alloc_create", _vp, [_i, _i, _i32p]),
+    ("pa_alloc_destroy", None, [_vp]),
+    ("pa_alloc_num_free", _i, [_vp]),
+    ("pa_alloc_ref_count", _i, [_vp, _i]),
+    ("pa_alloc_add_seq", _i, [_vp, _i, _ip]),
+    ("pa_alloc_fork", _i, [_vp, _i, _ip]),
+    ("pa_alloc_append_token", _i, [_vp, _i, _i32p, _i32p, _i32p]),
+    ("pa_alloc_free_seq", _i, [_vp, _i]),
+    ("pa_alloc_seq_len", _i, [_vp, _i]),
+    ("pa_alloc_seq_num_blocks", _i, [_vp, _i]),
+    ("pa_alloc_block_tables", _i, [_vp, _ip, _i, _i, _i32p]),
+    ("pa_alloc_seq_lens", _i, [_vp, _ip, _i, _i32p]),
+]
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"libpa error {code}: {message}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa.so (built by paged_kv_cache_120_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpa.so is not built ({LIB_PATH}); run "
+                               "`python -m paged_kv_cache_120_gb300.build`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise PAError(rc, lib().pa_last_error().decode())
+    return rc
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def pa_version() -> int:
+    return lib().pa_version()
+
+
+def pa_last_error() -> str:
+    return lib().pa_last_error().decode()
+
+
+def pa_reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None) -> None:
+    """key/value [T, Hkv, D], kv_cache (2, NB, B, Hkv, D), slot_mapping [T] int32."""
+    _, nb, bs, hkv, d = kv_cache.shape
+    _check(lib().pa_reshape_and_cache(
+        _dev(key, "key"), _dev(value, "value"), _dev(kv_cache, "kv_cache"),
+        _dev(slot_mapping, "slot_mapping"), int(slot_mapping.shape[0]), nb, bs, hkv, d,
+        _dtype_code(kv_cache), _stream(stream)))
+
+
+def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                             dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                          block_size, dtype, ctypes.byref(out)))
+    return out.value
+
+
+def decode_workspace(query, kv_cache):
+    """A correctly sized uint8 workspace tensor for pa_decode on this batch shape."""
+    import torch
+    s, hq, d = query.shape
+    _, _, bs, hkv, _ = kv_cache.shape
+    n = pa_decode_workspace_size(s, hq, hkv, d, bs, _dtype_code(kv_cache))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=query.device)
+
+
+def pa_decode(out, query, kv_cache, block_tables, seq_lens, scale, workspace,
+              stream=None) -> None:
+    """out/query [S, Hq, D]; kv_cache (2, NB, B, Hkv, D); block_tables [S, maxblk] int32;
+    seq_lens [S] int32; workspace: uint8 CUDA tensor (see decode_workspace)."""
+    s, hq, d = query.shape
+    _, nb, bs, hkv, _ = kv_cache.shape
+    _check(lib().pa_decode(
+        _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
+        _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
+        _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
+        _dtype_code(kv_cache), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:
+    """kv_caches: list of per-layer pools; src_dst_pairs [N, 2] int32 CUDA tensor."""
+    _, nb, bs, hkv, d = kv_caches[0].shape
+    ptrs = (ctypes.c_void_p * len(kv_caches))(*[_dev(c, "kv_cache").value for c in kv_caches])
+    _check(lib().pa_copy_blocks(ptrs, len(kv_caches), _dev(src_dst_pairs, "src_dst_pairs"),
+                                int(src_dst_pairs.shape[0]), nb, bs, hkv, d,
+                                _dtype_code(kv_caches[0]), _stream(stream)))
+
+
+def pa_get_device_error() -> int:
+    bits = ctypes.c_int(0)
+    _check(lib().pa_get_device_error(ctypes.byref(bits)))
+    return bits.value
+
+
+class BlockAllocator:
+    """Host block allocator (pa_alloc_*): free list, ref counts, copy-on-write."""
+
+    def __init__(self, num_blocks: int, block_size: int, order=None):
+        self.num_blocks, self.block_size = num_blocks, block_size
+        if order is not None:
+            self._order = np.ascontiguousarray(order, dtype=np.int32)
+            optr = self._order.ctypes.data_as(_i32p)
+        else:
+            optr = None
+        h = lib().pa_alloc_create(num_blocks, block_size, optr)
+        if not h:
+            raise PAError(PA_ERR_INVALID_ARG, pa_last_error())
+        self._h = ctypes.c_void_p(h)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pa_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return _check(lib().pa_alloc_num_free(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return _check(lib().pa_alloc_ref_count(self._h, block))
+
+    def add_seq(self, num_tokens: int) -> int:
+        sid = ctypes.c_int(0)
+        _check(lib().pa_alloc_add_seq(self._h, num_tokens, ctypes.byref(sid)))
+        return sid.value
+
+    def fork(self, parent: int) -> int:
+        sid = ctypes.c_int(0)
+        _check(lib().pa_alloc_fork(self._h, parent, ctypes.byref(sid)))
+        return sid.value
+
+    def append_token(self, seq: int):
+        """-> (slot, (cow_src, cow_dst) or None)."""
+        slot, src, dst = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(lib().pa_alloc_append_token(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                           ctypes.byref(dst)))
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def free_seq(self, seq: int) -> None:
+        _check(lib().pa_alloc_free_seq(self._h, seq))
+
+    def seq_len(self, seq: int) -> int:
+        return _check(lib().pa_alloc_seq_len(self._h, seq))
+
+    def num_blocks_of(self, seq: int) -> int:
+        return _check(lib().pa_alloc_seq_num_blocks(self._h, seq))
+
+    def table(self, seq: int):
+        n = self.num_blocks_of(seq)
+        return self.block_tables([seq], max(n, 1))[0, :n].tolist()
+
+    def block_tables(self, seqs, max_blocks_per_seq: int) -> np.ndarray:
+        ids = np.ascontiguousarray(seqs, dtype=np.int32)
+        out = np.empty((len(ids), max_blocks_per_seq), dtype=np.int32)
+        _check(lib().pa_alloc_block_tables(self._h, ids.ctypes.data_as(_ip), len(ids),
+                                           max_blocks_per_seq, out.ctypes.data_as(_i32p)))
+        return out
+
+    def seq_lens(self, seqs) -> np.ndarray:
+        ids = np.ascontiguousarray(seqs, dtype=np.int32)
+        out = np.empty(len(ids), dtype=np.int32)
+        _check(lib().pa_alloc_seq_lens(self._h, ids.ctypes.data_as(_ip), len(ids),
+                                       out.ctypes.data_as(_i32p)))
+        return out

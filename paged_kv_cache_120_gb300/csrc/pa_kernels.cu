@@ -1,0 +1,1095 @@
+// PagedAttention decode for GB300 (sm_103a): kernels and their C ABI.
+//
+// What is computed follows the PagedAttention pages (vLLM book chapter 4,
+// "第4章 PagedAttention：虚拟内存的启示": §4.3.1 pool layout, §4.4 block
+// table and slot mapping, §4.5 write-then-read call chain, §4.6 online
+// softmax; "PagedAttention: virtual memory for the KV cache": copy-on-write).
+// How it is computed is GB300-specific:
+//
+//  * pa_decode is HBM-bound (a few flops per byte). Each warp streams its own
+//    share of 16-token K/V tiles through a private ring of shared-memory
+//    stages filled by TMA (cp.async.bulk.tensor, 128-byte swizzle), one
+//    mbarrier per stage, with the block-table lookups for the next 32 tiles
+//    prefetched into registers. The tile is consumed with ldmatrix and
+//    mma.m16n8k16 (fp16/bf16 in, fp32 accumulate): S^T = K Q^T puts the GQA
+//    query group on the MMA's N side, P is transposed in registers with
+//    movmatrix, and O^T += V^T P^T. The softmax is an fp32 online softmax in
+//    base 2.
+//  * Work is split "stream-K" style: all 16-token tiles of all (sequence,
+//    kv-head, query-tile) segments are laid end to end and every warp of a
+//    persistent grid takes an equal contiguous share. A segment that fits in
+//    one warp's share is finished in place; a segment cut by share
+//    boundaries leaves one partial (m, l, O) record per piece and a small
+//    reduce kernel merges the pieces in ascending order with the online
+//    softmax rule. The split depends only on the sequence lengths and the
+//    grid size, never on physical block ids, so outputs are bit-identical
+//    under any permutation of block placement.
+//  * reshape_and_cache and copy_blocks are bit copies with 16-byte accesses.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- device state
+
+__device__ int g_device_error;  // PA_DEVERR_* bits, read and cleared by pa_get_device_error
+
+__device__ __forceinline__ void raise_error(int bit) { atomicOr(&g_device_error, bit); }
+
+// --------------------------------------------------------------- PTX wrappers
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Every wait on an mbarrier is bounded: after this long the kernel records
+// PA_DEVERR_TIMEOUT and stops instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One TMA tile load of a rank-5 tensor into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void sts128_zero(uint32_t addr)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// Round two floats to a packed 16-bit pair (low half = first), nearest-even.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t x)
+{
+    if constexpr (BF16) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&x));
+    } else {
+        return __half22float2(*reinterpret_cast<__half2 *>(&x));
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t to_elem(float x)
+{
+    if constexpr (BF16)
+        return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    else
+        return __half_as_ushort(__float2half_rn(x));
+}
+
+// ------------------------------------------------------------------- decode
+
+constexpr int kWarps = 4;       // warps per CTA, each an independent pipeline
+constexpr int kStages = 3;      // TMA ring depth per warp
+constexpr int kTile = 16;       // tokens per tile (the MMA's M)
+constexpr int kMaxSeqs = 4096;  // sequences per pa_decode call (prefix lives in smem)
+
+template <int D>
+struct TileGeo {
+    static constexpr int kBoxes = D / 64;             // 64-element (128-byte) swizzle boxes
+    static constexpr int kBoxBytes = 4096;            // [K|V][16 rows][128 B]
+    static constexpr int kStageBytes = kBoxes * kBoxBytes;
+};
+
+struct DecodeParams {
+    void *out;
+    const uint16_t *query;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    float *records;       // workspace: 2 records per warp
+    long long *prefix_ws; // workspace: unit prefix over sequences, [num_seqs + 1]
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;            // num_q_heads / num_kv_heads
+    int tile_q;           // query heads per query tile (<= 16)
+    int qtiles;           // query tiles per kv head
+    int num_blocks;
+    int block_size;
+    int tiles_per_block;  // block_size / 16
+    float scale_log2;     // scale * log2(e): scores live in base 2
+    int total_warps;
+};
+
+template <int D, int NT>
+constexpr int record_floats()
+{
+    return NT * 8 * (D + 2);  // m[GP], l[GP], O[D][GP]
+}
+
+template <int D>
+inline size_t decode_smem_bytes(int num_seqs)
+{
+    size_t b = 1024;  // alignment slack for the 1024-byte swizzle atoms
+    b += (size_t)kWarps * kStages * TileGeo<D>::kStageBytes;
+    b += (size_t)kWarps * kStages * sizeof(uint64_t);
+    b += (size_t)(num_seqs + 1) * sizeof(long long);
+    b += (size_t)num_seqs * sizeof(int);
+    return b;
+}
+
+// Main decode kernel. Template: head size D, N-tiles of 8 query heads NT,
+// element type. One CTA = kWarps independent warp pipelines.
+template <int D, int NT, bool BF16>
+__global__ void __launch_bounds__(kWarps * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
+{
+    constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of V^T P^T
+    constexpr int GP = NT * 8;
+    constexpr int STAGE = TileGeo<D>::kStageBytes;
+    constexpr int REC = record_floats<D, NT>();
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ long long warp_sums[kWarps];
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kWarps * kStages * STAGE);
+    long long *prefix = reinterpret_cast<long long *>(bars + kWarps * kStages);
+    int *lens = reinterpret_cast<int *>(prefix + p.num_seqs + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.num_seqs;
+    const int segs_per_seq = p.num_kv_heads * p.qtiles;
+    const int max_len = p.max_blocks_per_seq * p.block_size;
+
+    // 1. Sequence lengths and the exclusive prefix of units (tiles x segments).
+    {
+        const int per = (S + blockDim.x - 1) / blockDim.x;
+        const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+        long long local = 0;
+        for (int s = s0; s < s1; ++s) {
+            int L = p.seq_lens[s];
+            if (L < 0 || L > max_len) {
+                raise_error(PA_DEVERR_SEQ_LEN);
+                L = L < 0 ? 0 : max_len;
+            }
+            lens[s] = L;
+            local += (long long)((L + kTile - 1) / kTile) * segs_per_seq;
+        }
+        long long incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        if (lane == 31)
+            warp_sums[warp] = incl;
+        __syncthreads();
+        long long off = 0;
+        for (int w = 0; w < warp; ++w)
+            off += warp_sums[w];
+        long long run = off + incl - local;
+        for (int s = s0; s < s1; ++s) {
+            prefix[s] = run;
+            run += (long long)((lens[s] + kTile - 1) / kTile) * segs_per_seq;
+        }
+        if (tid == (int)blockDim.x - 1)
+            prefix[S] = off + incl;
+    }
+    if (lane == 0) {
+        for (int st = 0; st < kStages; ++st)
+            mbar_init(smem_addr(&bars[warp * kStages + st]), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const long long N = prefix[S];
+    if (blockIdx.x == 0)
+        for (int s = tid; s <= S; s += blockDim.x)
+            p.prefix_ws[s] = prefix[s];
+
+    // 2. This warp's contiguous share of the unit sequence.
+    const int gw = blockIdx.x * kWarps + warp;
+    const long long r0 = N * gw / p.total_warps;
+    const long long r1 = N * (gw + 1) / p.total_warps;
+    if (r0 >= r1)
+        return;  // no block-level synchronisation below this point
+
+    // Unit u -> physical block, segment id and (tile << 5 | valid tokens).
+    auto unit_info = [&](long long u, int &phys, int &seg, int &tv) {
+        phys = -1;
+        seg = -1;
+        tv = 0;
+        if (u >= r1)
+            return;
+        int lo = 0, hi = S;  // prefix[lo] <= u < prefix[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= u)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int L = lens[lo];
+        const int ntiles = (L + kTile - 1) / kTile;
+        const long long local = u - prefix[lo];
+        const int segl = (int)(local / ntiles);
+        const int tile = (int)(local - (long long)segl * ntiles);
+        int b = __ldg(p.block_tables + (long long)lo * p.max_blocks_per_seq + tile / p.tiles_per_block);
+        if ((unsigned)b >= (unsigned)p.num_blocks) {
+            raise_error(PA_DEVERR_BLOCK_ID);
+            b = p.num_blocks;  // outside the tensor map: TMA fills zeros
+        }
+        phys = b;
+        seg = lo * segs_per_seq + segl;
+        tv = (tile << 5) | min(kTile, L - tile * kTile);
+    };
+
+    // Register windows of unit info: A covers [wb, wb+32), B covers [wb+32, wb+64).
+    long long wb = r0;
+    int a_phys, a_seg, a_tv, b_phys, b_seg, b_tv;
+    unit_info(wb + lane, a_phys, a_seg, a_tv);
+    unit_info(wb + 32 + lane, b_phys, b_seg, b_tv);
+    auto fetch = [&](long long v, int &ph, int &sg, int &t) {
+        const int idx = (int)(v - wb);
+        const bool first = idx < 32;
+        const int src = idx & 31;
+        ph = __shfl_sync(kFull, first ? a_phys : b_phys, src);
+        sg = __shfl_sync(kFull, first ? a_seg : b_seg, src);
+        t = __shfl_sync(kFull, first ? a_tv : b_tv, src);
+    };
+
+    const uint32_t my_stage0 = base + (uint32_t)(warp * kStages * STAGE);
+    const uint32_t my_bar0 = smem_addr(&bars[warp * kStages]);
+    auto issue = [&](int phys, int seg, int tv, int st) {
+        if (lane == 0) {
+            const int h = (seg % segs_per_seq) / p.qtiles;
+            const int t0 = ((tv >> 5) % p.tiles_per_block) * kTile;
+            const uint32_t bar = my_bar0 + st * 8;
+            mbar_expect_tx(bar, STAGE);
+#pragma unroll
+            for (int bx = 0; bx < D / 64; ++bx)
+                tma_load_5d(my_stage0 + st * STAGE + bx * TileGeo<D>::kBoxBytes, &kv_map, bar,
+                            bx * 64, h, t0, phys, 0);
+        }
+    };
+
+    long long ip = r0;  // next unit to issue
+    for (int st = 0; st < kStages && ip < r1; ++st, ++ip) {
+        int ph, sg, t;
+        fetch(ip, ph, sg, t);
+        issue(ph, sg, t, st);
+    }
+
+    const int g = lane >> 2, tig = lane & 3;
+    const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix rows for K (A of S^T)
+    const int k_hi = lane >> 4;
+    const int v_row = (lane & 7) + ((lane >> 4) & 1) * 8;  // ldmatrix.trans rows for V (A of O^T)
+    const int v_hi = (lane >> 3) & 1;
+
+    float m_run[NT][2], l_run[NT][2], acc[KS][NT][4];
+    uint32_t qf[NT][KS][2];
+    int cur_seg = -1;
+
+    auto seg_coords = [&](int seg, int &s, int &segl, int &hq0) {
+        s = seg / segs_per_seq;
+        segl = seg - s * segs_per_seq;
+        const int h = segl / p.qtiles, qt = segl - (segl / p.qtiles) * p.qtiles;
+        hq0 = h * p.group + qt * 16;
+    };
+
+    auto begin_segment = [&](int seg) {
+        int s, segl, hq0;
+        seg_coords(seg, s, segl, hq0);
+        const uint16_t *qbase = p.query + ((long long)s * p.num_q_heads + hq0) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g;
+            const bool live = col < p.tile_q;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qbase + (long long)col * D);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                qf[nt][kk][0] = live ? __ldg(qrow + 8 * kk + tig) : 0u;
+                qf[nt][kk][1] = live ? __ldg(qrow + 8 * kk + 4 + tig) : 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                m_run[nt][e] = -INFINITY;
+                l_run[nt][e] = 0.f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    acc[mt][nt][c] = 0.f;
+        }
+    };
+
+    auto finish_segment = [&](int seg) {
+        float lsum[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float v = l_run[nt][e];
+                v += __shfl_xor_sync(kFull, v, 4);
+                v += __shfl_xor_sync(kFull, v, 8);
+                v += __shfl_xor_sync(kFull, v, 16);
+                lsum[nt][e] = v;
+            }
+        int s, segl, hq0;
+        seg_coords(seg, s, segl, hq0);
+        const int ntiles = (lens[s] + kTile - 1) / kTile;
+        const long long seg_start = prefix[s] + (long long)segl * ntiles;
+        const long long seg_end = seg_start + ntiles;
+        if (seg_start >= r0 && seg_end <= r1) {
+            // Whole segment in this warp's share: normalise and store.
+            uint16_t *out = static_cast<uint16_t *>(p.out) + ((long long)s * p.num_q_heads + hq0) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = nt * 8 + 2 * tig + e;
+                    if (col < p.tile_q) {
+                        const float inv = 1.f / lsum[nt][e];
+                        uint16_t *row = out + (long long)col * D;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            row[16 * mt + g] = to_elem<BF16>(acc[mt][nt][e] * inv);
+                            row[16 * mt + g + 8] = to_elem<BF16>(acc[mt][nt][2 + e] * inv);
+                        }
+                    }
+                }
+        } else {
+            // A piece of a segment: record (m, l, O) for the reduce kernel.
+            // Slot 2w holds the piece of the warp's first segment, 2w+1 its last.
+            const long long slot = (seg_start <= r0) ? 2LL * gw : 2LL * gw + 1;
+            float *rec = p.records + slot * REC;
+            if (g == 0) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = nt * 8 + 2 * tig + e;
+                        rec[col] = m_run[nt][e];
+                        rec[GP + col] = lsum[nt][e];
+                    }
+            }
+            float *ro = rec + 2 * GP;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int col = nt * 8 + 2 * tig;
+                    *reinterpret_cast<float2 *>(ro + (16 * mt + g) * GP + col) =
+                        make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+                    *reinterpret_cast<float2 *>(ro + (16 * mt + g + 8) * GP + col) =
+                        make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+                }
+        }
+    };
+
+    int st = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    long long i = r0;
+    for (; i < r1; ++i) {
+        if (i - wb >= 32) {
+            wb += 32;
+            a_phys = b_phys;
+            a_seg = b_seg;
+            a_tv = b_tv;
+            unit_info(wb + 32 + lane, b_phys, b_seg, b_tv);
+        }
+        int ph, sg, tv;
+        fetch(i, ph, sg, tv);
+        if (sg != cur_seg) {
+            if (cur_seg >= 0)
+                finish_segment(cur_seg);
+            cur_seg = sg;
+            begin_segment(sg);
+        }
+        if (!mbar_wait(my_bar0 + st * 8, phase)) {
+            raise_error(PA_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const uint32_t sbuf = my_stage0 + st * STAGE;
+        const int valid = tv & 31;
+        if (valid < kTile) {
+            // Rows past the sequence end hold stale data (possibly NaN): zero the
+            // V rows so that p = 0 times them stays 0. K rows are masked below.
+            const int per_box = (kTile - valid) * 8;
+            for (int z = lane; z < per_box * (D / 64); z += 32) {
+                const int bx = z / per_box, rem = z - bx * per_box;
+                const int r = valid + (rem >> 3), c = rem & 7;
+                sts128_zero(sbuf + bx * TileGeo<D>::kBoxBytes + 2048 + r * 128 + c * 16);
+            }
+            fence_proxy_async();
+            __syncwarp();
+        }
+
+        // S^T[16 tokens][8*NT queries] = K Q^T
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const int cg = 2 * kk + k_hi;
+            const uint32_t addr = sbuf + (cg >> 3) * TileGeo<D>::kBoxBytes + k_row * 128 +
+                                  (((cg & 7) ^ (k_row & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma16816<BF16>(sc[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+        }
+
+        // Online softmax (base 2) per query column; P rounded to the element type.
+        const bool tok0 = g < valid, tok1 = g + 8 < valid;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float pr[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float x0 = tok0 ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                const float x1 = tok1 ? sc[nt][2 + e] * p.scale_log2 : -INFINITY;
+                float mx = fmaxf(x0, x1);
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+                const float m_new = fmaxf(m_run[nt][e], mx);
+                const float alpha = exp2f(m_run[nt][e] - m_new);
+                m_run[nt][e] = m_new;
+                pr[e] = exp2f(x0 - m_new);
+                pr[2 + e] = exp2f(x1 - m_new);
+                l_run[nt][e] *= alpha;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[mt][nt][e] *= alpha;
+                    acc[mt][nt][2 + e] *= alpha;
+                }
+            }
+            const uint32_t r0p = pack2<BF16>(pr[0], pr[1]);  // token g,   columns 2tig, 2tig+1
+            const uint32_t r1p = pack2<BF16>(pr[2], pr[3]);  // token g+8
+            const float2 f0 = unpack2<BF16>(r0p), f1 = unpack2<BF16>(r1p);
+            l_run[nt][0] += f0.x + f1.x;
+            l_run[nt][1] += f0.y + f1.y;
+            pb[nt][0] = movm_t(r0p);  // P^T fragments as the B operand
+            pb[nt][1] = movm_t(r1p);
+        }
+
+        // O^T[D][8*NT] += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int cg = 2 * mt + v_hi;
+            const uint32_t addr = sbuf + 2048 + (cg >> 3) * TileGeo<D>::kBoxBytes + v_row * 128 +
+                                  (((cg & 7) ^ (v_row & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(addr, a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma16816<BF16>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+
+        __syncwarp();
+        if (ip < r1) {
+            int ph2, sg2, tv2;
+            fetch(ip, ph2, sg2, tv2);
+            issue(ph2, sg2, tv2, st);
+            ++ip;
+        }
+        if (++st == kStages) {
+            st = 0;
+            phase ^= 1;
+        }
+    }
+    if (ok) {
+        if (cur_seg >= 0)
+            finish_segment(cur_seg);
+    } else {
+        // Give the copies still in flight into this warp's stages a bounded
+        // chance to land before the CTA's shared memory goes away.
+        for (long long u = i; u < ip; ++u) {
+            const int rel = (int)(u - r0);
+            mbar_wait(my_bar0 + (rel % kStages) * 8, (uint32_t)((rel / kStages) & 1));
+        }
+    }
+}
+
+// Merge the pieces of segments that crossed warp-share boundaries, and write
+// zero rows for empty sequences. One CTA per segment.
+template <int D, int NT, bool BF16>
+__global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeParams p)
+{
+    constexpr int GP = NT * 8;
+    constexpr int REC = record_floats<D, NT>();
+    const int seg = blockIdx.x;
+    const int segs_per_seq = p.num_kv_heads * p.qtiles;
+    const int s = seg / segs_per_seq, segl = seg - (seg / segs_per_seq) * segs_per_seq;
+    const int h = segl / p.qtiles, qt = segl - (segl / p.qtiles) * p.qtiles;
+    const int hq0 = h * p.group + qt * 16;
+    const int max_len = p.max_blocks_per_seq * p.block_size;
+    int L = p.seq_lens[s];
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    const int ntiles = (L + kTile - 1) / kTile;
+    uint16_t *out = static_cast<uint16_t *>(p.out) + ((long long)s * p.num_q_heads + hq0) * D;
+    if (ntiles == 0) {
+        for (int idx = threadIdx.x; idx < p.tile_q * D; idx += blockDim.x)
+            out[idx] = 0;
+        return;
+    }
+    const long long N = p.prefix_ws[p.num_seqs];
+    const long long W = p.total_warps;
+    const long long a = p.prefix_ws[s] + (long long)segl * ntiles, e = a + ntiles;
+    const int w_lo = (int)(((a + 1) * W - 1) / N), w_hi = (int)((e * W - 1) / N);
+    if (w_lo == w_hi)
+        return;  // finished by the main kernel
+    for (int idx = threadIdx.x; idx < p.tile_q * D; idx += blockDim.x) {
+        const int d = idx / p.tile_q, col = idx - (idx / p.tile_q) * p.tile_q;
+        float M = -INFINITY;
+        for (int w = w_lo; w <= w_hi; ++w) {
+            const long long r0 = N * w / W, r1 = N * (w + 1) / W;
+            if (r0 >= r1)
+                continue;
+            const long long slot = (a <= r0) ? 2LL * w : 2LL * w + 1;
+            M = fmaxf(M, p.records[slot * REC + col]);
+        }
+        float lsum = 0.f, o = 0.f;
+        for (int w = w_lo; w <= w_hi; ++w) {
+            const long long r0 = N * w / W, r1 = N * (w + 1) / W;
+            if (r0 >= r1)
+                continue;
+            const long long slot = (a <= r0) ? 2LL * w : 2LL * w + 1;
+            const float *rec = p.records + slot * REC;
+            const float f = exp2f(rec[col] - M);
+            lsum += rec[GP + col] * f;
+            o += rec[2 * GP + d * GP + col] * f;
+        }
+        out[(long long)col * D + d] = to_elem<BF16>(o / lsum);
+    }
+}
+
+// ------------------------------------------------------- reshape and copy
+
+// One CTA per new token: the token's K row [num_kv_heads][head_size] and V
+// row are contiguous both in the input and in the pool, so each is one run
+// of 16-byte copies.
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                             uint4 *__restrict__ kv, const int32_t *__restrict__ slots,
+                             int row_vecs, long long num_slots, long long half_vecs)
+{
+    const int t = blockIdx.x;
+    const long long slot = slots[t];
+    if (slot < 0)
+        return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0)
+            raise_error(PA_DEVERR_SLOT);
+        return;
+    }
+    const uint4 *k = key + (long long)t * row_vecs;
+    const uint4 *v = value + (long long)t * row_vecs;
+    uint4 *dk = kv + slot * row_vecs;
+    uint4 *dv = dk + half_vecs;
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) {
+        dk[i] = __ldg(k + i);
+        dv[i] = __ldg(v + i);
+    }
+}
+
+constexpr int kMaxLayers = 512;
+struct LayerPtrs {
+    uint4 *p[kMaxLayers];
+};
+
+// One CTA per (pair, layer): validate the pair against every other pair,
+// then copy the K block and the V block with 16-byte accesses.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(const __grid_constant__ LayerPtrs layers, const int32_t *__restrict__ pairs,
+                       int num_pairs, int num_blocks, long long block_vecs, long long half_vecs)
+{
+    const int i = blockIdx.x, layer = blockIdx.y;
+    const int src = pairs[2 * i], dst = pairs[2 * i + 1];
+    int clash = ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks);
+    for (int j = threadIdx.x; j < num_pairs; j += blockDim.x) {
+        const int sj = pairs[2 * j], dj = pairs[2 * j + 1];
+        if (sj == dst || (j != i && dj == dst))
+            clash = 1;
+    }
+    if (__syncthreads_or(clash)) {
+        if (threadIdx.x == 0 && layer == 0)
+            raise_error(PA_DEVERR_PAIR);
+        return;
+    }
+    uint4 *pool = layers.p[layer];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const uint4 *s = pool + c * half_vecs + (long long)src * block_vecs;
+        uint4 *d = pool + c * half_vecs + (long long)dst * block_vecs;
+        long long k = threadIdx.x;
+        for (; k + 3 * blockDim.x < block_vecs; k += 4 * blockDim.x) {
+            const uint4 x0 = s[k], x1 = s[k + blockDim.x], x2 = s[k + 2 * blockDim.x],
+                        x3 = s[k + 3 * blockDim.x];
+            d[k] = x0;
+            d[k + blockDim.x] = x1;
+            d[k + 2 * blockDim.x] = x2;
+            d[k + 3 * blockDim.x] = x3;
+        }
+        for (; k < block_vecs; k += blockDim.x)
+            d[k] = s[k];
+    }
+}
+
+// ================================================================ host side
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return set_error(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Rank-5 view of the pool, innermost first: (head_size, kv_heads, block
+// slots, blocks, K|V). A box is 64 elements x 1 head x 16 slots x 1 block x
+// {K, V}: one 16-token tile of one head, K and V together, 128-byte swizzled.
+struct MapKey {
+    const void *ptr;
+    int d, h, b, nb, dev;
+};
+
+int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_size,
+                  int num_kv_heads, int head_size, int device)
+{
+    static std::mutex mu;
+    static MapKey keys[16];
+    static CUtensorMap maps[16];
+    static int used = 0, next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        const MapKey &k = keys[i];
+        if (k.ptr == kv && k.d == head_size && k.h == num_kv_heads && k.b == block_size &&
+            k.nb == num_blocks && k.dev == device) {
+            *map = maps[i];
+            return PA_OK;
+        }
+    }
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t e = 2;  // bytes per element
+    cuuint64_t dims[5] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks, 2};
+    cuuint64_t strides[4] = {head_size * e, (cuuint64_t)num_kv_heads * head_size * e,
+                             (cuuint64_t)block_size * num_kv_heads * head_size * e,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * head_size * e};
+    cuuint32_t box[5] = {64, 1, (cuuint32_t)kTile, 1, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUtensorMap m;
+    CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void *>(kv), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    const int slot = used < 16 ? used++ : (next++ % 16);
+    keys[slot] = MapKey{kv, head_size, num_kv_heads, block_size, num_blocks, device};
+    maps[slot] = m;
+    *map = m;
+    return PA_OK;
+}
+
+// Shape and kernel choice for one pa_decode call.
+struct DecodePlan {
+    int nt = 1;       // 8-query N-tiles
+    int tile_q = 1;
+    int qtiles = 1;
+    int grid = 0;     // CTAs
+    int total_warps = 0;
+    size_t smem = 0;
+    size_t prefix_bytes = 0;
+    size_t record_bytes = 0;
+    const void *main_fn = nullptr;
+    const void *reduce_fn = nullptr;
+};
+
+template <int D, int NT, bool BF16>
+void pick_kernels(DecodePlan &pl)
+{
+    pl.main_fn = reinterpret_cast<const void *>(&paged_decode_kernel<D, NT, BF16>);
+    pl.reduce_fn = reinterpret_cast<const void *>(&paged_decode_reduce_kernel<D, NT, BF16>);
+    pl.smem = decode_smem_bytes<D>(0);
+}
+
+int validate_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                          int block_size, int dtype)
+{
+    if (num_seqs < 0 || num_seqs > kMaxSeqs)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_decode: dtype %d (want PA_F16 or PA_BF16)", dtype);
+    if (head_size != 64 && head_size != 128)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_decode: head_size %d (built: 64, 128)", head_size);
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                         num_q_heads, num_kv_heads);
+    const int group = num_q_heads / num_kv_heads;
+    if (group > 16 && group % 16 != 0)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_decode: query group %d (want <= 16 or a multiple of 16)", group);
+    if (block_size < kTile || block_size % kTile != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: block_size %d must be a positive multiple of 16", block_size);
+    return PA_OK;
+}
+
+int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+              int dtype)
+{
+    const int group = num_q_heads / num_kv_heads;
+    pl.tile_q = group <= 16 ? group : 16;
+    pl.qtiles = group <= 16 ? 1 : group / 16;
+    pl.nt = pl.tile_q <= 8 ? 1 : 2;
+    const bool bf = dtype == PA_BF16;
+    if (head_size == 64) {
+        if (pl.nt == 1) bf ? pick_kernels<64, 1, true>(pl) : pick_kernels<64, 1, false>(pl);
+        else            bf ? pick_kernels<64, 2, true>(pl) : pick_kernels<64, 2, false>(pl);
+        pl.smem = decode_smem_bytes<64>(num_seqs);
+    } else {
+        if (pl.nt == 1) bf ? pick_kernels<128, 1, true>(pl) : pick_kernels<128, 1, false>(pl);
+        else            bf ? pick_kernels<128, 2, true>(pl) : pick_kernels<128, 2, false>(pl);
+        pl.smem = decode_smem_bytes<128>(num_seqs);
+    }
+    int dev = 0, sms = 0, occ = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaFuncSetAttribute(pl.main_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl.main_fn, kWarps * 32, pl.smem);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (occ < 1)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_decode: kernel does not fit on an SM (smem %zu)", pl.smem);
+    pl.grid = sms * occ;
+    pl.total_warps = pl.grid * kWarps;
+    pl.prefix_bytes = ((size_t)(num_seqs + 1) * sizeof(long long) + 255) / 256 * 256;
+    pl.record_bytes = (size_t)2 * pl.total_warps * pl.nt * 8 * (head_size + 2) * sizeof(float);
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_size, int block_size, int dtype, size_t *bytes)
+{
+    if (!bytes)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode_workspace_size: bytes is null");
+    int rc = validate_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size, dtype);
+    if (rc != PA_OK)
+        return rc;
+    DecodePlan pl;
+    rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype);
+    if (rc != PA_OK)
+        return rc;
+    *bytes = pl.prefix_bytes + pl.record_bytes;
+    return PA_OK;
+}
+
+extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int num_seqs, float scale, int num_q_heads,
+                         int num_kv_heads, int head_size, int num_blocks, int block_size,
+                         int dtype, void *workspace, size_t workspace_bytes, pa_stream_t stream)
+{
+    int rc = validate_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !query || !kv_cache || !block_tables || !seq_lens || !workspace)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: null pointer argument");
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_blocks and max_blocks_per_seq must be > 0");
+    if ((long long)max_blocks_per_seq * block_size > (1LL << 30))
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq * block_size too large");
+    if (!std::isfinite(scale))
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale is not finite");
+    if (!aligned(kv_cache, 16) || !aligned(query, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: misaligned pointer (pool/query/out 16 B, workspace 256 B)");
+    DecodePlan pl;
+    rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype);
+    if (rc != PA_OK)
+        return rc;
+    if (workspace_bytes < pl.prefix_bytes + pl.record_bytes)
+        return set_error(PA_ERR_WORKSPACE, "pa_decode: workspace %zu bytes < %zu needed", workspace_bytes,
+                         pl.prefix_bytes + pl.record_bytes);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    CUtensorMap map;
+    rc = encode_kv_map(&map, kv_cache, num_blocks, block_size, num_kv_heads, head_size, dev);
+    if (rc != PA_OK)
+        return rc;
+
+    DecodeParams prm;
+    prm.out = out;
+    prm.query = static_cast<const uint16_t *>(query);
+    prm.block_tables = block_tables;
+    prm.seq_lens = seq_lens;
+    prm.prefix_ws = static_cast<long long *>(workspace);
+    prm.records = reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.prefix_bytes);
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = num_q_heads / num_kv_heads;
+    prm.tile_q = pl.tile_q;
+    prm.qtiles = pl.qtiles;
+    prm.num_blocks = num_blocks;
+    prm.block_size = block_size;
+    prm.tiles_per_block = block_size / kTile;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.total_warps = pl.total_warps;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *main_args[] = {&map, &prm};
+    cudaError_t e = cudaLaunchKernel(pl.main_fn, dim3(pl.grid), dim3(kWarps * 32), main_args, pl.smem, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_decode: main kernel launch");
+    void *red_args[] = {&prm};
+    const int segs = num_seqs * num_kv_heads * pl.qtiles;
+    e = cudaLaunchKernel(pl.reduce_fn, dim3(segs), dim3(128), red_args, 0, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_decode: reduce kernel launch");
+    return PA_OK;
+}
+
+extern "C" int pa_reshape_and_cache(const void *key, const void *value, void *kv_cache,
+                                    const int32_t *slot_mapping, int num_tokens, int num_blocks,
+                                    int block_size, int num_kv_heads, int head_size, int dtype,
+                                    pa_stream_t stream)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache: dtype %d", dtype);
+    if (num_tokens < 0 || num_blocks <= 0 || block_size < kTile || block_size % kTile != 0 ||
+        num_kv_heads <= 0 || head_size <= 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: bad sizes");
+    if (((long long)num_kv_heads * head_size) % 8 != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: num_kv_heads * head_size must be a multiple of 8");
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!key || !value || !kv_cache || !slot_mapping)
+        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: null pointer argument");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 4))
+        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: misaligned pointer (16 B)");
+    const long long row_vecs = (long long)num_kv_heads * head_size * 2 / 16;
+    if (row_vecs > (1 << 30))
+        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: row too large");
+    const long long num_slots = (long long)num_blocks * block_size;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    reshape_and_cache_kernel<<<num_tokens, 128, 0, s>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(kv_cache), slot_mapping, (int)row_vecs, num_slots, num_slots * row_vecs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_reshape_and_cache: launch");
+    return PA_OK;
+}
+
+extern "C" int pa_copy_blocks(void *const *kv_caches, int num_layers, const int32_t *src_dst_pairs,
+                              int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                              int head_size, int dtype, pa_stream_t stream)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks: dtype %d", dtype);
+    if (num_pairs < 0 || num_layers < 1 || num_layers > kMaxLayers || num_blocks <= 0 ||
+        block_size < kTile || block_size % kTile != 0 || num_kv_heads <= 0 || head_size <= 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: bad sizes (1 <= num_layers <= %d)", kMaxLayers);
+    if (((long long)num_kv_heads * head_size) % 8 != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: num_kv_heads * head_size must be a multiple of 8");
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!kv_caches || !src_dst_pairs || !aligned(src_dst_pairs, 4))
+        return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: null or misaligned pointer argument");
+    LayerPtrs lp;
+    for (int l = 0; l < num_layers; ++l) {
+        if (!kv_caches[l] || !aligned(kv_caches[l], 16))
+            return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: layer %d pool null or misaligned", l);
+        lp.p[l] = static_cast<uint4 *>(kv_caches[l]);
+    }
+    for (int l = num_layers; l < kMaxLayers; ++l)
+        lp.p[l] = nullptr;
+    const long long block_vecs = (long long)block_size * num_kv_heads * head_size * 2 / 16;
+    const long long half_vecs = (long long)num_blocks * block_vecs;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    copy_blocks_kernel<<<dim3(num_pairs, num_layers), 256, 0, s>>>(lp, src_dst_pairs, num_pairs, num_blocks,
+                                                                  block_vecs, half_vecs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_copy_blocks: launch");
+    return PA_OK;
+}
+
+extern "C" int pa_get_device_error(int *bits)
+{
+    if (!bits)
+        return set_error(PA_ERR_INVALID_ARG, "pa_get_device_error: bits is null");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_get_device_error: synchronize");
+    int v = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_get_device_error: read");
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_get_device_error: clear");
+    *bits = v;
+    return PA_OK;
+}

@@ -1,0 +1,154 @@
+"""One decode step of the hot path on synthetic inputs.
+
+``plan_step`` uses the host block allocator (libpa's ``pa_alloc_*``) to lay
+out a workload's sequences in the pool and to reserve the slot of each
+sequence's new token; it returns the block tables, slot mapping, decode
+lengths and copy-on-write pairs of the step. ``DecodeStep`` holds the device
+buffers and runs the step as the pages order it (vLLM book chapter 4, §4.5:
+write this step's K/V by slot, then read the history through the block
+table), preceded by the COW copies the allocator asked for:
+
+    pa_copy_blocks(cow pairs) -> pa_reshape_and_cache(new K/V) -> pa_decode
+
+Everything here is marshalling around libpa calls; no arithmetic of the
+method runs in Python.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+from . import binding, workloads
+
+
+@dataclasses.dataclass
+class StepPlan:
+    seq_ids: list
+    seq_lens: np.ndarray        # decode lengths (this step's token included)
+    block_tables: np.ndarray    # [S, max_blocks] int32, padded with -1
+    slot_mapping: np.ndarray    # [S] int32: one new token per sequence
+    cow_pairs: np.ndarray       # [P, 2] int32 (src, dst)
+    allocator: object
+
+
+def _finish(alloc, ids, slots, pairs, block_size):
+    nblk = max(alloc.num_blocks_of(s) for s in ids)
+    max_blocks = max(1, nblk)
+    return StepPlan(
+        seq_ids=list(ids),
+        seq_lens=alloc.seq_lens(ids),
+        block_tables=alloc.block_tables(ids, max_blocks),
+        slot_mapping=np.asarray(slots, dtype=np.int32),
+        cow_pairs=np.asarray(pairs, dtype=np.int32).reshape(-1, 2),
+        allocator=alloc,
+    )
+
+
+def plan_step(name: str, seed: int, variant: str = "literal") -> StepPlan:
+    """Allocate a workload's sequences and reserve this step's slots.
+
+    Standard workloads: each sequence is created with L-1 tokens and then
+    appends its step token (decode length L). ``toy``: lengths 25/47/12 at
+    the worked example's placement, then one token each. ``prefix_cow``:
+    16 groups of 8 forked from a 1024-token prompt; ``variant="literal"``
+    gives each sibling its private tail first, ``variant="fork"`` makes the
+    prompt 1024 + r tokens (r in 1..15) so the step's first writes hit the
+    shared, partly filled last block and are copied on write.
+    """
+    w = workloads.WORKLOADS[name]
+    if name == "toy":
+        order = workloads.toy_free_order()
+    else:
+        order = workloads.free_order(w.num_blocks, seed)
+    alloc = binding.BlockAllocator(w.num_blocks, w.block_size, order)
+    slots, pairs = [], []
+
+    def step_token(sid):
+        slot, cow = alloc.append_token(sid)
+        slots.append(slot)
+        if cow is not None:
+            pairs.append(cow)
+
+    if name == "prefix_cow":
+        lens = workloads.seq_lens(name, seed)
+        extra = workloads.prefix_fork_extra(seed)
+        ids = []
+        for gi in range(workloads.PREFIX_GROUPS):
+            prompt = workloads.PREFIX_PROMPT + (int(extra[gi]) if variant == "fork" else 0)
+            parent = alloc.add_seq(prompt)
+            group = [parent] + [alloc.fork(parent) for _ in range(workloads.PREFIX_GROUP_SIZE - 1)]
+            ids += group
+        if variant == "literal":
+            for k, sid in enumerate(ids):
+                for _ in range(int(lens[k]) - 1 - alloc.seq_len(sid)):
+                    alloc.append_token(sid)
+        for sid in ids:
+            step_token(sid)
+        return _finish(alloc, ids, slots, pairs, w.block_size)
+
+    lens = workloads.seq_lens(name, seed)
+    if name == "toy":
+        ids = [alloc.add_seq(int(L)) for L in lens]
+    else:
+        ids = [alloc.add_seq(int(L) - 1) for L in lens]
+    for sid in ids:
+        step_token(sid)
+    return _finish(alloc, ids, slots, pairs, w.block_size)
+
+
+class DecodeStep:
+    """Device buffers of one step and the three libpa calls that run it."""
+
+    def __init__(self, name: str, plan: StepPlan, pool, query, key_new, value_new, device):
+        import torch
+        self.w = workloads.WORKLOADS[name]
+        self.pool = pool
+        self.query, self.key_new, self.value_new = query, key_new, value_new
+        self.block_tables = torch.from_numpy(plan.block_tables).to(device)
+        self.seq_lens = torch.from_numpy(plan.seq_lens).to(device)
+        self.slot_mapping = torch.from_numpy(plan.slot_mapping).to(device)
+        self.cow_pairs = (torch.from_numpy(plan.cow_pairs).to(device)
+                          if len(plan.cow_pairs) else None)
+        self.out = torch.empty_like(query)
+        self.workspace = binding.decode_workspace(query, pool)
+
+    def launches_per_step(self) -> int:
+        return (1 if self.cow_pairs is not None else 0) + 1 + 2
+
+    def run(self, stream=None) -> None:
+        if self.cow_pairs is not None:
+            binding.pa_copy_blocks([self.pool], self.cow_pairs, stream)
+        binding.pa_reshape_and_cache(self.key_new, self.value_new, self.pool, self.slot_mapping, stream)
+        self.decode(stream)
+
+    def run_host(self, host: dict, out_host, stream=None) -> None:
+        """The step end to end from pinned host buffers: copy this step's
+        inputs to the device, run the three calls, copy the output back and
+        wait for it. ``host`` holds pinned tensors named like the device
+        buffers (query, key_new, value_new, slot_mapping, block_tables,
+        seq_lens and, if the step has COW pairs, cow_pairs)."""
+        import torch
+        for name in ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens",
+                     "cow_pairs"):
+            if name in host:
+                getattr(self, name).copy_(host[name], non_blocking=True)
+        self.run(stream)
+        out_host.copy_(self.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def decode(self, stream=None) -> None:
+        binding.pa_decode(self.out, self.query, self.pool, self.block_tables, self.seq_lens,
+                          self.w.scale, self.workspace, stream)
+
+
+def make_device_inputs(name: str, plan: StepPlan, seed: int, device):
+    """Pool, queries and new K/V: seeded N(0, 1) values on ``device``."""
+    w = workloads.WORKLOADS[name]
+    s = len(plan.seq_ids)
+    pool = workloads.normal_values((2, w.num_blocks, w.block_size, w.num_kv_heads, w.head_size),
+                                   w.dtype, seed + 10, device)
+    query = workloads.normal_values((s, w.num_q_heads, w.head_size), w.dtype, seed + 11, device)
+    key_new = workloads.normal_values((s, w.num_kv_heads, w.head_size), w.dtype, seed + 12, device)
+    value_new = workloads.normal_values((s, w.num_kv_heads, w.head_size), w.dtype, seed + 13, device)
+    return pool, query, key_new, value_new

@@ -1,0 +1,92 @@
+"""Test-side helpers: the oracle's half of every parity case.
+
+The oracle side never takes an input from the CUDA path: its block tables,
+slots and COW pairs come from the oracle's own block-manager model driven by
+the same operation sequence as the product allocator, and its K/V/Q values
+are the seeded generator's output, snapshotted before any libpa kernel runs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from oracle.block_manager import BlockManagerModel
+from paged_kv_cache_120_gb300 import workloads
+
+TOL = {workloads.F16: 2e-3, workloads.BF16: 1e-2}
+
+
+def oracle_plan(name: str, seed: int, variant: str = "literal"):
+    """Same operation sequence as paged_kv_cache_120_gb300.step.plan_step, on the model."""
+    w = workloads.WORKLOADS[name]
+    order = workloads.toy_free_order() if name == "toy" else workloads.free_order(w.num_blocks, seed)
+    m = BlockManagerModel(w.num_blocks, w.block_size, order)
+    slots, pairs = [], []
+
+    def step_token(sid):
+        slot, cow = m.append_token(sid)
+        slots.append(slot)
+        if cow is not None:
+            pairs.append(cow)
+
+    if name == "prefix_cow":
+        lens = workloads.seq_lens(name, seed)
+        extra = workloads.prefix_fork_extra(seed)
+        ids = []
+        for gi in range(workloads.PREFIX_GROUPS):
+            prompt = workloads.PREFIX_PROMPT + (int(extra[gi]) if variant == "fork" else 0)
+            parent = m.add_seq(prompt)
+            ids += [parent] + [m.fork(parent) for _ in range(workloads.PREFIX_GROUP_SIZE - 1)]
+        if variant == "literal":
+            for k, sid in enumerate(ids):
+                for _ in range(int(lens[k]) - 1 - m.seq_len(sid)):
+                    m.append_token(sid)
+    else:
+        lens = workloads.seq_lens(name, seed)
+        ids = [m.add_seq(int(L) if name == "toy" else int(L) - 1) for L in lens]
+    for sid in ids:
+        step_token(sid)
+    max_blocks = max(1, max(len(m.table(s)) for s in ids))
+    bt = np.full((len(ids), max_blocks), -1, dtype=np.int32)
+    for i, s in enumerate(ids):
+        t = m.table(s)
+        bt[i, :len(t)] = t
+    return dict(model=m, ids=ids, block_tables=bt,
+                seq_lens=np.array([m.seq_len(s) for s in ids], dtype=np.int32),
+                slot_mapping=np.array(slots, dtype=np.int32),
+                cow_pairs=np.array(pairs, dtype=np.int32).reshape(-1, 2))
+
+
+def u16(t):
+    """torch CPU/GPU tensor (fp16/bf16) -> numpy uint16 bit patterns on the host."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def values(t, dtype):
+    return oracle.decode_elems(u16(t), dtype)
+
+
+def oracle_step(w, op, pool_bits, q_bits, k_bits, v_bits, sample=None):
+    """Apply the step (COW copies, writes, decode) on the oracle's host copy.
+    Returns decode outputs [S, Hq, D] (or [n, D] for sampled (seq, head) pairs)."""
+    if len(op["cow_pairs"]):
+        assert oracle.copy_blocks([pool_bits], op["cow_pairs"], w.num_blocks, w.block_size,
+                                  w.num_kv_heads, w.head_size) == 0
+    n = oracle.reshape_and_cache(k_bits, v_bits, pool_bits, op["slot_mapping"], w.num_blocks,
+                                 w.block_size, w.num_kv_heads, w.head_size)
+    assert n == (op["slot_mapping"] >= 0).sum()
+    if sample is None:
+        return oracle.decode(q_bits, pool_bits, op["block_tables"], op["seq_lens"], w.scale,
+                             w.num_q_heads, w.num_kv_heads, w.head_size, w.num_blocks,
+                             w.block_size, w.dtype)
+    seqs, heads = sample
+    return oracle.decode_sampled(seqs, heads, q_bits, pool_bits, op["block_tables"],
+                                 op["seq_lens"], w.scale, w.num_q_heads, w.num_kv_heads,
+                                 w.head_size, w.num_blocks, w.block_size, w.dtype)
+
+
+def max_abs_err(got, want):
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), "non-finite GPU output"
+    return float(np.max(np.abs(got - want))) if got.size else 0.0

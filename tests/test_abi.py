@@ -1,0 +1,137 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/pa.h declares, rejects bad arguments on the host (before any CUDA
+call), and its host allocator agrees op-for-op with the oracle's model."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.block_manager import BlockManagerModel, OutOfBlocks
+from paged_kv_cache_120_gb300 import binding, build, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+    assert sorted(n for n, _, _ in binding.SIGNATURES) == names
+
+
+def test_version(lib):
+    assert binding.pa_version() == 10000
+
+
+def test_host_side_validation_without_a_gpu(lib):
+    null = None
+    # dtype, head size and group checks come before any CUDA call
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16, 7, null, 0, null) \
+        == binding.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 96, 10, 16, 0, null, 0, null) \
+        == binding.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 3, 128, 10, 16, 0, null, 0, null) \
+        == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 40, 2, 128, 10, 16, 0, null, 0, null) \
+        == binding.PA_ERR_UNSUPPORTED          # group 20: neither <= 16 nor a multiple of 16
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 24, 0, null, 0, null) \
+        == binding.PA_ERR_INVALID_ARG          # block_size not a multiple of 16
+    assert "block_size" in binding.pa_last_error()
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16, 0, null, 0, null) \
+        == binding.PA_ERR_INVALID_ARG          # null pointers
+    assert lib.pa_decode(null, null, null, null, 1, null, 0, 1.0, 8, 8, 128, 10, 16, 0, null, 0, null) \
+        == binding.PA_OK                       # empty batch is a no-op
+    assert lib.pa_reshape_and_cache(null, null, null, null, 3, 10, 16, 8, 128, 0, null) \
+        == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(null, null, null, null, 0, 10, 16, 8, 128, 0, null) == binding.PA_OK
+    assert lib.pa_copy_blocks(null, 0, null, 1, 10, 16, 8, 128, 0, null) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(null, 1, null, 0, 10, 16, 8, 128, 0, null) == binding.PA_OK
+
+
+def _both(nb, bs, order):
+    return binding.BlockAllocator(nb, bs, order), BlockManagerModel(nb, bs, order)
+
+
+def test_allocator_reproduces_the_worked_example(lib):
+    a = binding.BlockAllocator(64, 16, workloads.toy_free_order())
+    ids = [a.add_seq(n) for n in workloads.TOY_LENGTHS]
+    assert [a.table(i) for i in ids] == [[3, 7], [0, 5, 9], [4]]
+    assert a.num_free() == 58
+    assert [a.append_token(i)[0] for i in ids] == [121, 159, 76]
+    while a.seq_len(ids[1]) < 49:
+        a.append_token(ids[1])
+    assert a.table(ids[1]) == [0, 5, 9, 11]
+
+
+def test_allocator_matches_the_oracle_model_on_random_operations(lib):
+    rng = np.random.default_rng(21)
+    for trial in range(4):
+        nb, bs = int(rng.integers(8, 80)), int(rng.choice([16, 32]))
+        order = rng.permutation(nb)
+        a, m = _both(nb, bs, order)
+        live = []
+        for step in range(1500):
+            op = int(rng.integers(0, 5))
+            if op == 0 or not live:
+                n = int(rng.integers(0, 4 * bs))
+                try:
+                    sm = m.add_seq(n)
+                except OutOfBlocks:
+                    with pytest.raises(binding.PAError) as e:
+                        a.add_seq(n)
+                    assert e.value.code == binding.PA_ERR_OUT_OF_BLOCKS
+                    continue
+                sa = a.add_seq(n)
+                live.append((sa, sm))
+            elif op == 1:
+                sa, sm = live[int(rng.integers(len(live)))]
+                live.append((a.fork(sa), m.fork(sm)))
+            elif op in (2, 3):
+                sa, sm = live[int(rng.integers(len(live)))]
+                try:
+                    want = m.append_token(sm)
+                except OutOfBlocks:
+                    with pytest.raises(binding.PAError) as e:
+                        a.append_token(sa)
+                    assert e.value.code == binding.PA_ERR_OUT_OF_BLOCKS
+                    continue
+                assert a.append_token(sa) == want
+            else:
+                sa, sm = live.pop(int(rng.integers(len(live))))
+                a.free_seq(sa)
+                m.free_seq(sm)
+            assert a.num_free() == m.num_free()
+        for sa, sm in live:
+            assert a.table(sa) == m.table(sm)
+            assert a.seq_len(sa) == m.seq_len(sm)
+        assert [a.ref_count(b) for b in range(nb)] == m.ref
+
+
+def test_allocator_block_tables_and_errors(lib):
+    a = binding.BlockAllocator(16, 16)
+    s0, s1 = a.add_seq(20), a.add_seq(0)
+    bt = a.block_tables([s0, s1], 3)
+    assert bt.tolist() == [[0, 1, -1], [-1, -1, -1]]
+    assert a.seq_lens([s0, s1]).tolist() == [20, 0]
+    with pytest.raises(binding.PAError) as e:
+        a.block_tables([s0], 1)
+    assert e.value.code == binding.PA_ERR_INVALID_ARG
+    with pytest.raises(binding.PAError) as e:
+        a.free_seq(99)
+    assert e.value.code == binding.PA_ERR_NOT_FOUND
+    with pytest.raises(binding.PAError):
+        binding.BlockAllocator(4, 16, [0, 1, 1, 2])
