@@ -129,9 +129,15 @@ int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  *                  be <= 16 or a multiple of 16.
  *   head_size      64 or 128
  *   workspace      device, >= pa_decode_workspace_size(...) bytes, 256-byte
- *                  aligned; scratch for the split-K partial results. Its
- *                  contents need no initialisation and are not preserved.
- *                  Calls that share a workspace must not overlap on the GPU.
+ *                  aligned: split-K partial results. Its contents need no
+ *                  initialisation and are not preserved. Calls that share a
+ *                  workspace must not overlap on the GPU.
+ *
+ * Launch: two kernels (the stream and the split-K merge), both with
+ * programmatic dependent launch. The first may start while the preceding
+ * kernel in the stream is finishing (typically this step's
+ * pa_reshape_and_cache); before waiting for that kernel it reads only
+ * seq_lens, and it reads the pool and writes anything only after the wait.
  *
  * Result: out[s][hq] = sum_i softmax_i(scale * q.k_i) v_i over the
  * seq_lens[s] logical tokens, computed with fp32 dot products, an fp32

@@ -52,21 +52,25 @@ def _nvcc():
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def build(force: bool = False, verbose: bool = False, extra_nvcc: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra_nvcc: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile and link libpa.so into ``out_dir`` (default: the in-tree _build)."""
     extra_nvcc = list(extra_nvcc or [])
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "libpa.stamp")
+    build_dir = out_dir or BUILD
+    lib_path = os.path.join(build_dir, "libpa.so")
+    os.makedirs(build_dir, exist_ok=True)
+    stamp = os.path.join(build_dir, "libpa.stamp")
     fp = _fingerprint(extra_nvcc)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == fp:
-                return LIB
+                return lib_path
     nvcc = _nvcc()
 
     def compile_unit(unit):
         name, tool = unit
         src = os.path.join(CSRC, name)
-        obj = os.path.join(BUILD, name + ".o")
+        obj = os.path.join(build_dir, name + ".o")
         if tool == "nvcc":
             cmd = [nvcc] + NVCC_FLAGS + extra_nvcc + ["-c", src, "-o", obj]
             if verbose:
@@ -84,15 +88,15 @@ def build(force: bool = False, verbose: bool = False, extra_nvcc: list[str] | No
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(fp)
-    return LIB
+    return lib_path
 
 
 def main():

@@ -17,13 +17,14 @@
 //    base 2.
 //  * Work is split "stream-K" style: all 16-token tiles of all (sequence,
 //    kv-head, query-tile) segments are laid end to end and every warp of a
-//    persistent grid takes an equal contiguous share. A segment that fits in
-//    one warp's share is finished in place; a segment cut by share
-//    boundaries leaves one partial (m, l, O) record per piece and a small
-//    reduce kernel merges the pieces in ascending order with the online
-//    softmax rule. The split depends only on the sequence lengths and the
-//    grid size, never on physical block ids, so outputs are bit-identical
-//    under any permutation of block placement.
+//    persistent grid takes an equal contiguous share. A segment inside one
+//    warp's share is finished in place; a segment cut by share boundaries
+//    leaves one partial (m, l, O) record per piece, and a second kernel,
+//    launched with programmatic dependent launch so that it is resident before
+//    the first one ends, merges each such segment's pieces in ascending order.
+//    The split depends only on the sequence lengths and the grid size, never
+//    on physical block ids, so outputs are bit-identical under any
+//    permutation of block placement.
 //  * reshape_and_cache and copy_blocks are bit copies with 16-byte accesses.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -110,6 +111,27 @@ __device__ __forceinline__ void fence_barrier_init()
 __device__ __forceinline__ void fence_proxy_async()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible / let the next kernel start
+// launching. Both are no-ops when the launch has no programmatic dependency.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 2^x with the hardware approximation (flushes denormals; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // One TMA tile load of a rank-5 tensor into shared memory, completing on `bar`.
@@ -206,8 +228,14 @@ __device__ __forceinline__ uint16_t to_elem(float x)
 
 // ------------------------------------------------------------------- decode
 
-constexpr int kWarps = 4;       // warps per CTA, each an independent pipeline
-constexpr int kStages = 3;      // TMA ring depth per warp
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 12
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 1
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;    // warps per CTA, each an independent pipeline
+constexpr int kStages = PA_DECODE_STAGES;  // TMA ring depth per warp
 constexpr int kTile = 16;       // tokens per tile (the MMA's M)
 constexpr int kMaxSeqs = 4096;  // sequences per pa_decode call (prefix lives in smem)
 
@@ -223,8 +251,10 @@ struct DecodeParams {
     const uint16_t *query;
     const int32_t *block_tables;
     const int32_t *seq_lens;
-    float *records;       // workspace: 2 records per warp
+    float *warp_records;  // workspace: 2 per warp, the warp's pieces of its first / last segment
     long long *prefix_ws; // workspace: unit prefix over sequences, [num_seqs + 1]
+    int *tasks;           // workspace: per warp, the split segment whose last piece it holds, or -1
+    long long *task_start;// workspace: per warp, that segment's first unit
     int max_blocks_per_seq;
     int num_seqs;
     int num_q_heads;
@@ -236,7 +266,7 @@ struct DecodeParams {
     int block_size;
     int tiles_per_block;  // block_size / 16
     float scale_log2;     // scale * log2(e): scores live in base 2
-    int total_warps;
+    int total_warps;      // grid * kWarps
 };
 
 template <int D, int NT>
@@ -254,6 +284,57 @@ inline size_t decode_smem_bytes(int num_seqs)
     b += (size_t)(num_seqs + 1) * sizeof(long long);
     b += (size_t)num_seqs * sizeof(int);
     return b;
+}
+
+// The unit sequence: every (sequence, kv head, query tile) segment's 16-token
+// tiles laid end to end, sequence-major. prefix[s] is the first unit of
+// sequence s; its segments follow one another, ceil(L_s / 16) units each.
+struct UnitMap {
+    const long long *prefix;  // [num_seqs + 1]
+    const int *lens;          // sequence lengths (clamped on read)
+    int num_seqs, segs_per_seq, max_len;
+
+    __device__ __forceinline__ int len(int s) const
+    {
+        const int L = lens[s];
+        return L < 0 ? 0 : (L > max_len ? max_len : L);
+    }
+    __device__ __forceinline__ int seq_of(long long u) const
+    {
+        int lo = 0, hi = num_seqs;  // prefix[lo] <= u < prefix[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= u)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        return lo;
+    }
+    __device__ __forceinline__ int seg_of(long long u) const
+    {
+        const int s = seq_of(u);
+        const int nt = (len(s) + kTile - 1) / kTile;
+        return s * segs_per_seq + (int)((u - prefix[s]) / nt);
+    }
+    __device__ __forceinline__ void bounds(int seg, long long &a, long long &e) const
+    {
+        const int s = seg / segs_per_seq, segl = seg - (seg / segs_per_seq) * segs_per_seq;
+        const int nt = (len(s) + kTile - 1) / kTile;
+        a = prefix[s] + (long long)segl * nt;
+        e = a + nt;
+    }
+};
+
+// Equal contiguous shares of N units among K owners: owner k has
+// [N k / K, N (k+1) / K); owner_of(u) inverts that.
+__device__ __forceinline__ long long share_lo(long long N, long long k, long long K)
+{
+    return N * k / K;
+}
+__device__ __forceinline__ int owner_of(long long u, long long N, long long K)
+{
+    return (int)(((u + 1) * K - 1) / N);
 }
 
 // Main decode kernel. Template: head size D, N-tiles of 8 query heads NT,
@@ -324,6 +405,13 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     __syncthreads();
 
+    // Let the reduce kernel start launching; it waits for this grid anyway.
+    grid_launch_dependents();
+    // Everything above read only inputs the caller produced (lengths). The
+    // pool may still be being written by the preceding kernel (this step's
+    // reshape_and_cache): wait for it before any pool read or global write.
+    grid_dependency_wait();
+
     const long long N = prefix[S];
     if (blockIdx.x == 0)
         for (int s = tid; s <= S; s += blockDim.x)
@@ -331,10 +419,12 @@ __global__ void __launch_bounds__(kWarps * 32)
 
     // 2. This warp's contiguous share of the unit sequence.
     const int gw = blockIdx.x * kWarps + warp;
-    const long long r0 = N * gw / p.total_warps;
-    const long long r1 = N * (gw + 1) / p.total_warps;
+    const long long r0 = share_lo(N, gw, p.total_warps);
+    const long long r1 = share_lo(N, gw + 1, p.total_warps);
+    if (lane == 0)
+        p.tasks[gw] = -1;
     if (r0 >= r1)
-        return;  // no block-level synchronisation below this point
+        return;
 
     // Unit u -> physical block, segment id and (tile << 5 | valid tokens).
     auto unit_info = [&](long long u, int &phys, int &seg, int &tv) {
@@ -356,12 +446,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         const long long local = u - prefix[lo];
         const int segl = (int)(local / ntiles);
         const int tile = (int)(local - (long long)segl * ntiles);
-        int b = __ldg(p.block_tables + (long long)lo * p.max_blocks_per_seq + tile / p.tiles_per_block);
-        if ((unsigned)b >= (unsigned)p.num_blocks) {
-            raise_error(PA_DEVERR_BLOCK_ID);
-            b = p.num_blocks;  // outside the tensor map: TMA fills zeros
-        }
-        phys = b;
+        // Not checked here: the load's latency is hidden until issue time.
+        phys = __ldg(p.block_tables + (long long)lo * p.max_blocks_per_seq + tile / p.tiles_per_block);
         seg = lo * segs_per_seq + segl;
         tv = (tile << 5) | min(kTile, L - tile * kTile);
     };
@@ -384,6 +470,10 @@ __global__ void __launch_bounds__(kWarps * 32)
     const uint32_t my_bar0 = smem_addr(&bars[warp * kStages]);
     auto issue = [&](int phys, int seg, int tv, int st) {
         if (lane == 0) {
+            if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                raise_error(PA_DEVERR_BLOCK_ID);
+                phys = p.num_blocks;  // outside the tensor map: TMA fills zeros
+            }
             const int h = (seg % segs_per_seq) / p.qtiles;
             const int t0 = ((tv >> 5) % p.tiles_per_block) * kTile;
             const uint32_t bar = my_bar0 + st * 8;
@@ -485,7 +575,11 @@ __global__ void __launch_bounds__(kWarps * 32)
             // A piece of a segment: record (m, l, O) for the reduce kernel.
             // Slot 2w holds the piece of the warp's first segment, 2w+1 its last.
             const long long slot = (seg_start <= r0) ? 2LL * gw : 2LL * gw + 1;
-            float *rec = p.records + slot * REC;
+            float *rec = p.warp_records + slot * REC;
+            if (lane == 0 && seg_start < r0 && seg_end <= r1) {
+                p.tasks[gw] = seg;  // this warp holds the segment's last piece
+                p.task_start[gw] = seg_start;
+            }
             if (g == 0) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -550,21 +644,52 @@ __global__ void __launch_bounds__(kWarps * 32)
             __syncwarp();
         }
 
-        // S^T[16 tokens][8*NT queries] = K Q^T
-        float sc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        // S^T[16 tokens][8*NT queries] = K Q^T. All K fragments are loaded
+        // first, and the k-steps alternate between two accumulators, so the
+        // MMA chain is half as long as the head dimension.
+        uint32_t kf[KS][4];
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             const int cg = 2 * kk + k_hi;
-            const uint32_t addr = sbuf + (cg >> 3) * TileGeo<D>::kBoxBytes + k_row * 128 +
-                                  (((cg & 7) ^ (k_row & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
+            ldsm_x4(sbuf + (cg >> 3) * TileGeo<D>::kBoxBytes + k_row * 128 +
+                        (((cg & 7) ^ (k_row & 7)) << 4),
+                    kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
+        }
+        // V^T fragments do not depend on P: load them up front as well.
+        uint32_t vf[KS][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma16816<BF16>(sc[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+        for (int mt = 0; mt < KS; ++mt) {
+            const int cg = 2 * mt + v_hi;
+            ldsm_x4_t(sbuf + 2048 + (cg >> 3) * TileGeo<D>::kBoxBytes + v_row * 128 +
+                          (((cg & 7) ^ (v_row & 7)) << 4),
+                      vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+        }
+
+        float sc[NT][4], sc2[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                sc[nt][c] = sc2[nt][c] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; kk += 2)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mma16816<BF16>(sc[nt], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], qf[nt][kk][0],
+                               qf[nt][kk][1]);
+                mma16816<BF16>(sc2[nt], kf[kk + 1][0], kf[kk + 1][1], kf[kk + 1][2], kf[kk + 1][3],
+                               qf[nt][kk + 1][0], qf[nt][kk + 1][1]);
+            }
+        // Every fragment of this tile is now in registers: hand the stage back
+        // to the TMA right away, so the ring stays full while the math runs.
+        __syncwarp();
+        if (ip < r1) {
+            int ph2, sg2, tv2;
+            fetch(ip, ph2, sg2, tv2);
+            if (lane == 0)
+                fence_proxy_async();
+            issue(ph2, sg2, tv2, st);
+            ++ip;
         }
 
         // Online softmax (base 2) per query column; P rounded to the element type.
@@ -575,17 +700,17 @@ __global__ void __launch_bounds__(kWarps * 32)
             float pr[4];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float x0 = tok0 ? sc[nt][e] * p.scale_log2 : -INFINITY;
-                const float x1 = tok1 ? sc[nt][2 + e] * p.scale_log2 : -INFINITY;
+                const float x0 = tok0 ? (sc[nt][e] + sc2[nt][e]) * p.scale_log2 : -INFINITY;
+                const float x1 = tok1 ? (sc[nt][2 + e] + sc2[nt][2 + e]) * p.scale_log2 : -INFINITY;
                 float mx = fmaxf(x0, x1);
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
                 const float m_new = fmaxf(m_run[nt][e], mx);
-                const float alpha = exp2f(m_run[nt][e] - m_new);
+                const float alpha = ex2(m_run[nt][e] - m_new);
                 m_run[nt][e] = m_new;
-                pr[e] = exp2f(x0 - m_new);
-                pr[2 + e] = exp2f(x1 - m_new);
+                pr[e] = ex2(x0 - m_new);
+                pr[2 + e] = ex2(x1 - m_new);
                 l_run[nt][e] *= alpha;
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
@@ -604,24 +729,12 @@ __global__ void __launch_bounds__(kWarps * 32)
 
         // O^T[D][8*NT] += V^T P^T
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int cg = 2 * mt + v_hi;
-            const uint32_t addr = sbuf + 2048 + (cg >> 3) * TileGeo<D>::kBoxBytes + v_row * 128 +
-                                  (((cg & 7) ^ (v_row & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(addr, a0, a1, a2, a3);
+        for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                mma16816<BF16>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-        }
+                mma16816<BF16>(acc[mt][nt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[nt][0],
+                               pb[nt][1]);
 
-        __syncwarp();
-        if (ip < r1) {
-            int ph2, sg2, tv2;
-            fetch(ip, ph2, sg2, tv2);
-            issue(ph2, sg2, tv2, st);
-            ++ip;
-        }
         if (++st == kStages) {
             st = 0;
             phase ^= 1;
@@ -640,85 +753,244 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
-// Merge the pieces of segments that crossed warp-share boundaries, and write
-// zero rows for empty sequences. One CTA per segment.
-template <int D, int NT, bool BF16>
-__global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeParams p)
-{
-    constexpr int GP = NT * 8;
-    constexpr int REC = record_floats<D, NT>();
-    const int seg = blockIdx.x;
-    const int segs_per_seq = p.num_kv_heads * p.qtiles;
-    const int s = seg / segs_per_seq, segl = seg - (seg / segs_per_seq) * segs_per_seq;
-    const int h = segl / p.qtiles, qt = segl - (segl / p.qtiles) * p.qtiles;
-    const int hq0 = h * p.group + qt * 16;
-    const int max_len = p.max_blocks_per_seq * p.block_size;
-    int L = p.seq_lens[s];
-    L = L < 0 ? 0 : (L > max_len ? max_len : L);
-    const int ntiles = (L + kTile - 1) / kTile;
-    uint16_t *out = static_cast<uint16_t *>(p.out) + ((long long)s * p.num_q_heads + hq0) * D;
-    if (ntiles == 0) {
-        for (int idx = threadIdx.x; idx < p.tile_q * D; idx += blockDim.x)
-            out[idx] = 0;
-        return;
+// Finish the segments cut by warp-share boundaries, and write zero rows for
+// empty sequences. Warp j of reduce CTA r serves main-grid warp
+// r * kReduceWarps + j: if that warp holds the last piece of a split segment,
+// the segment's pieces (one record per main-grid warp) are merged with the
+// online-softmax rule m = max m_p, l = sum l_p 2^(m_p - m),
+// O = sum O_p 2^(m_p - m). A task with few pieces is merged by its warp; a
+// task with many pieces is merged by the whole CTA, pieces split across the
+// warps and the warps' partial states combined in shared memory. Every merge
+// runs in a fixed order, so results do not depend on timing.
+constexpr int kSmallTask = 6;    // pieces a single warp merges on its own
+constexpr int kReduceWarps = 4;  // warps per reduce CTA
+
+// Lane layout of a merge: each lane owns one live column and the rows
+// d0, d0 + dstep, ... of it (columns rounded up to a power of two).
+struct MergeLanes {
+    int ct, col, d0, dstep, nk;
+    __device__ MergeLanes(int tile_q, int lane, int D)
+    {
+        ct = tile_q <= 1 ? 1 : tile_q <= 2 ? 2 : tile_q <= 4 ? 4 : tile_q <= 8 ? 8 : 16;
+        col = lane % ct;
+        d0 = lane / ct;
+        dstep = 32 / ct;
+        nk = D / dstep;
     }
-    const long long N = p.prefix_ws[p.num_seqs];
-    const long long W = p.total_warps;
-    const long long a = p.prefix_ws[s] + (long long)segl * ntiles, e = a + ntiles;
-    const int w_lo = (int)(((a + 1) * W - 1) / N), w_hi = (int)((e * W - 1) / N);
-    if (w_lo == w_hi)
-        return;  // finished by the main kernel
-    for (int idx = threadIdx.x; idx < p.tile_q * D; idx += blockDim.x) {
-        const int d = idx / p.tile_q, col = idx - (idx / p.tile_q) * p.tile_q;
-        float M = -INFINITY;
-        for (int w = w_lo; w <= w_hi; ++w) {
-            const long long r0 = N * w / W, r1 = N * (w + 1) / W;
-            if (r0 >= r1)
-                continue;
-            const long long slot = (a <= r0) ? 2LL * w : 2LL * w + 1;
-            M = fmaxf(M, p.records[slot * REC + col]);
+};
+
+// One warp folds the pieces o_first, o_first + ostep, ... <= o_hi of the
+// segment starting at unit `a` into its running state (M, l, acc) for its
+// column and rows. Record offsets are computed lane-parallel, 32 pieces at a
+// time, and loads are issued in batches so that they overlap.
+template <int D, int NT>
+__device__ void fold_pieces(const float *recs, long long a, int o_first, int ostep, int o_hi,
+                            long long N, long long K, const MergeLanes &ml, float &M, float &l,
+                            float (&acc)[D * NT * 8 / 32])
+{
+    constexpr int GP = NT * 8, REC = record_floats<D, NT>(), KMAX = D * GP / 32;
+    const int lane = threadIdx.x & 31;
+    for (int b = 0;; b += 32) {
+        const int ob = o_first + b * ostep;
+        if (ob > o_hi)
+            break;
+        const int nb = min(32, (o_hi - ob) / ostep + 1);
+        long long my = -1;
+        if (lane < nb) {
+            const int o = ob + lane * ostep;
+            const long long lo = share_lo(N, o, K);
+            if (lo < share_lo(N, o + 1, K))
+                my = ((a <= lo) ? 2LL * o : 2LL * o + 1) * REC;
         }
-        float lsum = 0.f, o = 0.f;
-        for (int w = w_lo; w <= w_hi; ++w) {
-            const long long r0 = N * w / W, r1 = N * (w + 1) / W;
-            if (r0 >= r1)
-                continue;
-            const long long slot = (a <= r0) ? 2LL * w : 2LL * w + 1;
-            const float *rec = p.records + slot * REC;
-            const float f = exp2f(rec[col] - M);
-            lsum += rec[GP + col] * f;
-            o += rec[2 * GP + d * GP + col] * f;
+        float mb = M;
+        for (int j0 = 0; j0 < nb; j0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const long long sl = __shfl_sync(kFull, my, (j0 + j) & 31);
+                v[j] = (j0 + j < nb && sl >= 0) ? __ldcg(recs + sl + ml.col) : -INFINITY;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                mb = fmaxf(mb, v[j]);
         }
-        out[(long long)col * D + d] = to_elem<BF16>(o / lsum);
+        // Rescale the running state to the new maximum: 0 while nothing has
+        // been folded yet (M = -inf), 1 while no valid piece has been seen.
+        const float scale = mb == -INFINITY ? 1.f : ex2(M - mb);
+        l *= scale;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            acc[k] *= scale;
+        M = mb;
+        for (int j0 = 0; j0 < nb; j0 += 4) {
+            long long sl[4];
+            float f[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sl[j] = __shfl_sync(kFull, my, (j0 + j) & 31);
+                if (j0 + j >= nb)
+                    sl[j] = -1;
+                const float mv = sl[j] >= 0 ? __ldcg(recs + sl[j] + ml.col) : -INFINITY;
+                const float lv = sl[j] >= 0 ? __ldcg(recs + sl[j] + GP + ml.col) : 0.f;
+                f[j] = sl[j] >= 0 ? ex2(mv - M) : 0.f;
+                l += f[j] * lv;
+            }
+#pragma unroll
+            for (int k0 = 0; k0 < KMAX; k0 += 8) {
+                float x[4][8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        x[j][k] = (sl[j] >= 0 && k0 + k < ml.nk)
+                                      ? __ldcg(recs + sl[j] + 2 * GP + (ml.d0 + (k0 + k) * ml.dstep) * GP + ml.col)
+                                      : 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        acc[k0 + k] += f[j] * x[j][k];
+            }
+        }
+    }
+}
+
+template <int D, int NT, bool BF16>
+__device__ __forceinline__ void store_rows(uint16_t *out, const MergeLanes &ml, int tile_q, float l,
+                                           const float (&acc)[D * NT * 8 / 32])
+{
+    constexpr int KMAX = D * NT * 8 / 32;
+    if (ml.col >= tile_q)
+        return;
+    const float inv = 1.f / l;
+    uint16_t *row = out + (long long)ml.col * D;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+        if (k < ml.nk)
+            row[ml.d0 + k * ml.dstep] = to_elem<BF16>(acc[k] * inv);
+}
+
+template <int D, int NT>
+constexpr size_t reduce_smem_bytes()
+{
+    return (size_t)kReduceWarps * (2 * NT * 8 + D * NT * 8) * sizeof(float);  // per warp: M, l, acc
+}
+
+template <int D, int NT, bool BF16>
+__global__ void __launch_bounds__(kReduceWarps * 32) paged_decode_reduce_kernel(const DecodeParams p)
+{
+    constexpr int GP = NT * 8, KMAX = D * GP / 32;
+    extern __shared__ float s_part[];  // [kReduceWarps][GP (M) + GP (l) + D * GP (acc)]
+    __shared__ int s_seg[kReduceWarps], s_olo[kReduceWarps];
+    __shared__ long long s_a[kReduceWarps];
+
+    grid_dependency_wait();  // the main grid's records and tasks are complete
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int w = blockIdx.x * kReduceWarps + warp;
+    const bool serving = w < p.total_warps;
+    const long long N = p.prefix_ws[p.num_seqs], TW = p.total_warps;
+    const int segs_per_seq = p.num_kv_heads * p.qtiles;
+    uint16_t *out_base = static_cast<uint16_t *>(p.out);
+    auto out_rows = [&](int seg) {
+        const int s = seg / segs_per_seq, segl = seg - (seg / segs_per_seq) * segs_per_seq;
+        const int h = segl / p.qtiles, qt = segl - (segl / p.qtiles) * p.qtiles;
+        return out_base + ((long long)s * p.num_q_heads + h * p.group + qt * 16) * D;
+    };
+
+    // Empty sequences: zero output rows (no warp of the main grid saw them).
+    for (int s = w; s < p.num_seqs; s += p.total_warps)
+        if (p.seq_lens[s] <= 0)
+            for (int i = lane; i < p.num_q_heads * D; i += 32)
+                out_base[(long long)s * p.num_q_heads * D + i] = 0;
+
+    const int seg = serving ? p.tasks[w] : -1;
+    const long long a = serving ? p.task_start[w] : 0;
+    const int o_lo = seg >= 0 ? owner_of(a, N, TW) : 0;
+    const MergeLanes ml(p.tile_q, lane, D);
+    if (lane == 0) {
+        s_seg[warp] = (seg >= 0 && w - o_lo + 1 > kSmallTask) ? seg : -1;
+        s_a[warp] = a;
+        s_olo[warp] = o_lo;
+    }
+    if (seg >= 0 && w - o_lo + 1 <= kSmallTask) {
+        float M = -INFINITY, l = 0.f, acc[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            acc[k] = 0.f;
+        fold_pieces<D, NT>(p.warp_records, a, o_lo, 1, w, N, TW, ml, M, l, acc);
+        store_rows<D, NT, BF16>(out_rows(seg), ml, p.tile_q, l, acc);
+    }
+    __syncthreads();
+    // Tasks with many pieces: the whole CTA, pieces split across warps.
+    for (int j = 0; j < kReduceWarps; ++j) {
+        const int bseg = s_seg[j];
+        if (bseg < 0)
+            continue;
+        const int last = blockIdx.x * kReduceWarps + j;
+        float M = -INFINITY, l = 0.f, acc[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            acc[k] = 0.f;
+        fold_pieces<D, NT>(p.warp_records, s_a[j], s_olo[j] + warp, kReduceWarps, last, N, TW, ml, M, l,
+                           acc);
+        float *mine = s_part + warp * (2 * GP + D * GP);
+        if (ml.d0 == 0) {
+            mine[ml.col] = M;
+            mine[GP + ml.col] = l;
+        }
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            if (k < ml.nk)
+                mine[2 * GP + (ml.d0 + k * ml.dstep) * GP + ml.col] = acc[k];
+        __syncthreads();
+        // Combine the warps' partial states (fixed order), elements across the CTA.
+        uint16_t *out = out_rows(bseg);
+        for (int e = threadIdx.x; e < p.tile_q * D; e += kReduceWarps * 32) {
+            const int d = e / p.tile_q, c = e - (e / p.tile_q) * p.tile_q;
+            float Mx = -INFINITY;
+            for (int v = 0; v < kReduceWarps; ++v)
+                Mx = fmaxf(Mx, s_part[v * (2 * GP + D * GP) + c]);
+            float lt = 0.f, ot = 0.f;
+            for (int v = 0; v < kReduceWarps; ++v) {
+                const float *pv = s_part + v * (2 * GP + D * GP);
+                const float f = pv[c] == -INFINITY ? 0.f : ex2(pv[c] - Mx);  // warp had no pieces
+                lt += f * pv[GP + c];
+                ot += f * pv[2 * GP + d * GP + c];
+            }
+            out[(long long)c * D + d] = to_elem<BF16>(ot / lt);
+        }
+        __syncthreads();
     }
 }
 
 // ------------------------------------------------------- reshape and copy
 
-// One CTA per new token: the token's K row [num_kv_heads][head_size] and V
-// row are contiguous both in the input and in the pool, so each is one run
-// of 16-byte copies.
-__global__ void __launch_bounds__(128)
+// Grid (token, row chunk): the token's K row [num_kv_heads][head_size] and
+// V row are contiguous both in the input and in the pool, so each CTA copies
+// one 16-byte element of each per thread.
+constexpr int kReshapeThreads = 256;
+
+__global__ void __launch_bounds__(kReshapeThreads)
     reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                              uint4 *__restrict__ kv, const int32_t *__restrict__ slots,
                              int row_vecs, long long num_slots, long long half_vecs)
 {
+    grid_launch_dependents();  // the decode that follows may start its prologue
     const int t = blockIdx.x;
+    const int i = blockIdx.y * kReshapeThreads + threadIdx.x;
     const long long slot = slots[t];
     if (slot < 0)
         return;
     if (slot >= num_slots) {
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0 && blockIdx.y == 0)
             raise_error(PA_DEVERR_SLOT);
         return;
     }
-    const uint4 *k = key + (long long)t * row_vecs;
-    const uint4 *v = value + (long long)t * row_vecs;
-    uint4 *dk = kv + slot * row_vecs;
-    uint4 *dv = dk + half_vecs;
-    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) {
-        dk[i] = __ldg(k + i);
-        dv[i] = __ldg(v + i);
+    if (i < row_vecs) {
+        const uint4 k = __ldg(key + (long long)t * row_vecs + i);
+        const uint4 v = __ldg(value + (long long)t * row_vecs + i);
+        kv[slot * row_vecs + i] = k;
+        kv[half_vecs + slot * row_vecs + i] = v;
     }
 }
 
@@ -839,6 +1111,25 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
     return PA_OK;
 }
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel in the stream finishes; it calls griddepcontrol.wait
+// before touching anything that kernel writes.
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, size_t smem,
+                       cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // Shape and kernel choice for one pa_decode call.
 struct DecodePlan {
     int nt = 1;       // 8-query N-tiles
@@ -848,9 +1139,12 @@ struct DecodePlan {
     int total_warps = 0;
     size_t smem = 0;
     size_t prefix_bytes = 0;
-    size_t record_bytes = 0;
+    size_t task_bytes = 0;  // tasks (int) and task starts (long long), per warp
+    size_t warp_record_bytes = 0;
     const void *main_fn = nullptr;
     const void *reduce_fn = nullptr;
+    size_t reduce_smem = 0;
+    size_t total() const { return prefix_bytes + task_bytes + warp_record_bytes; }
 };
 
 template <int D, int NT, bool BF16>
@@ -858,6 +1152,7 @@ void pick_kernels(DecodePlan &pl)
 {
     pl.main_fn = reinterpret_cast<const void *>(&paged_decode_kernel<D, NT, BF16>);
     pl.reduce_fn = reinterpret_cast<const void *>(&paged_decode_reduce_kernel<D, NT, BF16>);
+    pl.reduce_smem = reduce_smem_bytes<D, NT>();
     pl.smem = decode_smem_bytes<D>(0);
 }
 
@@ -908,6 +1203,9 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
     e = cudaFuncSetAttribute(pl.main_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
+    e = cudaFuncSetAttribute(pl.reduce_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.reduce_smem);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute (reduce)");
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl.main_fn, kWarps * 32, pl.smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
@@ -915,8 +1213,10 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
         return set_error(PA_ERR_UNSUPPORTED, "pa_decode: kernel does not fit on an SM (smem %zu)", pl.smem);
     pl.grid = sms * occ;
     pl.total_warps = pl.grid * kWarps;
+    const size_t rec = (size_t)pl.nt * 8 * (head_size + 2) * sizeof(float);
     pl.prefix_bytes = ((size_t)(num_seqs + 1) * sizeof(long long) + 255) / 256 * 256;
-    pl.record_bytes = (size_t)2 * pl.total_warps * pl.nt * 8 * (head_size + 2) * sizeof(float);
+    pl.task_bytes = ((size_t)pl.total_warps * (sizeof(int) + sizeof(long long)) + 511) / 256 * 256;
+    pl.warp_record_bytes = 2 * (size_t)pl.total_warps * rec;
     return PA_OK;
 }
 
@@ -937,7 +1237,7 @@ extern "C" int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_k
     rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype);
     if (rc != PA_OK)
         return rc;
-    *bytes = pl.prefix_bytes + pl.record_bytes;
+    *bytes = pl.total();
     return PA_OK;
 }
 
@@ -967,9 +1267,9 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype);
     if (rc != PA_OK)
         return rc;
-    if (workspace_bytes < pl.prefix_bytes + pl.record_bytes)
+    if (workspace_bytes < pl.total())
         return set_error(PA_ERR_WORKSPACE, "pa_decode: workspace %zu bytes < %zu needed", workspace_bytes,
-                         pl.prefix_bytes + pl.record_bytes);
+                         pl.total());
     int dev = 0;
     cudaGetDevice(&dev);
     CUtensorMap map;
@@ -982,8 +1282,11 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     prm.query = static_cast<const uint16_t *>(query);
     prm.block_tables = block_tables;
     prm.seq_lens = seq_lens;
-    prm.prefix_ws = static_cast<long long *>(workspace);
-    prm.records = reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.prefix_bytes);
+    char *ws = static_cast<char *>(workspace);
+    prm.prefix_ws = reinterpret_cast<long long *>(ws);
+    prm.task_start = reinterpret_cast<long long *>(ws + pl.prefix_bytes);
+    prm.tasks = reinterpret_cast<int *>(ws + pl.prefix_bytes + (size_t)pl.total_warps * sizeof(long long));
+    prm.warp_records = reinterpret_cast<float *>(ws + pl.prefix_bytes + pl.task_bytes);
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_seqs = num_seqs;
     prm.num_q_heads = num_q_heads;
@@ -998,13 +1301,13 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     prm.total_warps = pl.total_warps;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    void *main_args[] = {&map, &prm};
-    cudaError_t e = cudaLaunchKernel(pl.main_fn, dim3(pl.grid), dim3(kWarps * 32), main_args, pl.smem, s);
+    void *args[] = {&map, &prm};
+    cudaError_t e = launch_pdl(pl.main_fn, dim3(pl.grid), dim3(kWarps * 32), args, pl.smem, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "pa_decode: main kernel launch");
     void *red_args[] = {&prm};
-    const int segs = num_seqs * num_kv_heads * pl.qtiles;
-    e = cudaLaunchKernel(pl.reduce_fn, dim3(segs), dim3(128), red_args, 0, s);
+    e = launch_pdl(pl.reduce_fn, dim3((pl.total_warps + kReduceWarps - 1) / kReduceWarps),
+                   dim3(kReduceWarps * 32), red_args, pl.reduce_smem, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "pa_decode: reduce kernel launch");
     return PA_OK;
@@ -1033,7 +1336,8 @@ extern "C" int pa_reshape_and_cache(const void *key, const void *value, void *kv
         return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: row too large");
     const long long num_slots = (long long)num_blocks * block_size;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    reshape_and_cache_kernel<<<num_tokens, 128, 0, s>>>(
+    const dim3 grid(num_tokens, (unsigned)((row_vecs + kReshapeThreads - 1) / kReshapeThreads));
+    reshape_and_cache_kernel<<<grid, kReshapeThreads, 0, s>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(kv_cache), slot_mapping, (int)row_vecs, num_slots, num_slots * row_vecs);
     cudaError_t e = cudaGetLastError();

@@ -114,6 +114,7 @@ class DecodeStep:
         self.workspace = binding.decode_workspace(query, pool)
 
     def launches_per_step(self) -> int:
+        # copy_blocks (if any COW pairs) + reshape_and_cache + decode (stream + merge)
         return (1 if self.cow_pairs is not None else 0) + 1 + 2
 
     def run(self, stream=None) -> None:

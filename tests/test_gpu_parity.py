@@ -361,7 +361,7 @@ def test_cow_leaves_other_sharers_unchanged(dev):
     partial block; every other sibling's decode output is bit-identical to
     before, and the writer's output matches the oracle."""
     import torch
-    B, H, D, Hq, nb = 16, 8, 128, 32, 64
+    B, H, D, Hq, nb = 16, 8, 128, 32, 128
     dt = workloads.F16
     alloc = binding.BlockAllocator(nb, B, np.random.default_rng(1).permutation(nb))
     parent = alloc.add_seq(1024 + 7)
