@@ -155,6 +155,36 @@ int pa_decode(void *out, const void *query, const void *kv_cache,
               void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_static_scratch — pa_decode for callers that cannot allocate
+ * device memory. It has no counterpart on the PagedAttention pages; it
+ * exists because some callers cannot call cudaMalloc: a host framework whose
+ * allocator owns all of the GPU's memory, a plugin held to a fixed memory
+ * budget, or a latency-critical loop where an allocation (which can
+ * synchronise the device) is not allowed.
+ *
+ * Same arguments, result and launch behaviour as pa_decode, without the
+ * workspace: the split-K scratch lives in a 16 MiB static device array
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits. The call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).
+ *   - Shapes whose scratch need (pa_decode_workspace_size) exceeds 16 MiB are
+ *     rejected with PA_ERR_WORKSPACE and a message saying so. On a 152-SM
+ *     GB300 that admits every query group of up to 8 heads (and every shape
+ *     with head_size 64); groups of 9 or more at head_size 128 need pa_decode.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array. Nothing in it has to start
+ *     at zero (each call writes what it reads), but calls that overlap on the
+ *     GPU race on it: serialise them (one stream, or events).
+ */
+int pa_decode_static_scratch(void *out, const void *query, const void *kv_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *seq_lens, int num_seqs, float scale,
+                             int num_q_heads, int num_kv_heads, int head_size,
+                             int num_blocks, int block_size, int dtype,
+                             pa_stream_t stream);
+
+/*
  * pa_copy_blocks — copy-on-write clones of whole physical blocks
  * ([digest] "写时复制": a shared block is cloned before a write and the
  * writer's table retargeted; [lecture] §4.3 steps: allocate Q, copy P into

@@ -41,6 +41,7 @@ SIGNATURES = [
     ("pa_reshape_and_cache", _i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_decode_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     ("pa_decode", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    ("pa_decode_static_scratch", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_get_device_error", _i, [_ip]),
     ("pa_alloc_create", _vp, [_i, _i, _i32p]),
@@ -158,6 +159,19 @@ def pa_decode(out, query, kv_cache, block_tables, seq_lens, scale, workspace,
         _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
         _dtype_code(kv_cache), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def pa_decode_static_scratch(out, query, kv_cache, block_tables, seq_lens, scale,
+                             stream=None) -> None:
+    """pa_decode without a workspace: the scratch is the library's static
+    device array (for callers that cannot allocate device memory)."""
+    s, hq, d = query.shape
+    _, nb, bs, hkv, _ = kv_cache.shape
+    _check(lib().pa_decode_static_scratch(
+        _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
+        _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
+        _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
+        _dtype_code(kv_cache), _stream(stream)))
 
 
 def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:

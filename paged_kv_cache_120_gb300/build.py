@@ -27,6 +27,7 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra"]
 
 UNITS = [
     ("pa_kernels.cu", "nvcc"),
+    ("pa_static_scratch.cu", "nvcc"),
     ("block_allocator.cpp", "g++"),
     ("pa_errors.cpp", "g++"),
 ]
