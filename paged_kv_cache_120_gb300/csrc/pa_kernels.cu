@@ -253,8 +253,8 @@ struct DecodeParams {
     const int32_t *seq_lens;
     float *warp_records;  // workspace: 2 per warp, the warp's pieces of its first / last segment
     long long *prefix_ws; // workspace: unit prefix over sequences, [num_seqs + 1]
-    int *tasks;           // workspace: per warp, the split segment whose last piece it holds, or -1
-    long long *task_start;// workspace: per warp, that segment's first unit
+    int4 *tasks;          // workspace: per warp {segment, first owner, first slot, 0} of the
+                          // split segment whose last piece it holds; segment -1 if none
     int max_blocks_per_seq;
     int num_seqs;
     int num_q_heads;
@@ -272,7 +272,7 @@ struct DecodeParams {
 template <int D, int NT>
 constexpr int record_floats()
 {
-    return NT * 8 * (D + 2);  // m[GP], l[GP], O[D][GP]
+    return NT * 8 * (D + 2);  // m[GP], l[GP], O[GP][D]; only live query columns are written
 }
 
 template <int D>
@@ -422,9 +422,17 @@ __global__ void __launch_bounds__(kWarps * 32)
     const long long r0 = share_lo(N, gw, p.total_warps);
     const long long r1 = share_lo(N, gw + 1, p.total_warps);
     if (lane == 0)
-        p.tasks[gw] = -1;
-    if (r0 >= r1)
+        p.tasks[gw] = make_int4(-1, 0, 0, 0);
+    if (r0 >= r1) {
+        // An empty share is a zero-weight piece of whatever segment spans it:
+        // mark its first record (m = -inf, l = 0) so merges can skip it.
+        float *rec = p.warp_records + 2LL * gw * REC;
+        if (lane < p.tile_q) {
+            rec[lane] = -INFINITY;
+            rec[GP + lane] = 0.f;
+        }
         return;
+    }
 
     // Unit u -> physical block, segment id and (tile << 5 | valid tokens).
     auto unit_info = [&](long long u, int &phys, int &seg, int &tv) {
@@ -577,29 +585,29 @@ __global__ void __launch_bounds__(kWarps * 32)
             const long long slot = (seg_start <= r0) ? 2LL * gw : 2LL * gw + 1;
             float *rec = p.warp_records + slot * REC;
             if (lane == 0 && seg_start < r0 && seg_end <= r1) {
-                p.tasks[gw] = seg;  // this warp holds the segment's last piece
-                p.task_start[gw] = seg_start;
+                // This warp holds the segment's last piece: post the merge task
+                // with the segment's first owner and that owner's record slot.
+                const int o_lo = owner_of(seg_start, N, p.total_warps);
+                const int first = seg_start == share_lo(N, o_lo, p.total_warps) ? 2 * o_lo : 2 * o_lo + 1;
+                p.tasks[gw] = make_int4(seg, o_lo, first, 0);
             }
-            if (g == 0) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = nt * 8 + 2 * tig + e;
-                        rec[col] = m_run[nt][e];
-                        rec[GP + col] = lsum[nt][e];
+                for (int e = 0; e < 2; ++e) {
+                    const int col = nt * 8 + 2 * tig + e;
+                    if (col < p.tile_q) {
+                        if (g == 0) {
+                            rec[col] = m_run[nt][e];
+                            rec[GP + col] = lsum[nt][e];
+                        }
+                        float *ro = rec + 2 * GP + col * D;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            ro[16 * mt + g] = acc[mt][nt][e];
+                            ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
+                        }
                     }
-            }
-            float *ro = rec + 2 * GP;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int col = nt * 8 + 2 * tig;
-                    *reinterpret_cast<float2 *>(ro + (16 * mt + g) * GP + col) =
-                        make_float2(acc[mt][nt][0], acc[mt][nt][1]);
-                    *reinterpret_cast<float2 *>(ro + (16 * mt + g + 8) * GP + col) =
-                        make_float2(acc[mt][nt][2], acc[mt][nt][3]);
                 }
         }
     };
@@ -753,148 +761,140 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
-// Finish the segments cut by warp-share boundaries, and write zero rows for
-// empty sequences. Warp j of reduce CTA r serves main-grid warp
-// r * kReduceWarps + j: if that warp holds the last piece of a split segment,
-// the segment's pieces (one record per main-grid warp) are merged with the
-// online-softmax rule m = max m_p, l = sum l_p 2^(m_p - m),
-// O = sum O_p 2^(m_p - m). A task with few pieces is merged by its warp; a
-// task with many pieces is merged by the whole CTA, pieces split across the
-// warps and the warps' partial states combined in shared memory. Every merge
-// runs in a fixed order, so results do not depend on timing.
-constexpr int kSmallTask = 6;    // pieces a single warp merges on its own
-constexpr int kReduceWarps = 4;  // warps per reduce CTA
-
-// Lane layout of a merge: each lane owns one live column and the rows
-// d0, d0 + dstep, ... of it (columns rounded up to a power of two).
-struct MergeLanes {
-    int ct, col, d0, dstep, nk;
-    __device__ MergeLanes(int tile_q, int lane, int D)
+// Running merge state of one warp: for every live query column c, the
+// maximum M[c], the normaliser l[c] and the rows d = lane + 32 k of O.
+template <int D, int NT>
+struct MergeState {
+    static constexpr int GP = NT * 8, KD = D / 32;
+    float M[GP], l[GP], acc[GP][KD];
+    __device__ void clear()
     {
-        ct = tile_q <= 1 ? 1 : tile_q <= 2 ? 2 : tile_q <= 4 ? 4 : tile_q <= 8 ? 8 : 16;
-        col = lane % ct;
-        d0 = lane / ct;
-        dstep = 32 / ct;
-        nk = D / dstep;
+#pragma unroll
+        for (int c = 0; c < GP; ++c) {
+            M[c] = -INFINITY;
+            l[c] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KD; ++k)
+                acc[c][k] = 0.f;
+        }
     }
 };
 
-// One warp folds the pieces o_first, o_first + ostep, ... <= o_hi of the
-// segment starting at unit `a` into its running state (M, l, acc) for its
-// column and rows. Record offsets are computed lane-parallel, 32 pieces at a
-// time, and loads are issued in batches so that they overlap.
+// Fold the pieces o = o_first, o_first + ostep, ... <= o_hi into the state.
+// Piece o's record is slot first_slot when o == o_lo, else 2o. PPR pieces
+// are loaded per round (m, l and the O rows together) and folded with the
+// online-softmax rule; a piece with m = -inf (an empty share) weighs 0.
 template <int D, int NT>
-__device__ void fold_pieces(const float *recs, long long a, int o_first, int ostep, int o_hi,
-                            long long N, long long K, const MergeLanes &ml, float &M, float &l,
-                            float (&acc)[D * NT * 8 / 32])
+__device__ void fold_pieces(const float *recs, int o_first, int ostep, int o_hi, int o_lo,
+                            int first_slot, int tq, MergeState<D, NT> &st)
 {
-    constexpr int GP = NT * 8, REC = record_floats<D, NT>(), KMAX = D * GP / 32;
+    constexpr int GP = NT * 8, KD = D / 32, REC = record_floats<D, NT>();
+    constexpr int PPR = NT == 1 ? 2 : 1;
     const int lane = threadIdx.x & 31;
-    for (int b = 0;; b += 32) {
-        const int ob = o_first + b * ostep;
-        if (ob > o_hi)
-            break;
-        const int nb = min(32, (o_hi - ob) / ostep + 1);
-        long long my = -1;
-        if (lane < nb) {
-            const int o = ob + lane * ostep;
-            const long long lo = share_lo(N, o, K);
-            if (lo < share_lo(N, o + 1, K))
-                my = ((a <= lo) ? 2LL * o : 2LL * o + 1) * REC;
+    for (int o0 = o_first; o0 <= o_hi; o0 += PPR * ostep) {
+        float mp[PPR][GP], lp[PPR][GP], x[PPR][GP][KD];
+#pragma unroll
+        for (int j = 0; j < PPR; ++j) {
+            const int o = o0 + j * ostep;
+            const bool ok = o <= o_hi;
+            const float *r = recs + (long long)(o == o_lo ? first_slot : 2 * o) * REC;
+#pragma unroll
+            for (int c = 0; c < GP; ++c) {
+                const bool live = ok && c < tq;
+                mp[j][c] = live ? __ldcg(r + c) : -INFINITY;
+                lp[j][c] = live ? __ldcg(r + GP + c) : 0.f;
+#pragma unroll
+                for (int k = 0; k < KD; ++k)
+                    x[j][c][k] = live ? __ldcg(r + 2 * GP + c * D + lane + 32 * k) : 0.f;
+            }
         }
-        float mb = M;
-        for (int j0 = 0; j0 < nb; j0 += 8) {
-            float v[8];
+        // A marked empty share (m = -inf) has no O rows: never read them.
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const long long sl = __shfl_sync(kFull, my, (j0 + j) & 31);
-                v[j] = (j0 + j < nb && sl >= 0) ? __ldcg(recs + sl + ml.col) : -INFINITY;
+        for (int j = 0; j < PPR; ++j)
+#pragma unroll
+            for (int c = 0; c < GP; ++c)
+                if (mp[j][c] == -INFINITY) {
+                    lp[j][c] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < KD; ++k)
+                        x[j][c][k] = 0.f;
+                }
+#pragma unroll
+        for (int c = 0; c < GP; ++c) {
+            float mb = st.M[c];
+#pragma unroll
+            for (int j = 0; j < PPR; ++j)
+                mb = fmaxf(mb, mp[j][c]);
+            if (mb == -INFINITY)
+                continue;  // nothing valid in this column yet
+            const float scale = ex2(st.M[c] - mb);  // 0 on the first valid piece
+            float f[PPR];
+#pragma unroll
+            for (int j = 0; j < PPR; ++j)
+                f[j] = mp[j][c] == -INFINITY ? 0.f : ex2(mp[j][c] - mb);
+            float lv = st.l[c] * scale;
+#pragma unroll
+            for (int j = 0; j < PPR; ++j)
+                lv += f[j] * lp[j][c];
+            st.l[c] = lv;
+#pragma unroll
+            for (int k = 0; k < KD; ++k) {
+                float v = st.acc[c][k] * scale;
+#pragma unroll
+                for (int j = 0; j < PPR; ++j)
+                    v += f[j] * x[j][c][k];
+                st.acc[c][k] = v;
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                mb = fmaxf(mb, v[j]);
-        }
-        // Rescale the running state to the new maximum: 0 while nothing has
-        // been folded yet (M = -inf), 1 while no valid piece has been seen.
-        const float scale = mb == -INFINITY ? 1.f : ex2(M - mb);
-        l *= scale;
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-            acc[k] *= scale;
-        M = mb;
-        for (int j0 = 0; j0 < nb; j0 += 4) {
-            long long sl[4];
-            float f[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sl[j] = __shfl_sync(kFull, my, (j0 + j) & 31);
-                if (j0 + j >= nb)
-                    sl[j] = -1;
-                const float mv = sl[j] >= 0 ? __ldcg(recs + sl[j] + ml.col) : -INFINITY;
-                const float lv = sl[j] >= 0 ? __ldcg(recs + sl[j] + GP + ml.col) : 0.f;
-                f[j] = sl[j] >= 0 ? ex2(mv - M) : 0.f;
-                l += f[j] * lv;
-            }
-#pragma unroll
-            for (int k0 = 0; k0 < KMAX; k0 += 8) {
-                float x[4][8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        x[j][k] = (sl[j] >= 0 && k0 + k < ml.nk)
-                                      ? __ldcg(recs + sl[j] + 2 * GP + (ml.d0 + (k0 + k) * ml.dstep) * GP + ml.col)
-                                      : 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        acc[k0 + k] += f[j] * x[j][k];
-            }
+            st.M[c] = mb;
         }
     }
 }
 
-template <int D, int NT, bool BF16>
-__device__ __forceinline__ void store_rows(uint16_t *out, const MergeLanes &ml, int tile_q, float l,
-                                           const float (&acc)[D * NT * 8 / 32])
-{
-    constexpr int KMAX = D * NT * 8 / 32;
-    if (ml.col >= tile_q)
-        return;
-    const float inv = 1.f / l;
-    uint16_t *row = out + (long long)ml.col * D;
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k)
-        if (k < ml.nk)
-            row[ml.d0 + k * ml.dstep] = to_elem<BF16>(acc[k] * inv);
-}
+constexpr int kSmallTask = 6;    // pieces a single warp merges on its own
+constexpr int kReduceWarps = 4;  // warps per reduce CTA
 
 template <int D, int NT>
 constexpr size_t reduce_smem_bytes()
 {
-    return (size_t)kReduceWarps * (2 * NT * 8 + D * NT * 8) * sizeof(float);  // per warp: M, l, acc
+    return (size_t)kReduceWarps * (2 * NT * 8 + D * NT * 8) * sizeof(float);  // per warp: M, l, O
 }
 
+// Finish the segments cut by warp-share boundaries, and write zero rows for
+// empty sequences. Warp j of reduce CTA r serves main-grid warp
+// r * kReduceWarps + j: if that warp holds the last piece of a split segment,
+// the segment's pieces (one record per main-grid warp, ascending) are merged
+// with the online-softmax rule m = max m_p, l = sum l_p 2^(m_p - m),
+// O = sum O_p 2^(m_p - m). A task with few pieces is merged by its warp; a
+// task with many pieces by the whole CTA, pieces split across the warps and
+// the warps' states combined in shared memory. Every merge runs in a fixed
+// order, so results do not depend on timing.
 template <int D, int NT, bool BF16>
 __global__ void __launch_bounds__(kReduceWarps * 32) paged_decode_reduce_kernel(const DecodeParams p)
 {
-    constexpr int GP = NT * 8, KMAX = D * GP / 32;
-    extern __shared__ float s_part[];  // [kReduceWarps][GP (M) + GP (l) + D * GP (acc)]
-    __shared__ int s_seg[kReduceWarps], s_olo[kReduceWarps];
-    __shared__ long long s_a[kReduceWarps];
+    constexpr int GP = NT * 8, KD = D / 32, PART = 2 * GP + GP * D;
+    extern __shared__ float s_part[];  // [kReduceWarps][M GP | l GP | O GP x D]
+    __shared__ int4 s_task[kReduceWarps];
 
     grid_dependency_wait();  // the main grid's records and tasks are complete
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = blockIdx.x * kReduceWarps + warp;
-    const bool serving = w < p.total_warps;
-    const long long N = p.prefix_ws[p.num_seqs], TW = p.total_warps;
+    const int tq = p.tile_q;
     const int segs_per_seq = p.num_kv_heads * p.qtiles;
     uint16_t *out_base = static_cast<uint16_t *>(p.out);
     auto out_rows = [&](int seg) {
         const int s = seg / segs_per_seq, segl = seg - (seg / segs_per_seq) * segs_per_seq;
         const int h = segl / p.qtiles, qt = segl - (segl / p.qtiles) * p.qtiles;
         return out_base + ((long long)s * p.num_q_heads + h * p.group + qt * 16) * D;
+    };
+    auto store = [&](uint16_t *out, const MergeState<D, NT> &st) {
+#pragma unroll
+        for (int c = 0; c < GP; ++c)
+            if (c < tq) {
+                const float inv = 1.f / st.l[c];
+#pragma unroll
+                for (int k = 0; k < KD; ++k)
+                    out[(long long)c * D + lane + 32 * k] = to_elem<BF16>(st.acc[c][k] * inv);
+            }
     };
 
     // Empty sequences: zero output rows (no warp of the main grid saw them).
@@ -903,59 +903,51 @@ __global__ void __launch_bounds__(kReduceWarps * 32) paged_decode_reduce_kernel(
             for (int i = lane; i < p.num_q_heads * D; i += 32)
                 out_base[(long long)s * p.num_q_heads * D + i] = 0;
 
-    const int seg = serving ? p.tasks[w] : -1;
-    const long long a = serving ? p.task_start[w] : 0;
-    const int o_lo = seg >= 0 ? owner_of(a, N, TW) : 0;
-    const MergeLanes ml(p.tile_q, lane, D);
-    if (lane == 0) {
-        s_seg[warp] = (seg >= 0 && w - o_lo + 1 > kSmallTask) ? seg : -1;
-        s_a[warp] = a;
-        s_olo[warp] = o_lo;
-    }
-    if (seg >= 0 && w - o_lo + 1 <= kSmallTask) {
-        float M = -INFINITY, l = 0.f, acc[KMAX];
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-            acc[k] = 0.f;
-        fold_pieces<D, NT>(p.warp_records, a, o_lo, 1, w, N, TW, ml, M, l, acc);
-        store_rows<D, NT, BF16>(out_rows(seg), ml, p.tile_q, l, acc);
+    const int4 task = w < p.total_warps ? p.tasks[w] : make_int4(-1, 0, 0, 0);
+    const bool small = task.x >= 0 && w - task.y + 1 <= kSmallTask;
+    if (lane == 0)
+        s_task[warp] = (task.x >= 0 && !small) ? task : make_int4(-1, 0, 0, 0);
+    if (small) {
+        MergeState<D, NT> st;
+        st.clear();
+        fold_pieces<D, NT>(p.warp_records, task.y, 1, w, task.y, task.z, tq, st);
+        store(out_rows(task.x), st);
     }
     __syncthreads();
     // Tasks with many pieces: the whole CTA, pieces split across warps.
     for (int j = 0; j < kReduceWarps; ++j) {
-        const int bseg = s_seg[j];
-        if (bseg < 0)
+        const int4 t = s_task[j];
+        if (t.x < 0)
             continue;
         const int last = blockIdx.x * kReduceWarps + j;
-        float M = -INFINITY, l = 0.f, acc[KMAX];
+        MergeState<D, NT> st;
+        st.clear();
+        fold_pieces<D, NT>(p.warp_records, t.y + warp, kReduceWarps, last, t.y, t.z, tq, st);
+        float *mine = s_part + warp * PART;
 #pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-            acc[k] = 0.f;
-        fold_pieces<D, NT>(p.warp_records, s_a[j], s_olo[j] + warp, kReduceWarps, last, N, TW, ml, M, l,
-                           acc);
-        float *mine = s_part + warp * (2 * GP + D * GP);
-        if (ml.d0 == 0) {
-            mine[ml.col] = M;
-            mine[GP + ml.col] = l;
+        for (int c = 0; c < GP; ++c) {
+            if (lane == 0) {
+                mine[c] = st.M[c];
+                mine[GP + c] = st.l[c];
+            }
+#pragma unroll
+            for (int k = 0; k < KD; ++k)
+                mine[2 * GP + c * D + lane + 32 * k] = st.acc[c][k];
         }
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-            if (k < ml.nk)
-                mine[2 * GP + (ml.d0 + k * ml.dstep) * GP + ml.col] = acc[k];
         __syncthreads();
-        // Combine the warps' partial states (fixed order), elements across the CTA.
-        uint16_t *out = out_rows(bseg);
-        for (int e = threadIdx.x; e < p.tile_q * D; e += kReduceWarps * 32) {
-            const int d = e / p.tile_q, c = e - (e / p.tile_q) * p.tile_q;
+        // Combine the warps' states (fixed order), elements across the CTA.
+        uint16_t *out = out_rows(t.x);
+        for (int e = threadIdx.x; e < tq * D; e += kReduceWarps * 32) {
+            const int c = e / D, d = e - (e / D) * D;
             float Mx = -INFINITY;
             for (int v = 0; v < kReduceWarps; ++v)
-                Mx = fmaxf(Mx, s_part[v * (2 * GP + D * GP) + c]);
+                Mx = fmaxf(Mx, s_part[v * PART + c]);
             float lt = 0.f, ot = 0.f;
             for (int v = 0; v < kReduceWarps; ++v) {
-                const float *pv = s_part + v * (2 * GP + D * GP);
+                const float *pv = s_part + v * PART;
                 const float f = pv[c] == -INFINITY ? 0.f : ex2(pv[c] - Mx);  // warp had no pieces
                 lt += f * pv[GP + c];
-                ot += f * pv[2 * GP + d * GP + c];
+                ot += f * pv[2 * GP + c * D + d];
             }
             out[(long long)c * D + d] = to_elem<BF16>(ot / lt);
         }
@@ -1139,7 +1131,7 @@ struct DecodePlan {
     int total_warps = 0;
     size_t smem = 0;
     size_t prefix_bytes = 0;
-    size_t task_bytes = 0;  // tasks (int) and task starts (long long), per warp
+    size_t task_bytes = 0;  // one int4 task per warp
     size_t warp_record_bytes = 0;
     const void *main_fn = nullptr;
     const void *reduce_fn = nullptr;
@@ -1215,7 +1207,7 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
     pl.total_warps = pl.grid * kWarps;
     const size_t rec = (size_t)pl.nt * 8 * (head_size + 2) * sizeof(float);
     pl.prefix_bytes = ((size_t)(num_seqs + 1) * sizeof(long long) + 255) / 256 * 256;
-    pl.task_bytes = ((size_t)pl.total_warps * (sizeof(int) + sizeof(long long)) + 511) / 256 * 256;
+    pl.task_bytes = ((size_t)pl.total_warps * sizeof(int4) + 255) / 256 * 256;
     pl.warp_record_bytes = 2 * (size_t)pl.total_warps * rec;
     return PA_OK;
 }
@@ -1284,8 +1276,7 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     prm.seq_lens = seq_lens;
     char *ws = static_cast<char *>(workspace);
     prm.prefix_ws = reinterpret_cast<long long *>(ws);
-    prm.task_start = reinterpret_cast<long long *>(ws + pl.prefix_bytes);
-    prm.tasks = reinterpret_cast<int *>(ws + pl.prefix_bytes + (size_t)pl.total_warps * sizeof(long long));
+    prm.tasks = reinterpret_cast<int4 *>(ws + pl.prefix_bytes);
     prm.warp_records = reinterpret_cast<float *>(ws + pl.prefix_bytes + pl.task_bytes);
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_seqs = num_seqs;

@@ -155,6 +155,24 @@ def test_segments_split_across_many_warps(dev, dtype):
     assert max_abs_err(oracle.decode_elems(u16(out), dtype), want) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("heads", [(8, 2), (32, 8), (12, 1)])
+def test_stale_nan_workspace_does_not_leak(dev, heads):
+    """The workspace needs no initialisation: fill it with NaN bytes first
+    (what a reused buffer may hold) and the output must still match."""
+    import torch
+    Hq, Hkv = heads
+    c = Case(dev, workloads.F16, 64, Hq, Hkv, 16, LENS, seed=77 + Hq)
+    t = lambda a: torch.from_numpy(a).to(dev)
+    binding.pa_reshape_and_cache(c.k, c.v, c.pool, t(c.slots))
+    out = torch.empty_like(c.q)
+    ws = binding.decode_workspace(c.q, c.pool)
+    ws.fill_(0xFF)  # every float in it is a NaN
+    binding.pa_decode(out, c.q, c.pool, t(c.bt), t(c.seq_lens), c.scale, ws)
+    torch.cuda.synchronize()
+    want = c.oracle()
+    assert max_abs_err(oracle.decode_elems(u16(out), workloads.F16), want) <= TOL[workloads.F16]
+
+
 def test_single_token_sequences_return_value_rows(dev):
     """L = 1 everywhere: the output is the stored V row rounded once (exact)."""
     c = Case(dev, workloads.F16, 64, 4, 2, 16, [1] * 9, seed=3)
