@@ -234,7 +234,16 @@ __device__ __forceinline__ uint16_t to_elem(float x)
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 1
 #endif
-constexpr int kWarps = PA_DECODE_WARPS;    // warps per CTA, each an independent pipeline
+#ifndef PA_DECODE_WARPS_WIDE
+#define PA_DECODE_WARPS_WIDE 8
+#endif
+// Warps per CTA, each an independent pipeline: 12 for 8-column query tiles;
+// 16-column tiles need ~195 registers per thread, so 8 warps fit an SM.
+template <int NT>
+constexpr int decode_warps()
+{
+    return NT == 1 ? PA_DECODE_WARPS : PA_DECODE_WARPS_WIDE;
+}
 constexpr int kStages = PA_DECODE_STAGES;  // TMA ring depth per warp
 constexpr int kTile = 16;       // tokens per tile (the MMA's M)
 constexpr int kMaxSeqs = 4096;  // sequences per pa_decode call (prefix lives in smem)
@@ -266,7 +275,7 @@ struct DecodeParams {
     int block_size;
     int tiles_per_block;  // block_size / 16
     float scale_log2;     // scale * log2(e): scores live in base 2
-    int total_warps;      // grid * kWarps
+    int total_warps;      // grid * warps per CTA
 };
 
 template <int D, int NT>
@@ -275,12 +284,12 @@ constexpr int record_floats()
     return NT * 8 * (D + 2);  // m[GP], l[GP], O[GP][D]; only live query columns are written
 }
 
-template <int D>
+template <int D, int WARPS>
 inline size_t decode_smem_bytes(int num_seqs)
 {
     size_t b = 1024;  // alignment slack for the 1024-byte swizzle atoms
-    b += (size_t)kWarps * kStages * TileGeo<D>::kStageBytes;
-    b += (size_t)kWarps * kStages * sizeof(uint64_t);
+    b += (size_t)WARPS * kStages * TileGeo<D>::kStageBytes;
+    b += (size_t)WARPS * kStages * sizeof(uint64_t);
     b += (size_t)(num_seqs + 1) * sizeof(long long);
     b += (size_t)num_seqs * sizeof(int);
     return b;
@@ -338,11 +347,12 @@ __device__ __forceinline__ int owner_of(long long u, long long N, long long K)
 }
 
 // Main decode kernel. Template: head size D, N-tiles of 8 query heads NT,
-// element type. One CTA = kWarps independent warp pipelines.
+// element type. One CTA = decode_warps<NT>() independent warp pipelines.
 template <int D, int NT, bool BF16>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(decode_warps<NT>() * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
+    constexpr int kWarps = decode_warps<NT>();
     constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of V^T P^T
     constexpr int GP = NT * 8;
     constexpr int STAGE = TileGeo<D>::kStageBytes;
@@ -1128,6 +1138,7 @@ struct DecodePlan {
     int tile_q = 1;
     int qtiles = 1;
     int grid = 0;     // CTAs
+    int warps = 0;    // warps per CTA
     int total_warps = 0;
     size_t smem = 0;
     size_t prefix_bytes = 0;
@@ -1143,9 +1154,10 @@ template <int D, int NT, bool BF16>
 void pick_kernels(DecodePlan &pl)
 {
     pl.main_fn = reinterpret_cast<const void *>(&paged_decode_kernel<D, NT, BF16>);
+    pl.warps = decode_warps<NT>();
     pl.reduce_fn = reinterpret_cast<const void *>(&paged_decode_reduce_kernel<D, NT, BF16>);
     pl.reduce_smem = reduce_smem_bytes<D, NT>();
-    pl.smem = decode_smem_bytes<D>(0);
+    pl.smem = 0;
 }
 
 int validate_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
@@ -1179,11 +1191,13 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
     if (head_size == 64) {
         if (pl.nt == 1) bf ? pick_kernels<64, 1, true>(pl) : pick_kernels<64, 1, false>(pl);
         else            bf ? pick_kernels<64, 2, true>(pl) : pick_kernels<64, 2, false>(pl);
-        pl.smem = decode_smem_bytes<64>(num_seqs);
+        pl.smem = pl.nt == 1 ? decode_smem_bytes<64, decode_warps<1>()>(num_seqs)
+                             : decode_smem_bytes<64, decode_warps<2>()>(num_seqs);
     } else {
         if (pl.nt == 1) bf ? pick_kernels<128, 1, true>(pl) : pick_kernels<128, 1, false>(pl);
         else            bf ? pick_kernels<128, 2, true>(pl) : pick_kernels<128, 2, false>(pl);
-        pl.smem = decode_smem_bytes<128>(num_seqs);
+        pl.smem = pl.nt == 1 ? decode_smem_bytes<128, decode_warps<1>()>(num_seqs)
+                             : decode_smem_bytes<128, decode_warps<2>()>(num_seqs);
     }
     int dev = 0, sms = 0, occ = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1198,13 +1212,13 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
     e = cudaFuncSetAttribute(pl.reduce_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.reduce_smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute (reduce)");
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl.main_fn, kWarps * 32, pl.smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl.main_fn, pl.warps * 32, pl.smem);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (occ < 1)
         return set_error(PA_ERR_UNSUPPORTED, "pa_decode: kernel does not fit on an SM (smem %zu)", pl.smem);
     pl.grid = sms * occ;
-    pl.total_warps = pl.grid * kWarps;
+    pl.total_warps = pl.grid * pl.warps;
     const size_t rec = (size_t)pl.nt * 8 * (head_size + 2) * sizeof(float);
     pl.prefix_bytes = ((size_t)(num_seqs + 1) * sizeof(long long) + 255) / 256 * 256;
     pl.task_bytes = ((size_t)pl.total_warps * sizeof(int4) + 255) / 256 * 256;
@@ -1293,7 +1307,7 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *args[] = {&map, &prm};
-    cudaError_t e = launch_pdl(pl.main_fn, dim3(pl.grid), dim3(kWarps * 32), args, pl.smem, s);
+    cudaError_t e = launch_pdl(pl.main_fn, dim3(pl.grid), dim3(pl.warps * 32), args, pl.smem, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "pa_decode: main kernel launch");
     void *red_args[] = {&prm};
