@@ -59,6 +59,11 @@ typedef struct CUstream_st *pa_stream_t;
 #define PA_F16   0
 #define PA_BF16  1
 
+/* pa_decode flags. */
+#define PA_DECODE_SHARED_BLOCKS 1u  /* some physical block appears in more than one
+                                       sequence's table (prefix sharing, parallel
+                                       sampling): keep K/V at normal L2 priority */
+
 /* Bits of the device error word. */
 #define PA_DEVERR_BLOCK_ID  1   /* a block table entry outside [0, num_blocks) */
 #define PA_DEVERR_SLOT      2   /* a slot >= num_blocks * block_size */
@@ -133,6 +138,13 @@ int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  *                  initialisation and are not preserved. Calls that share a
  *                  workspace must not overlap on the GPU.
  *
+ *   flags          0 or PA_DECODE_SHARED_BLOCKS. Without it the K/V tiles
+ *                  are streamed with an L2 evict-first hint (each byte is
+ *                  read once per call, and the split-K records and tables
+ *                  stay in L2); with it they keep normal priority so that
+ *                  sequences sharing blocks hit L2. Results are identical
+ *                  either way; only the speed differs.
+ *
  * Launch: two kernels (the stream and the split-K merge), both with
  * programmatic dependent launch. The first may start while the preceding
  * kernel in the stream is finishing (typically this step's
@@ -152,7 +164,8 @@ int pa_decode(void *out, const void *query, const void *kv_cache,
               const int32_t *seq_lens, int num_seqs, float scale,
               int num_q_heads, int num_kv_heads, int head_size,
               int num_blocks, int block_size, int dtype,
-              void *workspace, size_t workspace_bytes, pa_stream_t stream);
+              void *workspace, size_t workspace_bytes, unsigned flags,
+              pa_stream_t stream);
 
 /*
  * pa_decode_static_scratch — pa_decode for callers that cannot allocate
@@ -182,7 +195,7 @@ int pa_decode_static_scratch(void *out, const void *query, const void *kv_cache,
                              const int32_t *seq_lens, int num_seqs, float scale,
                              int num_q_heads, int num_kv_heads, int head_size,
                              int num_blocks, int block_size, int dtype,
-                             pa_stream_t stream);
+                             unsigned flags, pa_stream_t stream);
 
 /*
  * pa_copy_blocks — copy-on-write clones of whole physical blocks

@@ -25,6 +25,7 @@ PA_ERR_OUT_OF_BLOCKS = -5
 PA_ERR_NOT_FOUND = -6
 PA_F16 = 0
 PA_BF16 = 1
+PA_DECODE_SHARED_BLOCKS = 1
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SLOT = 2
 PA_DEVERR_SEQ_LEN = 4
@@ -33,6 +34,7 @@ PA_DEVERR_TIMEOUT = 16
 
 # (name, restype, argtypes) of every exported function, in header order.
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_u = ctypes.c_uint
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = [
@@ -40,8 +42,8 @@ SIGNATURES = [
     ("pa_last_error", ctypes.c_char_p, []),
     ("pa_reshape_and_cache", _i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_decode_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
-    ("pa_decode", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
-    ("pa_decode_static_scratch", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp]),
+    ("pa_decode", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
+    ("pa_decode_static_scratch", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _u, _vp]),
     ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_get_device_error", _i, [_ip]),
     ("pa_alloc_create", _vp, [_i, _i, _i32p]),
@@ -148,9 +150,10 @@ def decode_workspace(query, kv_cache):
 
 
 def pa_decode(out, query, kv_cache, block_tables, seq_lens, scale, workspace,
-              stream=None) -> None:
+              flags=0, stream=None) -> None:
     """out/query [S, Hq, D]; kv_cache (2, NB, B, Hkv, D); block_tables [S, maxblk] int32;
-    seq_lens [S] int32; workspace: uint8 CUDA tensor (see decode_workspace)."""
+    seq_lens [S] int32; workspace: uint8 CUDA tensor (see decode_workspace);
+    flags: 0 or PA_DECODE_SHARED_BLOCKS."""
     s, hq, d = query.shape
     _, nb, bs, hkv, _ = kv_cache.shape
     _check(lib().pa_decode(
@@ -158,11 +161,11 @@ def pa_decode(out, query, kv_cache, block_tables, seq_lens, scale, workspace,
         _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
         _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
         _dtype_code(kv_cache), _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace.numel() * workspace.element_size(), int(flags), _stream(stream)))
 
 
 def pa_decode_static_scratch(out, query, kv_cache, block_tables, seq_lens, scale,
-                             stream=None) -> None:
+                             flags=0, stream=None) -> None:
     """pa_decode without a workspace: the scratch is the library's static
     device array (for callers that cannot allocate device memory)."""
     s, hq, d = query.shape
@@ -171,7 +174,7 @@ def pa_decode_static_scratch(out, query, kv_cache, block_tables, seq_lens, scale
         _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
         _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
         _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
-        _dtype_code(kv_cache), _stream(stream)))
+        _dtype_code(kv_cache), int(flags), _stream(stream)))
 
 
 def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:

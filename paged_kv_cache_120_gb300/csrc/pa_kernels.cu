@@ -145,6 +145,49 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The same load with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int c0, int c1, int c2, int c3, int c4,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar),
+        "l"(policy)
+        : "memory");
+}
+
+#ifndef PA_RECORD_EVICT_LAST
+#define PA_RECORD_EVICT_LAST 0  // store split-K records with an L2 evict-last hint
+#endif
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void st_hint(float *addr, float v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy) : "memory");
+}
+
 __device__ __forceinline__ void sts128_zero(uint32_t addr)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
@@ -275,6 +318,7 @@ struct DecodeParams {
     int block_size;
     int tiles_per_block;  // block_size / 16
     float scale_log2;     // scale * log2(e): scores live in base 2
+    int kv_stream;        // 1: stream K/V with the L2 evict-first hint (no block shared)
     int total_warps;      // grid * warps per CTA
 };
 
@@ -426,6 +470,11 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
     if (blockIdx.x == 0)
         for (int s = tid; s <= S; s += blockDim.x)
             p.prefix_ws[s] = prefix[s];
+    // Empty sequences get zero output rows (no warp streams them).
+    for (int s = blockIdx.x; s < S; s += gridDim.x)
+        if (lens[s] == 0)
+            for (int i = tid; i < p.num_q_heads * D; i += blockDim.x)
+                static_cast<uint16_t *>(p.out)[(long long)s * p.num_q_heads * D + i] = 0;
 
     // 2. This warp's contiguous share of the unit sequence.
     const int gw = blockIdx.x * kWarps + warp;
@@ -484,6 +533,7 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
         t = __shfl_sync(kFull, first ? a_tv : b_tv, src);
     };
 
+    const uint64_t kv_policy = p.kv_stream ? policy_evict_first() : policy_evict_normal();
     const uint32_t my_stage0 = base + (uint32_t)(warp * kStages * STAGE);
     const uint32_t my_bar0 = smem_addr(&bars[warp * kStages]);
     auto issue = [&](int phys, int seg, int tv, int st) {
@@ -498,8 +548,8 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
             mbar_expect_tx(bar, STAGE);
 #pragma unroll
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load_5d(my_stage0 + st * STAGE + bx * TileGeo<D>::kBoxBytes, &kv_map, bar,
-                            bx * 64, h, t0, phys, 0);
+                tma_load_5d_hint(my_stage0 + st * STAGE + bx * TileGeo<D>::kBoxBytes, &kv_map, bar,
+                                 bx * 64, h, t0, phys, 0, kv_policy);
         }
     };
 
@@ -607,15 +657,28 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
                 for (int e = 0; e < 2; ++e) {
                     const int col = nt * 8 + 2 * tig + e;
                     if (col < p.tile_q) {
-                        if (g == 0) {
-                            rec[col] = m_run[nt][e];
-                            rec[GP + col] = lsum[nt][e];
-                        }
                         float *ro = rec + 2 * GP + col * D;
+                        if constexpr (PA_RECORD_EVICT_LAST) {
+                            const uint64_t pol = policy_evict_last();
+                            if (g == 0) {
+                                st_hint(rec + col, m_run[nt][e], pol);
+                                st_hint(rec + GP + col, lsum[nt][e], pol);
+                            }
 #pragma unroll
-                        for (int mt = 0; mt < KS; ++mt) {
-                            ro[16 * mt + g] = acc[mt][nt][e];
-                            ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
+                            for (int mt = 0; mt < KS; ++mt) {
+                                st_hint(ro + 16 * mt + g, acc[mt][nt][e], pol);
+                                st_hint(ro + 16 * mt + g + 8, acc[mt][nt][2 + e], pol);
+                            }
+                        } else {
+                            if (g == 0) {
+                                rec[col] = m_run[nt][e];
+                                rec[GP + col] = lsum[nt][e];
+                            }
+#pragma unroll
+                            for (int mt = 0; mt < KS; ++mt) {
+                                ro[16 * mt + g] = acc[mt][nt][e];
+                                ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
+                            }
                         }
                     }
                 }
@@ -869,8 +932,8 @@ constexpr size_t reduce_smem_bytes()
     return (size_t)kReduceWarps * (2 * NT * 8 + D * NT * 8) * sizeof(float);  // per warp: M, l, O
 }
 
-// Finish the segments cut by warp-share boundaries, and write zero rows for
-// empty sequences. Warp j of reduce CTA r serves main-grid warp
+// Finish the segments cut by warp-share boundaries. Warp j of reduce CTA r
+// serves main-grid warp
 // r * kReduceWarps + j: if that warp holds the last piece of a split segment,
 // the segment's pieces (one record per main-grid warp, ascending) are merged
 // with the online-softmax rule m = max m_p, l = sum l_p 2^(m_p - m),
@@ -906,12 +969,6 @@ __global__ void __launch_bounds__(kReduceWarps * 32) paged_decode_reduce_kernel(
                     out[(long long)c * D + lane + 32 * k] = to_elem<BF16>(st.acc[c][k] * inv);
             }
     };
-
-    // Empty sequences: zero output rows (no warp of the main grid saw them).
-    for (int s = w; s < p.num_seqs; s += p.total_warps)
-        if (p.seq_lens[s] <= 0)
-            for (int i = lane; i < p.num_q_heads * D; i += 32)
-                out_base[(long long)s * p.num_q_heads * D + i] = 0;
 
     const int4 task = w < p.total_warps ? p.tasks[w] : make_int4(-1, 0, 0, 0);
     const bool small = task.x >= 0 && w - task.y + 1 <= kSmallTask;
@@ -1101,9 +1158,12 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
     cuuint32_t box[5] = {64, 1, (cuuint32_t)kTile, 1, 2};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUtensorMap m;
+#ifndef PA_KV_L2_PROMOTION
+#define PA_KV_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
     CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void *>(kv), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     PA_KV_L2_PROMOTION, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     const int slot = used < 16 ? used++ : (next++ % 16);
@@ -1251,7 +1311,8 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
                          const int32_t *block_tables, int max_blocks_per_seq,
                          const int32_t *seq_lens, int num_seqs, float scale, int num_q_heads,
                          int num_kv_heads, int head_size, int num_blocks, int block_size,
-                         int dtype, void *workspace, size_t workspace_bytes, pa_stream_t stream)
+                         int dtype, void *workspace, size_t workspace_bytes, unsigned flags,
+                         pa_stream_t stream)
 {
     int rc = validate_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size, dtype);
     if (rc != PA_OK)
@@ -1266,6 +1327,8 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
         return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq * block_size too large");
     if (!std::isfinite(scale))
         return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale is not finite");
+    if (flags & ~PA_DECODE_SHARED_BLOCKS)
+        return set_error(PA_ERR_INVALID_ARG, "pa_decode: unknown flags 0x%x", flags);
     if (!aligned(kv_cache, 16) || !aligned(query, 16) || !aligned(out, 16) ||
         !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return set_error(PA_ERR_INVALID_ARG, "pa_decode: misaligned pointer (pool/query/out 16 B, workspace 256 B)");
@@ -1303,6 +1366,7 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     prm.block_size = block_size;
     prm.tiles_per_block = block_size / kTile;
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.kv_stream = (flags & PA_DECODE_SHARED_BLOCKS) ? 0 : 1;
     prm.total_warps = pl.total_warps;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -59,7 +59,7 @@ extern "C" int pa_decode_static_scratch(void *out, const void *query, const void
                                         const int32_t *seq_lens, int num_seqs, float scale,
                                         int num_q_heads, int num_kv_heads, int head_size,
                                         int num_blocks, int block_size, int dtype,
-                                        pa_stream_t stream)
+                                        unsigned flags, pa_stream_t stream)
 {
     size_t need = 0;
     int rc = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
@@ -77,5 +77,5 @@ extern "C" int pa_decode_static_scratch(void *out, const void *query, const void
         return rc;
     return pa_decode(out, query, kv_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                      scale, num_q_heads, num_kv_heads, head_size, num_blocks, block_size, dtype,
-                     scratch, kStaticScratchBytes, stream);
+                     scratch, kStaticScratchBytes, flags, stream);
 }

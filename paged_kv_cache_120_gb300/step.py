@@ -112,6 +112,10 @@ class DecodeStep:
                           if len(plan.cow_pairs) else None)
         self.out = torch.empty_like(query)
         self.workspace = binding.decode_workspace(query, pool)
+        # Blocks that appear in more than one table are shared (prefix / fork):
+        # then K/V keep normal L2 priority, else they are streamed.
+        ids = plan.block_tables[plan.block_tables >= 0]
+        self.flags = binding.PA_DECODE_SHARED_BLOCKS if len(np.unique(ids)) < len(ids) else 0
 
     def launches_per_step(self) -> int:
         # copy_blocks (if any COW pairs) + reshape_and_cache + decode (stream + merge)
@@ -140,7 +144,7 @@ class DecodeStep:
 
     def decode(self, stream=None) -> None:
         binding.pa_decode(self.out, self.query, self.pool, self.block_tables, self.seq_lens,
-                          self.w.scale, self.workspace, stream)
+                          self.w.scale, self.workspace, self.flags, stream)
 
 
 def make_device_inputs(name: str, plan: StepPlan, seed: int, device):

@@ -40,20 +40,20 @@ def test_version(lib):
 def test_host_side_validation_without_a_gpu(lib):
     null = None
     # dtype, head size and group checks come before any CUDA call
-    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16, 7, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16, 7, null, 0, 0, null) \
         == binding.PA_ERR_UNSUPPORTED
-    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 96, 10, 16, 0, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 96, 10, 16, 0, null, 0, 0, null) \
         == binding.PA_ERR_UNSUPPORTED
-    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 3, 128, 10, 16, 0, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 3, 128, 10, 16, 0, null, 0, 0, null) \
         == binding.PA_ERR_INVALID_ARG
-    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 40, 2, 128, 10, 16, 0, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 40, 2, 128, 10, 16, 0, null, 0, 0, null) \
         == binding.PA_ERR_UNSUPPORTED          # group 20: neither <= 16 nor a multiple of 16
-    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 24, 0, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 24, 0, null, 0, 0, null) \
         == binding.PA_ERR_INVALID_ARG          # block_size not a multiple of 16
     assert "block_size" in binding.pa_last_error()
-    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16, 0, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16, 0, null, 0, 0, null) \
         == binding.PA_ERR_INVALID_ARG          # null pointers
-    assert lib.pa_decode(null, null, null, null, 1, null, 0, 1.0, 8, 8, 128, 10, 16, 0, null, 0, null) \
+    assert lib.pa_decode(null, null, null, null, 1, null, 0, 1.0, 8, 8, 128, 10, 16, 0, null, 0, 0, null) \
         == binding.PA_OK                       # empty batch is a no-op
     assert lib.pa_reshape_and_cache(null, null, null, null, 3, 10, 16, 8, 128, 0, null) \
         == binding.PA_ERR_INVALID_ARG

@@ -197,6 +197,22 @@ def test_decode_bit_identical_under_block_permutation(dev):
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
+def test_shared_blocks_flag_changes_speed_not_results(dev):
+    """PA_DECODE_SHARED_BLOCKS only changes an L2 cache hint: bit-identical output."""
+    import torch
+    c = Case(dev, workloads.BF16, 128, 32, 8, 16, [700, 5, 1234, 16, 999], seed=23)
+    out0 = c.gpu()
+    out1 = torch.empty_like(c.q)
+    ws = binding.decode_workspace(c.q, c.pool)
+    binding.pa_decode(out1, c.q, c.pool, c.bt_d, c.sl_d, c.scale, ws,
+                      flags=binding.PA_DECODE_SHARED_BLOCKS)
+    torch.cuda.synchronize()
+    assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
+    with pytest.raises(binding.PAError) as e:
+        binding.pa_decode(out1, c.q, c.pool, c.bt_d, c.sl_d, c.scale, ws, flags=4)
+    assert e.value.code == binding.PA_ERR_INVALID_ARG
+
+
 def test_copy_blocks_bit_exact_and_conflicts_rejected(dev):
     import torch
     rng = np.random.default_rng(4)
