@@ -134,18 +134,8 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// One TMA tile load of a rank-5 tensor into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, int c4)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
-        : "memory");
-}
-
-// The same load with an L2 eviction-priority hint (a createpolicy value).
+// One TMA tile load of a rank-5 tensor into shared memory, completing on `bar`,
+// with an L2 eviction-priority hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                  int c0, int c1, int c2, int c3, int c4,
                                                  uint64_t policy)
@@ -157,10 +147,6 @@ __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap
         "l"(policy)
         : "memory");
 }
-
-#ifndef PA_RECORD_EVICT_LAST
-#define PA_RECORD_EVICT_LAST 0  // store split-K records with an L2 evict-last hint
-#endif
 
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
@@ -176,17 +162,7 @@ __device__ __forceinline__ uint64_t policy_evict_normal()
     return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
 
-__device__ __forceinline__ void st_hint(float *addr, float v, uint64_t policy)
-{
-    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy) : "memory");
-}
 
 __device__ __forceinline__ void sts128_zero(uint32_t addr)
 {
@@ -657,28 +633,15 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
                 for (int e = 0; e < 2; ++e) {
                     const int col = nt * 8 + 2 * tig + e;
                     if (col < p.tile_q) {
+                        if (g == 0) {
+                            rec[col] = m_run[nt][e];
+                            rec[GP + col] = lsum[nt][e];
+                        }
                         float *ro = rec + 2 * GP + col * D;
-                        if constexpr (PA_RECORD_EVICT_LAST) {
-                            const uint64_t pol = policy_evict_last();
-                            if (g == 0) {
-                                st_hint(rec + col, m_run[nt][e], pol);
-                                st_hint(rec + GP + col, lsum[nt][e], pol);
-                            }
 #pragma unroll
-                            for (int mt = 0; mt < KS; ++mt) {
-                                st_hint(ro + 16 * mt + g, acc[mt][nt][e], pol);
-                                st_hint(ro + 16 * mt + g + 8, acc[mt][nt][2 + e], pol);
-                            }
-                        } else {
-                            if (g == 0) {
-                                rec[col] = m_run[nt][e];
-                                rec[GP + col] = lsum[nt][e];
-                            }
-#pragma unroll
-                            for (int mt = 0; mt < KS; ++mt) {
-                                ro[16 * mt + g] = acc[mt][nt][e];
-                                ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
-                            }
+                        for (int mt = 0; mt < KS; ++mt) {
+                            ro[16 * mt + g] = acc[mt][nt][e];
+                            ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
                         }
                     }
                 }
@@ -1158,12 +1121,9 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
     cuuint32_t box[5] = {64, 1, (cuuint32_t)kTile, 1, 2};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUtensorMap m;
-#ifndef PA_KV_L2_PROMOTION
-#define PA_KV_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-#endif
     CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void *>(kv), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     PA_KV_L2_PROMOTION, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     const int slot = used < 16 ? used++ : (next++ % 16);
