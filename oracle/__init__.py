@@ -71,6 +71,21 @@ def _load():
                                   i, i, i, i, i, i]
     lib.oracle_decode_sampled.argtypes = [c_dp, c_i32p, c_i32p, i, c_u16p, c_u16p, c_i32p, i,
                                           c_i32p, d, i, i, i, i, i, i]
+    c_u8p = ctypes.POINTER(ctypes.c_uint8)
+    f = ctypes.c_float
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = d
+    lib.oracle_e4m3_from_float.argtypes = [f]
+    lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+    lib.oracle_quantize_e4m3.argtypes = [ctypes.c_uint16, i, f]
+    lib.oracle_quantize_e4m3.restype = ctypes.c_uint8
+    lib.oracle_reshape_and_cache_fp8.argtypes = [c_u16p, c_u16p, c_u8p, c_i32p, i, i, i, i, i,
+                                                 i, f, f]
+    lib.oracle_reshape_and_cache_fp8.restype = i
+    lib.oracle_decode_fp8.argtypes = [c_dp, c_u16p, c_u8p, c_i32p, i, c_i32p, i, d,
+                                      i, i, i, i, i, i, d, d]
+    lib.oracle_decode_fp8_sampled.argtypes = [c_dp, c_i32p, c_i32p, i, c_u16p, c_u8p, c_i32p, i,
+                                              c_i32p, d, i, i, i, i, i, i, d, d]
     _lib = lib
     return lib
 
@@ -187,4 +202,73 @@ def decode_sampled(seq_ids, q_heads, query, pool, block_tables, seq_lens, scale,
                                   _p(kv, ctypes.c_uint16), _p(bt, ctypes.c_int32), bt.shape[1],
                                   _p(sl, ctypes.c_int32), float(scale), num_q_heads,
                                   num_kv_heads, head_size, num_blocks, block_size, dtype)
+    return out
+
+
+# ---------------------------------------------------------------- FP8 cache
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.int8:
+        a = a.view(np.uint8)
+    assert a.dtype == np.uint8, a.dtype
+    return a
+
+
+def e4m3_to_double(code: int) -> float:
+    """Exact value of an OCP E4M3 code (NaN for 0x7F / 0xFF)."""
+    return _load().oracle_e4m3_to_double(int(code))
+
+
+def e4m3_from_float(x: float) -> int:
+    """E4M3 code nearest to the fp32 value x (ties to even, saturating at +-448)."""
+    return int(_load().oracle_e4m3_from_float(float(x)))
+
+
+def quantize_e4m3(bits: int, dtype: int, scale: float) -> int:
+    """Cache code of one 16-bit element: e4m3(fp32(element) / fp32(scale))."""
+    return int(_load().oracle_quantize_e4m3(int(bits), dtype, float(scale)))
+
+
+def reshape_and_cache_fp8(key, value, pool, slot_mapping, num_blocks, block_size,
+                          num_kv_heads, head_size, dtype, k_scale, v_scale) -> int:
+    """Writes E4M3 codes in place into ``pool`` (uint8 array, pool layout)."""
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"]
+    k, v, s = _u16(key), _u16(value), _i32(slot_mapping)
+    return _load().oracle_reshape_and_cache_fp8(
+        _p(k, ctypes.c_uint16), _p(v, ctypes.c_uint16), _p(pool, ctypes.c_uint8),
+        _p(s, ctypes.c_int32), len(s), num_blocks, block_size, num_kv_heads, head_size,
+        dtype, float(k_scale), float(v_scale))
+
+
+def decode_fp8(query, pool, block_tables, seq_lens, scale, num_q_heads, num_kv_heads,
+               head_size, num_blocks, block_size, dtype, k_scale, v_scale) -> np.ndarray:
+    """Paged decode over an E4M3 pool -> [num_seqs, num_q_heads, head_size] float64."""
+    q, kv = _u16(query), _u8(pool)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    num_seqs = sl.shape[0]
+    max_blocks = bt.shape[1] if bt.ndim == 2 else 0
+    out = np.zeros((num_seqs, num_q_heads, head_size), dtype=np.float64)
+    _load().oracle_decode_fp8(_p(out, ctypes.c_double), _p(q, ctypes.c_uint16),
+                              _p(kv, ctypes.c_uint8), _p(bt, ctypes.c_int32), max_blocks,
+                              _p(sl, ctypes.c_int32), num_seqs, float(scale), num_q_heads,
+                              num_kv_heads, head_size, num_blocks, block_size, dtype,
+                              float(k_scale), float(v_scale))
+    return out
+
+
+def decode_fp8_sampled(seq_ids, q_heads, query, pool, block_tables, seq_lens, scale,
+                       num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                       dtype, k_scale, v_scale) -> np.ndarray:
+    """FP8-cache decode of sampled (seq, q_head) pairs -> [n, head_size] float64."""
+    q, kv = _u16(query), _u8(pool)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    si, hi = _i32(seq_ids), _i32(q_heads)
+    out = np.zeros((len(si), head_size), dtype=np.float64)
+    _load().oracle_decode_fp8_sampled(_p(out, ctypes.c_double), _p(si, ctypes.c_int32),
+                                      _p(hi, ctypes.c_int32), len(si), _p(q, ctypes.c_uint16),
+                                      _p(kv, ctypes.c_uint8), _p(bt, ctypes.c_int32),
+                                      bt.shape[1], _p(sl, ctypes.c_int32), float(scale),
+                                      num_q_heads, num_kv_heads, head_size, num_blocks,
+                                      block_size, dtype, float(k_scale), float(v_scale))
     return out

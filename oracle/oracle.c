@@ -25,6 +25,12 @@
  * Precision: inputs are 16-bit (fp16 or bf16) bit patterns, decoded exactly
  * to double; every sum, max, exp and division is done in double.
  *
+ * FP8 cache (a reading: the book names a lower-precision KV cache only as a
+ * capacity lever, §4.8): K and V are stored as OCP E4M3 codes (1 sign, 4
+ * exponent bits with bias 7, 3 fraction bits; no infinities; S.1111.111 is
+ * NaN; largest finite 448) of value / scale, one scale for K and one for V.
+ * A stored code c stands for decode(c) * scale.
+ *
  * Parity pins for every function here live in tests/test_oracle_pins.py.
  */
 #include <math.h>
@@ -75,6 +81,57 @@ void oracle_decode_elems(const uint16_t *bits, double *out, long long n, int dty
 {
     for (long long i = 0; i < n; ++i)
         out[i] = dtype == ORACLE_BF16 ? oracle_bf16_to_double(bits[i]) : oracle_f16_to_double(bits[i]);
+}
+
+/* ---- E4M3 (OCP FP8) ---- */
+
+/* Exact value of an E4M3 code. */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int expo = (c >> 3) & 0xf;
+    int frac = c & 7;
+    double mag;
+    if (expo == 15 && frac == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)frac, -9);              /* subnormal: frac/8 * 2^-6 */
+    else
+        mag = ldexp((double)(8 + frac), expo - 10); /* (1 + f/8) * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+/* Code of the E4M3 value nearest to x (ties to the even code), saturating
+ * beyond +-448; NaN gives 0x7F. Found by comparing x with every finite code:
+ * slow, and the plain definition of round-to-nearest-even. */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a > 448.0)
+        return sign | 0x7E;
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double err = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+/* Quantise one 16-bit element for the FP8 cache: the element divided by the
+ * scale in fp32 (one IEEE division, the precision the device uses, so that
+ * both sides round the same quotient), then rounded to E4M3. */
+uint8_t oracle_quantize_e4m3(uint16_t bits, int dtype, float scale)
+{
+    float v = (float)(dtype == ORACLE_BF16 ? oracle_bf16_to_double(bits) : oracle_f16_to_double(bits));
+    float y = v / scale;
+    return oracle_e4m3_from_float(y);
 }
 
 static double elem(const uint16_t *p, long long i, int dtype)
@@ -133,6 +190,38 @@ int oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_
     return written;
 }
 
+/* ---- FP8 cache write path ----
+ * The same placement as oracle_reshape_and_cache, into a byte pool of the
+ * same shape; every K element is stored as oracle_quantize_e4m3(k, k_scale)
+ * and every V element as oracle_quantize_e4m3(v, v_scale). */
+int oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value, uint8_t *pool,
+                                 const int32_t *slot_mapping, int num_tokens,
+                                 int num_blocks, int block_size, int num_kv_heads, int head_size,
+                                 int dtype, float k_scale, float v_scale)
+{
+    int written = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        long long slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= (long long)num_blocks * block_size)
+            return -1;
+        int b = (int)(slot / block_size);
+        int off = (int)(slot % block_size);
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_size; ++d) {
+                long long src = ((long long)t * num_kv_heads + h) * head_size + d;
+                pool[pool_index(0, b, off, h, d, num_blocks, block_size, num_kv_heads, head_size)] =
+                    oracle_quantize_e4m3(key[src], dtype, k_scale);
+                pool[pool_index(1, b, off, h, d, num_blocks, block_size, num_kv_heads, head_size)] =
+                    oracle_quantize_e4m3(value[src], dtype, v_scale);
+            }
+        }
+        ++written;
+    }
+    return written;
+}
+
 /* ---- copy-on-write block copy [P3 写时复制; P5 §4.3] ----
  * For each (src, dst) pair, in order, and for every layer pool: the whole
  * physical block (all B slots, K and V, all heads) of src is copied to dst.
@@ -160,11 +249,10 @@ int oracle_copy_blocks(uint16_t *const *pools, int num_layers,
 
 /* ---- read path: plain attention over a contiguous K/V [P4 §三.1] ----
  * out[d] = sum_i w_i V[i][d] / sum_i w_i, w_i = exp(x_i - max_j x_j),
- * x_i = scale * sum_d q[d] K[i][d]. K and V are [L][head_size]. L = 0
+ * x_i = scale * sum_d q[d] K[i][d]. K and V are [L][head_size] values. L = 0
  * gives a zero row (the pages are silent; this is the reading taken). */
-void oracle_attention_contiguous(double *out, const uint16_t *q, const uint16_t *k,
-                                 const uint16_t *v, int seq_len, int head_size,
-                                 double scale, int dtype)
+static void attention_values(double *out, const double *q, const double *k, const double *v,
+                             int seq_len, int head_size, double scale)
 {
     for (int d = 0; d < head_size; ++d)
         out[d] = 0.0;
@@ -175,7 +263,7 @@ void oracle_attention_contiguous(double *out, const uint16_t *q, const uint16_t 
     for (int i = 0; i < seq_len; ++i) {
         double dot = 0.0;
         for (int d = 0; d < head_size; ++d)
-            dot += elem(q, d, dtype) * elem(k, (long long)i * head_size + d, dtype);
+            dot += q[d] * k[(long long)i * head_size + d];
         x[i] = scale * dot;
         if (x[i] > mx)
             mx = x[i];
@@ -188,10 +276,32 @@ void oracle_attention_contiguous(double *out, const uint16_t *q, const uint16_t 
     for (int d = 0; d < head_size; ++d) {
         double acc = 0.0;
         for (int i = 0; i < seq_len; ++i)
-            acc += x[i] * elem(v, (long long)i * head_size + d, dtype);
+            acc += x[i] * v[(long long)i * head_size + d];
         out[d] = acc / denom;
     }
     free(x);
+}
+
+/* The same on 16-bit inputs: every element decoded exactly, then the
+ * definition above. */
+void oracle_attention_contiguous(double *out, const uint16_t *q, const uint16_t *k,
+                                 const uint16_t *v, int seq_len, int head_size,
+                                 double scale, int dtype)
+{
+    size_t n = seq_len > 0 ? (size_t)seq_len * head_size : 1;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)head_size);
+    double *kd = (double *)malloc(sizeof(double) * n);
+    double *vd = (double *)malloc(sizeof(double) * n);
+    for (int d = 0; d < head_size; ++d)
+        qd[d] = elem(q, d, dtype);
+    for (long long i = 0; i < (long long)(seq_len > 0 ? seq_len : 0) * head_size; ++i) {
+        kd[i] = elem(k, i, dtype);
+        vd[i] = elem(v, i, dtype);
+    }
+    attention_values(out, qd, kd, vd, seq_len, head_size, scale);
+    free(qd);
+    free(kd);
+    free(vd);
 }
 
 /* ---- read path: paged decode for one (sequence, q-head) [P1 §4.5, §4.4.1] ----
@@ -254,6 +364,75 @@ void oracle_decode_sampled(double *out, const int32_t *seq_ids, const int32_t *q
         oracle_decode_one(out + (long long)i * head_size, query, pool, block_tables,
                           max_blocks_per_seq, seq_lens, seq_ids[i], q_heads[i], scale,
                           num_q_heads, num_kv_heads, head_size, num_blocks, block_size, dtype);
+}
+
+/* ---- FP8 cache read path ----
+ * The paged decode of oracle_decode_one over a byte pool: a cached K element
+ * stands for e4m3(code) * k_scale and a V element for e4m3(code) * v_scale
+ * (exact in double); the query is the 16-bit input. The attention is the
+ * same two-pass definition (attention_values) on those values. */
+void oracle_decode_fp8_one(double *out, const uint16_t *query, const uint8_t *pool,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, int seq, int q_head,
+                           double scale, int num_q_heads, int num_kv_heads, int head_size,
+                           int num_blocks, int block_size, int dtype,
+                           double k_scale, double v_scale)
+{
+    int seq_len = seq_lens[seq];
+    int group = num_q_heads / num_kv_heads;
+    int kv_head = q_head / group;
+    const int32_t *table = block_tables + (long long)seq * max_blocks_per_seq;
+    size_t n = seq_len > 0 ? (size_t)seq_len * head_size : 1;
+    double *k = (double *)malloc(sizeof(double) * n);
+    double *v = (double *)malloc(sizeof(double) * n);
+    double *q = (double *)malloc(sizeof(double) * (size_t)head_size);
+    for (int i = 0; i < seq_len; ++i) {
+        int b = table[i / block_size];
+        int off = i % block_size;
+        for (int d = 0; d < head_size; ++d) {
+            uint8_t kc = pool[pool_index(0, b, off, kv_head, d, num_blocks, block_size, num_kv_heads, head_size)];
+            uint8_t vc = pool[pool_index(1, b, off, kv_head, d, num_blocks, block_size, num_kv_heads, head_size)];
+            k[(long long)i * head_size + d] = oracle_e4m3_to_double(kc) * k_scale;
+            v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * v_scale;
+        }
+    }
+    const uint16_t *qb = query + ((long long)seq * num_q_heads + q_head) * head_size;
+    for (int d = 0; d < head_size; ++d)
+        q[d] = elem(qb, d, dtype);
+    attention_values(out, q, k, v, seq_len, head_size, scale);
+    free(k);
+    free(v);
+    free(q);
+}
+
+/* FP8-cache decode for a whole batch: out is [num_seqs][num_q_heads][head_size]. */
+void oracle_decode_fp8(double *out, const uint16_t *query, const uint8_t *pool,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *seq_lens, int num_seqs,
+                       double scale, int num_q_heads, int num_kv_heads, int head_size,
+                       int num_blocks, int block_size, int dtype, double k_scale, double v_scale)
+{
+    for (int s = 0; s < num_seqs; ++s)
+        for (int hq = 0; hq < num_q_heads; ++hq)
+            oracle_decode_fp8_one(out + ((long long)s * num_q_heads + hq) * head_size, query, pool,
+                                  block_tables, max_blocks_per_seq, seq_lens, s, hq, scale,
+                                  num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                                  dtype, k_scale, v_scale);
+}
+
+/* FP8-cache decode for sampled (seq, q_head) pairs: out is [n][head_size]. */
+void oracle_decode_fp8_sampled(double *out, const int32_t *seq_ids, const int32_t *q_heads, int n,
+                               const uint16_t *query, const uint8_t *pool,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, double scale, int num_q_heads,
+                               int num_kv_heads, int head_size, int num_blocks, int block_size,
+                               int dtype, double k_scale, double v_scale)
+{
+    for (int i = 0; i < n; ++i)
+        oracle_decode_fp8_one(out + (long long)i * head_size, query, pool, block_tables,
+                              max_blocks_per_seq, seq_lens, seq_ids[i], q_heads[i], scale,
+                              num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                              dtype, k_scale, v_scale);
 }
 
 /* ---- the online-softmax recurrence [P1 §4.6] ----

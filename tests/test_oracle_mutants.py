@@ -11,6 +11,21 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
+# The gather prologue of the 16-bit and the FP8 decode (they differ in the
+# type of the K/V buffers): {0} is the q-head -> kv-head map, {1} the
+# logical-block index of token i.
+_GATHER = """    int kv_head = {0};
+    const int32_t *table = block_tables + (long long)seq * max_blocks_per_seq;
+    size_t n = seq_len > 0 ? (size_t)seq_len * head_size : 1;
+    %s *k = (%s *)malloc(sizeof(%s) * n);
+    %s *v = (%s *)malloc(sizeof(%s) * n);
+"""
+_GATHER16 = (_GATHER % (("uint16_t",) * 6)) + """    for (int i = 0; i < seq_len; ++i) {{
+        int b = table[{1}];"""
+_GATHER8 = (_GATHER % (("double",) * 6)) + """    double *q = (double *)malloc(sizeof(double) * (size_t)head_size);
+    for (int i = 0; i < seq_len; ++i) {{
+        int b = table[{1}];"""
+
 # (file, original text, planted slip, pin file expected to catch it)
 MUTANTS = [
     ("oracle/oracle.c", "expo - 25);", "expo - 24);", "test_oracle_pins.py"),          # f16 bias
@@ -28,14 +43,37 @@ MUTANTS = [
      "test_oracle_pins.py"),                                                           # copy K only
     ("oracle/oracle.c", "x[i] = scale * dot;", "x[i] = dot;", "test_oracle_pins.py"),  # no scale
     ("oracle/oracle.c", "denom += x[i];", "denom += 1.0;", "test_oracle_pins.py"),     # bad normaliser
-    ("oracle/oracle.c", "int kv_head = q_head / group;", "int kv_head = q_head % num_kv_heads;",
+    ("oracle/oracle.c", _GATHER16.format("q_head / group", "i / block_size"),
+     _GATHER16.format("q_head % num_kv_heads", "i / block_size"),
      "test_oracle_pins.py"),                                                           # GQA mapping
-    ("oracle/oracle.c", "int b = table[i / block_size];", "int b = table[i % block_size];",
+    ("oracle/oracle.c", _GATHER16.format("q_head / group", "i / block_size"),
+     _GATHER16.format("q_head / group", "i % block_size"),
      "test_oracle_pins.py"),                                                           # table walk
+    ("oracle/oracle.c", _GATHER8.format("q_head / group", "i / block_size"),
+     _GATHER8.format("q_head % num_kv_heads", "i / block_size"),
+     "test_oracle_fp8_pins.py"),                                                       # fp8 GQA mapping
+    ("oracle/oracle.c", _GATHER8.format("q_head / group", "i / block_size"),
+     _GATHER8.format("q_head / group", "i % block_size"),
+     "test_oracle_fp8_pins.py"),                                                       # fp8 table walk
     ("oracle/oracle.c", "double a_old = exp(m - m_new);", "double a_old = exp(m_new - m);",
      "test_oracle_pins.py"),                                                           # merge sign
     ("oracle/oracle.c", "s = s * a_old + sp * a_new;", "s = s * a_old + sp;",
      "test_oracle_pins.py"),                                                           # merge term
+    ("oracle/oracle.c", "mag = ldexp((double)(8 + frac), expo - 10);",
+     "mag = ldexp((double)(8 + frac), expo - 9);", "test_oracle_fp8_pins.py"),       # e4m3 bias
+    ("oracle/oracle.c", "mag = ldexp((double)frac, -9);", "mag = ldexp((double)frac, -10);",
+     "test_oracle_fp8_pins.py"),                                                      # subnormals
+    ("oracle/oracle.c", "(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0",
+     "test_oracle_fp8_pins.py"),                                                      # ties to odd
+    ("oracle/oracle.c", "return sign | 0x7E;", "return sign | 0x7F;",
+     "test_oracle_fp8_pins.py"),                                                      # no saturation
+    ("oracle/oracle.c", "float y = v / scale;", "float y = v * scale;",
+     "test_oracle_fp8_pins.py"),                                                      # scale inverted
+    ("oracle/oracle.c", "oracle_quantize_e4m3(value[src], dtype, v_scale);",
+     "oracle_quantize_e4m3(value[src], dtype, k_scale);", "test_oracle_fp8_pins.py"), # V with K scale
+    ("oracle/oracle.c", "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * v_scale;",
+     "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * k_scale;",
+     "test_oracle_fp8_pins.py"),                                                      # decode scale swap
     ("oracle/block_manager.py", "self.free.insert(0, b)", "self.free.append(b)",
      "test_block_manager.py"),                                                         # free to tail
     ("oracle/block_manager.py", "                self.ref[last] -= 1\n", "",
