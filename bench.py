@@ -10,6 +10,8 @@ head_dim 128, fp16, lengths uniform in [1, 2048], 9000-block pool).
 
 Prints one JSON line (rank 0). ``value`` is the step's algorithmic HBM bytes
 per second (GB/s); ``seq_steps_per_s`` is sequences decoded per second.
+``--kv-cache fp8`` runs the same step on a cache of E4M3 codes (one byte per
+K/V element, per-tensor scales): pa_reshape_and_cache_fp8 and pa_decode_fp8.
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead.
 Under torchrun every rank runs its own replica of the workload (weak
 scaling: sequences are independent, no collective on the data path).
@@ -40,20 +42,21 @@ L2_BYTES = 129 * 2 ** 20
 
 # ------------------------------------------------------------ bytes of a step
 
-def algorithmic_bytes(w, seq_lens, num_pairs: int, num_new_tokens: int) -> dict:
+def algorithmic_bytes(w, seq_lens, num_pairs: int, num_new_tokens: int, kv_elem: int = 2) -> dict:
     """Bytes a step must move at minimum: every valid K/V element once per kv
     head (padding slots of partial blocks not counted), Q, the output, block
-    table entries and lengths; the new K/V rows read and written; each COW
-    pair's K and V block read and written."""
+    table entries and lengths; the new K/V rows read (16-bit) and written
+    (kv_elem bytes per element); each COW pair's K and V block read and
+    written. kv_elem is 2 for a 16-bit cache, 1 for an FP8 cache."""
     e = 2
     L = np.asarray(seq_lens, dtype=np.int64)
     S = len(L)
-    kv = int((2 * L * w.num_kv_heads * w.head_size * e).sum())
+    kv = int((2 * L * w.num_kv_heads * w.head_size * kv_elem).sum())
     tables = int((4 * ((L + w.block_size - 1) // w.block_size)).sum())
     qo = 2 * S * w.num_q_heads * w.head_size * e
     decode = kv + qo + tables + 4 * S
-    reshape = num_new_tokens * (2 * 2 * w.num_kv_heads * w.head_size * e + 4)
-    copy = num_pairs * 2 * 2 * w.block_size * w.num_kv_heads * w.head_size * e + 8 * num_pairs
+    reshape = num_new_tokens * (2 * w.num_kv_heads * w.head_size * (e + kv_elem) + 4)
+    copy = num_pairs * 2 * 2 * w.block_size * w.num_kv_heads * w.head_size * kv_elem + 8 * num_pairs
     return dict(decode=decode, kv=kv, reshape=reshape, copy=copy, step=decode + reshape + copy)
 
 
@@ -67,11 +70,12 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
 
 
-def traffic_record(workload: str):
+def traffic_record(workload: str, kv_cache: str = "16bit"):
     """DRAM traffic per decode launch from a committed ncu summary, if the
     summary was taken on the current decode source (its hash matches)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
+    tag = "decode_fp8" if kv_cache == "fp8" else "decode"
+    path = os.path.join(ROOT, "profiles", f"{tag}_{workload}_traffic.txt")
     src = os.path.join(ROOT, "paged_kv_cache_120_gb300", "csrc", "pa_kernels.cu")
     try:
         kv = {}
@@ -186,7 +190,8 @@ def dist_barrier(world: int, device=None):
 
 # ------------------------------------------------------------ oracle timing
 
-def oracle_sample_time(name, plan, pool_bits, q_bits, budget_s: float, start_seq: int = 0):
+def oracle_sample_time(name, plan, pool_bits, q_bits, budget_s: float, start_seq: int = 0,
+                       kv_cache: str = "16bit"):
     """Time the oracle's decode on whole sequences (round-robin from
     start_seq) until about budget_s of CPU time is spent. Returns
     (seconds, algorithmic bytes covered, sequences, next start)."""
@@ -195,28 +200,42 @@ def oracle_sample_time(name, plan, pool_bits, q_bits, budget_s: float, start_seq
     S = len(plan.seq_lens)
     done_bytes, n, t = 0, 0, 0.0
     s = start_seq % S
+    fp8 = kv_cache == "fp8"
     while t < budget_s and n < S:
         seqs = np.full(w.num_q_heads, s, dtype=np.int32)
         heads = np.arange(w.num_q_heads, dtype=np.int32)
         t0 = time.perf_counter()
-        oracle.decode_sampled(seqs, heads, q_bits, pool_bits, plan.block_tables, plan.seq_lens,
-                              w.scale, w.num_q_heads, w.num_kv_heads, w.head_size, w.num_blocks,
-                              w.block_size, w.dtype)
+        if fp8:
+            oracle.decode_fp8_sampled(seqs, heads, q_bits, pool_bits, plan.block_tables,
+                                      plan.seq_lens, w.scale, w.num_q_heads, w.num_kv_heads,
+                                      w.head_size, w.num_blocks, w.block_size, w.dtype,
+                                      workloads.FP8_K_SCALE, workloads.FP8_V_SCALE)
+        else:
+            oracle.decode_sampled(seqs, heads, q_bits, pool_bits, plan.block_tables,
+                                  plan.seq_lens, w.scale, w.num_q_heads, w.num_kv_heads,
+                                  w.head_size, w.num_blocks, w.block_size, w.dtype)
         t += time.perf_counter() - t0
-        done_bytes += algorithmic_bytes(w, [plan.seq_lens[s]], 0, 0)["decode"]
+        done_bytes += algorithmic_bytes(w, [plan.seq_lens[s]], 0, 0, 1 if fp8 else 2)["decode"]
         n += 1
         s = (s + 1) % S
     return t, done_bytes, n, s
 
 
-def host_inputs(name, plan, seed):
+def pool_host_bits(pool):
+    """Host copy of a pool's bits: uint16 patterns, or the E4M3 bytes."""
+    import torch
+    if pool.dtype == torch.uint8:
+        return pool.cpu().numpy()
+    return pool.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_inputs(name, plan, seed, kv_cache="16bit"):
     """The oracle's host copies of the step's inputs (bit patterns)."""
     import torch
     from paged_kv_cache_120_gb300 import step as stepmod
     dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
-    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev)
-    to = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
-    pool_bits, q_bits = to(pool), to(q)
+    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev, kv_cache)
+    pool_bits, q_bits = pool_host_bits(pool), pool_host_bits(q)
     del pool
     return pool_bits, q_bits
 
@@ -229,14 +248,16 @@ def run_reference(args, rank, world):
     name = args.workload
     w = workloads.WORKLOADS[name]
     plan = stepmod.plan_step(name, args.seed)
-    pool_bits, q_bits = host_inputs(name, plan, args.seed)
+    pool_bits, q_bits = host_inputs(name, plan, args.seed, args.kv_cache)
     per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
     nxt = 0
     for _ in range(args.warmup):
-        _, _, _, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt)
+        _, _, _, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt,
+                                          args.kv_cache)
     tot_t, tot_b, tot_n = 0.0, 0, 0
     for _ in range(args.steps):
-        t, b, n, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt)
+        t, b, n, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt,
+                                          args.kv_cache)
         tot_t, tot_b, tot_n = tot_t + t, tot_b + b, tot_n + n
     gbs = tot_b / tot_t / 1e9
     sample = (f"{tot_n} whole sequences (all {w.num_q_heads} q heads each) of the {name} batch, "
@@ -245,7 +266,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": workload_config(name, plan),
+            "config": workload_config(name, plan, args.kv_cache),
             "seq_steps_per_s": tot_n / tot_t,
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -255,10 +276,15 @@ def run_reference(args, rank, world):
 METRIC = "paged-decode attention achieved HBM GB/s (% of GB300 peak); seq-steps/s"
 
 
-def workload_config(name, plan):
+def workload_config(name, plan, kv_cache="16bit"):
     w = workloads.WORKLOADS[name]
-    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), int((plan.slot_mapping >= 0).sum()))
-    return {"workload": f"{name}: {w.description}", "num_seqs": int(len(plan.seq_lens)),
+    fp8 = kv_cache == "fp8"
+    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), int((plan.slot_mapping >= 0).sum()),
+                           1 if fp8 else 2)
+    cache = (f"fp8 e4m3, k_scale {workloads.FP8_K_SCALE}, v_scale {workloads.FP8_V_SCALE}" if fp8
+             else ("f16" if w.dtype == workloads.F16 else "bf16"))
+    return {"workload": f"{name}: {w.description}" + (" [FP8 E4M3 cache]" if fp8 else ""),
+            "kv_cache": cache, "num_seqs": int(len(plan.seq_lens)),
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
             "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_seq_len": float(np.mean(plan.seq_lens)), "cow_pairs": int(len(plan.cow_pairs)),
@@ -279,10 +305,11 @@ def run_ours(args, rank, local_rank, world):
     w = workloads.WORKLOADS[name]
     seed = args.seed + 1000 * rank
     plan = stepmod.plan_step(name, seed, args.variant)
-    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev)
+    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev, args.kv_cache)
     st = stepmod.DecodeStep(name, plan, pool, q, k, v, dev)
     n_tokens = int((plan.slot_mapping >= 0).sum())
-    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens)
+    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens,
+                           1 if st.fp8 else 2)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(3, args.warmup)):
@@ -309,7 +336,7 @@ def run_ours(args, rank, local_rank, world):
     for i in range(K):
         if st.cow_pairs is not None:
             binding.pa_copy_blocks([st.pool], st.cow_pairs)
-        binding.pa_reshape_and_cache(st.key_new, st.value_new, st.pool, st.slot_mapping)
+        st.reshape()
         if i % EV_EVERY == 0:
             ev[i // EV_EVERY][0].record(stream)
             st.decode()
@@ -357,12 +384,12 @@ def run_ours(args, rank, local_rank, world):
     achieved = ab["decode"] / (dec_ms / 1e3) / 1e9
     value = world * ab["step"] * K / t_s / 1e9
     seq_steps = world * len(plan.seq_lens) * K / t_s
-    traffic = traffic_record(name)
+    traffic = traffic_record(name, args.kv_cache)
 
     # CPU baseline: the oracle, single-threaded, on a bounded sample.
-    pool_bits, q_bits = st.pool.view(torch.int16).cpu().numpy().view(np.uint16), \
-        st.query.view(torch.int16).cpu().numpy().view(np.uint16)
-    ot, ob, on, _ = oracle_sample_time(name, plan, pool_bits, q_bits, args.cpu_budget)
+    pool_bits, q_bits = pool_host_bits(st.pool), pool_host_bits(st.query)
+    ot, ob, on, _ = oracle_sample_time(name, plan, pool_bits, q_bits, args.cpu_budget, 0,
+                                       args.kv_cache)
     del pool_bits
 
     line = {
@@ -371,7 +398,7 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
         "data": "synthetic (seeded N(0,1) values, seeded block placement)",
-        "config": dict(workload_config(name, plan),
+        "config": dict(workload_config(name, plan, args.kv_cache),
                        kv_l2_policy="normal (blocks shared)" if st.flags else "evict-first (no block shared)"),
         "seq_steps_per_s": seq_steps,
         "pct_of_nominal_8TBps": 100.0 * value / NOMINAL_HBM_GBS,
@@ -380,7 +407,8 @@ def run_ours(args, rank, local_rank, world):
                         "sampled_launches": len(decode_ms)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "pa_decode (paged_decode_kernel + paged_decode_reduce_kernel)",
+                     "kernel": ("pa_decode_fp8" if st.fp8 else "pa_decode")
+                               + " (paged_decode_kernel + paged_decode_reduce_kernel)",
                      "peak_source": peak_note, "bytes_per_launch": ab["decode"]},
         "e2e": {"value": world * ab["step"] * ke / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -402,6 +430,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama13b", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--variant", default="literal", choices=["literal", "fork"])
+    ap.add_argument("--kv-cache", default="16bit", choices=["16bit", "fp8"],
+                    help="cache element type: the workload's 16-bit type, or E4M3 codes")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the cpu_baseline sample")

@@ -32,6 +32,13 @@
  *   pa_get_device_error() returns and clears.
  * - block_size must be a positive multiple of 16 ([book] §4.3.4: the CUDA
  *   backends require block_size % 16 == 0).
+ * - FP8 cache (the *_fp8 calls): the same pool shape with 1-byte elements,
+ *   each an OCP E4M3 code (1 sign, 4 exponent bits with bias 7, 3 fraction
+ *   bits; no infinities; 0x7F / 0xFF are NaN; largest finite 448). A K code
+ *   c stands for e4m3(c) * k_scale and a V code for e4m3(c) * v_scale, one
+ *   scale per tensor. The pages name a lower-precision KV cache only as a
+ *   capacity lever ([book] §4.8); the format, the per-tensor scales and the
+ *   rounding below are the reading this library takes.
  */
 #ifndef PAGED_KV_CACHE_PA_H
 #define PAGED_KV_CACHE_PA_H
@@ -58,6 +65,9 @@ typedef struct CUstream_st *pa_stream_t;
 /* Element types of Q, K, V and the output. */
 #define PA_F16   0
 #define PA_BF16  1
+/* Element type of an FP8 pool (pa_copy_blocks only; the FP8 calls below take
+ * the 16-bit type of their activations as `dtype`). */
+#define PA_FP8_E4M3  2
 
 /* pa_decode flags. */
 #define PA_DECODE_SHARED_BLOCKS 1u  /* some physical block appears in more than one
@@ -198,6 +208,51 @@ int pa_decode_static_scratch(void *out, const void *query, const void *kv_cache,
                              unsigned flags, pa_stream_t stream);
 
 /*
+ * pa_reshape_and_cache_fp8 — pa_reshape_and_cache into an FP8 pool: the same
+ * slots and skipping rules, with every element quantised on the way in.
+ *
+ *   key, value    device, [num_tokens][num_kv_heads][head_size], dtype
+ *                 (PA_F16 or PA_BF16)
+ *   kv_cache      device, the layer's FP8 pool (1-byte elements)
+ *   k_scale, v_scale  finite and > 0
+ * The code stored for a K element x is the E4M3 value nearest to the IEEE
+ * fp32 quotient x / k_scale (ties to the even code); quotients beyond +-448
+ * store +-448 (saturation); NaN stores a NaN code. V likewise with v_scale.
+ * Returns PA_OK or a PA_ERR_* code.
+ */
+int pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
+                             const int32_t *slot_mapping, int num_tokens,
+                             int num_blocks, int block_size, int num_kv_heads,
+                             int head_size, int dtype, float k_scale, float v_scale,
+                             pa_stream_t stream);
+
+/* Workspace bytes pa_decode_fp8 needs (same rules as pa_decode_workspace_size). */
+int pa_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                 int head_size, int block_size, int dtype,
+                                 size_t *bytes);
+
+/*
+ * pa_decode_fp8 — pa_decode over an FP8 pool. Arguments, launch behaviour
+ * and guarantees are those of pa_decode (dtype is the type of query and
+ * out), plus k_scale and v_scale (finite, > 0) as in the conventions. The
+ * workspace is sized by pa_decode_fp8_workspace_size.
+ *
+ * Result: the attention of pa_decode with every cached element replaced by
+ * its value e4m3(c) * scale. Codes are widened to dtype exactly (every E4M3
+ * value is an fp16 and a bf16 value); k_scale is applied to the fp32 score
+ * scale and v_scale at the final normalisation. A NaN code in a token that
+ * is attended to makes that output row NaN.
+ */
+int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
+                  const int32_t *block_tables, int max_blocks_per_seq,
+                  const int32_t *seq_lens, int num_seqs, float scale,
+                  int num_q_heads, int num_kv_heads, int head_size,
+                  int num_blocks, int block_size, int dtype,
+                  float k_scale, float v_scale,
+                  void *workspace, size_t workspace_bytes, unsigned flags,
+                  pa_stream_t stream);
+
+/*
  * pa_copy_blocks — copy-on-write clones of whole physical blocks
  * ([digest] "写时复制": a shared block is cloned before a write and the
  * writer's table retargeted; [lecture] §4.3 steps: allocate Q, copy P into
@@ -207,6 +262,9 @@ int pa_decode_static_scratch(void *out, const void *query, const void *kv_cache,
  *   kv_caches      HOST array of num_layers device pointers, one pool each;
  *                  1 <= num_layers <= 512
  *   src_dst_pairs  device, [num_pairs][2] int32 (src, dst)
+ *   dtype          PA_F16, PA_BF16 or PA_FP8_E4M3 (the pools' element type;
+ *                  a token's row, num_kv_heads * head_size elements, must be
+ *                  a multiple of 16 bytes)
  * For every pair and layer, kv_cache[c][dst] = kv_cache[c][src] for c in
  * {0, 1}: all block_size slots, all heads, bit for bit. Preconditions: ids in
  * [0, num_blocks); no dst appears twice; no dst is also a src. A pair that

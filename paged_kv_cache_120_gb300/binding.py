@@ -25,6 +25,7 @@ PA_ERR_OUT_OF_BLOCKS = -5
 PA_ERR_NOT_FOUND = -6
 PA_F16 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 PA_DECODE_SHARED_BLOCKS = 1
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SLOT = 2
@@ -44,6 +45,10 @@ SIGNATURES = [
     ("pa_decode_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     ("pa_decode", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
     ("pa_decode_static_scratch", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _u, _vp]),
+    ("pa_reshape_and_cache_fp8", _i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _f, _vp]),
+    ("pa_decode_fp8_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    ("pa_decode_fp8", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _f, _f,
+                           _vp, _sz, _u, _vp]),
     ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_get_device_error", _i, [_ip]),
     ("pa_alloc_create", _vp, [_i, _i, _i32p]),
@@ -107,6 +112,21 @@ def _dtype_code(t) -> int:
     if t.dtype == torch.bfloat16:
         return PA_BF16
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _pool_code(t) -> int:
+    """Element type of a pool: 16-bit, or E4M3 held as uint8 / float8_e4m3fn."""
+    import torch
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return PA_FP8_E4M3
+    return _dtype_code(t)
+
+
+def _fp8_pool(t, name):
+    import torch
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), not {t.dtype}")
+    return _dev(t, name)
 
 
 def _dev(t, name):
@@ -177,13 +197,55 @@ def pa_decode_static_scratch(out, query, kv_cache, block_tables, seq_lens, scale
         _dtype_code(kv_cache), int(flags), _stream(stream)))
 
 
+def pa_reshape_and_cache_fp8(key, value, kv_cache, slot_mapping, k_scale, v_scale,
+                             stream=None) -> None:
+    """key/value [T, Hkv, D] fp16/bf16; kv_cache (2, NB, B, Hkv, D) of E4M3 codes
+    (uint8 or float8_e4m3fn); slot_mapping [T] int32."""
+    _, nb, bs, hkv, d = kv_cache.shape
+    _check(lib().pa_reshape_and_cache_fp8(
+        _dev(key, "key"), _dev(value, "value"), _fp8_pool(kv_cache, "kv_cache"),
+        _dev(slot_mapping, "slot_mapping"), int(slot_mapping.shape[0]), nb, bs, hkv, d,
+        _dtype_code(key), float(k_scale), float(v_scale), _stream(stream)))
+
+
+def pa_decode_fp8_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                 dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pa_decode_fp8_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                              block_size, dtype, ctypes.byref(out)))
+    return out.value
+
+
+def decode_fp8_workspace(query, kv_cache):
+    """A correctly sized uint8 workspace tensor for pa_decode_fp8 on this batch shape."""
+    import torch
+    s, hq, d = query.shape
+    _, _, bs, hkv, _ = kv_cache.shape
+    n = pa_decode_fp8_workspace_size(s, hq, hkv, d, bs, _dtype_code(query))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=query.device)
+
+
+def pa_decode_fp8(out, query, kv_cache, block_tables, seq_lens, scale, k_scale, v_scale,
+                  workspace, flags=0, stream=None) -> None:
+    """pa_decode over an E4M3 pool; out/query fp16 or bf16 [S, Hq, D]."""
+    s, hq, d = query.shape
+    _, nb, bs, hkv, _ = kv_cache.shape
+    _check(lib().pa_decode_fp8(
+        _dev(out, "out"), _dev(query, "query"), _fp8_pool(kv_cache, "kv_cache"),
+        _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
+        _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
+        _dtype_code(query), float(k_scale), float(v_scale), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), int(flags), _stream(stream)))
+
+
 def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:
-    """kv_caches: list of per-layer pools; src_dst_pairs [N, 2] int32 CUDA tensor."""
+    """kv_caches: list of per-layer pools (fp16, bf16, or E4M3 codes as uint8 /
+    float8_e4m3fn); src_dst_pairs [N, 2] int32 CUDA tensor."""
     _, nb, bs, hkv, d = kv_caches[0].shape
     ptrs = (ctypes.c_void_p * len(kv_caches))(*[_dev(c, "kv_cache").value for c in kv_caches])
     _check(lib().pa_copy_blocks(ptrs, len(kv_caches), _dev(src_dst_pairs, "src_dst_pairs"),
                                 int(src_dst_pairs.shape[0]), nb, bs, hkv, d,
-                                _dtype_code(kv_caches[0]), _stream(stream)))
+                                _pool_code(kv_caches[0]), _stream(stream)))
 
 
 def pa_get_device_error() -> int:

@@ -26,6 +26,18 @@
 //    on physical block ids, so outputs are bit-identical under any
 //    permutation of block placement.
 //  * reshape_and_cache and copy_blocks are bit copies with 16-byte accesses.
+//  * FP8 cache (OCP E4M3 codes with one scale for K and one for V; a reading
+//    of the book's "lower-precision KV cache", §4.8): the same pipeline moves
+//    half the bytes. Codes are widened to fp16/bf16 in registers (exactly:
+//    every E4M3 value is representable in both), so the MMAs, the softmax and
+//    the split-K records are those of the 16-bit path; k_scale folds into the
+//    score scale and v_scale into the final normalisation. Because a dot
+//    product may sum its terms in any order, the head dimension is permuted
+//    (the same permutation on Q and K) so that every thread reads its K bytes
+//    as whole 16-byte chunks; V's head-dimension rows are permuted too, and
+//    the permutation is undone when O is stored.
+//  * reshape_and_cache_fp8 quantises with one IEEE fp32 division per element
+//    and a saturating round-to-nearest-even conversion.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -194,6 +206,67 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x)
     return y;
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+// Byte permute: result byte i = byte sel_i of the 8-byte value {b, a}.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Two E4M3 codes (low 16 bits of x: low byte -> low half) to an fp16 pair.
+// Exact: every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t x)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(d)
+        : "r"(x));
+    return d;
+}
+
+// The same for the high 16 bits of x.
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t x)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, hi;\n\t}"
+        : "=r"(d)
+        : "r"(x));
+    return d;
+}
+
+// The E4M3 codes in bytes 1 and 3 of x to a bf16 pair (byte 1 -> low half);
+// bytes 0 and 2 are ignored. A code s.eeee.fff placed as bf16 bits
+// s.0000eeee.fff0000 is the code's value times 2^-120, E4M3 subnormals
+// included (they become bf16 subnormals); one exact multiplication by 2^120
+// restores the value. bf16 multiplication keeps subnormal inputs.
+__device__ __forceinline__ uint32_t e4m3_b13_to_bf16x2(uint32_t x)
+{
+    const uint32_t bits = (x & 0x80008000u) | ((x >> 4) & 0x07F007F0u);
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(bits), "r"(0x7B807B80u));  // 2^120, 2^120
+    return d;
+}
+
 template <bool BF16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1)
@@ -256,6 +329,9 @@ __device__ __forceinline__ uint16_t to_elem(float x)
 #ifndef PA_DECODE_WARPS_WIDE
 #define PA_DECODE_WARPS_WIDE 8
 #endif
+#ifndef PA_DECODE_STAGES_FP8
+#define PA_DECODE_STAGES_FP8 2
+#endif
 // Warps per CTA, each an independent pipeline: 12 for 8-column query tiles;
 // 16-column tiles need ~195 registers per thread, so 8 warps fit an SM.
 template <int NT>
@@ -263,16 +339,40 @@ constexpr int decode_warps()
 {
     return NT == 1 ? PA_DECODE_WARPS : PA_DECODE_WARPS_WIDE;
 }
-constexpr int kStages = PA_DECODE_STAGES;  // TMA ring depth per warp
+// TMA ring depth per warp. An FP8 tile is half the bytes of a 16-bit one, so
+// the FP8 pipelines keep two in flight to hold the same bytes in flight.
+template <bool FP8>
+constexpr int decode_stages()
+{
+    return FP8 ? PA_DECODE_STAGES_FP8 : PA_DECODE_STAGES;
+}
 constexpr int kTile = 16;       // tokens per tile (the MMA's M)
 constexpr int kMaxSeqs = 4096;  // sequences per pa_decode call (prefix lives in smem)
 
-template <int D>
+// One pipeline stage: a 16-token tile of one kv head, K rows then V rows.
+// 16-bit cache: D/64 TMA boxes [K|V][16 rows][64 elements = 128 B], 128-byte
+// swizzle. FP8 cache: one box [K|V][16 rows][D bytes]; D = 128 gives 128-byte
+// rows (128-byte swizzle), D = 64 gives 64-byte rows (64-byte swizzle).
+template <int D, bool FP8 = false>
 struct TileGeo {
-    static constexpr int kBoxes = D / 64;             // 64-element (128-byte) swizzle boxes
-    static constexpr int kBoxBytes = 4096;            // [K|V][16 rows][128 B]
+    static constexpr int kBoxes = FP8 ? 1 : D / 64;
+    static constexpr int kBoxElems = FP8 ? D : 64;          // innermost box extent
+    static constexpr int kRowBytes = FP8 ? D : 128;
+    static constexpr int kBoxBytes = 2 * kTile * kRowBytes;
+    static constexpr int kVOffset = kTile * kRowBytes;      // V rows inside a box
     static constexpr int kStageBytes = kBoxes * kBoxBytes;
 };
+
+// Byte offset of 16-byte chunk c of row r inside an FP8 half-tile, after the
+// TMA swizzle (128-byte: chunk ^= r mod 8; 64-byte: chunk ^= (r / 2) mod 4).
+template <int D>
+__device__ __forceinline__ uint32_t fp8_off(int r, int c)
+{
+    if constexpr (D == 128)
+        return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+    else
+        return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
 
 struct DecodeParams {
     void *out;
@@ -293,7 +393,8 @@ struct DecodeParams {
     int num_blocks;
     int block_size;
     int tiles_per_block;  // block_size / 16
-    float scale_log2;     // scale * log2(e): scores live in base 2
+    float scale_log2;     // scale * log2(e) (* k_scale for an FP8 cache): scores in base 2
+    float v_scale;        // FP8 cache: value of a V code's unit; 1 otherwise
     int kv_stream;        // 1: stream K/V with the L2 evict-first hint (no block shared)
     int total_warps;      // grid * warps per CTA
 };
@@ -304,11 +405,12 @@ constexpr int record_floats()
     return NT * 8 * (D + 2);  // m[GP], l[GP], O[GP][D]; only live query columns are written
 }
 
-template <int D, int WARPS>
+template <int D, int WARPS, bool FP8>
 inline size_t decode_smem_bytes(int num_seqs)
 {
+    constexpr int kStages = decode_stages<FP8>();
     size_t b = 1024;  // alignment slack for the 1024-byte swizzle atoms
-    b += (size_t)WARPS * kStages * TileGeo<D>::kStageBytes;
+    b += (size_t)WARPS * kStages * TileGeo<D, FP8>::kStageBytes;
     b += (size_t)WARPS * kStages * sizeof(uint64_t);
     b += (size_t)(num_seqs + 1) * sizeof(long long);
     b += (size_t)num_seqs * sizeof(int);
@@ -367,16 +469,23 @@ __device__ __forceinline__ int owner_of(long long u, long long N, long long K)
 }
 
 // Main decode kernel. Template: head size D, N-tiles of 8 query heads NT,
-// element type. One CTA = decode_warps<NT>() independent warp pipelines.
-template <int D, int NT, bool BF16>
+// element type of Q and the output, FP8 cache or not. One CTA =
+// decode_warps<NT>() independent warp pipelines.
+template <int D, int NT, bool BF16, bool FP8>
 __global__ void __launch_bounds__(decode_warps<NT>() * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
+    using Geo = TileGeo<D, FP8>;
     constexpr int kWarps = decode_warps<NT>();
+    constexpr int kStages = decode_stages<FP8>();
     constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of V^T P^T
     constexpr int GP = NT * 8;
-    constexpr int STAGE = TileGeo<D>::kStageBytes;
+    constexpr int STAGE = Geo::kStageBytes;
     constexpr int REC = record_floats<D, NT>();
+    // FP8 fragment geometry: each thread reads CPT 16-byte K chunks per row
+    // and VB bytes of V per row (see the tile loop).
+    constexpr int CPT = D / 64;
+    constexpr int VB = D / 8;
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ long long warp_sums[kWarps];
@@ -523,9 +632,9 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
             const uint32_t bar = my_bar0 + st * 8;
             mbar_expect_tx(bar, STAGE);
 #pragma unroll
-            for (int bx = 0; bx < D / 64; ++bx)
-                tma_load_5d_hint(my_stage0 + st * STAGE + bx * TileGeo<D>::kBoxBytes, &kv_map, bar,
-                                 bx * 64, h, t0, phys, 0, kv_policy);
+            for (int bx = 0; bx < Geo::kBoxes; ++bx)
+                tma_load_5d_hint(my_stage0 + st * STAGE + bx * Geo::kBoxBytes, &kv_map, bar,
+                                 bx * Geo::kBoxElems, h, t0, phys, 0, kv_policy);
         }
     };
 
@@ -564,8 +673,23 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
             const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qbase + (long long)col * D);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-                qf[nt][kk][0] = live ? __ldg(qrow + 8 * kk + tig) : 0u;
-                qf[nt][kk][1] = live ? __ldg(qrow + 8 * kk + 4 + tig) : 0u;
+                if constexpr (FP8) {
+                    // Permuted k-step kk = 4j + w: dims 16c + 4w + {0..3} of
+                    // chunk c = CPT tig + j, the same dims the K fragments hold.
+                    const int c = CPT * tig + (kk >> 2), w = kk & 3;
+                    const uint2 u = live ? __ldg(reinterpret_cast<const uint2 *>(qrow) + 4 * c + w)
+                                         : make_uint2(0u, 0u);
+                    if constexpr (BF16) {
+                        qf[nt][kk][0] = prmt(u.x, u.y, 0x5410u);  // dims +0, +2
+                        qf[nt][kk][1] = prmt(u.x, u.y, 0x7632u);  // dims +1, +3
+                    } else {
+                        qf[nt][kk][0] = u.x;  // dims +0, +1
+                        qf[nt][kk][1] = u.y;  // dims +2, +3
+                    }
+                } else {
+                    qf[nt][kk][0] = live ? __ldg(qrow + 8 * kk + tig) : 0u;
+                    qf[nt][kk][1] = live ? __ldg(qrow + 8 * kk + 4 + tig) : 0u;
+                }
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -606,12 +730,21 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
                 for (int e = 0; e < 2; ++e) {
                     const int col = nt * 8 + 2 * tig + e;
                     if (col < p.tile_q) {
-                        const float inv = 1.f / lsum[nt][e];
                         uint16_t *row = out + (long long)col * D;
+                        if constexpr (FP8) {
+                            // Rows g / g+8 of m-tile mt are dims VB g + 2mt / + 1.
+                            const float inv = p.v_scale / lsum[nt][e];
+                            uint32_t *row2 = reinterpret_cast<uint32_t *>(row + VB * g);
 #pragma unroll
-                        for (int mt = 0; mt < KS; ++mt) {
-                            row[16 * mt + g] = to_elem<BF16>(acc[mt][nt][e] * inv);
-                            row[16 * mt + g + 8] = to_elem<BF16>(acc[mt][nt][2 + e] * inv);
+                            for (int mt = 0; mt < KS; ++mt)
+                                row2[mt] = pack2<BF16>(acc[mt][nt][e] * inv, acc[mt][nt][2 + e] * inv);
+                        } else {
+                            const float inv = 1.f / lsum[nt][e];
+#pragma unroll
+                            for (int mt = 0; mt < KS; ++mt) {
+                                row[16 * mt + g] = to_elem<BF16>(acc[mt][nt][e] * inv);
+                                row[16 * mt + g + 8] = to_elem<BF16>(acc[mt][nt][2 + e] * inv);
+                            }
                         }
                     }
                 }
@@ -638,10 +771,18 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
                             rec[GP + col] = lsum[nt][e];
                         }
                         float *ro = rec + 2 * GP + col * D;
+                        if constexpr (FP8) {
+                            float2 *ro2 = reinterpret_cast<float2 *>(ro + VB * g);
 #pragma unroll
-                        for (int mt = 0; mt < KS; ++mt) {
-                            ro[16 * mt + g] = acc[mt][nt][e];
-                            ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
+                            for (int mt = 0; mt < KS; ++mt)
+                                ro2[mt] = make_float2(acc[mt][nt][e] * p.v_scale,
+                                                      acc[mt][nt][2 + e] * p.v_scale);
+                        } else {
+#pragma unroll
+                            for (int mt = 0; mt < KS; ++mt) {
+                                ro[16 * mt + g] = acc[mt][nt][e];
+                                ro[16 * mt + g + 8] = acc[mt][nt][2 + e];
+                            }
                         }
                     }
                 }
@@ -678,11 +819,12 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
         if (valid < kTile) {
             // Rows past the sequence end hold stale data (possibly NaN): zero the
             // V rows so that p = 0 times them stays 0. K rows are masked below.
-            const int per_box = (kTile - valid) * 8;
-            for (int z = lane; z < per_box * (D / 64); z += 32) {
+            constexpr int CPR = Geo::kRowBytes / 16;  // 16-byte chunks per row
+            const int per_box = (kTile - valid) * CPR;
+            for (int z = lane; z < per_box * Geo::kBoxes; z += 32) {
                 const int bx = z / per_box, rem = z - bx * per_box;
-                const int r = valid + (rem >> 3), c = rem & 7;
-                sts128_zero(sbuf + bx * TileGeo<D>::kBoxBytes + 2048 + r * 128 + c * 16);
+                const int r = valid + rem / CPR, c = rem % CPR;
+                sts128_zero(sbuf + bx * Geo::kBoxBytes + Geo::kVOffset + r * Geo::kRowBytes + c * 16);
             }
             fence_proxy_async();
             __syncwarp();
@@ -690,23 +832,93 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
 
         // S^T[16 tokens][8*NT queries] = K Q^T. All K fragments are loaded
         // first, and the k-steps alternate between two accumulators, so the
-        // MMA chain is half as long as the head dimension.
+        // MMA chain is half as long as the head dimension. V^T fragments do
+        // not depend on P: they are loaded up front as well.
         uint32_t kf[KS][4];
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            const int cg = 2 * kk + k_hi;
-            ldsm_x4(sbuf + (cg >> 3) * TileGeo<D>::kBoxBytes + k_row * 128 +
-                        (((cg & 7) ^ (k_row & 7)) << 4),
-                    kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
-        }
-        // V^T fragments do not depend on P: load them up front as well.
         uint32_t vf[KS][4];
+        if constexpr (FP8) {
+            // K rows g and g+8, chunks c = CPT tig + j, widened in registers.
+            // Word w of chunk j holds the dims of permuted k-step 4j + w.
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int cg = 2 * mt + v_hi;
-            ldsm_x4_t(sbuf + 2048 + (cg >> 3) * TileGeo<D>::kBoxBytes + v_row * 128 +
-                          (((cg & 7) ^ (v_row & 7)) << 4),
-                      vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+            for (int j = 0; j < CPT; ++j) {
+                const int c = CPT * tig + j;
+                const uint4 r0 = lds128(sbuf + fp8_off<D>(g, c));
+                const uint4 r1 = lds128(sbuf + fp8_off<D>(g + 8, c));
+                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+                const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int kk = 4 * j + w;
+                    if constexpr (BF16) {
+                        kf[kk][0] = e4m3_b13_to_bf16x2(w0[w] << 8);  // dims +0, +2
+                        kf[kk][1] = e4m3_b13_to_bf16x2(w1[w] << 8);
+                        kf[kk][2] = e4m3_b13_to_bf16x2(w0[w]);       // dims +1, +3
+                        kf[kk][3] = e4m3_b13_to_bf16x2(w1[w]);
+                    } else {
+                        kf[kk][0] = e4m3x2_lo_to_f16x2(w0[w]);       // dims +0, +1
+                        kf[kk][1] = e4m3x2_lo_to_f16x2(w1[w]);
+                        kf[kk][2] = e4m3x2_hi_to_f16x2(w0[w]);       // dims +2, +3
+                        kf[kk][3] = e4m3x2_hi_to_f16x2(w1[w]);
+                    }
+                }
+            }
+            // V^T: this thread's dims VB g .. VB g + VB - 1 of tokens 2tig,
+            // 2tig+1, 2tig+8, 2tig+9; m-tile mt takes dims VB g + 2mt (row g)
+            // and VB g + 2mt + 1 (row g+8), paired across tokens with prmt.
+            const uint32_t vbase = sbuf + Geo::kVOffset;
+            uint32_t vw[4][VB / 4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int r = 2 * tig + (t & 1) + (t >> 1) * 8;
+                if constexpr (D == 128) {
+                    const uint4 x = lds128(vbase + fp8_off<D>(r, g));
+                    vw[t][0] = x.x;
+                    vw[t][1] = x.y;
+                    vw[t][2] = x.z;
+                    vw[t][3] = x.w;
+                } else {
+                    const uint2 x = lds64(vbase + fp8_off<D>(r, g >> 1) + ((g & 1) << 3));
+                    vw[t][0] = x.x;
+                    vw[t][1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int wi = mt >> 1;
+                if constexpr (BF16) {
+                    // Byte d (resp. d + 1) of the two tokens into bytes 1 and 3.
+                    const uint32_t s0 = (mt & 1) ? 0x6020u : 0x4000u;
+                    const uint32_t s1 = (mt & 1) ? 0x7030u : 0x5010u;
+                    vf[mt][0] = e4m3_b13_to_bf16x2(prmt(vw[0][wi], vw[1][wi], s0));
+                    vf[mt][1] = e4m3_b13_to_bf16x2(prmt(vw[0][wi], vw[1][wi], s1));
+                    vf[mt][2] = e4m3_b13_to_bf16x2(prmt(vw[2][wi], vw[3][wi], s0));
+                    vf[mt][3] = e4m3_b13_to_bf16x2(prmt(vw[2][wi], vw[3][wi], s1));
+                } else {
+                    // {t.d, t'.d, t.d+1, t'.d+1}: low pair -> row g, high -> row g+8.
+                    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                    const uint32_t x01 = prmt(vw[0][wi], vw[1][wi], sel);
+                    const uint32_t x23 = prmt(vw[2][wi], vw[3][wi], sel);
+                    vf[mt][0] = e4m3x2_lo_to_f16x2(x01);
+                    vf[mt][1] = e4m3x2_hi_to_f16x2(x01);
+                    vf[mt][2] = e4m3x2_lo_to_f16x2(x23);
+                    vf[mt][3] = e4m3x2_hi_to_f16x2(x23);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const int cg = 2 * kk + k_hi;
+                ldsm_x4(sbuf + (cg >> 3) * Geo::kBoxBytes + k_row * 128 +
+                            (((cg & 7) ^ (k_row & 7)) << 4),
+                        kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int cg = 2 * mt + v_hi;
+                ldsm_x4_t(sbuf + 2048 + (cg >> 3) * Geo::kBoxBytes + v_row * 128 +
+                              (((cg & 7) ^ (v_row & 7)) << 4),
+                          vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+            }
         }
 
         float sc[NT][4], sc2[NT][4];
@@ -1016,6 +1228,61 @@ __global__ void __launch_bounds__(kReshapeThreads)
     }
 }
 
+// Two fp32 values to E4M3 codes (saturating, nearest-even); `lo` goes to the
+// low byte of the result.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 r;\n\tcvt.rn.satfinite.e4m3x2.f32 r, %1, %2;\n\t"
+        "cvt.u32.u16 %0, r;\n\t}"
+        : "=r"(d)
+        : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Eight 16-bit elements to eight codes of element / scale (one IEEE fp32
+// division each).
+template <bool BF16>
+__device__ __forceinline__ uint2 quantize8(const uint4 x, float scale)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2<BF16>(w[i]);
+        c[i] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// FP8 write path, grid (token, row chunk) as above: each thread quantises 8
+// elements of the token's K row and 8 of its V row (16 bytes in, 8 out).
+template <bool BF16>
+__global__ void __launch_bounds__(kReshapeThreads)
+    reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                                 uint2 *__restrict__ kv, const int32_t *__restrict__ slots,
+                                 int row_vecs, long long num_slots, long long half_vecs,
+                                 float k_scale, float v_scale)
+{
+    grid_launch_dependents();
+    const int t = blockIdx.x;
+    const int i = blockIdx.y * kReshapeThreads + threadIdx.x;
+    const long long slot = slots[t];
+    if (slot < 0)
+        return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0 && blockIdx.y == 0)
+            raise_error(PA_DEVERR_SLOT);
+        return;
+    }
+    if (i < row_vecs) {
+        const uint4 k = __ldg(key + (long long)t * row_vecs + i);
+        const uint4 v = __ldg(value + (long long)t * row_vecs + i);
+        kv[slot * row_vecs + i] = quantize8<BF16>(k, k_scale);
+        kv[half_vecs + slot * row_vecs + i] = quantize8<BF16>(v, v_scale);
+    }
+}
+
 constexpr int kMaxLayers = 512;
 struct LayerPtrs {
     uint4 *p[kMaxLayers];
@@ -1090,11 +1357,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // {K, V}: one 16-token tile of one head, K and V together, 128-byte swizzled.
 struct MapKey {
     const void *ptr;
-    int d, h, b, nb, dev;
+    int d, h, b, nb, dev, fp8;
 };
 
+// FP8 pools use 1-byte elements and a box of the whole head (D bytes) with
+// the swizzle that matches that row length.
 int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_size,
-                  int num_kv_heads, int head_size, int device)
+                  int num_kv_heads, int head_size, int device, bool fp8)
 {
     static std::mutex mu;
     static MapKey keys[16];
@@ -1104,7 +1373,7 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
     for (int i = 0; i < used; ++i) {
         const MapKey &k = keys[i];
         if (k.ptr == kv && k.d == head_size && k.h == num_kv_heads && k.b == block_size &&
-            k.nb == num_blocks && k.dev == device) {
+            k.nb == num_blocks && k.dev == device && k.fp8 == (int)fp8) {
             *map = maps[i];
             return PA_OK;
         }
@@ -1112,22 +1381,24 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
     auto enc = tensor_map_encoder();
     if (!enc)
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-    const cuuint64_t e = 2;  // bytes per element
+    const cuuint64_t e = fp8 ? 1 : 2;  // bytes per element
     cuuint64_t dims[5] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
                           (cuuint64_t)num_blocks, 2};
     cuuint64_t strides[4] = {head_size * e, (cuuint64_t)num_kv_heads * head_size * e,
                              (cuuint64_t)block_size * num_kv_heads * head_size * e,
                              (cuuint64_t)num_blocks * block_size * num_kv_heads * head_size * e};
-    cuuint32_t box[5] = {64, 1, (cuuint32_t)kTile, 1, 2};
+    cuuint32_t box[5] = {fp8 ? (cuuint32_t)head_size : 64u, 1, (cuuint32_t)kTile, 1, 2};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUtensorMapSwizzle swz =
+        (fp8 && head_size == 64) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     CUtensorMap m;
-    CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void *>(kv), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 5,
+                     const_cast<void *>(kv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     const int slot = used < 16 ? used++ : (next++ % 16);
-    keys[slot] = MapKey{kv, head_size, num_kv_heads, block_size, num_blocks, device};
+    keys[slot] = MapKey{kv, head_size, num_kv_heads, block_size, num_blocks, device, (int)fp8};
     maps[slot] = m;
     *map = m;
     return PA_OK;
@@ -1170,14 +1441,23 @@ struct DecodePlan {
     size_t total() const { return prefix_bytes + task_bytes + warp_record_bytes; }
 };
 
-template <int D, int NT, bool BF16>
-void pick_kernels(DecodePlan &pl)
+template <int D, int NT, bool BF16, bool FP8>
+void pick_kernels(DecodePlan &pl, int num_seqs)
 {
-    pl.main_fn = reinterpret_cast<const void *>(&paged_decode_kernel<D, NT, BF16>);
+    pl.main_fn = reinterpret_cast<const void *>(&paged_decode_kernel<D, NT, BF16, FP8>);
     pl.warps = decode_warps<NT>();
     pl.reduce_fn = reinterpret_cast<const void *>(&paged_decode_reduce_kernel<D, NT, BF16>);
     pl.reduce_smem = reduce_smem_bytes<D, NT>();
-    pl.smem = 0;
+    pl.smem = decode_smem_bytes<D, decode_warps<NT>(), FP8>(num_seqs);
+}
+
+template <int D, int NT>
+void pick_kernels(DecodePlan &pl, int num_seqs, bool bf, bool fp8)
+{
+    if (fp8)
+        bf ? pick_kernels<D, NT, true, true>(pl, num_seqs) : pick_kernels<D, NT, false, true>(pl, num_seqs);
+    else
+        bf ? pick_kernels<D, NT, true, false>(pl, num_seqs) : pick_kernels<D, NT, false, false>(pl, num_seqs);
 }
 
 int validate_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
@@ -1201,24 +1481,17 @@ int validate_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int h
 }
 
 int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
-              int dtype)
+              int dtype, bool fp8)
 {
     const int group = num_q_heads / num_kv_heads;
     pl.tile_q = group <= 16 ? group : 16;
     pl.qtiles = group <= 16 ? 1 : group / 16;
     pl.nt = pl.tile_q <= 8 ? 1 : 2;
     const bool bf = dtype == PA_BF16;
-    if (head_size == 64) {
-        if (pl.nt == 1) bf ? pick_kernels<64, 1, true>(pl) : pick_kernels<64, 1, false>(pl);
-        else            bf ? pick_kernels<64, 2, true>(pl) : pick_kernels<64, 2, false>(pl);
-        pl.smem = pl.nt == 1 ? decode_smem_bytes<64, decode_warps<1>()>(num_seqs)
-                             : decode_smem_bytes<64, decode_warps<2>()>(num_seqs);
-    } else {
-        if (pl.nt == 1) bf ? pick_kernels<128, 1, true>(pl) : pick_kernels<128, 1, false>(pl);
-        else            bf ? pick_kernels<128, 2, true>(pl) : pick_kernels<128, 2, false>(pl);
-        pl.smem = pl.nt == 1 ? decode_smem_bytes<128, decode_warps<1>()>(num_seqs)
-                             : decode_smem_bytes<128, decode_warps<2>()>(num_seqs);
-    }
+    if (head_size == 64)
+        pl.nt == 1 ? pick_kernels<64, 1>(pl, num_seqs, bf, fp8) : pick_kernels<64, 2>(pl, num_seqs, bf, fp8);
+    else
+        pl.nt == 1 ? pick_kernels<128, 1>(pl, num_seqs, bf, fp8) : pick_kernels<128, 2>(pl, num_seqs, bf, fp8);
     int dev = 0, sms = 0, occ = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -1251,58 +1524,61 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
 
 using namespace pa;
 
-extern "C" int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
-                                        int head_size, int block_size, int dtype, size_t *bytes)
+namespace {
+
+int workspace_size_impl(const char *fn, int num_seqs, int num_q_heads, int num_kv_heads,
+                        int head_size, int block_size, int dtype, bool fp8, size_t *bytes)
 {
     if (!bytes)
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode_workspace_size: bytes is null");
+        return set_error(PA_ERR_INVALID_ARG, "%s: bytes is null", fn);
     int rc = validate_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size, dtype);
     if (rc != PA_OK)
         return rc;
     DecodePlan pl;
-    rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype);
+    rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype, fp8);
     if (rc != PA_OK)
         return rc;
     *bytes = pl.total();
     return PA_OK;
 }
 
-extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
-                         const int32_t *block_tables, int max_blocks_per_seq,
-                         const int32_t *seq_lens, int num_seqs, float scale, int num_q_heads,
-                         int num_kv_heads, int head_size, int num_blocks, int block_size,
-                         int dtype, void *workspace, size_t workspace_bytes, unsigned flags,
-                         pa_stream_t stream)
+int decode_impl(const char *fn, void *out, const void *query, const void *kv_cache,
+                const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                int num_seqs, float scale, int num_q_heads, int num_kv_heads, int head_size,
+                int num_blocks, int block_size, int dtype, bool fp8, float k_scale, float v_scale,
+                void *workspace, size_t workspace_bytes, unsigned flags, pa_stream_t stream)
 {
     int rc = validate_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size, dtype);
     if (rc != PA_OK)
         return rc;
+    if (fp8 && !(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return set_error(PA_ERR_INVALID_ARG, "%s: k_scale and v_scale must be finite and > 0", fn);
     if (num_seqs == 0)
         return PA_OK;
     if (!out || !query || !kv_cache || !block_tables || !seq_lens || !workspace)
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode: null pointer argument");
+        return set_error(PA_ERR_INVALID_ARG, "%s: null pointer argument", fn);
     if (num_blocks <= 0 || max_blocks_per_seq <= 0)
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode: num_blocks and max_blocks_per_seq must be > 0");
+        return set_error(PA_ERR_INVALID_ARG, "%s: num_blocks and max_blocks_per_seq must be > 0", fn);
     if ((long long)max_blocks_per_seq * block_size > (1LL << 30))
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode: max_blocks_per_seq * block_size too large");
+        return set_error(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq * block_size too large", fn);
     if (!std::isfinite(scale))
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode: scale is not finite");
+        return set_error(PA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
     if (flags & ~PA_DECODE_SHARED_BLOCKS)
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode: unknown flags 0x%x", flags);
+        return set_error(PA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
     if (!aligned(kv_cache, 16) || !aligned(query, 16) || !aligned(out, 16) ||
         !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
-        return set_error(PA_ERR_INVALID_ARG, "pa_decode: misaligned pointer (pool/query/out 16 B, workspace 256 B)");
+        return set_error(PA_ERR_INVALID_ARG, "%s: misaligned pointer (pool/query/out 16 B, workspace 256 B)", fn);
     DecodePlan pl;
-    rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype);
+    rc = make_plan(pl, num_seqs, num_q_heads, num_kv_heads, head_size, dtype, fp8);
     if (rc != PA_OK)
         return rc;
     if (workspace_bytes < pl.total())
-        return set_error(PA_ERR_WORKSPACE, "pa_decode: workspace %zu bytes < %zu needed", workspace_bytes,
+        return set_error(PA_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, workspace_bytes,
                          pl.total());
     int dev = 0;
     cudaGetDevice(&dev);
     CUtensorMap map;
-    rc = encode_kv_map(&map, kv_cache, num_blocks, block_size, num_kv_heads, head_size, dev);
+    rc = encode_kv_map(&map, kv_cache, num_blocks, block_size, num_kv_heads, head_size, dev, fp8);
     if (rc != PA_OK)
         return rc;
 
@@ -1325,7 +1601,8 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     prm.num_blocks = num_blocks;
     prm.block_size = block_size;
     prm.tiles_per_block = block_size / kTile;
-    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.scale_log2 = (fp8 ? scale * k_scale : scale) * 1.4426950408889634f;
+    prm.v_scale = fp8 ? v_scale : 1.f;
     prm.kv_stream = (flags & PA_DECODE_SHARED_BLOCKS) ? 0 : 1;
     prm.total_warps = pl.total_warps;
 
@@ -1333,13 +1610,79 @@ extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
     void *args[] = {&map, &prm};
     cudaError_t e = launch_pdl(pl.main_fn, dim3(pl.grid), dim3(pl.warps * 32), args, pl.smem, s);
     if (e != cudaSuccess)
-        return cuda_fail(e, "pa_decode: main kernel launch");
+        return set_error(PA_ERR_CUDA, "%s: main kernel launch: %s", fn, cudaGetErrorString(e));
     void *red_args[] = {&prm};
     e = launch_pdl(pl.reduce_fn, dim3((pl.total_warps + kReduceWarps - 1) / kReduceWarps),
                    dim3(kReduceWarps * 32), red_args, pl.reduce_smem, s);
     if (e != cudaSuccess)
-        return cuda_fail(e, "pa_decode: reduce kernel launch");
+        return set_error(PA_ERR_CUDA, "%s: reduce kernel launch: %s", fn, cudaGetErrorString(e));
     return PA_OK;
+}
+
+// Checks shared by both write paths; *row_vecs = 8-element groups per row.
+int validate_reshape(const char *fn, const void *key, const void *value, const void *kv_cache,
+                     const int32_t *slot_mapping, int num_tokens, int num_blocks, int block_size,
+                     int num_kv_heads, int head_size, int dtype, long long *row_elems)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return set_error(PA_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
+    if (num_tokens < 0 || num_blocks <= 0 || block_size < kTile || block_size % kTile != 0 ||
+        num_kv_heads <= 0 || head_size <= 0)
+        return set_error(PA_ERR_INVALID_ARG, "%s: bad sizes", fn);
+    if (((long long)num_kv_heads * head_size) % 8 != 0)
+        return set_error(PA_ERR_INVALID_ARG, "%s: num_kv_heads * head_size must be a multiple of 8", fn);
+    *row_elems = (long long)num_kv_heads * head_size;
+    if (*row_elems > (1LL << 32))
+        return set_error(PA_ERR_INVALID_ARG, "%s: row too large", fn);
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!key || !value || !kv_cache || !slot_mapping)
+        return set_error(PA_ERR_INVALID_ARG, "%s: null pointer argument", fn);
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 4))
+        return set_error(PA_ERR_INVALID_ARG, "%s: misaligned pointer (16 B)", fn);
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_size, int block_size, int dtype, size_t *bytes)
+{
+    return workspace_size_impl("pa_decode_workspace_size", num_seqs, num_q_heads, num_kv_heads,
+                               head_size, block_size, dtype, false, bytes);
+}
+
+extern "C" int pa_decode(void *out, const void *query, const void *kv_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int num_seqs, float scale, int num_q_heads,
+                         int num_kv_heads, int head_size, int num_blocks, int block_size,
+                         int dtype, void *workspace, size_t workspace_bytes, unsigned flags,
+                         pa_stream_t stream)
+{
+    return decode_impl("pa_decode", out, query, kv_cache, block_tables, max_blocks_per_seq,
+                       seq_lens, num_seqs, scale, num_q_heads, num_kv_heads, head_size, num_blocks,
+                       block_size, dtype, false, 1.f, 1.f, workspace, workspace_bytes, flags, stream);
+}
+
+extern "C" int pa_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_size, int block_size, int dtype,
+                                            size_t *bytes)
+{
+    return workspace_size_impl("pa_decode_fp8_workspace_size", num_seqs, num_q_heads,
+                               num_kv_heads, head_size, block_size, dtype, true, bytes);
+}
+
+extern "C" int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *seq_lens, int num_seqs, float scale, int num_q_heads,
+                             int num_kv_heads, int head_size, int num_blocks, int block_size,
+                             int dtype, float k_scale, float v_scale, void *workspace,
+                             size_t workspace_bytes, unsigned flags, pa_stream_t stream)
+{
+    return decode_impl("pa_decode_fp8", out, query, kv_cache, block_tables, max_blocks_per_seq,
+                       seq_lens, num_seqs, scale, num_q_heads, num_kv_heads, head_size, num_blocks,
+                       block_size, dtype, true, k_scale, v_scale, workspace, workspace_bytes, flags,
+                       stream);
 }
 
 extern "C" int pa_reshape_and_cache(const void *key, const void *value, void *kv_cache,
@@ -1347,22 +1690,12 @@ extern "C" int pa_reshape_and_cache(const void *key, const void *value, void *kv
                                     int block_size, int num_kv_heads, int head_size, int dtype,
                                     pa_stream_t stream)
 {
-    if (dtype != PA_F16 && dtype != PA_BF16)
-        return set_error(PA_ERR_UNSUPPORTED, "pa_reshape_and_cache: dtype %d", dtype);
-    if (num_tokens < 0 || num_blocks <= 0 || block_size < kTile || block_size % kTile != 0 ||
-        num_kv_heads <= 0 || head_size <= 0)
-        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: bad sizes");
-    if (((long long)num_kv_heads * head_size) % 8 != 0)
-        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: num_kv_heads * head_size must be a multiple of 8");
-    if (num_tokens == 0)
-        return PA_OK;
-    if (!key || !value || !kv_cache || !slot_mapping)
-        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: null pointer argument");
-    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 4))
-        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: misaligned pointer (16 B)");
-    const long long row_vecs = (long long)num_kv_heads * head_size * 2 / 16;
-    if (row_vecs > (1 << 30))
-        return set_error(PA_ERR_INVALID_ARG, "pa_reshape_and_cache: row too large");
+    long long row_elems = 0;
+    int rc = validate_reshape("pa_reshape_and_cache", key, value, kv_cache, slot_mapping, num_tokens,
+                              num_blocks, block_size, num_kv_heads, head_size, dtype, &row_elems);
+    if (rc != PA_OK || num_tokens == 0)
+        return rc;
+    const long long row_vecs = row_elems * 2 / 16;
     const long long num_slots = (long long)num_blocks * block_size;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const dim3 grid(num_tokens, (unsigned)((row_vecs + kReshapeThreads - 1) / kReshapeThreads));
@@ -1375,17 +1708,55 @@ extern "C" int pa_reshape_and_cache(const void *key, const void *value, void *kv
     return PA_OK;
 }
 
+extern "C" int pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
+                                        const int32_t *slot_mapping, int num_tokens,
+                                        int num_blocks, int block_size, int num_kv_heads,
+                                        int head_size, int dtype, float k_scale, float v_scale,
+                                        pa_stream_t stream)
+{
+    long long row_elems = 0;
+    int rc = validate_reshape("pa_reshape_and_cache_fp8", key, value, kv_cache, slot_mapping,
+                              num_tokens, num_blocks, block_size, num_kv_heads, head_size, dtype,
+                              &row_elems);
+    if (rc != PA_OK)
+        return rc;
+    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return set_error(PA_ERR_INVALID_ARG,
+                         "pa_reshape_and_cache_fp8: k_scale and v_scale must be finite and > 0");
+    if (num_tokens == 0)
+        return PA_OK;
+    const long long row_vecs = row_elems / 8;  // 8 elements: 16 bytes in, 8 bytes out
+    const long long num_slots = (long long)num_blocks * block_size;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const dim3 grid(num_tokens, (unsigned)((row_vecs + kReshapeThreads - 1) / kReshapeThreads));
+    if (dtype == PA_BF16)
+        reshape_and_cache_fp8_kernel<true><<<grid, kReshapeThreads, 0, s>>>(
+            static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+            static_cast<uint2 *>(kv_cache), slot_mapping, (int)row_vecs, num_slots,
+            num_slots * row_vecs, k_scale, v_scale);
+    else
+        reshape_and_cache_fp8_kernel<false><<<grid, kReshapeThreads, 0, s>>>(
+            static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+            static_cast<uint2 *>(kv_cache), slot_mapping, (int)row_vecs, num_slots,
+            num_slots * row_vecs, k_scale, v_scale);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pa_reshape_and_cache_fp8: launch");
+    return PA_OK;
+}
+
 extern "C" int pa_copy_blocks(void *const *kv_caches, int num_layers, const int32_t *src_dst_pairs,
                               int num_pairs, int num_blocks, int block_size, int num_kv_heads,
                               int head_size, int dtype, pa_stream_t stream)
 {
-    if (dtype != PA_F16 && dtype != PA_BF16)
+    if (dtype != PA_F16 && dtype != PA_BF16 && dtype != PA_FP8_E4M3)
         return set_error(PA_ERR_UNSUPPORTED, "pa_copy_blocks: dtype %d", dtype);
+    const long long esize = dtype == PA_FP8_E4M3 ? 1 : 2;
     if (num_pairs < 0 || num_layers < 1 || num_layers > kMaxLayers || num_blocks <= 0 ||
         block_size < kTile || block_size % kTile != 0 || num_kv_heads <= 0 || head_size <= 0)
         return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: bad sizes (1 <= num_layers <= %d)", kMaxLayers);
-    if (((long long)num_kv_heads * head_size) % 8 != 0)
-        return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: num_kv_heads * head_size must be a multiple of 8");
+    if (((long long)num_kv_heads * head_size * esize) % 16 != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_copy_blocks: a token's row (num_kv_heads * head_size elements) must be a multiple of 16 bytes");
     if (num_pairs == 0)
         return PA_OK;
     if (!kv_caches || !src_dst_pairs || !aligned(src_dst_pairs, 4))
@@ -1398,7 +1769,7 @@ extern "C" int pa_copy_blocks(void *const *kv_caches, int num_layers, const int3
     }
     for (int l = num_layers; l < kMaxLayers; ++l)
         lp.p[l] = nullptr;
-    const long long block_vecs = (long long)block_size * num_kv_heads * head_size * 2 / 16;
+    const long long block_vecs = (long long)block_size * num_kv_heads * head_size * esize / 16;
     const long long half_vecs = (long long)num_blocks * block_vecs;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     copy_blocks_kernel<<<dim3(num_pairs, num_layers), 256, 0, s>>>(lp, src_dst_pairs, num_pairs, num_blocks,

@@ -10,6 +10,10 @@ table), preceded by the COW copies the allocator asked for:
 
     pa_copy_blocks(cow pairs) -> pa_reshape_and_cache(new K/V) -> pa_decode
 
+A pool of E4M3 codes (uint8) selects the FP8 cache calls instead
+(pa_reshape_and_cache_fp8, pa_decode_fp8) with the workload's per-tensor
+scales.
+
 Everything here is marshalling around libpa calls; no arithmetic of the
 method runs in Python.
 """
@@ -100,9 +104,12 @@ def plan_step(name: str, seed: int, variant: str = "literal") -> StepPlan:
 class DecodeStep:
     """Device buffers of one step and the three libpa calls that run it."""
 
-    def __init__(self, name: str, plan: StepPlan, pool, query, key_new, value_new, device):
+    def __init__(self, name: str, plan: StepPlan, pool, query, key_new, value_new, device,
+                 k_scale: float = workloads.FP8_K_SCALE, v_scale: float = workloads.FP8_V_SCALE):
         import torch
         self.w = workloads.WORKLOADS[name]
+        self.fp8 = pool.dtype == torch.uint8
+        self.k_scale, self.v_scale = k_scale, v_scale
         self.pool = pool
         self.query, self.key_new, self.value_new = query, key_new, value_new
         self.block_tables = torch.from_numpy(plan.block_tables).to(device)
@@ -111,7 +118,8 @@ class DecodeStep:
         self.cow_pairs = (torch.from_numpy(plan.cow_pairs).to(device)
                           if len(plan.cow_pairs) else None)
         self.out = torch.empty_like(query)
-        self.workspace = binding.decode_workspace(query, pool)
+        self.workspace = (binding.decode_fp8_workspace(query, pool) if self.fp8
+                          else binding.decode_workspace(query, pool))
         # Blocks that appear in more than one table are shared (prefix / fork):
         # then K/V keep normal L2 priority, else they are streamed.
         ids = plan.block_tables[plan.block_tables >= 0]
@@ -124,8 +132,16 @@ class DecodeStep:
     def run(self, stream=None) -> None:
         if self.cow_pairs is not None:
             binding.pa_copy_blocks([self.pool], self.cow_pairs, stream)
-        binding.pa_reshape_and_cache(self.key_new, self.value_new, self.pool, self.slot_mapping, stream)
+        self.reshape(stream)
         self.decode(stream)
+
+    def reshape(self, stream=None) -> None:
+        if self.fp8:
+            binding.pa_reshape_and_cache_fp8(self.key_new, self.value_new, self.pool,
+                                             self.slot_mapping, self.k_scale, self.v_scale, stream)
+        else:
+            binding.pa_reshape_and_cache(self.key_new, self.value_new, self.pool,
+                                         self.slot_mapping, stream)
 
     def run_host(self, host: dict, out_host, stream=None) -> None:
         """The step end to end from pinned host buffers: copy this step's
@@ -143,16 +159,31 @@ class DecodeStep:
         torch.cuda.current_stream().synchronize()
 
     def decode(self, stream=None) -> None:
-        binding.pa_decode(self.out, self.query, self.pool, self.block_tables, self.seq_lens,
-                          self.w.scale, self.workspace, self.flags, stream)
+        if self.fp8:
+            binding.pa_decode_fp8(self.out, self.query, self.pool, self.block_tables,
+                                  self.seq_lens, self.w.scale, self.k_scale, self.v_scale,
+                                  self.workspace, self.flags, stream)
+        else:
+            binding.pa_decode(self.out, self.query, self.pool, self.block_tables, self.seq_lens,
+                              self.w.scale, self.workspace, self.flags, stream)
 
 
-def make_device_inputs(name: str, plan: StepPlan, seed: int, device):
-    """Pool, queries and new K/V: seeded N(0, 1) values on ``device``."""
+def make_device_inputs(name: str, plan: StepPlan, seed: int, device, kv_cache: str = "16bit"):
+    """Pool, queries and new K/V: seeded N(0, 1) values on ``device``.
+    ``kv_cache="fp8"`` gives a pool of E4M3 codes of N(0, 1) draws under the
+    workload's FP8 scales (K half with FP8_K_SCALE, V half with FP8_V_SCALE)."""
+    import torch
     w = workloads.WORKLOADS[name]
     s = len(plan.seq_ids)
-    pool = workloads.normal_values((2, w.num_blocks, w.block_size, w.num_kv_heads, w.head_size),
-                                   w.dtype, seed + 10, device)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_size)
+    if kv_cache == "fp8":
+        pool = torch.empty((2,) + shape, dtype=torch.uint8, device=device)
+        pool[0] = workloads.fp8_codes(shape, workloads.FP8_K_SCALE, seed + 10, device)
+        pool[1] = workloads.fp8_codes(shape, workloads.FP8_V_SCALE, seed + 14, device)
+    elif kv_cache == "16bit":
+        pool = workloads.normal_values((2,) + shape, w.dtype, seed + 10, device)
+    else:
+        raise ValueError(f"kv_cache must be '16bit' or 'fp8', not {kv_cache!r}")
     query = workloads.normal_values((s, w.num_q_heads, w.head_size), w.dtype, seed + 11, device)
     key_new = workloads.normal_values((s, w.num_kv_heads, w.head_size), w.dtype, seed + 12, device)
     value_new = workloads.normal_values((s, w.num_kv_heads, w.head_size), w.dtype, seed + 13, device)

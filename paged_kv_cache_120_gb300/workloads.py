@@ -133,6 +133,33 @@ def normal_values(shape, dtype: int, seed: int, device="cpu"):
     return out
 
 
+# Per-tensor scales of the FP8 (E4M3) cache variant of every workload: a code
+# c stands for e4m3(c) * scale. N(0, 1) draws use the E4M3 range down to
+# about 2^-6 * scale and saturate beyond 448 * scale (5.6 for K, 4.48 for V).
+FP8_K_SCALE = 0.0125
+FP8_V_SCALE = 0.01
+
+
+def fp8_codes(shape, scale: float, seed: int, device="cpu"):
+    """E4M3 codes (uint8 tensor on ``device``) of N(0, 1) draws for a cache
+    with the given per-tensor scale: draws of N(0, 1 / scale^2), clipped to
+    +-448, rounded by PyTorch's float8_e4m3fn cast. An input generator only:
+    it is not the write path's quantisation (that is an fp32 division by the
+    scale, done by the kernel and by the oracle)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    out = torch.empty(tuple(shape), dtype=torch.uint8, device=device)
+    flat = out.view(-1)
+    step = 1 << 26
+    sigma = 1.0 / float(scale)
+    for i in range(0, flat.numel(), step):
+        n = min(step, flat.numel() - i)
+        x = torch.randn(n, generator=gen, device=device, dtype=torch.float32) * sigma
+        flat[i:i + n] = x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
 def torch_dtype(dtype: int):
     import torch
     return torch.float16 if dtype == F16 else torch.bfloat16

@@ -27,7 +27,7 @@ def _declared_functions():
 
 def test_every_declared_function_is_exported(lib):
     names = _declared_functions()
-    assert len(names) >= 19
+    assert len(names) >= 22
     for n in names:
         assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
     assert sorted(n for n, _, _ in binding.SIGNATURES) == names
@@ -60,6 +60,29 @@ def test_host_side_validation_without_a_gpu(lib):
     assert lib.pa_reshape_and_cache(null, null, null, null, 0, 10, 16, 8, 128, 0, null) == binding.PA_OK
     assert lib.pa_copy_blocks(null, 0, null, 1, 10, 16, 8, 128, 0, null) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_copy_blocks(null, 1, null, 0, 10, 16, 8, 128, 0, null) == binding.PA_OK
+    assert lib.pa_copy_blocks(null, 1, null, 0, 10, 16, 1, 8, binding.PA_FP8_E4M3, null) \
+        == binding.PA_ERR_INVALID_ARG          # an 8-byte FP8 row cannot be copied in 16-byte units
+    assert lib.pa_copy_blocks(null, 1, null, 0, 10, 16, 8, 128, 3, null) == binding.PA_ERR_UNSUPPORTED
+
+
+def test_fp8_host_side_validation_without_a_gpu(lib):
+    null = None
+    args = (null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16)
+    # dtype is the activations' type: E4M3 is not a query type
+    assert lib.pa_decode_fp8(*args, binding.PA_FP8_E4M3, 1.0, 1.0, null, 0, 0, null) \
+        == binding.PA_ERR_UNSUPPORTED
+    for ks, vs in ((0.0, 1.0), (1.0, -2.0), (float("inf"), 1.0), (1.0, float("nan"))):
+        assert lib.pa_decode_fp8(*args, 0, ks, vs, null, 0, 0, null) == binding.PA_ERR_INVALID_ARG
+        assert "k_scale" in binding.pa_last_error()
+        assert lib.pa_reshape_and_cache_fp8(null, null, null, null, 3, 10, 16, 8, 128, 0, ks, vs,
+                                            null) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_fp8(*args, 0, 1.0, 1.0, null, 0, 0, null) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_fp8(null, null, null, null, 1, null, 0, 1.0, 8, 8, 128, 10, 16, 1, 0.5,
+                             2.0, null, 0, 0, null) == binding.PA_OK
+    assert lib.pa_reshape_and_cache_fp8(null, null, null, null, 0, 10, 16, 8, 128, 1, 1.0, 1.0,
+                                        null) == binding.PA_OK
+    assert lib.pa_reshape_and_cache_fp8(null, null, null, null, 3, 10, 16, 8, 128, 2, 1.0, 1.0,
+                                        null) == binding.PA_ERR_UNSUPPORTED
 
 
 def _both(nb, bs, order):
