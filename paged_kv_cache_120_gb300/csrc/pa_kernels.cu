@@ -254,19 +254,6 @@ __device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t x)
     return d;
 }
 
-// The E4M3 codes in bytes 1 and 3 of x to a bf16 pair (byte 1 -> low half);
-// bytes 0 and 2 are ignored. A code s.eeee.fff placed as bf16 bits
-// s.0000eeee.fff0000 is the code's value times 2^-120, E4M3 subnormals
-// included (they become bf16 subnormals); one exact multiplication by 2^120
-// restores the value. bf16 multiplication keeps subnormal inputs.
-__device__ __forceinline__ uint32_t e4m3_b13_to_bf16x2(uint32_t x)
-{
-    const uint32_t bits = (x & 0x80008000u) | ((x >> 4) & 0x07F007F0u);
-    uint32_t d;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(bits), "r"(0x7B807B80u));  // 2^120, 2^120
-    return d;
-}
-
 template <bool BF16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1)
@@ -332,12 +319,16 @@ __device__ __forceinline__ uint16_t to_elem(float x)
 #ifndef PA_DECODE_STAGES_FP8
 #define PA_DECODE_STAGES_FP8 2
 #endif
+
 // Warps per CTA, each an independent pipeline: 12 for 8-column query tiles;
 // 16-column tiles need ~195 registers per thread, so 8 warps fit an SM.
-template <int NT>
+#ifndef PA_DECODE_WARPS_FP8
+#define PA_DECODE_WARPS_FP8 12
+#endif
+template <int NT, bool FP8 = false>
 constexpr int decode_warps()
 {
-    return NT == 1 ? PA_DECODE_WARPS : PA_DECODE_WARPS_WIDE;
+    return NT == 1 ? (FP8 ? PA_DECODE_WARPS_FP8 : PA_DECODE_WARPS) : PA_DECODE_WARPS_WIDE;
 }
 // TMA ring depth per warp. An FP8 tile is half the bytes of a 16-bit one, so
 // the FP8 pipelines keep two in flight to hold the same bytes in flight.
@@ -472,11 +463,11 @@ __device__ __forceinline__ int owner_of(long long u, long long N, long long K)
 // element type of Q and the output, FP8 cache or not. One CTA =
 // decode_warps<NT>() independent warp pipelines.
 template <int D, int NT, bool BF16, bool FP8>
-__global__ void __launch_bounds__(decode_warps<NT>() * 32)
+__global__ void __launch_bounds__(decode_warps<NT, FP8>() * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
     using Geo = TileGeo<D, FP8>;
-    constexpr int kWarps = decode_warps<NT>();
+    constexpr int kWarps = decode_warps<NT, FP8>();
     constexpr int kStages = decode_stages<FP8>();
     constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of V^T P^T
     constexpr int GP = NT * 8;
@@ -486,6 +477,12 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
     // and VB bytes of V per row (see the tile loop).
     constexpr int CPT = D / 64;
     constexpr int VB = D / 8;
+    // Operand type of both MMAs: the element type, or fp16 for an FP8 cache
+    // (every E4M3 value is an fp16 value; bf16 queries are converted per
+    // column, see begin_segment). kPShift scales P by 2^8 in the FP8 case so
+    // that fp16 keeps weights down to 2^-32 of the largest.
+    constexpr bool MBF16 = BF16 && !FP8;
+    constexpr float kPShift = FP8 ? 8.f : 0.f;
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ long long warp_sums[kWarps];
@@ -578,7 +575,9 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
         return;
     }
 
-    // Unit u -> physical block, segment id and (tile << 5 | valid tokens).
+    // Unit u -> physical block, segment id and tv = kv head << 16 | tile
+    // index inside its block << 5 | valid tokens (what the TMA issue needs,
+    // so that no division runs per tile).
     auto unit_info = [&](long long u, int &phys, int &seg, int &tv) {
         phys = -1;
         seg = -1;
@@ -598,10 +597,12 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
         const long long local = u - prefix[lo];
         const int segl = (int)(local / ntiles);
         const int tile = (int)(local - (long long)segl * ntiles);
+        const int blk = tile / p.tiles_per_block;
         // Not checked here: the load's latency is hidden until issue time.
-        phys = __ldg(p.block_tables + (long long)lo * p.max_blocks_per_seq + tile / p.tiles_per_block);
+        phys = __ldg(p.block_tables + (long long)lo * p.max_blocks_per_seq + blk);
         seg = lo * segs_per_seq + segl;
-        tv = (tile << 5) | min(kTile, L - tile * kTile);
+        tv = ((segl / p.qtiles) << 16) | ((tile - blk * p.tiles_per_block) << 5) |
+             min(kTile, L - tile * kTile);
     };
 
     // Register windows of unit info: A covers [wb, wb+32), B covers [wb+32, wb+64).
@@ -627,8 +628,8 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
                 raise_error(PA_DEVERR_BLOCK_ID);
                 phys = p.num_blocks;  // outside the tensor map: TMA fills zeros
             }
-            const int h = (seg % segs_per_seq) / p.qtiles;
-            const int t0 = ((tv >> 5) % p.tiles_per_block) * kTile;
+            const int h = tv >> 16;
+            const int t0 = ((tv >> 5) & 0x7FF) * kTile;
             const uint32_t bar = my_bar0 + st * 8;
             mbar_expect_tx(bar, STAGE);
 #pragma unroll
@@ -653,6 +654,7 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
 
     float m_run[NT][2], l_run[NT][2], acc[KS][NT][4];
     uint32_t qf[NT][KS][2];
+    float xscale[NT][2];  // per-column score scale (bf16 queries on an FP8 cache)
     int cur_seg = -1;
 
     auto seg_coords = [&](int seg, int &s, int &segl, int &hq0) {
@@ -671,22 +673,53 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
             const int col = nt * 8 + g;
             const bool live = col < p.tile_q;
             const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qbase + (long long)col * D);
+            if constexpr (FP8) {
+                // Permuted k-step kk = 4j + w: dims 16c + 4w + {0..3} of chunk
+                // c = CPT tig + j, the same dims the K fragments hold.
+                const uint2 *q4 = reinterpret_cast<const uint2 *>(qrow);
+                auto q_at = [&](int kk) {
+                    return live ? __ldg(q4 + 4 * (CPT * tig + (kk >> 2)) + (kk & 3)) : make_uint2(0u, 0u);
+                };
+                if constexpr (BF16) {
+                    // bf16 column -> fp16 times 2^sh, sh putting the column's
+                    // largest element in [2^14, 2^15): exact for every element
+                    // within 2^-28 of it (smaller ones round with an error
+                    // below 2^-39 of it). The column's score scale takes 2^-sh.
+                    int emax = 0;
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                if constexpr (FP8) {
-                    // Permuted k-step kk = 4j + w: dims 16c + 4w + {0..3} of
-                    // chunk c = CPT tig + j, the same dims the K fragments hold.
-                    const int c = CPT * tig + (kk >> 2), w = kk & 3;
-                    const uint2 u = live ? __ldg(reinterpret_cast<const uint2 *>(qrow) + 4 * c + w)
-                                         : make_uint2(0u, 0u);
-                    if constexpr (BF16) {
-                        qf[nt][kk][0] = prmt(u.x, u.y, 0x5410u);  // dims +0, +2
-                        qf[nt][kk][1] = prmt(u.x, u.y, 0x7632u);  // dims +1, +3
-                    } else {
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint2 u = q_at(kk);
+                        emax = max(emax, max(max(u.x & 0x7F80, (u.x >> 16) & 0x7F80),
+                                             max(u.y & 0x7F80, (u.y >> 16) & 0x7F80)));
+                    }
+                    emax = max(emax, __shfl_xor_sync(kFull, emax, 1));
+                    emax = max(emax, __shfl_xor_sync(kFull, emax, 2));
+                    const int sh = min(126, 141 - (emax >> 7));
+                    const float s2 = __int_as_float((sh + 127) << 23);
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint2 u = q_at(kk);
+                        qf[nt][kk][0] = pack2<false>(__uint_as_float(u.x << 16) * s2,
+                                                     __uint_as_float(u.x & 0xFFFF0000u) * s2);
+                        qf[nt][kk][1] = pack2<false>(__uint_as_float(u.y << 16) * s2,
+                                                     __uint_as_float(u.y & 0xFFFF0000u) * s2);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int sh_c = __shfl_sync(kFull, sh, (2 * tig + e) << 2);
+                        xscale[nt][e] = p.scale_log2 * __int_as_float((127 - sh_c) << 23);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint2 u = q_at(kk);
                         qf[nt][kk][0] = u.x;  // dims +0, +1
                         qf[nt][kk][1] = u.y;  // dims +2, +3
                     }
-                } else {
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
                     qf[nt][kk][0] = live ? __ldg(qrow + 8 * kk + tig) : 0u;
                     qf[nt][kk][1] = live ? __ldg(qrow + 8 * kk + 4 + tig) : 0u;
                 }
@@ -793,6 +826,17 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
     uint32_t phase = 0;
     bool ok = true;
     long long i = r0;
+    auto refill = [&]() {
+        __syncwarp();
+        if (ip < r1) {
+            int ph2, sg2, tv2;
+            fetch(ip, ph2, sg2, tv2);
+            if (lane == 0)
+                fence_proxy_async();
+            issue(ph2, sg2, tv2, st);
+            ++ip;
+        }
+    };
     for (; i < r1; ++i) {
         if (i - wb >= 32) {
             wb += 32;
@@ -849,17 +893,10 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     const int kk = 4 * j + w;
-                    if constexpr (BF16) {
-                        kf[kk][0] = e4m3_b13_to_bf16x2(w0[w] << 8);  // dims +0, +2
-                        kf[kk][1] = e4m3_b13_to_bf16x2(w1[w] << 8);
-                        kf[kk][2] = e4m3_b13_to_bf16x2(w0[w]);       // dims +1, +3
-                        kf[kk][3] = e4m3_b13_to_bf16x2(w1[w]);
-                    } else {
-                        kf[kk][0] = e4m3x2_lo_to_f16x2(w0[w]);       // dims +0, +1
-                        kf[kk][1] = e4m3x2_lo_to_f16x2(w1[w]);
-                        kf[kk][2] = e4m3x2_hi_to_f16x2(w0[w]);       // dims +2, +3
-                        kf[kk][3] = e4m3x2_hi_to_f16x2(w1[w]);
-                    }
+                    kf[kk][0] = e4m3x2_lo_to_f16x2(w0[w]);  // dims +0, +1
+                    kf[kk][1] = e4m3x2_lo_to_f16x2(w1[w]);
+                    kf[kk][2] = e4m3x2_hi_to_f16x2(w0[w]);  // dims +2, +3
+                    kf[kk][3] = e4m3x2_hi_to_f16x2(w1[w]);
                 }
             }
             // V^T: this thread's dims VB g .. VB g + VB - 1 of tokens 2tig,
@@ -885,24 +922,14 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int wi = mt >> 1;
-                if constexpr (BF16) {
-                    // Byte d (resp. d + 1) of the two tokens into bytes 1 and 3.
-                    const uint32_t s0 = (mt & 1) ? 0x6020u : 0x4000u;
-                    const uint32_t s1 = (mt & 1) ? 0x7030u : 0x5010u;
-                    vf[mt][0] = e4m3_b13_to_bf16x2(prmt(vw[0][wi], vw[1][wi], s0));
-                    vf[mt][1] = e4m3_b13_to_bf16x2(prmt(vw[0][wi], vw[1][wi], s1));
-                    vf[mt][2] = e4m3_b13_to_bf16x2(prmt(vw[2][wi], vw[3][wi], s0));
-                    vf[mt][3] = e4m3_b13_to_bf16x2(prmt(vw[2][wi], vw[3][wi], s1));
-                } else {
-                    // {t.d, t'.d, t.d+1, t'.d+1}: low pair -> row g, high -> row g+8.
-                    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                    const uint32_t x01 = prmt(vw[0][wi], vw[1][wi], sel);
-                    const uint32_t x23 = prmt(vw[2][wi], vw[3][wi], sel);
-                    vf[mt][0] = e4m3x2_lo_to_f16x2(x01);
-                    vf[mt][1] = e4m3x2_hi_to_f16x2(x01);
-                    vf[mt][2] = e4m3x2_lo_to_f16x2(x23);
-                    vf[mt][3] = e4m3x2_hi_to_f16x2(x23);
-                }
+                // {t.d, t'.d, t.d+1, t'.d+1}: low pair -> row g, high -> row g+8.
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t x01 = prmt(vw[0][wi], vw[1][wi], sel);
+                const uint32_t x23 = prmt(vw[2][wi], vw[3][wi], sel);
+                vf[mt][0] = e4m3x2_lo_to_f16x2(x01);
+                vf[mt][1] = e4m3x2_hi_to_f16x2(x01);
+                vf[mt][2] = e4m3x2_lo_to_f16x2(x23);
+                vf[mt][3] = e4m3x2_hi_to_f16x2(x23);
             }
         } else {
 #pragma unroll
@@ -931,52 +958,61 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
         for (int kk = 0; kk < KS; kk += 2)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                mma16816<BF16>(sc[nt], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], qf[nt][kk][0],
-                               qf[nt][kk][1]);
-                mma16816<BF16>(sc2[nt], kf[kk + 1][0], kf[kk + 1][1], kf[kk + 1][2], kf[kk + 1][3],
-                               qf[nt][kk + 1][0], qf[nt][kk + 1][1]);
+                mma16816<MBF16>(sc[nt], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], qf[nt][kk][0],
+                                qf[nt][kk][1]);
+                mma16816<MBF16>(sc2[nt], kf[kk + 1][0], kf[kk + 1][1], kf[kk + 1][2], kf[kk + 1][3],
+                                qf[nt][kk + 1][0], qf[nt][kk + 1][1]);
             }
         // Every fragment of this tile is now in registers: hand the stage back
         // to the TMA right away, so the ring stays full while the math runs.
-        __syncwarp();
-        if (ip < r1) {
-            int ph2, sg2, tv2;
-            fetch(ip, ph2, sg2, tv2);
-            if (lane == 0)
-                fence_proxy_async();
-            issue(ph2, sg2, tv2, st);
-            ++ip;
-        }
+        refill();
 
-        // Online softmax (base 2) per query column; P rounded to the element type.
+        // Online softmax (base 2) per query column. P is rounded to the
+        // element type; with an FP8 cache it is rounded to fp16 (V is widened
+        // to fp16) and carries a factor 2^8 (P <= 256), which l and O share.
         const bool tok0 = g < valid, tok1 = g + 8 < valid;
-        uint32_t pb[NT][2];
+        float alpha[NT][2];
+        bool grew = false;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float pr[4];
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float x0 = tok0 ? (sc[nt][e] + sc2[nt][e]) * p.scale_log2 : -INFINITY;
-                const float x1 = tok1 ? (sc[nt][2 + e] + sc2[nt][2 + e]) * p.scale_log2 : -INFINITY;
+                const float xs = (FP8 && BF16) ? xscale[nt][e] : p.scale_log2;
+                const float x0 = tok0 ? (sc[nt][e] + sc2[nt][e]) * xs : -INFINITY;
+                const float x1 = tok1 ? (sc[nt][2 + e] + sc2[nt][2 + e]) * xs : -INFINITY;
                 float mx = fmaxf(x0, x1);
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
                 const float m_new = fmaxf(m_run[nt][e], mx);
-                const float alpha = ex2(m_run[nt][e] - m_new);
+                grew |= m_new != m_run[nt][e];
+                alpha[nt][e] = ex2(m_run[nt][e] - m_new);
                 m_run[nt][e] = m_new;
-                pr[e] = ex2(x0 - m_new);
-                pr[2 + e] = ex2(x1 - m_new);
-                l_run[nt][e] *= alpha;
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    acc[mt][nt][e] *= alpha;
-                    acc[mt][nt][2 + e] *= alpha;
-                }
+                const float mref = m_new - kPShift;
+                sc[nt][e] = ex2(x0 - mref);
+                sc[nt][2 + e] = ex2(x1 - mref);
             }
-            const uint32_t r0p = pack2<BF16>(pr[0], pr[1]);  // token g,   columns 2tig, 2tig+1
-            const uint32_t r1p = pack2<BF16>(pr[2], pr[3]);  // token g+8
-            const float2 f0 = unpack2<BF16>(r0p), f1 = unpack2<BF16>(r1p);
+        // Rescale l and O only when some column's maximum grew (alpha != 1):
+        // after the first tiles of a segment that is rare.
+        if (__any_sync(kFull, grew)) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    l_run[nt][e] *= alpha[nt][e];
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        acc[mt][nt][e] *= alpha[nt][e];
+                        acc[mt][nt][2 + e] *= alpha[nt][e];
+                    }
+                }
+        }
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t r0p = pack2<MBF16>(sc[nt][0], sc[nt][1]);  // token g,   columns 2tig, 2tig+1
+            const uint32_t r1p = pack2<MBF16>(sc[nt][2], sc[nt][3]);  // token g+8
+            const float2 f0 = unpack2<MBF16>(r0p), f1 = unpack2<MBF16>(r1p);
             l_run[nt][0] += f0.x + f1.x;
             l_run[nt][1] += f0.y + f1.y;
             pb[nt][0] = movm_t(r0p);  // P^T fragments as the B operand
@@ -988,8 +1024,8 @@ __global__ void __launch_bounds__(decode_warps<NT>() * 32)
         for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                mma16816<BF16>(acc[mt][nt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[nt][0],
-                               pb[nt][1]);
+                mma16816<MBF16>(acc[mt][nt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[nt][0],
+                                pb[nt][1]);
 
         if (++st == kStages) {
             st = 0;
@@ -1391,10 +1427,15 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     const CUtensorMapSwizzle swz =
         (fp8 && head_size == 64) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    // A 16-bit row of one head is 256 bytes (fetched as two 128-byte boxes):
+    // promote to 256-byte L2 lines. An FP8 row is at most 128 bytes, and a
+    // 256-byte promotion would also pull the next head's row from DRAM.
+    const CUtensorMapL2promotion promo =
+        fp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     CUtensorMap m;
     CUresult r = enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 5,
                      const_cast<void *>(kv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     const int slot = used < 16 ? used++ : (next++ % 16);
@@ -1445,10 +1486,10 @@ template <int D, int NT, bool BF16, bool FP8>
 void pick_kernels(DecodePlan &pl, int num_seqs)
 {
     pl.main_fn = reinterpret_cast<const void *>(&paged_decode_kernel<D, NT, BF16, FP8>);
-    pl.warps = decode_warps<NT>();
+    pl.warps = decode_warps<NT, FP8>();
     pl.reduce_fn = reinterpret_cast<const void *>(&paged_decode_reduce_kernel<D, NT, BF16>);
     pl.reduce_smem = reduce_smem_bytes<D, NT>();
-    pl.smem = decode_smem_bytes<D, decode_warps<NT>(), FP8>(num_seqs);
+    pl.smem = decode_smem_bytes<D, decode_warps<NT, FP8>(), FP8>(num_seqs);
 }
 
 template <int D, int NT>
@@ -1477,6 +1518,9 @@ int validate_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int h
         return set_error(PA_ERR_UNSUPPORTED, "pa_decode: query group %d (want <= 16 or a multiple of 16)", group);
     if (block_size < kTile || block_size % kTile != 0)
         return set_error(PA_ERR_INVALID_ARG, "pa_decode: block_size %d must be a positive multiple of 16", block_size);
+    if (block_size > 2048 * kTile || num_kv_heads > 65535)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_decode: block_size %d (max %d) or num_kv_heads %d (max 65535)",
+                         block_size, 2048 * kTile, num_kv_heads);
     return PA_OK;
 }
 

@@ -195,6 +195,21 @@ def test_fp8_subnormal_codes_are_not_flushed(dev, dtype, D):
     assert np.max(np.abs(want)) > 0.25
 
 
+def test_fp8_bf16_queries_with_wide_dynamic_range(dev):
+    """bf16 queries meet fp16-widened K: each query column is moved to fp16
+    with its own power-of-two scale. Columns scaled from 2^-30 to 2^12, with
+    a few elements 2^-40 below their column's largest, still match."""
+    import torch
+    c = Fp8Case(dev, workloads.BF16, 128, 16, 2, 16, [5, 70, 16, 1, 300, 33], seed=47)
+    gen = torch.Generator().manual_seed(5)
+    exps = torch.randint(-30, 13, (1, 16, 1), generator=gen).float()
+    q = (c.q.float().cpu() * torch.exp2(exps))
+    q[:, :, :3] *= 2.0 ** -40
+    c.q = q.to(torch.bfloat16).to(dev)
+    c.q_bits = u16(c.q)
+    c.check(c.gpu())
+
+
 def test_fp8_padding_slots_holding_nan_are_ignored(dev):
     c = Fp8Case(dev, workloads.F16, 128, 8, 8, 16, [3, 18, 40, 77, 16], seed=5, poison=True)
     c.check(c.gpu())
