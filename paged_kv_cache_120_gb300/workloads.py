@@ -3,7 +3,8 @@
 This module serves both the CUDA path and the oracle, so it holds none of the
 method's arithmetic: no block counts, no slots, no attention. It only fixes
 shapes, draws sequence lengths from the stated distributions, draws the
-physical-block free-list order, and draws N(0, 1) values.
+physical-block free-list order, and draws N(0, 1) values (and, for the FP8
+cache variant, E4M3 codes of N(0, 1) draws rounded by PyTorch's cast).
 
 Workloads (shapes follow the PagedAttention pages: the Llama-2-13B shape of
 the vLLM book chapter "第4章 PagedAttention：虚拟内存的启示" §4.1.1/§4.3.1;
