@@ -435,6 +435,38 @@ void oracle_decode_fp8_sampled(double *out, const int32_t *seq_ids, const int32_
                               dtype, k_scale, v_scale);
 }
 
+/* ---- read path: chunked prefill [P1 §4.5 step 2] ----
+ * The FlashAttention backend hands the cache, the block table, the query
+ * offsets cu_seqlens_q and the used lengths seqused_k to one varlen call.
+ * Reading: sequence s brings q_len = cu_seqlens_q[s+1] - cu_seqlens_q[s]
+ * query tokens, the last q_len of its seq_lens[s] cached tokens (this step's
+ * tokens were written by slot first); query i sits at position
+ * p = seq_lens[s] - q_len + i and attends causally to tokens 0..p. Each
+ * output row is therefore the decode definition over the first p + 1 tokens
+ * of the sequence, and is computed by oracle_decode_one on exactly that:
+ * out is [total_q][num_q_heads][head_size], row cu_seqlens_q[s] + i. */
+void oracle_prefill(double *out, const uint16_t *query, const uint16_t *pool,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
+                    double scale, int num_q_heads, int num_kv_heads, int head_size,
+                    int num_blocks, int block_size, int dtype)
+{
+    for (int s = 0; s < num_seqs; ++s) {
+        int q0 = cu_seqlens_q[s];
+        int q_len = cu_seqlens_q[s + 1] - q0;
+        const int32_t *table = block_tables + (long long)s * max_blocks_per_seq;
+        for (int i = 0; i < q_len; ++i) {
+            int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */
+            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;
+            for (int hq = 0; hq < num_q_heads; ++hq)
+                oracle_decode_one(out + ((long long)(q0 + i) * num_q_heads + hq) * head_size, q_row,
+                                  pool, table, max_blocks_per_seq, &visible, 0, hq, scale,
+                                  num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                                  dtype);
+        }
+    }
+}
+
 /* ---- the online-softmax recurrence [P1 §4.6] ----
  * The same attention, computed the way the method streams it: the logical
  * tokens are cut into consecutive parts of `part_len` tokens; each part

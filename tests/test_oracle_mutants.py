@@ -74,6 +74,13 @@ MUTANTS = [
     ("oracle/oracle.c", "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * v_scale;",
      "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * k_scale;",
      "test_oracle_fp8_pins.py"),                                                      # decode scale swap
+    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1;",
+     "int32_t visible = seq_lens[s] - q_len + i + 2;", "test_oracle_prefill_pins.py"),  # sees p+1
+    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1;",
+     "int32_t visible = seq_lens[s] - q_len + 1;", "test_oracle_prefill_pins.py"),      # not causal in i
+    ("oracle/oracle.c", "const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;",
+     "const uint16_t *q_row = query + (long long)(q0) * num_q_heads * head_size;",
+     "test_oracle_prefill_pins.py"),                                                      # wrong query row
     ("oracle/block_manager.py", "self.free.insert(0, b)", "self.free.append(b)",
      "test_block_manager.py"),                                                         # free to tail
     ("oracle/block_manager.py", "                self.ref[last] -= 1\n", "",
