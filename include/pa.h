@@ -253,6 +253,42 @@ int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
                   pa_stream_t stream);
 
 /*
+ * pa_prefill — causal attention of a chunk of new query tokens per sequence
+ * over the paged cache (chunked prefill). [book] §4.5 step 2: the backend
+ * hands the cache, the block table, the query offsets cu_seqlens_q and the
+ * used lengths seqused_k to one varlen attention call; §4.6 for the online
+ * softmax. Reading taken: the chunk of sequence s is the last
+ * q_len = cu_seqlens_q[s+1] - cu_seqlens_q[s] of its seq_lens[s] cached
+ * tokens (written first by pa_reshape_and_cache), and query i of the chunk,
+ * at position p = seq_lens[s] - q_len + i, attends to tokens 0..p. With
+ * q_len = 1 this is pa_decode's result (computed by a different kernel).
+ *
+ *   out, query     device, [total_q][num_q_heads][head_size], dtype; row
+ *                  cu_seqlens_q[s] + i belongs to query i of sequence s
+ *   kv_cache, block_tables, max_blocks_per_seq: as for pa_decode
+ *   cu_seqlens_q   device, [num_seqs + 1] int32, non-decreasing, from 0 to
+ *                  total_q
+ *   seq_lens       device, [num_seqs] int32, >= the sequence's q_len
+ *   total_q        rows of query / out (host int)
+ *   max_seqlen_q   host int >= every q_len (sizes the grid; larger is only
+ *                  slower)
+ *   head_size      128; the group num_q_heads / num_kv_heads must be <= 16
+ *                  or a multiple of 16
+ * Rows of sequences whose offsets or lengths are inconsistent are not
+ * written and set PA_DEVERR_SEQ_LEN; block ids outside the pool read as
+ * zeros and set PA_DEVERR_BLOCK_ID. Computed on the tcgen05 tensor cores:
+ * S = Q K^T and O = P V in fp32 (tensor memory), an fp32 online softmax in
+ * base 2 with P rounded once to dtype, one rounding of O / l at the end.
+ * Allocates nothing and needs no workspace. Returns PA_OK or a PA_ERR_* code.
+ */
+int pa_prefill(void *out, const void *query, const void *kv_cache,
+               const int32_t *block_tables, int max_blocks_per_seq,
+               const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
+               int total_q, int max_seqlen_q, float scale,
+               int num_q_heads, int num_kv_heads, int head_size,
+               int num_blocks, int block_size, int dtype, pa_stream_t stream);
+
+/*
  * pa_copy_blocks — copy-on-write clones of whole physical blocks
  * ([digest] "写时复制": a shared block is cloned before a write and the
  * writer's table retargeted; [lecture] §4.3 steps: allocate Q, copy P into

@@ -49,6 +49,7 @@ SIGNATURES = [
     ("pa_decode_fp8_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     ("pa_decode_fp8", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _f, _f,
                            _vp, _sz, _u, _vp]),
+    ("pa_prefill", _i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_get_device_error", _i, [_ip]),
     ("pa_alloc_create", _vp, [_i, _i, _i32p]),
@@ -236,6 +237,20 @@ def pa_decode_fp8(out, query, kv_cache, block_tables, seq_lens, scale, k_scale, 
         _dev(seq_lens, "seq_lens"), s, float(scale), hq, hkv, d, nb, bs,
         _dtype_code(query), float(k_scale), float(v_scale), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), int(flags), _stream(stream)))
+
+
+def pa_prefill(out, query, kv_cache, block_tables, cu_seqlens_q, seq_lens, scale, max_seqlen_q,
+               stream=None) -> None:
+    """out/query [total_q, Hq, D]; kv_cache (2, NB, B, Hkv, D); block_tables [S, maxblk] int32;
+    cu_seqlens_q [S + 1] int32; seq_lens [S] int32 (chunk included); max_seqlen_q: host int."""
+    total_q, hq, d = query.shape
+    _, nb, bs, hkv, _ = kv_cache.shape
+    _check(lib().pa_prefill(
+        _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
+        _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
+        _dev(cu_seqlens_q, "cu_seqlens_q"), _dev(seq_lens, "seq_lens"), int(seq_lens.shape[0]),
+        total_q, int(max_seqlen_q), float(scale), hq, hkv, d, nb, bs, _dtype_code(kv_cache),
+        _stream(stream)))
 
 
 def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:

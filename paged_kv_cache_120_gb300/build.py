@@ -27,6 +27,7 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra"]
 
 UNITS = [
     ("pa_kernels.cu", "nvcc"),
+    ("pa_prefill.cu", "nvcc"),
     ("pa_static_scratch.cu", "nvcc"),
     ("block_allocator.cpp", "g++"),
     ("pa_errors.cpp", "g++"),
@@ -35,7 +36,8 @@ UNITS = [
 
 def _sources():
     files = [os.path.join(CSRC, f) for f, _ in UNITS]
-    files += [os.path.join(CSRC, "pa_internal.h"), HEADER, os.path.abspath(__file__)]
+    files += [os.path.join(CSRC, "pa_internal.h"), os.path.join(CSRC, "pa_device.cuh"), HEADER,
+              os.path.abspath(__file__)]
     return files
 
 

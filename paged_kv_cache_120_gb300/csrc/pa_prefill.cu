@@ -1,0 +1,608 @@
+// Causal chunked prefill over the paged pool on GB300's fifth-generation
+// tensor cores (tcgen05 with accumulators in tensor memory).
+//
+// What is computed follows the varlen read of the vLLM book's chapter 4
+// ("第4章 PagedAttention：虚拟内存的启示", §4.5 step 2: the backend hands
+// the cache, cu_seqlens_q, seqused_k and the block table to one call): a
+// chunk of q_len query tokens is the last q_len of the sequence's seq_len
+// cached tokens, query i sits at position p = seq_len - q_len + i, and it
+// attends to tokens 0..p through the block table, with the online softmax
+// of §4.6.
+//
+// How it is computed (one CTA = 128 query rows of one (sequence, kv head)):
+//  * Rows are (query head of the kv head's group, query token) pairs, so the
+//    heads that share a kv head share every K/V tile. A TMEM lane per row.
+//  * Warp 4 loads Q once and then 128-token K and V tiles by TMA (16-token
+//    boxes looked up through the block table, 128-byte swizzle) into a
+//    two-stage ring. Warp 5 issues the MMAs from one thread: S = Q K^T into
+//    one of two TMEM buffers, then O += P V (V read as an MN-major operand)
+//    into a third, so the next tile's scores overlap this tile's softmax.
+//  * Warps 0-3 own one row each: they read the row of S from TMEM, mask it
+//    causally, run the fp32 online softmax in base 2, rescale O in TMEM when
+//    the row's maximum grew, and write P (rounded to the element type) to
+//    shared memory in the MMA's swizzled layout. At the end they read O,
+//    divide by the row sum and store.
+//  * Every wait is bounded; the K/V rows past a sequence's end (padding slots
+//    of its last block, possibly NaN) are zeroed before P V reads them.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__device__ int g_prefill_error;  // PA_DEVERR_* bits of the prefill kernels
+
+namespace {
+
+__device__ __forceinline__ void prefill_raise(int bit) { atomicOr(&g_prefill_error, bit); }
+
+// ------------------------------------------------------------- tcgen05 PTX
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both fp16
+// or both bf16, A K-major, B K-major or MN-major, M x N.
+__device__ __forceinline__ uint32_t instr_desc(int m, int n, bool bf16, bool b_mn)
+{
+    uint32_t d = 1u << 4;
+    d |= (bf16 ? 1u : 0u) << 7;
+    d |= (bf16 ? 1u : 0u) << 10;
+    d |= (b_mn ? 1u : 0u) << 16;
+    d |= (uint32_t)(n >> 3) << 17;
+    d |= (uint32_t)(m >> 4) << 24;
+    return d;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float *v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+        "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// ----------------------------------------------------------------- layout
+
+constexpr int kD = 128;                    // head size (the one built)
+constexpr int kM = 128;                    // query rows per CTA (TMEM lanes)
+constexpr int kN = 128;                    // cached tokens per K/V tile
+constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
+constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit operand: 32 KB
+constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size is a multiple)
+constexpr int kThreads = 192;              // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kOffQ = 0;
+constexpr int kOffK = kTileBytes;          // two stages
+constexpr int kOffV = 3 * kTileBytes;      // two stages
+constexpr int kOffP = 5 * kTileBytes;
+constexpr int kSmemBytes = 6 * kTileBytes + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 512;        // S (two buffers) and O, 128 columns each
+constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+
+struct PrefillParams {
+    void *out;
+    const int32_t *block_tables;
+    const int32_t *cu_q;
+    const int32_t *seq_lens;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_q_heads;
+    int group;          // num_q_heads / num_kv_heads
+    int heads_per_cta;  // query heads of one kv head that share a CTA (<= 16)
+    int head_tiles;     // group / heads_per_cta
+    int rows_per_head;  // query tokens per CTA (multiple of 8)
+    int q_tiles;        // ceil(max_seqlen_q / rows_per_head)
+    int num_blocks;
+    int block_size;
+    int total_q;
+    int max_len;        // max_blocks_per_seq * block_size
+    float scale_log2;   // scale * log2(e)
+};
+
+struct PrefillBars {
+    uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full, pv_done;
+    uint32_t tmem_base;
+    int fail;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap kv_map,
+                         const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PrefillBars bars;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s = blockIdx.z, h = blockIdx.y;
+    const int ht = blockIdx.x % p.head_tiles;
+    const int qt = (p.q_tiles - 1) - blockIdx.x / p.head_tiles;  // heaviest tiles start first
+    const int T = p.rows_per_head, HPC = p.heads_per_cta;
+
+    // The unit (uniform across the CTA); bad offsets or lengths are flagged
+    // by the first CTA of the sequence and skipped.
+    const int q0 = p.cu_q[s];
+    const int q_len = p.cu_q[s + 1] - q0;
+    const int L = p.seq_lens[s];
+    if (q_len < 0 || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len) {
+        if (tid == 0 && blockIdx.x == 0 && h == 0)
+            prefill_raise(PA_DEVERR_SEQ_LEN);
+        return;
+    }
+    const int t0 = qt * T;
+    if (t0 >= q_len)
+        return;
+    const int t_end = min(q_len, t0 + T);
+    const int n_tiles = (L - q_len + t_end + kN - 1) / kN;  // tiles the tile's last query sees
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - raw);
+    const uint32_t sQ = base + kOffQ, sP = base + kOffP;
+    const uint32_t b_q = smem_addr(&bars.q_full), b_p = smem_addr(&bars.p_full),
+                   b_pv = smem_addr(&bars.pv_done);
+    auto sK = [&](int st) { return base + kOffK + st * kTileBytes; };
+    auto sV = [&](int st) { return base + kOffV + st * kTileBytes; };
+    auto b_k = [&](int st) { return smem_addr(&bars.k_full[st]); };
+    auto b_v = [&](int st) { return smem_addr(&bars.v_full[st]); };
+    auto b_e = [&](int st) { return smem_addr(&bars.kv_empty[st]); };
+    auto b_s = [&](int st) { return smem_addr(&bars.s_full[st]); };
+
+    if (tid == 0) {
+        mbar_init(b_q, 1);
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(b_k(st), 1);
+            mbar_init(b_v(st), 1);
+            mbar_init(b_e(st), 1);
+            mbar_init(b_s(st), 1);
+        }
+        mbar_init(b_p, 128);
+        mbar_init(b_pv, 1);
+        bars.fail = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&bars.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    (void)sm;
+
+    // Give up on a wait that runs out (recorded once per CTA); every role then
+    // drains to the teardown.
+    auto wait_or_fail = [&](uint32_t bar, uint32_t parity) {
+        if (mbar_wait(bar, parity))
+            return true;
+        if (atomicExch(&bars.fail, 1) == 0)
+            prefill_raise(PA_DEVERR_TIMEOUT);
+        return false;
+    };
+
+    if (warp == 4) {
+        // ---------------------------------------------------------- TMA
+        const int head0 = h * p.group + ht * HPC;
+        if (lane == 0) {
+            mbar_expect_tx(b_q, (uint32_t)(2 * HPC * T * 128));
+            for (int c = 0; c < 2; ++c)
+                for (int g = 0; g < HPC; ++g)
+                    tma_load_3d(sQ + c * kChunkBytes + g * T * 128, &q_map, b_q, c * 64, head0 + g, q0 + t0);
+        }
+        const int32_t *table = p.block_tables + (long long)s * p.max_blocks_per_seq;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            if (j >= 2 && !wait_or_fail(b_e(st), ((j - 2) >> 1) & 1))
+                break;
+            // lane i < 8 fetches the 16-token box i of the tile
+            int phys = p.num_blocks, tib = 0;
+            const int kt = j * kN + kBoxTokens * lane;
+            if (lane < 8 && kt < L) {
+                const int lb = kt / p.block_size;
+                tib = kt - lb * p.block_size;
+                phys = __ldg(table + lb);
+                if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                    prefill_raise(PA_DEVERR_BLOCK_ID);
+                    phys = p.num_blocks;  // outside the map: the TMA fills zeros
+                }
+            }
+            if (lane == 0) {
+                mbar_expect_tx(b_k(st), kTileBytes);
+                mbar_expect_tx(b_v(st), kTileBytes);
+            }
+            __syncwarp();
+            if (lane < 8) {
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t off = c * kChunkBytes + lane * (kBoxTokens * 128);
+                    tma_load_5d(sK(st) + off, &kv_map, b_k(st), c * 64, h, tib, phys, 0);
+                    tma_load_5d(sV(st) + off, &kv_map, b_v(st), c * 64, h, tib, phys, 1);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t id_s = instr_desc(kM, kN, BF16, false);
+            const uint32_t id_o = instr_desc(kM, kD, BF16, true);
+            auto issue_pv = [&](int jj) {
+                if (!wait_or_fail(b_p, jj & 1) || !wait_or_fail(b_v(jj & 1), (jj >> 1) & 1))
+                    return false;
+                tc_fence_after();
+                // O += P V: A = P (K-major over tokens), B = V (MN-major:
+                // 64-dim chunks 16 KB apart, 8-token groups 1 KB apart).
+                for (int k = 0; k < kN / 16; ++k)
+                    tc_mma(tmem + kTmemO,
+                           smem_desc(sP + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
+                           smem_desc(sV(jj & 1) + k * 2048, kChunkBytes, 1024), id_o,
+                           (jj > 0 || k > 0) ? 1u : 0u);
+                tc_commit(b_pv);
+                tc_commit(b_e(jj & 1));
+                return true;
+            };
+            bool go = wait_or_fail(b_q, 0);
+            for (int j = 0; go && j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (!wait_or_fail(b_k(st), (j >> 1) & 1))
+                    break;
+                tc_fence_after();
+                // S = Q K^T over the head dimension, 16 per MMA.
+                const uint32_t tS = tmem + (st ? kTmemS1 : kTmemS0);
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+                    tc_mma(tS, smem_desc(sQ + off, 16, 1024), smem_desc(sK(st) + off, 16, 1024), id_s,
+                           k > 0 ? 1u : 0u);
+                }
+                tc_commit(b_s(st));
+                if (j > 0)
+                    go = issue_pv(j - 1);
+            }
+            if (go)
+                issue_pv(n_tiles - 1);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax (rows)
+        const int r = tid;  // 0..127, this thread's TMEM lane
+        const int g = r / T, t = r - g * T;
+        const bool valid = g < HPC && t0 + t < q_len;
+        const int pos = valid ? L - q_len + t0 + t : -1;  // last token this row sees
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool alive = true;
+        float sv[kN];
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            if (!__all_sync(kFull, wait_or_fail(b_s(st), (j >> 1) & 1))) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + (st ? kTmemS1 : kTmemS0);
+#pragma unroll
+            for (int c = 0; c < kN / 32; ++c)
+                tc_ld32(tS + c * 32, sv + c * 32);
+            const int kbase = j * kN;
+            float mx = -INFINITY;
+            if (kbase + kN - 1 <= pos) {
+#pragma unroll
+                for (int c = 0; c < kN; ++c) {
+                    sv[c] *= p.scale_log2;
+                    mx = fmaxf(mx, sv[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kN; ++c) {
+                    sv[c] = (kbase + c <= pos) ? sv[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sv[c]);
+                }
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+            const float ref = m_new == -INFINITY ? 0.f : m_new;
+            // The previous P V must be done before O and P are touched.
+            if (j > 0 && !__all_sync(kFull, wait_or_fail(b_pv, (j - 1) & 1))) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+                const uint32_t tO = tmem + lane_off + kTmemO;
+                float o[32];
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    tc_ld32(tO + c * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] *= alpha;
+                    tc_st32(tO + c * 32, o);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            // P, rounded to the element type, into its K-major 128-byte
+            // swizzled rows; the row sum adds the same rounded values.
+            float ls = 0.f;
+#pragma unroll
+            for (int u = 0; u < kN / 8; ++u) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    w[e] = pack2<BF16>(ex2(sv[8 * u + 2 * e] - ref), ex2(sv[8 * u + 2 * e + 1] - ref));
+                    const float2 f = unpack2<BF16>(w[e]);
+                    ls += f.x + f.y;
+                }
+                const int c2 = u >> 3, uu = u & 7;
+                sts128(sP + c2 * kChunkBytes + r * 128 + ((uu ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+            l_run = l_run * alpha + ls;
+            m_run = m_new;
+            // The last tile's V rows past the sequence end hold whatever the
+            // pool's padding slots hold: zero them (P is 0 there) once V lands.
+            if (kbase + kN > L) {
+                if (!__all_sync(kFull, wait_or_fail(b_v(st), (j >> 1) & 1))) {
+                    alive = false;
+                    break;
+                }
+                if (kbase + r >= L)
+                    for (int c = 0; c < 2; ++c)
+                        for (int u = 0; u < 8; ++u)
+                            sts128(sV(st) + c * kChunkBytes + r * 128 + u * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(b_p);
+        }
+        // Epilogue: O / l for the valid rows.
+        if (alive && __all_sync(kFull, wait_or_fail(b_pv, (n_tiles - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t tO = tmem + lane_off + kTmemO;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            uint16_t *out = static_cast<uint16_t *>(p.out) +
+                            ((long long)(q0 + t0 + t) * p.num_q_heads + h * p.group + ht * HPC + g) * kD;
+            float o[32];
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+                tc_ld32(tO + c * 32, o);
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 v;
+                        v.x = pack2<BF16>(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+                        v.y = pack2<BF16>(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+                        v.z = pack2<BF16>(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+                        v.w = pack2<BF16>(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+                        reinterpret_cast<uint4 *>(out + c * 32)[q] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+}
+
+// ================================================================ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Pool as rank 5 (head_size, kv_heads, block slots, blocks, K|V), box of 64
+// dims x one head x 16 slots x one block x one of K/V: 2 KB, 128-byte swizzle.
+int encode_kv_map(CUtensorMap *m, const void *kv, int num_blocks, int block_size, int num_kv_heads)
+{
+    const cuuint64_t e = 2;
+    cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks, 2};
+    cuuint64_t strides[4] = {kD * e, (cuuint64_t)num_kv_heads * kD * e,
+                             (cuuint64_t)block_size * num_kv_heads * kD * e,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * kD * e};
+    cuuint32_t box[5] = {64, 1, (cuuint32_t)kBoxTokens, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void *>(kv), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : set_error(PA_ERR_CUDA, "pa_prefill: K/V tensor map (%d)", (int)r);
+}
+
+// Queries as rank 3 (head_size, q_heads, tokens), box of 64 dims x one head x
+// rows_per_head tokens.
+int encode_q_map(CUtensorMap *m, const void *q, int total_q, int num_q_heads, int rows)
+{
+    const cuuint64_t e = 2;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {kD * e, (cuuint64_t)num_q_heads * kD * e};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(q), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : set_error(PA_ERR_CUDA, "pa_prefill: query tensor map (%d)", (int)r);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+int prefill_take_device_error(int *bits)
+{
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(int));
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(int));
+    *bits = e == cudaSuccess ? v : 0;
+    return (int)e;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                          int num_seqs, int total_q, int max_seqlen_q, float scale, int num_q_heads,
+                          int num_kv_heads, int head_size, int num_blocks, int block_size, int dtype,
+                          pa_stream_t stream)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: dtype %d (want PA_F16 or PA_BF16)", dtype);
+    if (head_size != kD)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: head_size %d (built: 128)", head_size);
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return set_error(PA_ERR_INVALID_ARG,
+                         "pa_prefill: num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                         num_q_heads, num_kv_heads);
+    const int group = num_q_heads / num_kv_heads;
+    if (group > 16 && group % 16 != 0)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: query group %d (want <= 16 or a multiple of 16)",
+                         group);
+    if (block_size < kBoxTokens || block_size % kBoxTokens != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: block_size %d must be a positive multiple of 16",
+                         block_size);
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: bad sizes");
+    if (num_seqs > 65535 || num_kv_heads > 65535)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: num_seqs and num_kv_heads must be <= 65535");
+    if ((long long)max_blocks_per_seq * block_size > (1LL << 30))
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: max_blocks_per_seq * block_size too large");
+    if (!std::isfinite(scale))
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: scale is not finite");
+    if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0)
+        return PA_OK;
+    if (!out || !query || !kv_cache || !block_tables || !cu_seqlens_q || !seq_lens)
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: null pointer argument");
+    if (!aligned16(out) || !aligned16(query) || !aligned16(kv_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3) || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3))
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: misaligned pointer (query/out/pool 16 B)");
+    if (!encoder())
+        return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+
+    PrefillParams prm;
+    prm.out = out;
+    prm.block_tables = block_tables;
+    prm.cu_q = cu_seqlens_q;
+    prm.seq_lens = seq_lens;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.group = group;
+    prm.heads_per_cta = group < 16 ? group : 16;
+    prm.head_tiles = group / prm.heads_per_cta;
+    prm.rows_per_head = (kM / prm.heads_per_cta) & ~7;
+    prm.q_tiles = (max_seqlen_q + prm.rows_per_head - 1) / prm.rows_per_head;
+    prm.num_blocks = num_blocks;
+    prm.block_size = block_size;
+    prm.total_q = total_q;
+    prm.max_len = max_blocks_per_seq * block_size;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    if ((long long)prm.q_tiles * prm.head_tiles > 0x7fffffffLL)
+        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: too many query tiles");
+
+    CUtensorMap kv_map, q_map;
+    int rc = encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads);
+    if (rc != PA_OK)
+        return rc;
+    rc = encode_q_map(&q_map, query, total_q, num_q_heads, prm.rows_per_head);
+    if (rc != PA_OK)
+        return rc;
+
+    const void *fn = dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true>)
+                                      : reinterpret_cast<const void *>(&paged_prefill_kernel<false>);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess)
+        return set_error(PA_ERR_CUDA, "pa_prefill: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    const dim3 grid((unsigned)(prm.q_tiles * prm.head_tiles), (unsigned)num_kv_heads, (unsigned)num_seqs);
+    void *args[] = {&kv_map, &q_map, &prm};
+    e = cudaLaunchKernel(fn, grid, dim3(kThreads), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return set_error(PA_ERR_CUDA, "pa_prefill: launch: %s", cudaGetErrorString(e));
+    return PA_OK;
+}

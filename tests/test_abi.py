@@ -27,7 +27,7 @@ def _declared_functions():
 
 def test_every_declared_function_is_exported(lib):
     names = _declared_functions()
-    assert len(names) >= 22
+    assert len(names) >= 23
     for n in names:
         assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
     assert sorted(n for n, _, _ in binding.SIGNATURES) == names
@@ -63,6 +63,28 @@ def test_host_side_validation_without_a_gpu(lib):
     assert lib.pa_copy_blocks(null, 1, null, 0, 10, 16, 1, 8, binding.PA_FP8_E4M3, null) \
         == binding.PA_ERR_INVALID_ARG          # an 8-byte FP8 row cannot be copied in 16-byte units
     assert lib.pa_copy_blocks(null, 1, null, 0, 10, 16, 8, 128, 3, null) == binding.PA_ERR_UNSUPPORTED
+
+
+def test_prefill_host_side_validation_without_a_gpu(lib):
+    null = None
+    ok_args = dict(bt=null, maxb=4, cu=null, sl=null, S=2, total=10, maxq=8, scale=0.1, hq=8, hkv=2,
+                   d=128, nb=16, bs=16, dt=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.pa_prefill(null, null, null, a["bt"], a["maxb"], a["cu"], a["sl"], a["S"], a["total"],
+                              a["maxq"], a["scale"], a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["dt"],
+                              null)
+    assert call(d=64) == binding.PA_ERR_UNSUPPORTED
+    assert call(dt=2) == binding.PA_ERR_UNSUPPORTED
+    assert call(hq=40, hkv=2) == binding.PA_ERR_UNSUPPORTED      # group 20
+    assert call(hkv=3) == binding.PA_ERR_INVALID_ARG
+    assert call(bs=24) == binding.PA_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == binding.PA_ERR_INVALID_ARG
+    assert call() == binding.PA_ERR_INVALID_ARG                  # null pointers
+    assert call(S=0) == binding.PA_OK
+    assert call(total=0) == binding.PA_OK
+    assert call(maxq=0) == binding.PA_OK
 
 
 def test_fp8_host_side_validation_without_a_gpu(lib):
