@@ -12,6 +12,10 @@ Prints one JSON line (rank 0). ``value`` is the step's algorithmic HBM bytes
 per second (GB/s); ``seq_steps_per_s`` is sequences decoded per second.
 ``--kv-cache fp8`` runs the same step on a cache of E4M3 codes (one byte per
 K/V element, per-tensor scales): pa_reshape_and_cache_fp8 and pa_decode_fp8.
+``--workload prefill_llama13b|prefill_gqa8b`` times a chunked-prefill step
+instead (pa_reshape_and_cache of each sequence's 1024-token chunk, then the
+tcgen05 pa_prefill): ``value`` is causal attention TFLOP/s and the roofline is
+the tensor-core one.
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead.
 Under torchrun every rank runs its own replica of the workload (weak
 scaling: sequences are independent, no collective on the data path).
@@ -422,13 +426,199 @@ def run_ours(args, rank, local_rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ prefill
+
+PREFILL_METRIC = "paged chunked-prefill causal attention TFLOP/s"
+
+
+def measured_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (the prefill step is timed inside a long
+    loop); fp16 runs at the same nominal rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS)"
+    except Exception:
+        return 1700.0, "fallback 1.7 PFLOP/s sustained (MEASURED_PEAKS.json absent)"
+
+
+def prefill_config(name, plan):
+    w = workloads.PREFILL_WORKLOADS[name]
+    return {"workload": f"{name}: {w.description}", "num_seqs": w.num_seqs,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
+            "block_size": w.block_size, "num_blocks": int(plan.num_blocks),
+            "seq_lens": [int(x) for x in plan.seq_lens], "chunk": w.chunk,
+            "l2": "K/V of all sequences read per step (~%.0f MB) and reused across query tiles; no flush"
+                  % (2 * int(plan.seq_lens.sum()) * w.num_kv_heads * w.head_size * 2 / 1e6)}
+
+
+def oracle_prefill_sample(name, plan, pool_bits, q_bits, budget_s: float, start: int = 0):
+    """The oracle on prefill rows (every query head of one chunk row at a
+    time, round-robin over rows) for about budget_s. Returns (seconds, flops
+    covered, rows, next start)."""
+    import oracle
+    w = workloads.PREFILL_WORKLOADS[name]
+    S = len(plan.seq_lens)
+    rows = int(plan.cu_seqlens_q[-1])
+    t, flops, n = 0.0, 0, 0
+    k = start
+    heads = np.arange(w.num_q_heads, dtype=np.int32)
+    while t < budget_s and n < rows:
+        row = (k * 7919) % rows
+        s = int(np.searchsorted(plan.cu_seqlens_q, row, side="right") - 1)
+        i = row - int(plan.cu_seqlens_q[s])
+        vis = int(plan.seq_lens[s]) - int(plan.chunk_lens[s]) + i + 1
+        t0 = time.perf_counter()
+        oracle.decode_sampled(np.zeros(w.num_q_heads, np.int32), heads, q_bits[row:row + 1], pool_bits,
+                              plan.block_tables[s:s + 1], np.array([vis], np.int32), w.scale,
+                              w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks, w.block_size,
+                              w.dtype)
+        t += time.perf_counter() - t0
+        flops += 4 * w.head_size * w.num_q_heads * vis
+        n += 1
+        k += 1
+    return t, flops, n, k
+
+
+def run_prefill(args, rank, local_rank, world):
+    import torch
+    from paged_kv_cache_120_gb300 import binding, build, step as stepmod
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name = args.workload
+    w = workloads.PREFILL_WORKLOADS[name]
+    seed = args.seed + 1000 * rank
+    plan = stepmod.plan_prefill(name, seed)
+    st = stepmod.PrefillStep(name, plan, seed, dev)
+    flops = stepmod.prefill_flops(plan, w.num_q_heads, w.head_size)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        st.run()
+    torch.cuda.synchronize(dev)
+    if binding.pa_get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    K = args.steps
+    EV_EVERY = 8
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range((K + EV_EVERY - 1) // EV_EVERY)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(K):
+        st.reshape()
+        if i % EV_EVERY == 0:
+            ev[i // EV_EVERY][0].record(stream)
+            st.prefill()
+            ev[i // EV_EVERY][1].record(stream)
+        else:
+            st.prefill()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world, dev)
+    if clocks:
+        clocks.stop()
+    t_s = dist_max(start.elapsed_time(end) / 1e3, world, dev)
+    pre_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    dev_err = binding.pa_get_device_error()
+    if dev_err:
+        raise RuntimeError(f"device error word {dev_err} set during the timed region")
+
+    host = {n: getattr(st, n).cpu().pin_memory() for n in
+            ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens", "cu_seqlens_q")}
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    for _ in range(3):
+        st.run_host(host, out_host)
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ke = max(1, min(K, 200))
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        st.run_host(host, out_host)
+    e2e_s = dist_max(time.perf_counter() - t0, world, dev)
+    dist_barrier(world, dev)
+    if rank != 0:
+        return
+    peak, peak_note = measured_tensor_peak()
+    achieved = flops / (pre_ms / 1e3) / 1e12
+    value = world * flops * K / t_s / 1e12
+    pool_bits = st.pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    q_bits = st.query.view(torch.int16).cpu().numpy().view(np.uint16)
+    ot, of, on, _ = oracle_prefill_sample(name, plan, pool_bits, q_bits, args.cpu_budget)
+    del pool_bits
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_s * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
+        "data": "synthetic (seeded N(0,1) values, seeded block placement)",
+        "config": prefill_config(name, plan),
+        "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) * K / t_s,
+        "prefill_only": {"ms": pre_ms, "tflops": achieved, "sampled_launches": len(ev)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill (paged_prefill_kernel)",
+                     "peak_source": peak_note, "flops_per_launch": flops},
+        "e2e": {"value": world * flops * ke / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3 / ke},
+        "gpu_launches": st.launches_per_step() * K,
+        "cpu_baseline": {"value": of / ot / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{on} query rows x {w.num_q_heads} heads of the same batch "
+                                   f"({ot:.1f} s, single-threaded fp64 C)"},
+        "clocks": clocks.summary() if clocks else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill_reference(args, rank, world):
+    """The reference arm for a prefill workload: the oracle on sampled rows."""
+    if rank != 0:
+        return
+    import torch
+    from paged_kv_cache_120_gb300 import step as stepmod
+    name = args.workload
+    w = workloads.PREFILL_WORKLOADS[name]
+    plan = stepmod.plan_prefill(name, args.seed)
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
+    st = stepmod.PrefillStep(name, plan, args.seed, dev)
+    pool_bits = st.pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    q_bits = st.query.view(torch.int16).cpu().numpy().view(np.uint16)
+    del st
+    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    nxt = 0
+    for _ in range(args.warmup):
+        _, _, _, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt)
+    tt, tf, tn = 0.0, 0, 0
+    for _ in range(args.steps):
+        a, b, c, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt)
+        tt, tf, tn = tt + a, tf + b, tn + c
+    v = tf / tt / 1e12
+    sample = f"{tn} query rows x {w.num_q_heads} heads of the {name} batch, about {per_step:.2f} s per step"
+    print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "TFLOP/s",
+                      "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": prefill_config(name, plan),
+                      "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                       "sample": sample},
+                      "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama13b", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="llama13b",
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.PREFILL_WORKLOADS))
     ap.add_argument("--variant", default="literal", choices=["literal", "fork"])
     ap.add_argument("--kv-cache", default="16bit", choices=["16bit", "fp8"],
                     help="cache element type: the workload's 16-bit type, or E4M3 codes")
@@ -439,10 +629,13 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     rank, local_rank, world = dist_setup()
+    prefill = args.workload in workloads.PREFILL_WORKLOADS
+    if prefill and args.kv_cache != "16bit":
+        ap.error("--kv-cache fp8 applies to the decode workloads")
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_prefill_reference(args, rank, world) if prefill else run_reference(args, rank, world))
     else:
-        run_ours(args, rank, local_rank, world)
+        (run_prefill(args, rank, local_rank, world) if prefill else run_ours(args, rank, local_rank, world))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

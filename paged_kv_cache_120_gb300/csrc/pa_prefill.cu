@@ -13,13 +13,15 @@
 //  * Rows are (query head of the kv head's group, query token) pairs, so the
 //    heads that share a kv head share every K/V tile. A TMEM lane per row.
 //  * Warp 4 loads Q once and then 128-token K and V tiles by TMA (16-token
-//    boxes looked up through the block table, 128-byte swizzle) into a
-//    two-stage ring. Warp 5 issues the MMAs from one thread: S = Q K^T into
+//    boxes looked up through the block table, 128-byte swizzle) into rings
+//    of three K and two V stages, K and V each produced at its own pace. Warp 5 issues the MMAs from one thread: S = Q K^T into
 //    one of two TMEM buffers, then O += P V (V read as an MN-major operand)
 //    into a third, so the next tile's scores overlap this tile's softmax.
 //  * Warps 0-3 own one row each: they read the row of S from TMEM, mask it
-//    causally, run the fp32 online softmax in base 2, rescale O in TMEM when
-//    the row's maximum grew, and write P (rounded to the element type) to
+//    causally, run the fp32 online softmax in base 2 (the reference maximum
+//    moves only when a score exceeds it by 2^8, so O in TMEM is rarely
+//    rescaled and the next tile's softmax need not wait for this tile's
+//    P V), and write P (rounded to the element type) to
 //    shared memory in the MMA's swizzled layout. At the end they read O,
 //    divide by the row sum and store.
 //  * Every wait is bounded; the K/V rows past a sequence's end (padding slots
@@ -92,7 +94,25 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective);
+// the registers are valid after tc_wait_ld().
+__device__ __forceinline__ void tc_ld32_async(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// The same, waited for and converted.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float *v)
 {
     uint32_t r[32];
@@ -138,14 +158,17 @@ constexpr int kN = 128;                    // cached tokens per K/V tile
 constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
 constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit operand: 32 KB
 constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size is a multiple)
-constexpr int kThreads = 192;              // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kThreads = 224;              // warps 0-3 softmax, 4 Q/K TMA, 5 MMA, 6 V TMA
+constexpr int kKStages = 3;                // K ring (freed when S = Q K^T is done)
+constexpr int kVStages = 2;                // V ring (freed when O += P V is done)
 constexpr int kOffQ = 0;
-constexpr int kOffK = kTileBytes;          // two stages
-constexpr int kOffV = 3 * kTileBytes;      // two stages
-constexpr int kOffP = 5 * kTileBytes;
-constexpr int kSmemBytes = 6 * kTileBytes + 1024;  // + slack to align the base to 1024
+constexpr int kOffK = kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffP = kOffV + kVStages * kTileBytes;
+constexpr int kSmemBytes = kOffP + kTileBytes + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 512;        // S (two buffers) and O, 128 columns each
 constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
 
 struct PrefillParams {
     void *out;
@@ -168,7 +191,8 @@ struct PrefillParams {
 };
 
 struct PrefillBars {
-    uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full, pv_done;
+    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full[2], p_full, pv_done;
     uint32_t tmem_base;
     int fail;
 };
@@ -205,25 +229,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *sm = smem_raw + (base - raw);
     const uint32_t sQ = base + kOffQ, sP = base + kOffP;
-    const uint32_t b_q = smem_addr(&bars.q_full), b_p = smem_addr(&bars.p_full),
-                   b_pv = smem_addr(&bars.pv_done);
     auto sK = [&](int st) { return base + kOffK + st * kTileBytes; };
     auto sV = [&](int st) { return base + kOffV + st * kTileBytes; };
-    auto b_k = [&](int st) { return smem_addr(&bars.k_full[st]); };
-    auto b_v = [&](int st) { return smem_addr(&bars.v_full[st]); };
-    auto b_e = [&](int st) { return smem_addr(&bars.kv_empty[st]); };
-    auto b_s = [&](int st) { return smem_addr(&bars.s_full[st]); };
+    const uint32_t b_q = smem_addr(&bars.q_full), b_p = smem_addr(&bars.p_full),
+                   b_pv = smem_addr(&bars.pv_done);
+    auto b_kf = [&](int st) { return smem_addr(&bars.k_full[st]); };
+    auto b_ke = [&](int st) { return smem_addr(&bars.k_empty[st]); };
+    auto b_vf = [&](int st) { return smem_addr(&bars.v_full[st]); };
+    auto b_ve = [&](int st) { return smem_addr(&bars.v_empty[st]); };
+    auto b_s = [&](int b) { return smem_addr(&bars.s_full[b]); };
 
     if (tid == 0) {
         mbar_init(b_q, 1);
-        for (int st = 0; st < 2; ++st) {
-            mbar_init(b_k(st), 1);
-            mbar_init(b_v(st), 1);
-            mbar_init(b_e(st), 1);
-            mbar_init(b_s(st), 1);
+        for (int st = 0; st < kKStages; ++st) {
+            mbar_init(b_kf(st), 1);
+            mbar_init(b_ke(st), 1);
         }
+        for (int st = 0; st < kVStages; ++st) {
+            mbar_init(b_vf(st), 1);
+            mbar_init(b_ve(st), 1);
+        }
+        mbar_init(b_s(0), 1);
+        mbar_init(b_s(1), 1);
         mbar_init(b_p, 128);
         mbar_init(b_pv, 1);
         bars.fail = 0;
@@ -240,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    (void)sm;
 
     // Give up on a wait that runs out (recorded once per CTA); every role then
     // drains to the teardown.
@@ -252,43 +279,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
     };
 
-    if (warp == 4) {
+    if (warp == 4 || warp == 6) {
         // ---------------------------------------------------------- TMA
-        const int head0 = h * p.group + ht * HPC;
-        if (lane == 0) {
+        // Warp 4 produces Q and the K tiles, warp 6 the V tiles, each at its
+        // own pace (separate warps, so that one producer's wait never holds
+        // up the other); lane i < 8 moves the 16-token box i of each tile.
+        // The block-table entry of the next tile is loaded while the current
+        // one waits for its stage.
+        const int32_t *table = p.block_tables + (long long)s * p.max_blocks_per_seq;
+        const bool is_k = warp == 4;
+        if (is_k && lane == 0) {
+            const int head0 = h * p.group + ht * HPC;
             mbar_expect_tx(b_q, (uint32_t)(2 * HPC * T * 128));
             for (int c = 0; c < 2; ++c)
                 for (int g = 0; g < HPC; ++g)
                     tma_load_3d(sQ + c * kChunkBytes + g * T * 128, &q_map, b_q, c * 64, head0 + g, q0 + t0);
         }
-        const int32_t *table = p.block_tables + (long long)s * p.max_blocks_per_seq;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
-            if (j >= 2 && !wait_or_fail(b_e(st), ((j - 2) >> 1) & 1))
-                break;
-            // lane i < 8 fetches the 16-token box i of the tile
-            int phys = p.num_blocks, tib = 0;
-            const int kt = j * kN + kBoxTokens * lane;
-            if (lane < 8 && kt < L) {
-                const int lb = kt / p.block_size;
-                tib = kt - lb * p.block_size;
-                phys = __ldg(table + lb);
-                if ((unsigned)phys >= (unsigned)p.num_blocks) {
+        if (lane < 8) {
+            const int box = lane, leader = 0;
+            const unsigned group_mask = 0x000000FFu;
+            const int stages = is_k ? kKStages : kVStages;
+            auto lookup = [&](int j) {
+                const int kt = j * kN + kBoxTokens * box;
+                return (j < n_tiles && kt < L) ? __ldg(table + kt / p.block_size) : -1;
+            };
+            int next = lookup(0);
+            for (int j = 0; j < n_tiles; ++j) {
+                int phys = next;
+                next = lookup(j + 1);
+                const int st = j % stages;
+                if (j >= stages &&
+                    !wait_or_fail(is_k ? b_ke(st) : b_ve(st), ((j - stages) / stages) & 1))
+                    break;
+                const int kt = j * kN + kBoxTokens * box;
+                const int tib = kt % p.block_size;
+                if (phys >= p.num_blocks || (phys < 0 && kt < L)) {
                     prefill_raise(PA_DEVERR_BLOCK_ID);
-                    phys = p.num_blocks;  // outside the map: the TMA fills zeros
+                    phys = p.num_blocks;
                 }
-            }
-            if (lane == 0) {
-                mbar_expect_tx(b_k(st), kTileBytes);
-                mbar_expect_tx(b_v(st), kTileBytes);
-            }
-            __syncwarp();
-            if (lane < 8) {
-                for (int c = 0; c < 2; ++c) {
-                    const uint32_t off = c * kChunkBytes + lane * (kBoxTokens * 128);
-                    tma_load_5d(sK(st) + off, &kv_map, b_k(st), c * 64, h, tib, phys, 0);
-                    tma_load_5d(sV(st) + off, &kv_map, b_v(st), c * 64, h, tib, phys, 1);
-                }
+                if (phys < 0)
+                    phys = p.num_blocks;  // past the sequence end: outside the map, zeros
+                const uint32_t full = is_k ? b_kf(st) : b_vf(st);
+                if (lane == leader)
+                    mbar_expect_tx(full, kTileBytes);
+                __syncwarp(group_mask);
+                const uint32_t dst = (is_k ? sK(st) : sV(st)) + box * (kBoxTokens * 128);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, h, tib, phys, is_k ? 0 : 1);
             }
         }
     } else if (warp == 5) {
@@ -297,34 +334,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_s = instr_desc(kM, kN, BF16, false);
             const uint32_t id_o = instr_desc(kM, kD, BF16, true);
             auto issue_pv = [&](int jj) {
-                if (!wait_or_fail(b_p, jj & 1) || !wait_or_fail(b_v(jj & 1), (jj >> 1) & 1))
+                const int vs = jj % kVStages;
+                if (!wait_or_fail(b_p, jj & 1) || !wait_or_fail(b_vf(vs), (jj / kVStages) & 1))
                     return false;
                 tc_fence_after();
                 // O += P V: A = P (K-major over tokens), B = V (MN-major:
                 // 64-dim chunks 16 KB apart, 8-token groups 1 KB apart).
                 for (int k = 0; k < kN / 16; ++k)
-                    tc_mma(tmem + kTmemO,
-                           smem_desc(sP + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
-                           smem_desc(sV(jj & 1) + k * 2048, kChunkBytes, 1024), id_o,
+                    tc_mma(tmem + kTmemO, smem_desc(sP + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
+                           smem_desc(sV(vs) + k * 2048, kChunkBytes, 1024), id_o,
                            (jj > 0 || k > 0) ? 1u : 0u);
                 tc_commit(b_pv);
-                tc_commit(b_e(jj & 1));
+                tc_commit(b_ve(vs));
                 return true;
             };
             bool go = wait_or_fail(b_q, 0);
             for (int j = 0; go && j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (!wait_or_fail(b_k(st), (j >> 1) & 1))
+                const int ks = j % kKStages;
+                if (!wait_or_fail(b_kf(ks), (j / kKStages) & 1))
                     break;
                 tc_fence_after();
                 // S = Q K^T over the head dimension, 16 per MMA.
-                const uint32_t tS = tmem + (st ? kTmemS1 : kTmemS0);
+                const uint32_t tS = tmem + ((j & 1) ? kTmemS1 : kTmemS0);
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-                    tc_mma(tS, smem_desc(sQ + off, 16, 1024), smem_desc(sK(st) + off, 16, 1024), id_s,
+                    tc_mma(tS, smem_desc(sQ + off, 16, 1024), smem_desc(sK(ks) + off, 16, 1024), id_s,
                            k > 0 ? 1u : 0u);
                 }
-                tc_commit(b_s(st));
+                tc_commit(b_s(j & 1));
+                tc_commit(b_ke(ks));
                 if (j > 0)
                     go = issue_pv(j - 1);
             }
@@ -341,37 +379,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         float m_run = -INFINITY, l_run = 0.f;
         bool alive = true;
-        float sv[kN];
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
-            if (!__all_sync(kFull, wait_or_fail(b_s(st), (j >> 1) & 1))) {
+            const int b = j & 1;
+            if (!__all_sync(kFull, wait_or_fail(b_s(b), (j >> 1) & 1))) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t tS = tmem + lane_off + (st ? kTmemS1 : kTmemS0);
+            float sv[kN];
+            {
+                const uint32_t tS = tmem + lane_off + (b ? kTmemS1 : kTmemS0);
+                uint32_t *rawv = reinterpret_cast<uint32_t *>(sv);
 #pragma unroll
-            for (int c = 0; c < kN / 32; ++c)
-                tc_ld32(tS + c * 32, sv + c * 32);
+                for (int c = 0; c < kN / 32; ++c)
+                    tc_ld32_async(tS + c * 32, rawv + c * 32);
+                tc_wait_ld();
+            }
             const int kbase = j * kN;
-            float mx = -INFINITY;
+            // Scale (and mask) the row; its maximum over 8 independent chains.
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                m8[i] = -INFINITY;
             if (kbase + kN - 1 <= pos) {
 #pragma unroll
                 for (int c = 0; c < kN; ++c) {
                     sv[c] *= p.scale_log2;
-                    mx = fmaxf(mx, sv[c]);
+                    m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < kN; ++c) {
                     sv[c] = (kbase + c <= pos) ? sv[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
+                    m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
                 }
             }
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            // The row's reference maximum moves only when a score exceeds it
+            // by more than kRescaleLog2 (P then stays <= 2^kRescaleLog2, which
+            // the element type holds with full relative precision); O and l
+            // are rescaled only then.
+            const bool grow = mx > m_run + kRescaleLog2;
+            const float m_new = grow ? mx : m_run;
+            const float alpha = grow ? ex2(m_run - m_new) : 1.f;
             const float ref = m_new == -INFINITY ? 0.f : m_new;
-            // The previous P V must be done before O and P are touched.
+            // P, rounded to the element type, packed in registers; the row
+            // sum adds the same rounded values.
+            uint32_t pw[kN / 2];
+            float l8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                l8[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kN / 2; ++c) {
+                pw[c] = pack2<BF16>(ex2(sv[2 * c] - ref), ex2(sv[2 * c + 1] - ref));
+                const float2 f = unpack2<BF16>(pw[c]);
+                l8[c & 7] += f.x + f.y;
+            }
+            const float ls = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            // The previous tile's P V must be done before P is overwritten
+            // and before O is rescaled.
             if (j > 0 && !__all_sync(kFull, wait_or_fail(b_pv, (j - 1) & 1))) {
                 alive = false;
                 break;
@@ -390,34 +458,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            // P, rounded to the element type, into its K-major 128-byte
-            // swizzled rows; the row sum adds the same rounded values.
-            float ls = 0.f;
+            // P into its K-major 128-byte swizzled rows.
 #pragma unroll
             for (int u = 0; u < kN / 8; ++u) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    w[e] = pack2<BF16>(ex2(sv[8 * u + 2 * e] - ref), ex2(sv[8 * u + 2 * e + 1] - ref));
-                    const float2 f = unpack2<BF16>(w[e]);
-                    ls += f.x + f.y;
-                }
                 const int c2 = u >> 3, uu = u & 7;
-                sts128(sP + c2 * kChunkBytes + r * 128 + ((uu ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+                sts128(sP + c2 * kChunkBytes + r * 128 + ((uu ^ (r & 7)) << 4), pw[4 * u], pw[4 * u + 1],
+                       pw[4 * u + 2], pw[4 * u + 3]);
             }
             l_run = l_run * alpha + ls;
             m_run = m_new;
             // The last tile's V rows past the sequence end hold whatever the
             // pool's padding slots hold: zero them (P is 0 there) once V lands.
             if (kbase + kN > L) {
-                if (!__all_sync(kFull, wait_or_fail(b_v(st), (j >> 1) & 1))) {
+                const int vs = j % kVStages;
+                if (!__all_sync(kFull, wait_or_fail(b_vf(vs), (j / kVStages) & 1))) {
                     alive = false;
                     break;
                 }
                 if (kbase + r >= L)
                     for (int c = 0; c < 2; ++c)
                         for (int u = 0; u < 8; ++u)
-                            sts128(sV(st) + c * kChunkBytes + r * 128 + u * 16, 0u, 0u, 0u, 0u);
+                            sts128(sV(vs) + c * kChunkBytes + r * 128 + u * 16, 0u, 0u, 0u, 0u);
             }
             fence_proxy_async();
             tc_fence_before();

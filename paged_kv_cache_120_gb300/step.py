@@ -188,3 +188,95 @@ def make_device_inputs(name: str, plan: StepPlan, seed: int, device, kv_cache: s
     key_new = workloads.normal_values((s, w.num_kv_heads, w.head_size), w.dtype, seed + 12, device)
     value_new = workloads.normal_values((s, w.num_kv_heads, w.head_size), w.dtype, seed + 13, device)
     return pool, query, key_new, value_new
+
+
+# ------------------------------------------------------------------ prefill
+
+@dataclasses.dataclass
+class PrefillPlan:
+    seq_ids: list
+    seq_lens: np.ndarray        # prefix + chunk per sequence
+    chunk_lens: np.ndarray      # query tokens per sequence
+    cu_seqlens_q: np.ndarray    # [S + 1]
+    block_tables: np.ndarray
+    slot_mapping: np.ndarray    # [total_q]: the chunk's slots, sequence-major
+    num_blocks: int
+    allocator: object
+
+
+def plan_prefill(name: str, seed: int) -> PrefillPlan:
+    """Lay out each sequence's cached prefix, then reserve its chunk's slots."""
+    w = workloads.PREFILL_WORKLOADS[name]
+    pref = workloads.prefill_prefixes(name, seed)
+    chunk = np.full(w.num_seqs, w.chunk, dtype=np.int32)
+    need = int(((pref + chunk + w.block_size - 1) // w.block_size).sum())
+    num_blocks = need + 64
+    alloc = binding.BlockAllocator(num_blocks, w.block_size,
+                                   workloads.free_order(num_blocks, seed))
+    ids = [alloc.add_seq(int(p)) for p in pref]
+    slots = [alloc.append_token(sid)[0] for sid in ids for _ in range(w.chunk)]
+    lens = alloc.seq_lens(ids)
+    max_blocks = max(1, max(alloc.num_blocks_of(sid) for sid in ids))
+    return PrefillPlan(seq_ids=ids, seq_lens=lens, chunk_lens=chunk,
+                       cu_seqlens_q=np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32),
+                       block_tables=alloc.block_tables(ids, max_blocks),
+                       slot_mapping=np.asarray(slots, dtype=np.int32), num_blocks=num_blocks,
+                       allocator=alloc)
+
+
+class PrefillStep:
+    """Device buffers of one chunked-prefill step: the chunk's K/V are written
+    by slot (pa_reshape_and_cache), then pa_prefill reads the whole causal
+    context of every query through the block table."""
+
+    def __init__(self, name: str, plan: PrefillPlan, seed: int, device):
+        import torch
+        self.w = w = workloads.PREFILL_WORKLOADS[name]
+        total = int(plan.cu_seqlens_q[-1])
+        self.pool = workloads.normal_values(
+            (2, plan.num_blocks, w.block_size, w.num_kv_heads, w.head_size), w.dtype, seed + 20, device)
+        self.query = workloads.normal_values((total, w.num_q_heads, w.head_size), w.dtype, seed + 21, device)
+        self.key_new = workloads.normal_values((total, w.num_kv_heads, w.head_size), w.dtype, seed + 22, device)
+        self.value_new = workloads.normal_values((total, w.num_kv_heads, w.head_size), w.dtype, seed + 23,
+                                                 device)
+        t = lambda a: torch.from_numpy(a).to(device)
+        self.block_tables, self.seq_lens = t(plan.block_tables), t(plan.seq_lens)
+        self.cu_seqlens_q, self.slot_mapping = t(plan.cu_seqlens_q), t(plan.slot_mapping)
+        self.max_seqlen_q = int(plan.chunk_lens.max())
+        self.out = torch.empty_like(self.query)
+
+    def launches_per_step(self) -> int:
+        return 2  # reshape_and_cache + prefill
+
+    def run(self, stream=None) -> None:
+        self.reshape(stream)
+        self.prefill(stream)
+
+    def reshape(self, stream=None) -> None:
+        binding.pa_reshape_and_cache(self.key_new, self.value_new, self.pool, self.slot_mapping, stream)
+
+    def prefill(self, stream=None) -> None:
+        binding.pa_prefill(self.out, self.query, self.pool, self.block_tables, self.cu_seqlens_q,
+                           self.seq_lens, self.w.scale, self.max_seqlen_q, stream)
+
+    def run_host(self, host: dict, out_host, stream=None) -> None:
+        """The step from pinned host buffers (query, key_new, value_new,
+        slot_mapping, block_tables, seq_lens, cu_seqlens_q), output back."""
+        import torch
+        for name in ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens",
+                     "cu_seqlens_q"):
+            getattr(self, name).copy_(host[name], non_blocking=True)
+        self.run(stream)
+        out_host.copy_(self.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+
+def prefill_flops(plan: PrefillPlan, num_q_heads: int, head_size: int) -> int:
+    """Causal attention flops of a step: every (query, head) row attends to its
+    p + 1 visible tokens with a dot product and a weighted sum (4 D flops per
+    token)."""
+    total = 0
+    for L, q in zip(plan.seq_lens.tolist(), plan.chunk_lens.tolist()):
+        first = L - q + 1  # visible tokens of the chunk's first query
+        total += (first + L) * q // 2
+    return 4 * head_size * num_q_heads * total

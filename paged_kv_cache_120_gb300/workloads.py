@@ -66,6 +66,42 @@ WORKLOADS = {
                            "prefix sharing + COW: 16x8 seqs, 1024-token shared prompt, tails U[1,512]"),
 }
 
+# Chunked-prefill workloads (many queries per sequence, causal): each
+# sequence holds a cached prefix of U[0, max_prefix] tokens and this step
+# brings a chunk of `chunk` new tokens whose K/V are written first, as the
+# varlen read of the book's §4.5 receives them.
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    name: str
+    block_size: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_size: int
+    dtype: int
+    num_seqs: int
+    max_prefix: int
+    chunk: int
+    scale: float
+    description: str
+
+
+PREFILL_WORKLOADS = {
+    "prefill_llama13b": PrefillWorkload(
+        "prefill_llama13b", 16, 40, 40, 128, F16, 8, 2048, 1024, 128 ** -0.5,
+        "Llama-2-13B layer chunked prefill: 40/40 heads, d=128, fp16, 8 seqs, "
+        "prefix U[0,2048] + 1024-token chunk"),
+    "prefill_gqa8b": PrefillWorkload(
+        "prefill_gqa8b", 16, 32, 8, 128, BF16, 8, 4096, 1024, 128 ** -0.5,
+        "GQA 8B chunked prefill: 32/8 heads, d=128, bf16, 8 seqs, prefix U[0,4096] + 1024-token chunk"),
+}
+
+
+def prefill_prefixes(name: str, seed: int) -> np.ndarray:
+    """Cached prefix length of every sequence of a prefill workload."""
+    w = PREFILL_WORKLOADS[name]
+    return rng(seed + 3).integers(0, w.max_prefix + 1, size=w.num_seqs).astype(np.int32)
+
+
 TOY_LENGTHS = (25, 47, 12)
 TOY_PLACEMENT = ((3, 7), (0, 5, 9), (4,))
 TOY_GROWTH_BLOCKS = (11, 12)      # B's next blocks as it grows by 20 tokens
