@@ -309,6 +309,8 @@ def run_ours(args, rank, local_rank, world):
     w = workloads.WORKLOADS[name]
     seed = args.seed + 1000 * rank
     plan = stepmod.plan_step(name, seed, args.variant)
+    if args.layers > 1:
+        return run_model_step(args, rank, world, dev, name, plan, seed)
     pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev, args.kv_cache)
     st = stepmod.DecodeStep(name, plan, pool, q, k, v, dev)
     n_tokens = int((plan.slot_mapping >= 0).sum())
@@ -421,6 +423,76 @@ def run_ours(args, rank, local_rank, world):
         "cpu_baseline": {"value": ob / ot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{on} whole sequences x {w.num_q_heads} q heads of the same batch "
                                    f"({ot:.1f} s, single-threaded fp64 C)"},
+        "clocks": clocks.summary() if clocks else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- model step
+
+def run_model_step(args, rank, world, dev, name, plan, seed):
+    """A decode step of a whole model: COW copies in every layer pool (one
+    pa_copy_blocks call), then reshape_and_cache + decode for each of
+    args.layers layers, eagerly or replayed from a CUDA graph (--graph)."""
+    import torch
+    from paged_kv_cache_120_gb300 import binding, step as stepmod
+    w = workloads.WORKLOADS[name]
+    ms = stepmod.ModelStep(name, plan, args.layers, seed, dev, args.kv_cache)
+    fp8 = ms.layers[0].fp8
+    n_tokens = int((plan.slot_mapping >= 0).sum())
+    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens, 1 if fp8 else 2)
+    step_bytes = args.layers * ab["step"]
+    for _ in range(max(3, args.warmup)):
+        ms.run()
+    if args.graph:
+        ms.capture()
+        for _ in range(3):
+            ms.run()
+    torch.cuda.synchronize(dev)
+    if binding.pa_get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    K = max(1, args.steps // args.layers)
+    stream = torch.cuda.current_stream(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(K):
+        ms.run()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world, dev)
+    if clocks:
+        clocks.stop()
+    t_s = dist_max(start.elapsed_time(end) / 1e3, world, dev)
+    if binding.pa_get_device_error():
+        raise RuntimeError("device error word set during the timed region")
+    if rank != 0:
+        return
+    peak, peak_note = measured_peak()
+    achieved = step_bytes / (t_s / K) / 1e9
+    copy_bytes = args.layers * ab["copy"]
+    line = {
+        "metric": METRIC, "value": world * step_bytes * K / t_s / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": t_s * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
+        "data": "synthetic (seeded N(0,1) values per layer, seeded block placement)",
+        "config": dict(workload_config(name, plan, args.kv_cache), layers=args.layers,
+                       launch="CUDA graph replay" if args.graph else "eager",
+                       cow_bytes_per_step=copy_bytes,
+                       complete_block_bytes=2 * args.layers * w.block_size * w.num_kv_heads * w.head_size
+                       * (1 if fp8 else 2)),
+        "seq_steps_per_s": world * len(plan.seq_lens) * K / t_s,
+        "ms_per_layer": t_s * 1e3 / K / args.layers,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "whole model step (copy_blocks + per-layer reshape and decode)",
+                     "peak_source": peak_note, "bytes_per_step": step_bytes},
+        "gpu_launches": ms.launches_per_step() * K,
         "clocks": clocks.summary() if clocks else None,
     }
     print(json.dumps(line), flush=True)
@@ -622,6 +694,10 @@ def main():
     ap.add_argument("--variant", default="literal", choices=["literal", "fork"])
     ap.add_argument("--kv-cache", default="16bit", choices=["16bit", "fp8"],
                     help="cache element type: the workload's 16-bit type, or E4M3 codes")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="decode workloads: layers per model step (one pool per layer)")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --layers: replay the model step from a CUDA graph")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the cpu_baseline sample")

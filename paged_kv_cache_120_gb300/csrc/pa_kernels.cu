@@ -1251,8 +1251,11 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
                   int num_kv_heads, int head_size, int device, bool fp8)
 {
     static std::mutex mu;
-    static MapKey keys[16];
-    static CUtensorMap maps[16];
+    // One entry per (pool, shape, device): enough for every layer of a model
+    // (each layer has its own pool), so a model step re-encodes nothing.
+    constexpr int kMapCache = 128;
+    static MapKey keys[kMapCache];
+    static CUtensorMap maps[kMapCache];
     static int used = 0, next = 0;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i) {
@@ -1287,7 +1290,7 @@ int encode_kv_map(CUtensorMap *map, const void *kv, int num_blocks, int block_si
                      swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    const int slot = used < 16 ? used++ : (next++ % 16);
+    const int slot = used < kMapCache ? used++ : (next++ % kMapCache);
     keys[slot] = MapKey{kv, head_size, num_kv_heads, block_size, num_blocks, device, (int)fp8};
     maps[slot] = m;
     *map = m;
@@ -1373,6 +1376,49 @@ int validate_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int h
     return PA_OK;
 }
 
+// Per (kernel, device): the dynamic shared memory the kernel may use (raised
+// on demand) and the occupancy at the last size asked for, so that a call
+// makes no attribute or occupancy query once its shape has been seen (and a
+// call being captured into a CUDA graph makes none).
+cudaError_t kernel_setup(const void *fn, int dev, size_t smem, int threads, int *occ)
+{
+    struct Entry {
+        const void *fn;
+        int dev;
+        size_t allowed, occ_smem;
+        int occ;
+    };
+    constexpr int kEntries = 64;
+    static Entry table[kEntries];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry *e = nullptr;
+    for (int i = 0; i < used; ++i)
+        if (table[i].fn == fn && table[i].dev == dev)
+            e = &table[i];
+    if (!e) {
+        e = &table[used < kEntries ? used++ : kEntries - 1];
+        *e = Entry{fn, dev, 0, (size_t)-1, 0};
+    }
+    if (smem > e->allowed) {
+        cudaError_t r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r != cudaSuccess)
+            return r;
+        e->allowed = smem;
+    }
+    if (occ) {
+        if (e->occ_smem != smem) {
+            cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&e->occ, fn, threads, smem);
+            if (r != cudaSuccess)
+                return r;
+            e->occ_smem = smem;
+        }
+        *occ = e->occ;
+    }
+    return cudaSuccess;
+}
+
 int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
               int dtype, bool fp8)
 {
@@ -1392,15 +1438,12 @@ int make_plan(DecodePlan &pl, int num_seqs, int num_q_heads, int num_kv_heads, i
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = cudaFuncSetAttribute(pl.main_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    e = kernel_setup(pl.main_fn, dev, pl.smem, pl.warps * 32, &occ);
     if (e != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute");
-    e = cudaFuncSetAttribute(pl.reduce_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.reduce_smem);
+        return cuda_fail(e, "pa_decode: kernel attributes / occupancy");
+    e = kernel_setup(pl.reduce_fn, dev, pl.reduce_smem, kReduceWarps * 32, nullptr);
     if (e != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute (reduce)");
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl.main_fn, pl.warps * 32, pl.smem);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        return cuda_fail(e, "pa_decode: reduce kernel attributes");
     if (occ < 1)
         return set_error(PA_ERR_UNSUPPORTED, "pa_decode: kernel does not fit on an SM (smem %zu)", pl.smem);
     pl.grid = sms * occ;

@@ -657,9 +657,24 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
 
     const void *fn = dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true>)
                                       : reinterpret_cast<const void *>(&paged_prefill_kernel<false>);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // Raise the kernel's shared-memory limit once per device (a call being
+    // captured into a CUDA graph then makes no attribute call).
+    static std::mutex mu;
+    static bool raised[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
-        return set_error(PA_ERR_CUDA, "pa_prefill: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return set_error(PA_ERR_CUDA, "pa_prefill: cudaGetDevice: %s", cudaGetErrorString(e));
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        bool &done = raised[dtype == PA_BF16][dev & 63];
+        if (!done) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess)
+                return set_error(PA_ERR_CUDA, "pa_prefill: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            done = dev < 64;
+        }
+    }
     const dim3 grid((unsigned)(prm.q_tiles * prm.head_tiles), (unsigned)num_kv_heads, (unsigned)num_seqs);
     void *args[] = {&kv_map, &q_map, &prm};
     e = cudaLaunchKernel(fn, grid, dim3(kThreads), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));

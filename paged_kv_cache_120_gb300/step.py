@@ -168,6 +168,61 @@ class DecodeStep:
                               self.w.scale, self.workspace, self.flags, stream)
 
 
+class ModelStep:
+    """One decode step of a whole model: `layers` layer pools (each its own
+    (2, num_blocks, B, Hkv, D) cache, as the book's §4.3.1 allocates one per
+    layer) sharing the block tables, slots and COW pairs of one allocator.
+    The step copies every COW pair in all layer pools with one
+    pa_copy_blocks call (a complete block spans every layer), then writes and
+    decodes layer after layer. `capture()` records the step in a CUDA graph;
+    `run()` then replays it."""
+
+    def __init__(self, name: str, plan: StepPlan, layers: int, seed: int, device,
+                 kv_cache: str = "16bit"):
+        import torch
+        self.w = workloads.WORKLOADS[name]
+        self.layers = []
+        pool0, q, k, v = make_device_inputs(name, plan, seed, device, kv_cache)
+        pools = [pool0]
+        for l in range(1, layers):
+            pool, _, _, _ = make_device_inputs(name, plan, seed + 97 * l, device, kv_cache)
+            pools.append(pool)
+        for pool in pools:
+            self.layers.append(DecodeStep(name, plan, pool, q, k, v, device))
+        self.pools = pools
+        self.cow_pairs = self.layers[0].cow_pairs
+        self.graph = None
+
+    def launches_per_step(self) -> int:
+        return (1 if self.cow_pairs is not None else 0) + 3 * len(self.layers)
+
+    def run_eager(self, stream=None) -> None:
+        if self.cow_pairs is not None:
+            binding.pa_copy_blocks(self.pools, self.cow_pairs, stream)
+        for st in self.layers:
+            st.reshape(stream)
+            st.decode(stream)
+
+    def capture(self) -> None:
+        import torch
+        self.run_eager()  # first calls set up kernel attributes and tensor maps
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                self.run_eager()
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
+
+    def run(self, stream=None) -> None:
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.run_eager(stream)
+
+
 def make_device_inputs(name: str, plan: StepPlan, seed: int, device, kv_cache: str = "16bit"):
     """Pool, queries and new K/V: seeded N(0, 1) values on ``device``.
     ``kv_cache="fp8"`` gives a pool of E4M3 codes of N(0, 1) draws under the
