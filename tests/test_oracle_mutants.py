@@ -81,6 +81,16 @@ MUTANTS = [
     ("oracle/oracle.c", "const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;",
      "const uint16_t *q_row = query + (long long)(q0) * num_q_heads * head_size;",
      "test_oracle_prefill_pins.py"),                                                      # wrong query row
+    ("oracle/prefix_cache.py", "if (i + 1) * B > n - 1 or h not in self.cached:",
+     "if (i + 1) * B > n or h not in self.cached:", "test_prefix_cache_model.py"),   # hit limit
+    ("oracle/prefix_cache.py", "                    self.free.append(b)",
+     "                    self.free.insert(0, b)", "test_prefix_cache_model.py"),    # cached to head
+    ("oracle/prefix_cache.py", "for b in reversed(s[\"table\"]):", "for b in s[\"table\"]:",
+     "test_prefix_cache_model.py"),                                                   # free order
+    ("oracle/prefix_cache.py", "        self._evict(b)\n        self.ref[b] = 1",
+     "        self.ref[b] = 1", "test_prefix_cache_model.py"),                         # no eviction
+    ("oracle/prefix_cache.py", 'parent = s["hashes"][-1] if s["hashes"] else NONE_HASH',
+     "parent = NONE_HASH", "test_prefix_cache_model.py"),                             # chain broken
     ("oracle/block_manager.py", "self.free.insert(0, b)", "self.free.append(b)",
      "test_block_manager.py"),                                                         # free to tail
     ("oracle/block_manager.py", "                self.ref[last] -= 1\n", "",
