@@ -382,6 +382,74 @@ int pa_alloc_block_tables(const pa_allocator *a, const int *seq_ids, int n,
 /* Fill out[n] (host, int32) with the sequences' lengths. */
 int pa_alloc_seq_lens(const pa_allocator *a, const int *seq_ids, int n, int32_t *out);
 
+/* ------------------------------------------------------------------ */
+/* Host prefix-cache block pool ([codex] §4.2-§4.5, §5): full blocks carry */
+/* a chained hash, a new prompt reuses the longest cached prefix, freed  */
+/* blocks stay cached until reused. Host memory only; not thread-safe.   */
+/* ------------------------------------------------------------------ */
+
+typedef struct pa_prefix_cache pa_prefix_cache;
+
+/*
+ * Create a pool of num_blocks blocks of block_size tokens. Block 0 is the
+ * null block and is never handed out; the free queue starts as 1, 2, ...,
+ * num_blocks - 1 (head first = evicted first). Returns NULL on bad
+ * arguments (num_blocks >= 2, block_size > 0).
+ *
+ * Hashes: a full block's hash is SHA-256(parent hash || its token ids as
+ * little-endian int32), the first block's parent being 32 zero bytes
+ * ([codex] §4.4; the serialisation and the root are the reading taken).
+ */
+pa_prefix_cache *pa_pcache_create(int num_blocks, int block_size);
+void pa_pcache_destroy(pa_prefix_cache *c);
+
+/* Blocks on the free queue (cached ones included). */
+int pa_pcache_num_free(const pa_prefix_cache *c);
+
+/*
+ * New sequence with the prompt tokens[num_tokens] (num_tokens > 0). Its full
+ * blocks' hash chain is matched against the cache from the first block; the
+ * match ends at the first miss and covers at most num_tokens - 1 tokens (the
+ * last prompt token is always recomputed). Matched blocks are touched
+ * (count + 1, taken off the free queue if they were on it); the rest come
+ * from the free queue's head, each losing any hash it still carried (lazy
+ * eviction), and the prompt's full new blocks are recorded as cached.
+ * *num_cached_tokens = the matched tokens (a multiple of block_size): the
+ * caller writes K/V only for positions >= that. All-or-nothing:
+ * PA_ERR_OUT_OF_BLOCKS leaves the pool unchanged.
+ */
+int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens,
+                      int *seq_id, int *num_cached_tokens);
+
+/* Reserve the next token's slot (*slot = table[pos / B] * B + pos % B); a
+ * block that becomes full is hashed and recorded as cached. */
+int pa_pcache_append_token(pa_prefix_cache *c, int seq_id, int32_t token, int32_t *slot);
+
+/* Release a sequence: its blocks in reverse table order, count - 1; a block
+ * reaching 0 goes to the free queue's head if it has no hash and to its tail
+ * if it has one ([codex] §4.3). */
+int pa_pcache_free_seq(pa_prefix_cache *c, int seq_id);
+
+/* Tokens of a sequence, or a PA_ERR_* code. */
+int pa_pcache_seq_len(const pa_prefix_cache *c, int seq_id);
+
+/* Block tables of the given sequences into out[n][max_blocks_per_seq]
+ * (host, int32, padded with -1). */
+int pa_pcache_block_tables(const pa_prefix_cache *c, const int *seq_ids, int n,
+                           int max_blocks_per_seq, int32_t *out);
+
+/* Slots of positions first_pos .. first_pos + n - 1 of a sequence (host). */
+int pa_pcache_slots(const pa_prefix_cache *c, int seq_id, int first_pos, int n, int32_t *out);
+
+/* The free queue, head first, into out[capacity]; returns its length. */
+int pa_pcache_free_queue(const pa_prefix_cache *c, int32_t *out, int capacity);
+
+/* Reference count of a block, or PA_ERR_INVALID_ARG. */
+int pa_pcache_ref_count(const pa_prefix_cache *c, int block);
+
+/* 1 and the block's 32-byte hash in out if it carries one, else 0. */
+int pa_pcache_block_hash(const pa_prefix_cache *c, int block, uint8_t *out);
+
 #ifdef __cplusplus
 }
 #endif

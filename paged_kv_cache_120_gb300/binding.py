@@ -64,6 +64,18 @@ SIGNATURES = [
     ("pa_alloc_seq_num_blocks", _i, [_vp, _i]),
     ("pa_alloc_block_tables", _i, [_vp, _ip, _i, _i, _i32p]),
     ("pa_alloc_seq_lens", _i, [_vp, _ip, _i, _i32p]),
+    ("pa_pcache_create", _vp, [_i, _i]),
+    ("pa_pcache_destroy", None, [_vp]),
+    ("pa_pcache_num_free", _i, [_vp]),
+    ("pa_pcache_add_seq", _i, [_vp, _i32p, _i, _ip, _ip]),
+    ("pa_pcache_append_token", _i, [_vp, _i, ctypes.c_int32, _i32p]),
+    ("pa_pcache_free_seq", _i, [_vp, _i]),
+    ("pa_pcache_seq_len", _i, [_vp, _i]),
+    ("pa_pcache_block_tables", _i, [_vp, _ip, _i, _i, _i32p]),
+    ("pa_pcache_slots", _i, [_vp, _i, _i, _i, _i32p]),
+    ("pa_pcache_free_queue", _i, [_vp, _i32p, _i]),
+    ("pa_pcache_ref_count", _i, [_vp, _i]),
+    ("pa_pcache_block_hash", _i, [_vp, _i, ctypes.POINTER(ctypes.c_uint8)]),
 ]
 
 _lib = None
@@ -344,3 +356,78 @@ class BlockAllocator:
         _check(lib().pa_alloc_seq_lens(self._h, ids.ctypes.data_as(_ip), len(ids),
                                        out.ctypes.data_as(_i32p)))
         return out
+
+
+class PrefixCache:
+    """Host prefix-cache block pool (pa_pcache_*): chained block hashes, a
+    free queue with lazy eviction, prompts that reuse cached prefixes."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self.num_blocks, self.block_size = num_blocks, block_size
+        h = lib().pa_pcache_create(num_blocks, block_size)
+        if not h:
+            raise PAError(PA_ERR_INVALID_ARG, pa_last_error())
+        self._h = ctypes.c_void_p(h)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pa_pcache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return _check(lib().pa_pcache_num_free(self._h))
+
+    def add_seq(self, tokens):
+        """-> (seq_id, tokens found in the cache)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        sid, hit = ctypes.c_int(0), ctypes.c_int(0)
+        _check(lib().pa_pcache_add_seq(self._h, t.ctypes.data_as(_i32p), len(t), ctypes.byref(sid),
+                                       ctypes.byref(hit)))
+        return sid.value, hit.value
+
+    def append_token(self, seq: int, token: int) -> int:
+        slot = ctypes.c_int32(0)
+        _check(lib().pa_pcache_append_token(self._h, seq, int(token), ctypes.byref(slot)))
+        return slot.value
+
+    def free_seq(self, seq: int) -> None:
+        _check(lib().pa_pcache_free_seq(self._h, seq))
+
+    def seq_len(self, seq: int) -> int:
+        return _check(lib().pa_pcache_seq_len(self._h, seq))
+
+    def block_tables(self, seqs, max_blocks_per_seq: int) -> np.ndarray:
+        ids = np.ascontiguousarray(seqs, dtype=np.int32)
+        out = np.empty((len(ids), max_blocks_per_seq), dtype=np.int32)
+        _check(lib().pa_pcache_block_tables(self._h, ids.ctypes.data_as(_ip), len(ids), max_blocks_per_seq,
+                                            out.ctypes.data_as(_i32p)))
+        return out
+
+    def table(self, seq: int):
+        n = -(-self.seq_len(seq) // self.block_size)
+        return self.block_tables([seq], max(n, 1))[0, :n].tolist()
+
+    def slots(self, seq: int, first_pos: int, n: int) -> np.ndarray:
+        out = np.empty(n, dtype=np.int32)
+        _check(lib().pa_pcache_slots(self._h, seq, first_pos, n, out.ctypes.data_as(_i32p)))
+        return out
+
+    def free_queue(self):
+        cap = self.num_blocks
+        out = np.empty(cap, dtype=np.int32)
+        n = _check(lib().pa_pcache_free_queue(self._h, out.ctypes.data_as(_i32p), cap))
+        return out[:n].tolist()
+
+    def ref_count(self, block: int) -> int:
+        return _check(lib().pa_pcache_ref_count(self._h, block))
+
+    def block_hash(self, block: int):
+        buf = (ctypes.c_uint8 * 32)()
+        r = _check(lib().pa_pcache_block_hash(self._h, block, buf))
+        return bytes(buf) if r == 1 else None

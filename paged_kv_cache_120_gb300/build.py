@@ -30,6 +30,7 @@ UNITS = [
     ("pa_prefill.cu", "nvcc"),
     ("pa_static_scratch.cu", "nvcc"),
     ("block_allocator.cpp", "g++"),
+    ("prefix_cache.cpp", "g++"),
     ("pa_errors.cpp", "g++"),
 ]
 

@@ -1,0 +1,447 @@
+// Host prefix-cache block pool: chained block hashes, a doubly linked free
+// queue with lazy eviction, and sequences whose tables share cached blocks.
+//
+// The bookkeeping follows "01 · PagedAttention 与 KV cache 块管理":
+//  §4.2 the free queue is a doubly linked list through the blocks (O(1)
+//       removal from the middle), head = evicted first;
+//  §4.3 allocation pops the head and drops the popped block's cached hash
+//       (lazy eviction); a cache hit "touches" the block (count + 1, and off
+//       the free queue if it was there); freeing returns blocks whose count
+//       reaches 0 to the head if they have no hash (LIFO reuse) and to the
+//       tail if they do (FIFO, so cached blocks live longest), walking the
+//       table in reverse so that a chain's tail is evicted before its head;
+//  §4.4 a full block's hash chains the parent block's hash and the block's
+//       token ids (SHA-256); matching runs from the first block and stops at
+//       the first miss;
+//  §4.5 a match covers at most num_tokens - 1 tokens (the last prompt token
+//       is always recomputed); a request that cannot get its blocks changes
+//       nothing;
+//  §5   block 0 is the null block: never free, never handed out.
+// Readings: the chain's root is 32 zero bytes; token ids are hashed as
+// little-endian int32; a prompt's full blocks are recorded as cached when
+// they are allocated (their K/V are written in the same step, before any
+// other request can read them), a decode block when its last slot is
+// reserved; if two blocks carry the same hash the first stays the lookup
+// target.
+//
+// Like the plain allocator it only builds inputs (block tables and slots)
+// for the device calls and never touches device memory.
+#include <algorithm>
+#include <array>
+#include <cstdint>
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+// ------------------------------------------------------------ SHA-256
+// FIPS 180-4, section 6.2: eight 32-bit working variables, 64 rounds per
+// 512-bit block, message padded with a 1 bit, zeros and the 64-bit length.
+using Digest = std::array<uint8_t, 32>;
+
+constexpr uint32_t kRound[64] = {
+    0x428a2f98, 0x71374491, 0xb5c0fbcf, 0xe9b5dba5, 0x3956c25b, 0x59f111f1, 0x923f82a4, 0xab1c5ed5,
+    0xd807aa98, 0x12835b01, 0x243185be, 0x550c7dc3, 0x72be5d74, 0x80deb1fe, 0x9bdc06a7, 0xc19bf174,
+    0xe49b69c1, 0xefbe4786, 0x0fc19dc6, 0x240ca1cc, 0x2de92c6f, 0x4a7484aa, 0x5cb0a9dc, 0x76f988da,
+    0x983e5152, 0xa831c66d, 0xb00327c8, 0xbf597fc7, 0xc6e00bf3, 0xd5a79147, 0x06ca6351, 0x14292967,
+    0x27b70a85, 0x2e1b2138, 0x4d2c6dfc, 0x53380d13, 0x650a7354, 0x766a0abb, 0x81c2c92e, 0x92722c85,
+    0xa2bfe8a1, 0xa81a664b, 0xc24b8b70, 0xc76c51a3, 0xd192e819, 0xd6990624, 0xf40e3585, 0x106aa070,
+    0x19a4c116, 0x1e376c08, 0x2748774c, 0x34b0bcb5, 0x391c0cb3, 0x4ed8aa4a, 0x5b9cca4f, 0x682e6ff3,
+    0x748f82ee, 0x78a5636f, 0x84c87814, 0x8cc70208, 0x90befffa, 0xa4506ceb, 0xbef9a3f7, 0xc67178f2};
+
+inline uint32_t rotr(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
+
+class Sha256 {
+  public:
+    Sha256() : state_{0x6a09e667, 0xbb67ae85, 0x3c6ef372, 0xa54ff53a, 0x510e527f, 0x9b05688c, 0x1f83d9ab,
+                      0x5be0cd19} {}
+    void update(const uint8_t *p, size_t n)
+    {
+        total_ += n;
+        while (n > 0) {
+            const size_t k = std::min(n, sizeof(buf_) - used_);
+            std::memcpy(buf_ + used_, p, k);
+            used_ += k;
+            p += k;
+            n -= k;
+            if (used_ == sizeof(buf_)) {
+                compress(buf_);
+                used_ = 0;
+            }
+        }
+    }
+    Digest finish()
+    {
+        const uint64_t bits = total_ * 8;
+        const uint8_t one = 0x80, zero = 0;
+        update(&one, 1);
+        while (used_ != 56)
+            update(&zero, 1);
+        uint8_t len[8];
+        for (int i = 0; i < 8; ++i)
+            len[i] = (uint8_t)(bits >> (56 - 8 * i));
+        update(len, 8);
+        Digest d;
+        for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 4; ++j)
+                d[4 * i + j] = (uint8_t)(state_[i] >> (24 - 8 * j));
+        return d;
+    }
+
+  private:
+    void compress(const uint8_t *blk)
+    {
+        uint32_t w[64];
+        for (int t = 0; t < 16; ++t)
+            w[t] = (uint32_t)blk[4 * t] << 24 | (uint32_t)blk[4 * t + 1] << 16 | (uint32_t)blk[4 * t + 2] << 8 |
+                   (uint32_t)blk[4 * t + 3];
+        for (int t = 16; t < 64; ++t) {
+            const uint32_t s0 = rotr(w[t - 15], 7) ^ rotr(w[t - 15], 18) ^ (w[t - 15] >> 3);
+            const uint32_t s1 = rotr(w[t - 2], 17) ^ rotr(w[t - 2], 19) ^ (w[t - 2] >> 10);
+            w[t] = w[t - 16] + s0 + w[t - 7] + s1;
+        }
+        uint32_t a = state_[0], b = state_[1], c = state_[2], d = state_[3], e = state_[4], f = state_[5],
+                 g = state_[6], h = state_[7];
+        for (int t = 0; t < 64; ++t) {
+            const uint32_t t1 = h + (rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25)) + ((e & f) ^ (~e & g)) + kRound[t] + w[t];
+            const uint32_t t2 = (rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22)) + ((a & b) ^ (a & c) ^ (b & c));
+            h = g;
+            g = f;
+            f = e;
+            e = d + t1;
+            d = c;
+            c = b;
+            b = a;
+            a = t1 + t2;
+        }
+        state_[0] += a;
+        state_[1] += b;
+        state_[2] += c;
+        state_[3] += d;
+        state_[4] += e;
+        state_[5] += f;
+        state_[6] += g;
+        state_[7] += h;
+    }
+    uint32_t state_[8];
+    uint8_t buf_[64] = {};
+    size_t used_ = 0;
+    uint64_t total_ = 0;
+};
+
+// Hash of a full block: SHA-256(parent hash || token ids as little-endian int32).
+Digest block_hash(const Digest &parent, const int32_t *tokens, int n)
+{
+    Sha256 h;
+    h.update(parent.data(), parent.size());
+    for (int i = 0; i < n; ++i) {
+        const uint32_t t = (uint32_t)tokens[i];
+        const uint8_t b[4] = {(uint8_t)t, (uint8_t)(t >> 8), (uint8_t)(t >> 16), (uint8_t)(t >> 24)};
+        h.update(b, 4);
+    }
+    return h.finish();
+}
+
+struct DigestHash {
+    size_t operator()(const Digest &d) const
+    {
+        uint64_t x;
+        std::memcpy(&x, d.data(), sizeof(x));
+        return (size_t)x;
+    }
+};
+
+}  // namespace
+
+struct pa_prefix_cache {
+    int num_blocks = 0, block_size = 0;
+    std::vector<int32_t> ref, prev, next;
+    std::vector<char> in_free, hashed;
+    std::vector<Digest> hash;
+    int32_t head = -1, tail = -1, nfree = 0;
+    std::unordered_map<Digest, std::vector<int32_t>, DigestHash> cached;  // first = lookup target
+    struct Seq {
+        std::vector<int32_t> table, tokens;
+        std::vector<Digest> hashes;
+    };
+    std::unordered_map<int, Seq> seqs;
+    int next_id = 0;
+
+    // free queue
+    void unlink(int32_t b)
+    {
+        (prev[b] >= 0 ? next[prev[b]] : head) = next[b];
+        (next[b] >= 0 ? prev[next[b]] : tail) = prev[b];
+        prev[b] = next[b] = -1;
+        in_free[b] = 0;
+        --nfree;
+    }
+    void push_head(int32_t b)
+    {
+        prev[b] = -1;
+        next[b] = head;
+        (head >= 0 ? prev[head] : tail) = b;
+        head = b;
+        in_free[b] = 1;
+        ++nfree;
+    }
+    void push_tail(int32_t b)
+    {
+        next[b] = -1;
+        prev[b] = tail;
+        (tail >= 0 ? next[tail] : head) = b;
+        tail = b;
+        in_free[b] = 1;
+        ++nfree;
+    }
+    // cache
+    void evict(int32_t b)
+    {
+        if (!hashed[b])
+            return;
+        auto it = cached.find(hash[b]);
+        if (it != cached.end()) {
+            auto &v = it->second;
+            for (size_t i = 0; i < v.size(); ++i)
+                if (v[i] == b) {
+                    v.erase(v.begin() + (long)i);
+                    break;
+                }
+            if (v.empty())
+                cached.erase(it);
+        }
+        hashed[b] = 0;
+    }
+    void record(int32_t b, const Digest &d)
+    {
+        hash[b] = d;
+        hashed[b] = 1;
+        cached[d].push_back(b);
+    }
+    int32_t pop()
+    {
+        const int32_t b = head;
+        unlink(b);
+        evict(b);
+        ref[b] = 1;
+        return b;
+    }
+};
+
+using pa::set_error;
+
+namespace {
+
+const pa_prefix_cache::Seq *find_seq(const pa_prefix_cache *c, int id)
+{
+    auto it = c->seqs.find(id);
+    return it == c->seqs.end() ? nullptr : &it->second;
+}
+
+}  // namespace
+
+extern "C" pa_prefix_cache *pa_pcache_create(int num_blocks, int block_size)
+{
+    if (num_blocks < 2 || block_size <= 0) {
+        set_error(PA_ERR_INVALID_ARG, "pa_pcache_create: need num_blocks >= 2 (block 0 is the null block) "
+                                      "and block_size > 0");
+        return nullptr;
+    }
+    auto *c = new pa_prefix_cache();
+    c->num_blocks = num_blocks;
+    c->block_size = block_size;
+    c->ref.assign(num_blocks, 0);
+    c->prev.assign(num_blocks, -1);
+    c->next.assign(num_blocks, -1);
+    c->in_free.assign(num_blocks, 0);
+    c->hashed.assign(num_blocks, 0);
+    c->hash.assign(num_blocks, Digest{});
+    for (int32_t b = 1; b < num_blocks; ++b)
+        c->push_tail(b);
+    return c;
+}
+
+extern "C" void pa_pcache_destroy(pa_prefix_cache *c) { delete c; }
+
+extern "C" int pa_pcache_num_free(const pa_prefix_cache *c)
+{
+    if (!c)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_num_free: null cache");
+    return c->nfree;
+}
+
+extern "C" int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens, int *seq_id,
+                                 int *num_cached_tokens)
+{
+    if (!c || !seq_id || !num_cached_tokens || num_tokens <= 0 || !tokens)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_add_seq: bad arguments (num_tokens must be > 0)");
+    const int B = c->block_size;
+    const int full = num_tokens / B, nblk = (num_tokens + B - 1) / B;
+    std::vector<Digest> hashes;
+    hashes.reserve(full);
+    Digest parent{};
+    for (int i = 0; i < full; ++i) {
+        parent = block_hash(parent, tokens + (size_t)i * B, B);
+        hashes.push_back(parent);
+    }
+    std::vector<int32_t> hits;
+    for (int i = 0; i < full; ++i) {
+        if ((long long)(i + 1) * B > num_tokens - 1)
+            break;
+        auto it = c->cached.find(hashes[i]);
+        if (it == c->cached.end())
+            break;
+        hits.push_back(it->second.front());
+    }
+    int touched_free = 0;
+    for (int32_t b : hits)
+        touched_free += c->in_free[b] ? 1 : 0;
+    const int need = nblk - (int)hits.size();
+    if (need > c->nfree - touched_free)
+        return set_error(PA_ERR_OUT_OF_BLOCKS, "pa_pcache_add_seq: need %d blocks, %d free", need,
+                         c->nfree - touched_free);
+    pa_prefix_cache::Seq s;
+    s.table.reserve(nblk);
+    for (int32_t b : hits) {
+        if (c->in_free[b])
+            c->unlink(b);
+        ++c->ref[b];
+        s.table.push_back(b);
+    }
+    for (int i = (int)hits.size(); i < nblk; ++i) {
+        const int32_t b = c->pop();
+        s.table.push_back(b);
+        if (i < full)
+            c->record(b, hashes[i]);
+    }
+    s.tokens.assign(tokens, tokens + num_tokens);
+    s.hashes = std::move(hashes);
+    const int id = c->next_id++;
+    c->seqs.emplace(id, std::move(s));
+    *seq_id = id;
+    *num_cached_tokens = (int)hits.size() * B;
+    return PA_OK;
+}
+
+extern "C" int pa_pcache_append_token(pa_prefix_cache *c, int seq_id, int32_t token, int32_t *slot)
+{
+    if (!c || !slot)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_append_token: null argument");
+    auto it = c->seqs.find(seq_id);
+    if (it == c->seqs.end())
+        return set_error(PA_ERR_NOT_FOUND, "pa_pcache_append_token: unknown sequence %d", seq_id);
+    auto &s = it->second;
+    const int B = c->block_size;
+    const int pos = (int)s.tokens.size();
+    if (pos % B == 0) {
+        if (c->nfree == 0)
+            return set_error(PA_ERR_OUT_OF_BLOCKS, "pa_pcache_append_token: no free block");
+        s.table.push_back(c->pop());
+    }
+    s.tokens.push_back(token);
+    if ((pos + 1) % B == 0) {
+        const Digest parent = s.hashes.empty() ? Digest{} : s.hashes.back();
+        const Digest d = block_hash(parent, s.tokens.data() + (pos + 1 - B), B);
+        s.hashes.push_back(d);
+        c->record(s.table[pos / B], d);
+    }
+    *slot = s.table[pos / B] * B + pos % B;
+    return PA_OK;
+}
+
+extern "C" int pa_pcache_free_seq(pa_prefix_cache *c, int seq_id)
+{
+    if (!c)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_free_seq: null cache");
+    auto it = c->seqs.find(seq_id);
+    if (it == c->seqs.end())
+        return set_error(PA_ERR_NOT_FOUND, "pa_pcache_free_seq: unknown sequence %d", seq_id);
+    const auto &t = it->second.table;
+    for (auto r = t.rbegin(); r != t.rend(); ++r) {
+        const int32_t b = *r;
+        if (--c->ref[b] == 0)
+            c->hashed[b] ? c->push_tail(b) : c->push_head(b);
+    }
+    c->seqs.erase(it);
+    return PA_OK;
+}
+
+extern "C" int pa_pcache_seq_len(const pa_prefix_cache *c, int seq_id)
+{
+    if (!c)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_seq_len: null cache");
+    const auto *s = find_seq(c, seq_id);
+    if (!s)
+        return set_error(PA_ERR_NOT_FOUND, "pa_pcache_seq_len: unknown sequence %d", seq_id);
+    return (int)s->tokens.size();
+}
+
+extern "C" int pa_pcache_block_tables(const pa_prefix_cache *c, const int *seq_ids, int n,
+                                      int max_blocks_per_seq, int32_t *out)
+{
+    if (!c || (n > 0 && (!seq_ids || !out)) || n < 0 || max_blocks_per_seq <= 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_block_tables: bad arguments");
+    for (int i = 0; i < n; ++i) {
+        const auto *s = find_seq(c, seq_ids[i]);
+        if (!s)
+            return set_error(PA_ERR_NOT_FOUND, "pa_pcache_block_tables: unknown sequence %d", seq_ids[i]);
+        if ((int)s->table.size() > max_blocks_per_seq)
+            return set_error(PA_ERR_INVALID_ARG, "pa_pcache_block_tables: sequence %d has %zu blocks > %d",
+                             seq_ids[i], s->table.size(), max_blocks_per_seq);
+        int32_t *row = out + (size_t)i * max_blocks_per_seq;
+        for (int j = 0; j < max_blocks_per_seq; ++j)
+            row[j] = j < (int)s->table.size() ? s->table[j] : -1;
+    }
+    return PA_OK;
+}
+
+extern "C" int pa_pcache_slots(const pa_prefix_cache *c, int seq_id, int first_pos, int n, int32_t *out)
+{
+    if (!c || n < 0 || first_pos < 0 || (n > 0 && !out))
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_slots: bad arguments");
+    const auto *s = find_seq(c, seq_id);
+    if (!s)
+        return set_error(PA_ERR_NOT_FOUND, "pa_pcache_slots: unknown sequence %d", seq_id);
+    if ((long long)first_pos + n > (long long)s->tokens.size())
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_slots: positions beyond the sequence");
+    const int B = c->block_size;
+    for (int i = 0; i < n; ++i) {
+        const int pos = first_pos + i;
+        out[i] = s->table[pos / B] * B + pos % B;
+    }
+    return PA_OK;
+}
+
+extern "C" int pa_pcache_free_queue(const pa_prefix_cache *c, int32_t *out, int capacity)
+{
+    if (!c || capacity < 0 || (capacity > 0 && !out))
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_free_queue: bad arguments");
+    int k = 0;
+    for (int32_t b = c->head; b >= 0; b = c->next[b]) {
+        if (k < capacity)
+            out[k] = b;
+        ++k;
+    }
+    return k;
+}
+
+extern "C" int pa_pcache_ref_count(const pa_prefix_cache *c, int block)
+{
+    if (!c || block < 0 || block >= c->num_blocks)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_ref_count: bad block");
+    return c->ref[block];
+}
+
+extern "C" int pa_pcache_block_hash(const pa_prefix_cache *c, int block, uint8_t *out)
+{
+    if (!c || !out || block < 0 || block >= c->num_blocks)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_block_hash: bad arguments");
+    if (!c->hashed[block])
+        return 0;
+    std::memcpy(out, c->hash[block].data(), 32);
+    return 1;
+}
