@@ -74,13 +74,28 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
 
 
-def traffic_record(workload: str, kv_cache: str = "16bit"):
-    """DRAM traffic per decode launch from a committed ncu summary, if the
-    summary was taken on the current decode source (its hash matches)."""
+KERNEL_SOURCES = {
+    "decode": ("pa_kernels.cu", "pa_device.cuh"),
+    "decode_fp8": ("pa_kernels.cu", "pa_device.cuh"),
+    "prefill": ("pa_prefill.cu", "pa_device.cuh"),
+}
+
+
+def kernel_source_hash(tag: str) -> str:
+    """SHA-256 over the CUDA sources a kernel family is built from, in order."""
     import hashlib
-    tag = "decode_fp8" if kv_cache == "fp8" else "decode"
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[tag]:
+        with open(os.path.join(ROOT, "paged_kv_cache_120_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_record(tag: str, workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary (profiles/<tag>_<workload>_traffic.txt), if the summary was taken
+    on the current sources (their hash matches); else None."""
     path = os.path.join(ROOT, "profiles", f"{tag}_{workload}_traffic.txt")
-    src = os.path.join(ROOT, "paged_kv_cache_120_gb300", "csrc", "pa_kernels.cu")
     try:
         kv = {}
         with open(path) as f:
@@ -88,9 +103,7 @@ def traffic_record(workload: str, kv_cache: str = "16bit"):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
-        if kv.get("source_sha256") != h:
+        if kv.get("source_sha256") != kernel_source_hash(tag):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -390,7 +403,7 @@ def run_ours(args, rank, local_rank, world):
     achieved = ab["decode"] / (dec_ms / 1e3) / 1e9
     value = world * ab["step"] * K / t_s / 1e9
     seq_steps = world * len(plan.seq_lens) * K / t_s
-    traffic = traffic_record(name, args.kv_cache)
+    traffic = traffic_record("decode_fp8" if args.kv_cache == "fp8" else "decode", name)
 
     # CPU baseline: the oracle, single-threaded, on a bounded sample.
     pool_bits, q_bits = pool_host_bits(st.pool), pool_host_bits(st.query)
@@ -635,7 +648,7 @@ def run_prefill(args, rank, local_rank, world):
         "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) * K / t_s,
         "prefill_only": {"ms": pre_ms, "tflops": achieved, "sampled_launches": len(ev)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill (paged_prefill_kernel)",
+                     "frac": achieved / peak, "traffic": traffic_record("prefill", name), "kernel": "pa_prefill (paged_prefill_kernel)",
                      "peak_source": peak_note, "flops_per_launch": flops},
         "e2e": {"value": world * flops * ke / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3 / ke},
@@ -646,6 +659,199 @@ def run_prefill(args, rank, local_rank, world):
         "clocks": clocks.summary() if clocks else None,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_prefix_cache(args, rank, local_rank, world):
+    """A serving wave per step: SHARED_PROMPT["requests"] requests with a common
+    system prompt and private suffixes arrive; the prefix cache hands out
+    tables (cached system blocks shared), only uncached tokens are written
+    (pa_reshape_and_cache) and prefilled (pa_prefill); the requests are then
+    freed (their blocks stay cached). --no-prefix-cache computes every
+    prompt in full. Host bookkeeping and device time are reported apart."""
+    import torch
+    from paged_kv_cache_120_gb300 import binding, build
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = workloads.SHARED_PROMPT
+    R, B, D = cfg["requests"], cfg["block_size"], cfg["head_size"]
+    Hq, Hkv, dt = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["dtype"]
+    system, g = workloads.shared_prompt_tokens(args.seed + 1000 * rank)
+    max_tok = R * (cfg["system"] + cfg["suffix_hi"])
+    nb = 4 * (max_tok // B + R) + 1
+    pool = workloads.normal_values((2, nb, B, Hkv, D), dt, 51, dev)
+    q = workloads.normal_values((max_tok, Hq, D), dt, 52, dev)
+    k = workloads.normal_values((max_tok, Hkv, D), dt, 53, dev)
+    v = workloads.normal_values((max_tok, Hkv, D), dt, 54, dev)
+    out = torch.empty_like(q)
+    use_cache = not args.no_prefix_cache
+    pc = binding.PrefixCache(nb, B)
+    flags = 0 if use_cache else binding.PA_PCACHE_NO_CACHE
+    maxb = (cfg["system"] + cfg["suffix_hi"] + B - 1) // B
+    pin = lambda n: torch.empty(n, dtype=torch.int32).pin_memory()
+    host = {"seq_ids": torch.empty(R, dtype=torch.int32), "num_cached": torch.empty(R, dtype=torch.int32),
+            "cu_seqlens_q": pin(R + 1), "seq_lens": pin(R), "slot_mapping": pin(max_tok),
+            "block_tables": pin(R * maxb)}
+    d_slots = torch.empty(max_tok, dtype=torch.int32, device=dev)
+    d_bt = torch.empty(R, maxb, dtype=torch.int32, device=dev)
+    d_cu = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    d_sl = torch.empty(R, dtype=torch.int32, device=dev)
+    copied = torch.cuda.Event()
+    copied.record()
+    scale = D ** -0.5
+    stream = torch.cuda.current_stream(dev)
+    events = None
+
+    def wave(w, times):
+        """One wave (tokens, cu_tokens, prompt tokens); returns (tokens computed, flops)."""
+        tokens, cu_tokens, served = w
+        copied.synchronize()        # the previous wave's pinned inputs are on the device
+        t0 = time.perf_counter()
+        count, _ = pc.admit(tokens, cu_tokens, maxb, flags, host)
+        if count != R:
+            raise RuntimeError(f"pool admitted {count} of {R} requests")
+        cu = host["cu_seqlens_q"].numpy()
+        news = int(cu[R])
+        t1 = time.perf_counter()
+        d_slots[:news].copy_(host["slot_mapping"][:news], non_blocking=True)
+        d_bt.view(-1).copy_(host["block_tables"], non_blocking=True)
+        d_cu.copy_(host["cu_seqlens_q"], non_blocking=True)
+        d_sl.copy_(host["seq_lens"], non_blocking=True)
+        copied.record()
+        binding.pa_reshape_and_cache(k[:news], v[:news], pool, d_slots[:news])
+        if events is not None:
+            events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+            events[-1][0].record(stream)
+        binding.pa_prefill(out[:news], q[:news], pool, d_bt, d_cu, d_sl, scale, int(np.diff(cu).max()))
+        if events is not None:
+            events[-1][1].record(stream)
+        t2 = time.perf_counter()
+        pc.free_seqs(host["seq_ids"])
+        times[0] += (t1 - t0) + (time.perf_counter() - t2)
+        hits = host["num_cached"].numpy().astype(np.int64)
+        n_new = np.diff(cu).astype(np.int64)
+        flops = int((4 * D * Hq * ((2 * hits + 1 + n_new) * n_new // 2)).sum())
+        return news, flops
+
+    def prompts_for_wave():
+        prompts = [np.concatenate([system, g.integers(0, cfg["vocab"], size=int(g.integers(
+            cfg["suffix_lo"], cfg["suffix_hi"] + 1)))]).astype(np.int32) for _ in range(R)]
+        cu_tokens = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+        return np.concatenate(prompts), cu_tokens, int(cu_tokens[-1])
+
+    # 64 distinct waves, cycled: a wave's private blocks are long evicted
+    # (about 20 waves of allocation refill the pool) before it comes round again
+    waves = [prompts_for_wave() for _ in range(64)]
+    host_s = [0.0]
+    for i in range(max(3, args.warmup)):
+        wave(waves[i % len(waves)], host_s)
+    torch.cuda.synchronize(dev)
+    if binding.pa_get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    host_s = [0.0]
+    K = args.steps
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    computed = served = flops = 0
+    events = []
+    t0 = time.perf_counter()
+    for i in range(K):
+        w = waves[(args.warmup + i) % len(waves)]
+        a, c = wave(w, host_s)
+        computed, served, flops = computed + a, served + w[2], flops + c
+    torch.cuda.synchronize(dev)
+    t_s = dist_max(time.perf_counter() - t0, world, dev)
+    dist_barrier(world, dev)
+    if clocks:
+        clocks.stop()
+    if binding.pa_get_device_error():
+        raise RuntimeError("device error word set during the timed region")
+    if rank != 0:
+        return
+    pre_ms = sum(a.elapsed_time(b) for a, b in events) / K
+    achieved = flops / K / (pre_ms * 1e-3) / 1e12
+    peak, peak_note = measured_tensor_peak()
+    cpu = prefix_wave_cpu_baseline(args, cfg, waves, host, pool, q, maxb, scale)
+    line = {
+        "metric": "prefix-cache serving wave: prompt tokens served/s", "value": world * served / t_s,
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded token ids and N(0,1) values)",
+        "config": {"workload": f"prefix-cache serving wave: {R} requests, {cfg['system']}-token system prompt "
+                               f"+ suffix U[{cfg['suffix_lo']},{cfg['suffix_hi']}], 40/40 heads, d=128, fp16",
+                   "prefix_cache": use_cache, "num_blocks": nb, "waves": len(waves),
+                   "l2": "the shared prompt K/V (21 MB) is re-read by every request and may stay in L2; no flush"},
+        "computed_tokens_per_s": world * computed / t_s,
+        "computed_fraction": computed / served,
+        "host_bookkeeping_us_per_request": 1e6 * host_s[0] / (K * R),
+        "prefill_tflops_per_s": world * flops / t_s / 1e12,
+        "prefill_only": {"ms_per_wave": pre_ms, "tflops": achieved},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill (paged_prefill_kernel)",
+                     "peak_source": peak_note, "flops_per_launch": flops / K},
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary() if clocks else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def prefix_wave_cpu_baseline(args, cfg, waves, host, pool, q, maxb, scale):
+    """The oracle on the serving wave: the prefix-cache pool model admits and
+    frees whole waves (timed), and the attention oracle runs query rows of the
+    last timed wave (all heads of one row at a time) for the rest of the
+    budget; a wave's CPU time = its admission time + its causal flops at the
+    oracle's measured flop rate."""
+    import torch
+    import oracle
+    from oracle.prefix_cache import PrefixCacheModel
+    R, B = cfg["requests"], cfg["block_size"]
+    Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_size"]
+    budget = args.cpu_budget
+    m = PrefixCacheModel(pool.shape[1], B)
+    t_adm, n_adm, i = 0.0, 0, 0
+    while (t_adm < budget / 3 or n_adm < 2) and n_adm < len(waves):
+        tokens, cu_tokens, _ = waves[i % len(waves)]
+        t0 = time.perf_counter()
+        ids = [m.add_seq(tokens[cu_tokens[r]:cu_tokens[r + 1]],
+                         cache=not args.no_prefix_cache)[0] for r in range(R)]
+        for sid in ids:
+            m.free_seq(sid)
+        dt = time.perf_counter() - t0
+        if i > 0:              # the first wave fills the cache
+            t_adm, n_adm = t_adm + dt, n_adm + 1
+        i += 1
+    pool_bits = pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    q_bits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    cu = host["cu_seqlens_q"].numpy().copy()
+    sl = host["seq_lens"].numpy().copy()
+    bt = host["block_tables"].numpy().reshape(R, maxb).copy()
+    heads = np.arange(Hq, dtype=np.int32)
+    rows = int(cu[R])
+    t_att, fl, n, k = 0.0, 0, 0, 0
+    while t_att < budget * 2 / 3 and n < rows:
+        row = (k * 7919) % rows
+        s = int(np.searchsorted(cu, row, side="right") - 1)
+        vis = int(sl[s]) - int(cu[s + 1] - cu[s]) + (row - int(cu[s])) + 1
+        t0 = time.perf_counter()
+        oracle.decode_sampled(np.zeros(Hq, np.int32), heads, q_bits[row:row + 1], pool_bits, bt[s:s + 1],
+                              np.array([vis], np.int32), scale, Hq, Hkv, D, pool.shape[1], B, cfg["dtype"])
+        t_att += time.perf_counter() - t0
+        fl += 4 * D * Hq * vis
+        n, k = n + 1, k + 1
+    # causal flops of the average timed wave, from the last wave's admission
+    hits = host["num_cached"].numpy().astype(np.int64)
+    n_new = np.diff(cu).astype(np.int64)
+    last_flops = float((4 * D * Hq * ((2 * hits + 1 + n_new) * n_new // 2)).sum())
+    served = float(sl.astype(np.int64).sum())
+    wave_s = t_adm / n_adm + last_flops / (fl / t_att)
+    return {"value": served / wave_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"pool model over {n_adm} whole waves ({1e3 * t_adm / n_adm:.1f} ms/wave) + attention "
+                      f"oracle on {n} query rows of the last wave x {Hq} heads ({fl / t_att / 1e9:.2f} GFLOP/s), "
+                      f"scaled to that wave's {last_flops / 1e9:.1f} GFLOP"}
 
 
 def run_prefill_reference(args, rank, world):
@@ -690,7 +896,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama13b",
-                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.PREFILL_WORKLOADS))
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.PREFILL_WORKLOADS)
+                    + ["prefix_cache_prefill"])
+    ap.add_argument("--no-prefix-cache", action="store_true",
+                    help="prefix_cache_prefill: compute every prompt in full")
     ap.add_argument("--variant", default="literal", choices=["literal", "fork"])
     ap.add_argument("--kv-cache", default="16bit", choices=["16bit", "fp8"],
                     help="cache element type: the workload's 16-bit type, or E4M3 codes")
@@ -705,6 +914,17 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     rank, local_rank, world = dist_setup()
+    if args.workload == "prefix_cache_prefill":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the prefix-cache wave is host "
+                                  "bookkeeping plus pa_prefill; its oracle arm is the prefill one"}))
+        else:
+            run_prefix_cache(args, rank, local_rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     prefill = args.workload in workloads.PREFILL_WORKLOADS
     if prefill and args.kv_cache != "16bit":
         ap.error("--kv-cache fp8 applies to the decode workloads")

@@ -421,6 +421,35 @@ int pa_pcache_num_free(const pa_prefix_cache *c);
 int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens,
                       int *seq_id, int *num_cached_tokens);
 
+/* pa_pcache_admit flag: the requests neither match nor record (every block
+ * fresh and unhashed, freed to the queue's head) - prefix caching off. */
+#define PA_PCACHE_NO_CACHE 1
+
+/*
+ * Admit a wave of n prompts, in order, each as pa_pcache_add_seq does (or,
+ * with PA_PCACHE_NO_CACHE, without matching or recording), and build the
+ * prefill inputs for them in one call. Request r's tokens are
+ * tokens[cu_tokens[r] .. cu_tokens[r+1]) (host; cu_tokens[0] = 0, every
+ * request non-empty, at most max_blocks_per_seq blocks).
+ *
+ * Outputs (host int32, caller-owned; may be pinned memory that is then
+ * copied to the device), for the admitted requests r < return value:
+ *   seq_ids[r], num_cached[r]      the sequence and its matched tokens;
+ *   seq_lens[r]                    the prompt length;
+ *   cu_seqlens_q[0 .. r+1]         offsets of the uncached tokens, whose
+ *                                  queries the caller packs in this order;
+ *   slot_mapping[cu_seqlens_q[r] + i]  slot of position num_cached[r] + i
+ *                                  (slot_capacity >= cu_tokens[n] entries);
+ *   block_tables[r][max_blocks_per_seq] the table, padded with -1.
+ * Admission stops at the first request the free queue cannot supply (that
+ * request and the rest are untouched). Returns the number admitted (0..n),
+ * or a negative PA_ERR_* on bad arguments (nothing admitted).
+ */
+int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const int64_t *cu_tokens, int n,
+                    int flags, int max_blocks_per_seq, int32_t *seq_ids, int32_t *num_cached,
+                    int32_t *cu_seqlens_q, int32_t *seq_lens, int32_t *slot_mapping,
+                    int64_t slot_capacity, int32_t *block_tables);
+
 /* Reserve the next token's slot (*slot = table[pos / B] * B + pos % B); a
  * block that becomes full is hashed and recorded as cached. */
 int pa_pcache_append_token(pa_prefix_cache *c, int seq_id, int32_t token, int32_t *slot);
@@ -429,6 +458,10 @@ int pa_pcache_append_token(pa_prefix_cache *c, int seq_id, int32_t token, int32_
  * reaching 0 goes to the free queue's head if it has no hash and to its tail
  * if it has one ([codex] §4.3). */
 int pa_pcache_free_seq(pa_prefix_cache *c, int seq_id);
+
+/* pa_pcache_free_seq for seq_ids[n] in order; every id must be live and
+ * listed once, else nothing is freed. */
+int pa_pcache_free_seqs(pa_prefix_cache *c, const int32_t *seq_ids, int n);
 
 /* Tokens of a sequence, or a PA_ERR_* code. */
 int pa_pcache_seq_len(const pa_prefix_cache *c, int seq_id);

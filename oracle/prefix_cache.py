@@ -27,6 +27,10 @@ Rules (each from the page, readings marked):
     step writes their K/V before anything reads them; a decode block when
     its last slot is reserved). If another block already holds that hash,
     the first one stays the lookup target.
+  * With caching off for a request (cache=False) it neither matches nor
+    records, at admission or when decode fills a block: every block is
+    popped fresh and stays unhashed (the plain allocation of §4.3 without
+    the hash steps of §4.4).
   * Free: the sequence's blocks in reverse table order, count - 1; a block
     reaching 0 goes to the queue head if it has no hash (LIFO reuse) and to
     the tail if it has one (FIFO, so cached blocks live longest) (§4.3).
@@ -90,11 +94,11 @@ class PrefixCacheModel:
         self.cached.setdefault(h, []).append(b)
 
     # -- operations
-    def add_seq(self, tokens):
+    def add_seq(self, tokens, cache=True):
         """Returns (seq_id, tokens found in the cache)."""
         tokens = [int(t) for t in tokens]
         B, n = self.block_size, len(tokens)
-        hashes = chain_hashes(tokens, B)
+        hashes = chain_hashes(tokens, B) if cache else []
         hits = []
         for i, h in enumerate(hashes):
             if (i + 1) * B > n - 1 or h not in self.cached:
@@ -116,7 +120,7 @@ class PrefixCacheModel:
                 self._record(b, hashes[i])
         sid = self.next_id
         self.next_id += 1
-        self.seqs[sid] = {"table": table, "tokens": tokens, "hashes": hashes}
+        self.seqs[sid] = {"table": table, "tokens": tokens, "hashes": hashes, "cache": cache}
         return sid, len(hits) * B
 
     def append_token(self, sid, token):
@@ -129,7 +133,7 @@ class PrefixCacheModel:
                 raise OutOfBlocks("no free block")
             s["table"].append(self._pop())
         s["tokens"].append(int(token))
-        if (pos + 1) % B == 0:
+        if (pos + 1) % B == 0 and s["cache"]:
             parent = s["hashes"][-1] if s["hashes"] else NONE_HASH
             h = block_hash(parent, s["tokens"][pos + 1 - B:pos + 1])
             s["hashes"].append(h)

@@ -27,6 +27,7 @@ PA_F16 = 0
 PA_BF16 = 1
 PA_FP8_E4M3 = 2
 PA_DECODE_SHARED_BLOCKS = 1
+PA_PCACHE_NO_CACHE = 1
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SLOT = 2
 PA_DEVERR_SEQ_LEN = 4
@@ -68,8 +69,10 @@ SIGNATURES = [
     ("pa_pcache_destroy", None, [_vp]),
     ("pa_pcache_num_free", _i, [_vp]),
     ("pa_pcache_add_seq", _i, [_vp, _i32p, _i, _ip, _ip]),
+    ("pa_pcache_admit", _i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp]),
     ("pa_pcache_append_token", _i, [_vp, _i, ctypes.c_int32, _i32p]),
     ("pa_pcache_free_seq", _i, [_vp, _i]),
+    ("pa_pcache_free_seqs", _i, [_vp, _vp, _i]),
     ("pa_pcache_seq_len", _i, [_vp, _i]),
     ("pa_pcache_block_tables", _i, [_vp, _ip, _i, _i, _i32p]),
     ("pa_pcache_slots", _i, [_vp, _i, _i, _i, _i32p]),
@@ -146,6 +149,21 @@ def _dev(t, name):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_array(a, dtype, name):
+    """A contiguous host array of the given dtype (numpy, or a CPU tensor viewed as numpy)."""
+    if hasattr(a, "is_cuda"):
+        if a.is_cuda or not a.is_contiguous():
+            raise PAError(PA_ERR_INVALID_ARG, f"{name}: needs a contiguous host tensor")
+        a = a.numpy()
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags.c_contiguous:
+        raise PAError(PA_ERR_INVALID_ARG, f"{name}: needs a contiguous {np.dtype(dtype).name} array")
+    return a
+
+
+def _host_addr(a) -> int:
+    return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
 
 
 def pa_version() -> int:
@@ -390,6 +408,36 @@ class PrefixCache:
         _check(lib().pa_pcache_add_seq(self._h, t.ctypes.data_as(_i32p), len(t), ctypes.byref(sid),
                                        ctypes.byref(hit)))
         return sid.value, hit.value
+
+    _ADMIT_OUT = ("seq_ids", "num_cached", "cu_seqlens_q", "seq_lens", "slot_mapping", "block_tables")
+
+    def admit(self, tokens, cu_tokens, max_blocks_per_seq: int, flags: int = 0, out=None):
+        """pa_pcache_admit: -> (number admitted, out). tokens is int32 and
+        cu_tokens int64 (numpy or CPU tensors); out maps the six output names
+        to int32 host buffers (numpy or CPU tensors, e.g. pinned), allocated
+        here when not given."""
+        tok, cu = _host_array(tokens, np.int32, "tokens"), _host_array(cu_tokens, np.int64, "cu_tokens")
+        n = len(cu) - 1
+        total = int(cu[-1]) if n > 0 else 0
+        sizes = {"seq_ids": n, "num_cached": n, "cu_seqlens_q": n + 1, "seq_lens": n,
+                 "slot_mapping": total, "block_tables": n * max_blocks_per_seq}
+        if out is None:
+            out = {k: np.empty(v, np.int32) for k, v in sizes.items()}
+            out["block_tables"] = out["block_tables"].reshape(n, max_blocks_per_seq)
+        ptrs = []
+        for k in self._ADMIT_OUT:
+            a = _host_array(out[k], np.int32, k)
+            if a.size < sizes[k]:
+                raise PAError(PA_ERR_INVALID_ARG, f"admit: {k} holds {a.size} < {sizes[k]}")
+            ptrs.append(_host_addr(out[k]))
+        slot_cap = _host_array(out["slot_mapping"], np.int32, "slot_mapping").size
+        count = _check(lib().pa_pcache_admit(self._h, _host_addr(tokens), _host_addr(cu_tokens), n, flags,
+                                             max_blocks_per_seq, *ptrs[:5], slot_cap, ptrs[5]))
+        return count, out
+
+    def free_seqs(self, seqs) -> None:
+        ids = _host_array(seqs, np.int32, "seqs")
+        _check(lib().pa_pcache_free_seqs(self._h, _host_addr(seqs), len(ids)))
 
     def append_token(self, seq: int, token: int) -> int:
         slot = ctypes.c_int32(0)

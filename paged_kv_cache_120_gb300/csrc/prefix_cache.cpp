@@ -28,6 +28,7 @@
 // for the device calls and never touches device memory.
 #include <algorithm>
 #include <array>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <unordered_map>
@@ -55,105 +56,195 @@ constexpr uint32_t kRound[64] = {
 
 inline uint32_t rotr(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
 
-class Sha256 {
-  public:
-    Sha256() : state_{0x6a09e667, 0xbb67ae85, 0x3c6ef372, 0xa54ff53a, 0x510e527f, 0x9b05688c, 0x1f83d9ab,
-                      0x5be0cd19} {}
-    void update(const uint8_t *p, size_t n)
-    {
-        total_ += n;
-        while (n > 0) {
-            const size_t k = std::min(n, sizeof(buf_) - used_);
-            std::memcpy(buf_ + used_, p, k);
-            used_ += k;
-            p += k;
-            n -= k;
-            if (used_ == sizeof(buf_)) {
-                compress(buf_);
-                used_ = 0;
-            }
+// One 512-bit block into the eight working variables.
+void sha256_compress(uint32_t st[8], const uint8_t *blk)
+{
+    uint32_t w[64];
+    for (int t = 0; t < 16; ++t)
+        w[t] = (uint32_t)blk[4 * t] << 24 | (uint32_t)blk[4 * t + 1] << 16 | (uint32_t)blk[4 * t + 2] << 8 |
+               (uint32_t)blk[4 * t + 3];
+    for (int t = 16; t < 64; ++t) {
+        const uint32_t s0 = rotr(w[t - 15], 7) ^ rotr(w[t - 15], 18) ^ (w[t - 15] >> 3);
+        const uint32_t s1 = rotr(w[t - 2], 17) ^ rotr(w[t - 2], 19) ^ (w[t - 2] >> 10);
+        w[t] = w[t - 16] + s0 + w[t - 7] + s1;
+    }
+    uint32_t a = st[0], b = st[1], c = st[2], d = st[3], e = st[4], f = st[5], g = st[6], h = st[7];
+    for (int t = 0; t < 64; ++t) {
+        const uint32_t t1 = h + (rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25)) + ((e & f) ^ (~e & g)) + kRound[t] + w[t];
+        const uint32_t t2 = (rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22)) + ((a & b) ^ (a & c) ^ (b & c));
+        h = g;
+        g = f;
+        f = e;
+        e = d + t1;
+        d = c;
+        c = b;
+        b = a;
+        a = t1 + t2;
+    }
+    st[0] += a;
+    st[1] += b;
+    st[2] += c;
+    st[3] += d;
+    st[4] += e;
+    st[5] += f;
+    st[6] += g;
+    st[7] += h;
+}
+
+// Hash of a full block: SHA-256(parent hash || token ids as little-endian
+// int32). The message is staged 64 bytes at a time; padding is a 1 bit,
+// zeros, and the 64-bit big-endian bit length.
+Digest block_hash(const Digest &parent, const int32_t *tokens, int n)
+{
+    uint32_t st[8] = {0x6a09e667, 0xbb67ae85, 0x3c6ef372, 0xa54ff53a, 0x510e527f, 0x9b05688c, 0x1f83d9ab,
+                      0x5be0cd19};
+    uint8_t blk[64];
+    std::memcpy(blk, parent.data(), 32);
+    int used = 32;
+    for (int i = 0; i < n; ++i) {
+        const uint32_t t = (uint32_t)tokens[i];
+        blk[used] = (uint8_t)t;
+        blk[used + 1] = (uint8_t)(t >> 8);
+        blk[used + 2] = (uint8_t)(t >> 16);
+        blk[used + 3] = (uint8_t)(t >> 24);
+        used += 4;
+        if (used == 64) {
+            sha256_compress(st, blk);
+            used = 0;
         }
     }
-    Digest finish()
+    const uint64_t bits = (32 + 4 * (uint64_t)n) * 8;
+    blk[used++] = 0x80;
+    if (used > 56) {
+        std::memset(blk + used, 0, 64 - used);
+        sha256_compress(st, blk);
+        used = 0;
+    }
+    std::memset(blk + used, 0, 56 - used);
+    for (int i = 0; i < 8; ++i)
+        blk[56 + i] = (uint8_t)(bits >> (56 - 8 * i));
+    sha256_compress(st, blk);
+    Digest d;
+    for (int i = 0; i < 8; ++i)
+        for (int j = 0; j < 4; ++j)
+            d[4 * i + j] = (uint8_t)(st[i] >> (24 - 8 * j));
+    return d;
+}
+
+// Key of (parent hash, block tokens) in the digest memo: a multiply-xorshift
+// mix of the 64-bit words; candidates are always verified in full.
+uint64_t memo_key(const Digest &parent, const int32_t *tokens, int n)
+{
+    uint64_t h = 0x243f6a8885a308d3ull;
+    auto mix = [&h](uint64_t w) {
+        h = (h ^ w) * 0x9e3779b97f4a7c15ull;
+        h ^= h >> 29;
+    };
+    for (int i = 0; i < 4; ++i) {
+        uint64_t w;
+        std::memcpy(&w, parent.data() + 8 * i, 8);
+        mix(w);
+    }
+    for (int i = 0; i < n; ++i)
+        mix((uint64_t)(uint32_t)tokens[i] | (uint64_t)i << 32);
+    return h;
+}
+
+// Index from a 64-bit key to the blocks that carry it, allocation-free:
+// open addressing with linear probing over 2^k >= 2 * num_blocks slots (so at
+// most half full), each slot holding the first block of a chain threaded
+// through next[] in insertion order. Several keys' worth of blocks never share
+// a chain; callers compare the full identity along the chain.
+class BlockIndex {
+  public:
+    void init(int num_blocks)
     {
-        const uint64_t bits = total_ * 8;
-        const uint8_t one = 0x80, zero = 0;
-        update(&one, 1);
-        while (used_ != 56)
-            update(&zero, 1);
-        uint8_t len[8];
-        for (int i = 0; i < 8; ++i)
-            len[i] = (uint8_t)(bits >> (56 - 8 * i));
-        update(len, 8);
-        Digest d;
-        for (int i = 0; i < 8; ++i)
-            for (int j = 0; j < 4; ++j)
-                d[4 * i + j] = (uint8_t)(state_[i] >> (24 - 8 * j));
-        return d;
+        size_t cap = 16;
+        while (cap < 2 * (size_t)num_blocks)
+            cap <<= 1;
+        mask_ = cap - 1;
+        keys_.assign(cap, 0);
+        head_.assign(cap, -1);
+        next_.assign(num_blocks, -1);
+    }
+    // First block under key, or -1; then next(b) walks the chain.
+    int32_t first(uint64_t key) const
+    {
+        const size_t i = find(key);
+        return head_[i];
+    }
+    int32_t next(int32_t b) const { return next_[b]; }
+    void insert(uint64_t key, int32_t b)
+    {
+        const size_t i = find(key);
+        next_[b] = -1;
+        if (head_[i] < 0) {
+            keys_[i] = key;
+            head_[i] = b;
+            return;
+        }
+        int32_t t = head_[i];
+        while (next_[t] >= 0)
+            t = next_[t];
+        next_[t] = b;
+    }
+    void erase(uint64_t key, int32_t b)
+    {
+        const size_t i = find(key);
+        if (head_[i] == b) {
+            head_[i] = next_[b];
+            if (head_[i] < 0)
+                remove_slot(i);
+        } else {
+            for (int32_t t = head_[i]; t >= 0; t = next_[t])
+                if (next_[t] == b) {
+                    next_[t] = next_[b];
+                    break;
+                }
+        }
+        next_[b] = -1;
     }
 
   private:
-    void compress(const uint8_t *blk)
+    // The slot holding key, or the empty slot where it would go.
+    size_t find(uint64_t key) const
     {
-        uint32_t w[64];
-        for (int t = 0; t < 16; ++t)
-            w[t] = (uint32_t)blk[4 * t] << 24 | (uint32_t)blk[4 * t + 1] << 16 | (uint32_t)blk[4 * t + 2] << 8 |
-                   (uint32_t)blk[4 * t + 3];
-        for (int t = 16; t < 64; ++t) {
-            const uint32_t s0 = rotr(w[t - 15], 7) ^ rotr(w[t - 15], 18) ^ (w[t - 15] >> 3);
-            const uint32_t s1 = rotr(w[t - 2], 17) ^ rotr(w[t - 2], 19) ^ (w[t - 2] >> 10);
-            w[t] = w[t - 16] + s0 + w[t - 7] + s1;
-        }
-        uint32_t a = state_[0], b = state_[1], c = state_[2], d = state_[3], e = state_[4], f = state_[5],
-                 g = state_[6], h = state_[7];
-        for (int t = 0; t < 64; ++t) {
-            const uint32_t t1 = h + (rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25)) + ((e & f) ^ (~e & g)) + kRound[t] + w[t];
-            const uint32_t t2 = (rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22)) + ((a & b) ^ (a & c) ^ (b & c));
-            h = g;
-            g = f;
-            f = e;
-            e = d + t1;
-            d = c;
-            c = b;
-            b = a;
-            a = t1 + t2;
-        }
-        state_[0] += a;
-        state_[1] += b;
-        state_[2] += c;
-        state_[3] += d;
-        state_[4] += e;
-        state_[5] += f;
-        state_[6] += g;
-        state_[7] += h;
+        size_t i = key & mask_;
+        while (head_[i] >= 0 && keys_[i] != key)
+            i = (i + 1) & mask_;
+        return i;
     }
-    uint32_t state_[8];
-    uint8_t buf_[64] = {};
-    size_t used_ = 0;
-    uint64_t total_ = 0;
+    // Backward-shift deletion: later entries of the probe run whose home is
+    // not cyclically within (hole, their slot] move into the hole.
+    void remove_slot(size_t i)
+    {
+        size_t j = i;
+        for (;;) {
+            j = (j + 1) & mask_;
+            if (head_[j] < 0)
+                break;
+            const size_t k = keys_[j] & mask_;
+            const bool stays = i <= j ? (i < k && k <= j) : (i < k || k <= j);
+            if (!stays) {
+                keys_[i] = keys_[j];
+                head_[i] = head_[j];
+                i = j;
+            }
+        }
+        head_[i] = -1;
+    }
+    size_t mask_ = 0;
+    std::vector<uint64_t> keys_;
+    std::vector<int32_t> head_, next_;
 };
 
-// Hash of a full block: SHA-256(parent hash || token ids as little-endian int32).
-Digest block_hash(const Digest &parent, const int32_t *tokens, int n)
+// Index key of a digest: its first 8 bytes (SHA-256 output is uniform).
+uint64_t digest_key(const Digest &d)
 {
-    Sha256 h;
-    h.update(parent.data(), parent.size());
-    for (int i = 0; i < n; ++i) {
-        const uint32_t t = (uint32_t)tokens[i];
-        const uint8_t b[4] = {(uint8_t)t, (uint8_t)(t >> 8), (uint8_t)(t >> 16), (uint8_t)(t >> 24)};
-        h.update(b, 4);
-    }
-    return h.finish();
+    uint64_t x;
+    std::memcpy(&x, d.data(), sizeof(x));
+    return x;
 }
-
-struct DigestHash {
-    size_t operator()(const Digest &d) const
-    {
-        uint64_t x;
-        std::memcpy(&x, d.data(), sizeof(x));
-        return (size_t)x;
-    }
-};
 
 }  // namespace
 
@@ -163,10 +254,21 @@ struct pa_prefix_cache {
     std::vector<char> in_free, hashed;
     std::vector<Digest> hash;
     int32_t head = -1, tail = -1, nfree = 0;
-    std::unordered_map<Digest, std::vector<int32_t>, DigestHash> cached;  // first = lookup target
+    // Recorded (cached) blocks by hash; among blocks with the same hash the
+    // earliest recorded is the lookup target.
+    BlockIndex cached;
+    // Digest memo: a recorded block keeps its parent hash and token ids, so a
+    // later (parent, tokens) pair equal to them reuses its hash instead of
+    // running SHA-256 again. Only a full match of both is taken: the digest
+    // is exactly the one SHA-256 would give.
+    BlockIndex memo;
+    std::vector<Digest> parent_of;
+    std::vector<int32_t> tokens_of;  // block_size ids per block
+    std::vector<uint64_t> memo_key_of;
     struct Seq {
         std::vector<int32_t> table, tokens;
         std::vector<Digest> hashes;
+        bool cache = true;  // false: never matched against nor recorded
     };
     std::unordered_map<int, Seq> seqs;
     int next_id = 0;
@@ -198,29 +300,43 @@ struct pa_prefix_cache {
         in_free[b] = 1;
         ++nfree;
     }
+    // Digest of a full block: from the memo when a recorded block has the
+    // same parent hash and token ids, else SHA-256.
+    Digest digest(const Digest &parent, const int32_t *tokens)
+    {
+        const int B = block_size;
+        for (int32_t b = memo.first(memo_key(parent, tokens, B)); b >= 0; b = memo.next(b))
+            if (parent_of[b] == parent &&
+                std::memcmp(tokens_of.data() + (size_t)b * B, tokens, sizeof(int32_t) * (size_t)B) == 0)
+                return hash[b];
+        return block_hash(parent, tokens, B);
+    }
+    // The lookup target for a hash, or -1.
+    int32_t lookup(const Digest &d) const
+    {
+        for (int32_t b = cached.first(digest_key(d)); b >= 0; b = cached.next(b))
+            if (hash[b] == d)
+                return b;
+        return -1;
+    }
     // cache
     void evict(int32_t b)
     {
         if (!hashed[b])
             return;
-        auto it = cached.find(hash[b]);
-        if (it != cached.end()) {
-            auto &v = it->second;
-            for (size_t i = 0; i < v.size(); ++i)
-                if (v[i] == b) {
-                    v.erase(v.begin() + (long)i);
-                    break;
-                }
-            if (v.empty())
-                cached.erase(it);
-        }
+        memo.erase(memo_key_of[b], b);
+        cached.erase(digest_key(hash[b]), b);
         hashed[b] = 0;
     }
-    void record(int32_t b, const Digest &d)
+    void record(int32_t b, const Digest &d, const Digest &parent, const int32_t *tokens)
     {
         hash[b] = d;
         hashed[b] = 1;
-        cached[d].push_back(b);
+        cached.insert(digest_key(d), b);
+        parent_of[b] = parent;
+        std::memcpy(tokens_of.data() + (size_t)b * block_size, tokens, sizeof(int32_t) * (size_t)block_size);
+        memo_key_of[b] = memo_key(parent, tokens, block_size);
+        memo.insert(memo_key_of[b], b);
     }
     int32_t pop()
     {
@@ -260,6 +376,11 @@ extern "C" pa_prefix_cache *pa_pcache_create(int num_blocks, int block_size)
     c->in_free.assign(num_blocks, 0);
     c->hashed.assign(num_blocks, 0);
     c->hash.assign(num_blocks, Digest{});
+    c->parent_of.assign(num_blocks, Digest{});
+    c->tokens_of.assign((size_t)num_blocks * block_size, 0);
+    c->memo_key_of.assign(num_blocks, 0);
+    c->cached.init(num_blocks);
+    c->memo.init(num_blocks);
     for (int32_t b = 1; b < num_blocks; ++b)
         c->push_tail(b);
     return c;
@@ -274,36 +395,42 @@ extern "C" int pa_pcache_num_free(const pa_prefix_cache *c)
     return c->nfree;
 }
 
-extern "C" int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens, int *seq_id,
-                                 int *num_cached_tokens)
+namespace {
+
+// One prompt into the pool (pa_pcache_add_seq's rules). With cache false the
+// prompt neither matches nor records: every block is fresh and unhashed.
+// Returns PA_OK or PA_ERR_OUT_OF_BLOCKS, the latter with the pool unchanged
+// and no error text set.
+int admit_one(pa_prefix_cache *c, const int32_t *tokens, int num_tokens, bool cache, int *seq_id,
+              int *num_cached_tokens, int *need_out, int *avail_out)
 {
-    if (!c || !seq_id || !num_cached_tokens || num_tokens <= 0 || !tokens)
-        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_add_seq: bad arguments (num_tokens must be > 0)");
     const int B = c->block_size;
-    const int full = num_tokens / B, nblk = (num_tokens + B - 1) / B;
+    const int full = cache ? num_tokens / B : 0, nblk = (num_tokens + B - 1) / B;
     std::vector<Digest> hashes;
     hashes.reserve(full);
     Digest parent{};
     for (int i = 0; i < full; ++i) {
-        parent = block_hash(parent, tokens + (size_t)i * B, B);
+        parent = c->digest(parent, tokens + (size_t)i * B);
         hashes.push_back(parent);
     }
     std::vector<int32_t> hits;
     for (int i = 0; i < full; ++i) {
         if ((long long)(i + 1) * B > num_tokens - 1)
             break;
-        auto it = c->cached.find(hashes[i]);
-        if (it == c->cached.end())
+        const int32_t b = c->lookup(hashes[i]);
+        if (b < 0)
             break;
-        hits.push_back(it->second.front());
+        hits.push_back(b);
     }
     int touched_free = 0;
     for (int32_t b : hits)
         touched_free += c->in_free[b] ? 1 : 0;
     const int need = nblk - (int)hits.size();
-    if (need > c->nfree - touched_free)
-        return set_error(PA_ERR_OUT_OF_BLOCKS, "pa_pcache_add_seq: need %d blocks, %d free", need,
-                         c->nfree - touched_free);
+    if (need > c->nfree - touched_free) {
+        *need_out = need;
+        *avail_out = c->nfree - touched_free;
+        return PA_ERR_OUT_OF_BLOCKS;
+    }
     pa_prefix_cache::Seq s;
     s.table.reserve(nblk);
     for (int32_t b : hits) {
@@ -316,15 +443,78 @@ extern "C" int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int 
         const int32_t b = c->pop();
         s.table.push_back(b);
         if (i < full)
-            c->record(b, hashes[i]);
+            c->record(b, hashes[i], i ? hashes[i - 1] : Digest{}, tokens + (size_t)i * B);
     }
     s.tokens.assign(tokens, tokens + num_tokens);
     s.hashes = std::move(hashes);
+    s.cache = cache;
     const int id = c->next_id++;
     c->seqs.emplace(id, std::move(s));
     *seq_id = id;
     *num_cached_tokens = (int)hits.size() * B;
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens, int *seq_id,
+                                 int *num_cached_tokens)
+{
+    if (!c || !seq_id || !num_cached_tokens || num_tokens <= 0 || !tokens)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_add_seq: bad arguments (num_tokens must be > 0)");
+    int need = 0, avail = 0;
+    const int r = admit_one(c, tokens, num_tokens, true, seq_id, num_cached_tokens, &need, &avail);
+    if (r == PA_ERR_OUT_OF_BLOCKS)
+        return set_error(PA_ERR_OUT_OF_BLOCKS, "pa_pcache_add_seq: need %d blocks, %d free", need, avail);
+    return r;
+}
+
+extern "C" int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const int64_t *cu_tokens, int n,
+                               int flags, int max_blocks_per_seq, int32_t *seq_ids, int32_t *num_cached,
+                               int32_t *cu_seqlens_q, int32_t *seq_lens, int32_t *slot_mapping,
+                               int64_t slot_capacity, int32_t *block_tables)
+{
+    if (!c || n < 0 || !cu_tokens || max_blocks_per_seq <= 0 || (flags & ~PA_PCACHE_NO_CACHE) ||
+        (n > 0 && (!tokens || !seq_ids || !num_cached || !cu_seqlens_q || !seq_lens || !slot_mapping ||
+                   !block_tables)))
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: bad arguments");
+    const int B = c->block_size;
+    if (cu_tokens[0] != 0)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: cu_tokens[0] must be 0");
+    for (int r = 0; r < n; ++r) {
+        const int64_t len = cu_tokens[r + 1] - cu_tokens[r];
+        if (len <= 0 || len > INT32_MAX)
+            return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: request %d has %lld tokens", r, (long long)len);
+        if ((len + B - 1) / B > max_blocks_per_seq)
+            return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: request %d needs %lld blocks > %d", r,
+                             (long long)((len + B - 1) / B), max_blocks_per_seq);
+    }
+    if (n > 0 && cu_tokens[n] > slot_capacity)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: slot_capacity %lld < %lld prompt tokens",
+                         (long long)slot_capacity, (long long)cu_tokens[n]);
+    if (n > 0 && cu_tokens[n] > INT32_MAX)
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: more than 2^31 - 1 prompt tokens");
+    const bool cache = !(flags & PA_PCACHE_NO_CACHE);
+    cu_seqlens_q[0] = 0;
+    int32_t q = 0;
+    int admitted = 0;
+    for (; admitted < n; ++admitted) {
+        const int len = (int)(cu_tokens[admitted + 1] - cu_tokens[admitted]);
+        int sid = 0, hit = 0, need = 0, avail = 0;
+        if (admit_one(c, tokens + cu_tokens[admitted], len, cache, &sid, &hit, &need, &avail) != PA_OK)
+            break;
+        const auto &table = c->seqs.find(sid)->second.table;
+        seq_ids[admitted] = sid;
+        num_cached[admitted] = hit;
+        seq_lens[admitted] = len;
+        for (int pos = hit; pos < len; ++pos)
+            slot_mapping[q++] = table[pos / B] * B + pos % B;
+        cu_seqlens_q[admitted + 1] = q;
+        int32_t *row = block_tables + (size_t)admitted * max_blocks_per_seq;
+        for (int j = 0; j < max_blocks_per_seq; ++j)
+            row[j] = j < (int)table.size() ? table[j] : -1;
+    }
+    return admitted;
 }
 
 extern "C" int pa_pcache_append_token(pa_prefix_cache *c, int seq_id, int32_t token, int32_t *slot)
@@ -343,11 +533,12 @@ extern "C" int pa_pcache_append_token(pa_prefix_cache *c, int seq_id, int32_t to
         s.table.push_back(c->pop());
     }
     s.tokens.push_back(token);
-    if ((pos + 1) % B == 0) {
+    if ((pos + 1) % B == 0 && s.cache) {
         const Digest parent = s.hashes.empty() ? Digest{} : s.hashes.back();
-        const Digest d = block_hash(parent, s.tokens.data() + (pos + 1 - B), B);
+        const int32_t *blk = s.tokens.data() + (pos + 1 - B);
+        const Digest d = c->digest(parent, blk);
         s.hashes.push_back(d);
-        c->record(s.table[pos / B], d);
+        c->record(s.table[pos / B], d, parent, blk);
     }
     *slot = s.table[pos / B] * B + pos % B;
     return PA_OK;
@@ -367,6 +558,25 @@ extern "C" int pa_pcache_free_seq(pa_prefix_cache *c, int seq_id)
             c->hashed[b] ? c->push_tail(b) : c->push_head(b);
     }
     c->seqs.erase(it);
+    return PA_OK;
+}
+
+extern "C" int pa_pcache_free_seqs(pa_prefix_cache *c, const int32_t *seq_ids, int n)
+{
+    if (!c || n < 0 || (n > 0 && !seq_ids))
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_free_seqs: bad arguments");
+    for (int i = 0; i < n; ++i)
+        if (c->seqs.find(seq_ids[i]) == c->seqs.end())
+            return set_error(PA_ERR_NOT_FOUND, "pa_pcache_free_seqs: unknown sequence %d", seq_ids[i]);
+    std::vector<int32_t> ids(seq_ids, seq_ids + n);
+    std::sort(ids.begin(), ids.end());
+    if (std::adjacent_find(ids.begin(), ids.end()) != ids.end())
+        return set_error(PA_ERR_INVALID_ARG, "pa_pcache_free_seqs: a sequence is listed twice");
+    for (int i = 0; i < n; ++i) {
+        const int r = pa_pcache_free_seq(c, seq_ids[i]);
+        if (r != PA_OK)
+            return r;
+    }
     return PA_OK;
 }
 

@@ -96,6 +96,19 @@ PREFILL_WORKLOADS = {
 }
 
 
+# Prefix-cache serving wave: requests sharing a system prompt, each with a
+# private suffix; Llama-2-13B layer shape (40/40 heads, d=128, fp16).
+SHARED_PROMPT = dict(requests=16, system=1024, suffix_lo=64, suffix_hi=512, num_q_heads=40,
+                     num_kv_heads=40, head_size=128, dtype=F16, block_size=16, vocab=32000)
+
+
+def shared_prompt_tokens(seed: int):
+    """The system prompt's token ids and a generator of request suffixes."""
+    g = rng(seed + 5)
+    system = g.integers(0, SHARED_PROMPT["vocab"], size=SHARED_PROMPT["system"]).astype(np.int32)
+    return system, g
+
+
 def prefill_prefixes(name: str, seed: int) -> np.ndarray:
     """Cached prefix length of every sequence of a prefill workload."""
     w = PREFILL_WORKLOADS[name]
