@@ -91,6 +91,10 @@ MUTANTS = [
      "        self.ref[b] = 1", "test_prefix_cache_model.py"),                         # no eviction
     ("oracle/prefix_cache.py", 'parent = s["hashes"][-1] if s["hashes"] else NONE_HASH',
      "parent = NONE_HASH", "test_prefix_cache_model.py"),                             # chain broken
+    ("oracle/prefix_cache.py", "            if self.ref[b] == 0:\n                self.free.remove(b)\n",
+     "", "test_prefix_cache_model.py"),                                                # no touch
+    ("oracle/prefix_cache.py", "hashes = chain_hashes(tokens, B) if cache else []",
+     "hashes = chain_hashes(tokens, B)", "test_prefix_cache_model.py"),              # caching never off
     ("oracle/block_manager.py", "self.free.insert(0, b)", "self.free.append(b)",
      "test_block_manager.py"),                                                         # free to tail
     ("oracle/block_manager.py", "                self.ref[last] -= 1\n", "",

@@ -122,3 +122,24 @@ def test_decode_blocks_become_cached_when_full():
     _, hit = m.add_seq(toks + [1])
     assert hit == 32
     m.check_invariants()
+
+
+def test_caching_off_is_plain_allocation():
+    """With caching off a request neither matches nor records: the same
+    prompt twice gets fresh blocks, none carries a hash, and freeing returns
+    them all to the head (LIFO), exactly the plain pool of section 4.3."""
+    m = PrefixCacheModel(16, B)
+    p = _toks(11, 40)
+    s0, hit0 = m.add_seq(p, cache=False)
+    s1, hit1 = m.add_seq(p, cache=False)
+    assert (hit0, hit1) == (0, 0)
+    assert m.table(s0) == [1, 2, 3] and m.table(s1) == [4, 5, 6]
+    assert all(h is None for h in m.hash) and m.cached == {}
+    for t in range(8):                            # block 3 fills at token 48: still unhashed
+        m.append_token(s0, t)
+    assert m.hash[3] is None
+    m.free_seq(s0)
+    assert m.free[:3] == [1, 2, 3]
+    _, hit = m.add_seq(p)                         # a caching request finds nothing either
+    assert hit == 0
+    m.check_invariants()
