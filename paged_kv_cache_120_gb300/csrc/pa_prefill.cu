@@ -12,18 +12,23 @@
 // How it is computed (one CTA = 128 query rows of one (sequence, kv head)):
 //  * Rows are (query head of the kv head's group, query token) pairs, so the
 //    heads that share a kv head share every K/V tile. A TMEM lane per row.
-//  * Warp 4 loads Q once and then 128-token K and V tiles by TMA (16-token
-//    boxes looked up through the block table, 128-byte swizzle) into rings
-//    of three K and two V stages, K and V each produced at its own pace. Warp 5 issues the MMAs from one thread: S = Q K^T into
-//    one of two TMEM buffers, then O += P V (V read as an MN-major operand)
-//    into a third, so the next tile's scores overlap this tile's softmax.
-//  * Warps 0-3 own one row each: they read the row of S from TMEM, mask it
-//    causally, run the fp32 online softmax in base 2 (the reference maximum
-//    moves only when a score exceeds it by 2^8, so O in TMEM is rarely
-//    rescaled and the next tile's softmax need not wait for this tile's
-//    P V), and write P (rounded to the element type) to
-//    shared memory in the MMA's swizzled layout. At the end they read O,
-//    divide by the row sum and store.
+//  * Warp 8 loads Q once and the K tiles, warp 10 the V tiles, by TMA
+//    (16-token boxes looked up through the block table, 128-byte swizzle),
+//    into rings of three K and two V stages, each at its own pace. One
+//    thread of warp 9 issues the MMAs: S = Q K^T into one of two TMEM
+//    buffers, then O += P V (V read as an MN-major operand) into a third,
+//    so the next tile's scores overlap this tile's softmax.
+//  * Warps 0-7 run the softmax, two warps per row: warp w and w + 4 share
+//    the TMEM lanes of row quarter w % 4 and take the row's columns 0-63 and
+//    64-127. Each scales and masks its half causally, the two swap partial
+//    maxima through TMEM, and both run the same fp32 online softmax in base
+//    2 (the reference maximum moves only when a score exceeds it by 2^8, so
+//    O in TMEM is rarely rescaled and the next tile's softmax need not wait
+//    for this tile's P V), writing their half of P (rounded to the element
+//    type) to shared memory in the MMA's swizzled layout. Two warps per
+//    row keep two softmax warps issuing on every SM sub-partition. At the
+//    end the partial row sums meet, and each warp divides and stores its
+//    half of O.
 //  * Every wait is bounded; the K/V rows past a sequence's end (padding slots
 //    of its last block, possibly NaN) are zeroed before P V reads them.
 #include <cuda.h>
@@ -144,6 +149,20 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float *v)
         : "memory");
 }
 
+// One fp32 column of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tc_st1(uint32_t taddr, float v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float tc_ld1(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    return __uint_as_float(r);
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -158,7 +177,9 @@ constexpr int kN = 128;                    // cached tokens per K/V tile
 constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
 constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit operand: 32 KB
 constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size is a multiple)
-constexpr int kThreads = 224;              // warps 0-3 softmax, 4 Q/K TMA, 5 MMA, 6 V TMA
+constexpr int kThreads = 352;              // warps 0-7 softmax, 8 Q/K TMA, 9 MMA, 10 V TMA
+constexpr int kSoftmaxThreads = 256;       // two warps per row quarter, one per 64-column half
+constexpr int kWarpQK = 8, kWarpMMA = 9, kWarpV = 10;
 constexpr int kKStages = 3;                // K ring (freed when S = Q K^T is done)
 constexpr int kVStages = 2;                // V ring (freed when O += P V is done)
 constexpr int kOffQ = 0;
@@ -166,8 +187,9 @@ constexpr int kOffK = kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffP = kOffV + kVStages * kTileBytes;
 constexpr int kSmemBytes = kOffP + kTileBytes + 1024;  // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 512;        // S (two buffers) and O, 128 columns each
+constexpr uint32_t kTmemCols = 512;        // S (two buffers) and O, 128 columns each, + exchange
 constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+constexpr uint32_t kTmemX = 384;           // row maxima (2 parities x 2 halves) and row sums (2 halves)
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
 
 struct PrefillParams {
@@ -193,6 +215,7 @@ struct PrefillParams {
 struct PrefillBars {
     uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full, pv_done;
+    uint64_t xch[4];  // per row quarter: the two half-row warps exchanged their values
     uint32_t tmem_base;
     int fail;
 };
@@ -252,12 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(b_s(0), 1);
         mbar_init(b_s(1), 1);
-        mbar_init(b_p, 128);
+        mbar_init(b_p, kSoftmaxThreads);
         mbar_init(b_pv, 1);
+        for (int i = 0; i < 4; ++i)
+            mbar_init(smem_addr(&bars.xch[i]), 64);
         bars.fail = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMMA) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(&bars.tmem_base)),
                      "r"(kTmemCols)
@@ -279,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
     };
 
-    if (warp == 4 || warp == 6) {
+    if (warp == kWarpQK || warp == kWarpV) {
         // ---------------------------------------------------------- TMA
         // Warp 4 produces Q and the K tiles, warp 6 the V tiles, each at its
         // own pace (separate warps, so that one producer's wait never holds
@@ -287,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The block-table entry of the next tile is loaded while the current
         // one waits for its stage.
         const int32_t *table = p.block_tables + (long long)s * p.max_blocks_per_seq;
-        const bool is_k = warp == 4;
+        const bool is_k = warp == kWarpQK;
         if (is_k && lane == 0) {
             const int head0 = h * p.group + ht * HPC;
             mbar_expect_tx(b_q, (uint32_t)(2 * HPC * T * 128));
@@ -328,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, h, tib, phys, is_k ? 0 : 1);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMMA) {
         // ---------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t id_s = instr_desc(kM, kN, BF16, false);
@@ -370,15 +395,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_pv(n_tiles - 1);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------ softmax (rows)
-        const int r = tid;  // 0..127, this thread's TMEM lane
+    } else if (warp < 8) {
+        // ------------------------------------------- softmax (half rows)
+        // Warps w and w + 4 share the TMEM lanes of row quarter w % 4 (a
+        // warp may only touch its quarter); warp w takes columns 0-63 of
+        // each row, warp w + 4 columns 64-127. They swap their partial row
+        // maxima (and at the end their partial row sums) through TMEM
+        // columns kTmemX.., with a per-quarter mbarrier in between, so both
+        // take identical rescaling decisions.
+        const int quarter = warp & 3, hf = warp >> 2;
+        const int r = quarter * 32 + lane;  // this thread's TMEM lane (row)
         const int g = r / T, t = r - g * T;
         const bool valid = g < HPC && t0 + t < q_len;
         const int pos = valid ? L - q_len + t0 + t : -1;  // last token this row sees
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t b_x = smem_addr(&bars.xch[quarter]);
+        const int c0 = hf * 64;  // first column of this warp's half
         float m_run = -INFINITY, l_run = 0.f;
         bool alive = true;
+        // Publish v in exchange column `col`, meet the partner warp (phase
+        // `ph`), return the partner's value from column `col ^ 1`.
+        auto swap = [&](uint32_t col, float v, uint32_t ph, float &other) {
+            tc_st1(tmem + lane_off + col, v);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(b_x);
+            if (!__all_sync(kFull, wait_or_fail(b_x, ph)))
+                return false;
+            tc_fence_after();
+            other = tc_ld1(tmem + lane_off + (col ^ 1u));
+            return true;
+        };
         for (int j = 0; j < n_tiles; ++j) {
             const int b = j & 1;
             if (!__all_sync(kFull, wait_or_fail(b_s(b), (j >> 1) & 1))) {
@@ -386,53 +433,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            float sv[kN];
+            float sv[64];
             {
-                const uint32_t tS = tmem + lane_off + (b ? kTmemS1 : kTmemS0);
+                const uint32_t tS = tmem + lane_off + (b ? kTmemS1 : kTmemS0) + c0;
                 uint32_t *rawv = reinterpret_cast<uint32_t *>(sv);
-#pragma unroll
-                for (int c = 0; c < kN / 32; ++c)
-                    tc_ld32_async(tS + c * 32, rawv + c * 32);
+                tc_ld32_async(tS, rawv);
+                tc_ld32_async(tS + 32, rawv + 32);
                 tc_wait_ld();
             }
-            const int kbase = j * kN;
-            // Scale (and mask) the row; its maximum over 8 independent chains.
+            const int kbase = j * kN + c0;
+            // Scale (and mask) the half row; its maximum over 8 chains.
             float m8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 m8[i] = -INFINITY;
-            if (kbase + kN - 1 <= pos) {
+            if (kbase + 63 <= pos) {
 #pragma unroll
-                for (int c = 0; c < kN; ++c) {
+                for (int c = 0; c < 64; ++c) {
                     sv[c] *= p.scale_log2;
                     m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < kN; ++c) {
+                for (int c = 0; c < 64; ++c) {
                     sv[c] = (kbase + c <= pos) ? sv[c] * p.scale_log2 : -INFINITY;
                     m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
                 }
             }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+            const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            float mo;
+            if (!swap(kTmemX + 2 * b + hf, mh, b, mo)) {
+                alive = false;
+                break;
+            }
+            const float mx = fmaxf(mh, mo);
             // The row's reference maximum moves only when a score exceeds it
             // by more than kRescaleLog2 (P then stays <= 2^kRescaleLog2, which
             // the element type holds with full relative precision); O and l
-            // are rescaled only then.
+            // are rescaled only then. Both halves see the same mx.
             const bool grow = mx > m_run + kRescaleLog2;
             const float m_new = grow ? mx : m_run;
             const float alpha = grow ? ex2(m_run - m_new) : 1.f;
             const float ref = m_new == -INFINITY ? 0.f : m_new;
             // P, rounded to the element type, packed in registers; the row
             // sum adds the same rounded values.
-            uint32_t pw[kN / 2];
+            uint32_t pw[32];
             float l8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 l8[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kN / 2; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 pw[c] = pack2<BF16>(ex2(sv[2 * c] - ref), ex2(sv[2 * c + 1] - ref));
                 const float2 f = unpack2<BF16>(pw[c]);
                 l8[c & 7] += f.x + f.y;
@@ -446,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
-                const uint32_t tO = tmem + lane_off + kTmemO;
+                const uint32_t tO = tmem + lane_off + kTmemO + c0;
                 float o[32];
 #pragma unroll
-                for (int c = 0; c < kD / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     tc_ld32(tO + c * 32, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -458,42 +510,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            // P into its K-major 128-byte swizzled rows.
+            // P into its K-major 128-byte swizzled rows: this half is the
+            // 64-column chunk hf.
 #pragma unroll
-            for (int u = 0; u < kN / 8; ++u) {
-                const int c2 = u >> 3, uu = u & 7;
-                sts128(sP + c2 * kChunkBytes + r * 128 + ((uu ^ (r & 7)) << 4), pw[4 * u], pw[4 * u + 1],
+            for (int u = 0; u < 8; ++u)
+                sts128(sP + hf * kChunkBytes + r * 128 + ((u ^ (r & 7)) << 4), pw[4 * u], pw[4 * u + 1],
                        pw[4 * u + 2], pw[4 * u + 3]);
-            }
             l_run = l_run * alpha + ls;
             m_run = m_new;
             // The last tile's V rows past the sequence end hold whatever the
-            // pool's padding slots hold: zero them (P is 0 there) once V lands.
-            if (kbase + kN > L) {
+            // pool's padding slots hold: zero them (P is 0 there) once V lands;
+            // each half-row warp clears its 64-dim chunk of the row.
+            if (j * kN + kN > L) {
                 const int vs = j % kVStages;
                 if (!__all_sync(kFull, wait_or_fail(b_vf(vs), (j / kVStages) & 1))) {
                     alive = false;
                     break;
                 }
-                if (kbase + r >= L)
-                    for (int c = 0; c < 2; ++c)
-                        for (int u = 0; u < 8; ++u)
-                            sts128(sV(vs) + c * kChunkBytes + r * 128 + u * 16, 0u, 0u, 0u, 0u);
+                if (j * kN + r >= L)
+                    for (int u = 0; u < 8; ++u)
+                        sts128(sV(vs) + hf * kChunkBytes + r * 128 + u * 16, 0u, 0u, 0u, 0u);
             }
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(b_p);
         }
-        // Epilogue: O / l for the valid rows.
-        if (alive && __all_sync(kFull, wait_or_fail(b_pv, (n_tiles - 1) & 1))) {
+        // Epilogue: the two partial row sums meet, then each warp stores its
+        // 64 output columns, O / l, for the valid rows.
+        float lo = 0.f;
+        if (alive && swap(kTmemX + 4 + hf, l_run, (uint32_t)(n_tiles & 1), lo) &&
+            __all_sync(kFull, wait_or_fail(b_pv, (n_tiles - 1) & 1))) {
             tc_fence_after();
-            const uint32_t tO = tmem + lane_off + kTmemO;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float l_tot = l_run + lo;
+            const uint32_t tO = tmem + lane_off + kTmemO + c0;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             uint16_t *out = static_cast<uint16_t *>(p.out) +
-                            ((long long)(q0 + t0 + t) * p.num_q_heads + h * p.group + ht * HPC + g) * kD;
+                            ((long long)(q0 + t0 + t) * p.num_q_heads + h * p.group + ht * HPC + g) * kD + c0;
             float o[32];
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 tc_ld32(tO + c * 32, o);
                 if (valid) {
 #pragma unroll
@@ -513,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5)
+    if (warp == kWarpMMA)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
 }
