@@ -9,7 +9,9 @@
 // attends to tokens 0..p through the block table, with the online softmax
 // of §4.6.
 //
-// How it is computed (one CTA = 128 query rows of one (sequence, kv head)):
+// How it is computed (a work unit = 128 query rows of one (sequence, kv
+// head); one persistent CTA per SM walks its share of the units, heaviest
+// first, with its TMA rings and barrier phases running on across units):
 //  * Rows are (query head of the kv head's group, query token) pairs, so the
 //    heads that share a kv head share every K/V tile. A TMEM lane per row.
 //  * Warp 8 loads Q once and the K tiles, warp 10 the V tiles, by TMA
@@ -39,6 +41,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/pa.h"
@@ -149,18 +152,45 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float *v)
         : "memory");
 }
 
-// One fp32 column of this thread's TMEM lane (warp-collective).
-__device__ __forceinline__ void tc_st1(uint32_t taddr, float v)
+// O += A B with A read from TMEM (32-bit columns holding two 16-bit
+// elements, the lower-indexed one in the low half) and B from shared memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate)
 {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "f"(v) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
-__device__ __forceinline__ float tc_ld1(uint32_t taddr)
+// acc + the two 16-bit elements of a packed pair (low half first), each added
+// exactly as fp32 then rounded: mixed-precision adds, no unpacking.
+template <bool BF16>
+__device__ __forceinline__ float add_pair(float acc, uint32_t w)
 {
-    uint32_t r;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    return __uint_as_float(r);
+    const unsigned short lo = (unsigned short)(w & 0xFFFFu), hi = (unsigned short)(w >> 16);
+    if constexpr (BF16) {
+        asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(acc) : "h"(lo));
+        asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(acc) : "h"(hi));
+    } else {
+        asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(lo));
+        asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(hi));
+    }
+    return acc;
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane from raw words.
+__device__ __forceinline__ void tc_st32u(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
@@ -172,25 +202,24 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 // ----------------------------------------------------------------- layout
 
 constexpr int kD = 128;                    // head size (the one built)
-constexpr int kM = 128;                    // query rows per CTA (TMEM lanes)
+constexpr int kM = 128;                    // query rows per tile (TMEM lanes)
 constexpr int kN = 128;                    // cached tokens per K/V tile
 constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
 constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit operand: 32 KB
 constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size is a multiple)
-constexpr int kThreads = 352;              // warps 0-7 softmax, 8 Q/K TMA, 9 MMA, 10 V TMA
-constexpr int kSoftmaxThreads = 256;       // two warps per row quarter, one per 64-column half
-constexpr int kWarpQK = 8, kWarpMMA = 9, kWarpV = 10;
-constexpr int kKStages = 3;                // K ring (freed when S = Q K^T is done)
-constexpr int kVStages = 2;                // V ring (freed when O += P V is done)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kTileBytes;
+constexpr int kThreads = 384;              // warps 0-3 softmax A, 4-7 softmax B, 8 K, 9 MMA, 10 V, 11 Q
+constexpr int kWarpK = 8, kWarpMMA = 9, kWarpV = 10, kWarpQ = 11;
+constexpr int kKStages = 3;                // K ring (freed when both tiles' S = Q K^T are done)
+constexpr int kVStages = 2;                // V ring (freed when both tiles' O += P V are done)
+constexpr int kOffQ = 0;                   // Q of tile A, then of tile B
+constexpr int kOffK = 2 * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffP = kOffV + kVStages * kTileBytes;
-constexpr int kSmemBytes = kOffP + kTileBytes + 1024;  // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 512;        // S (two buffers) and O, 128 columns each, + exchange
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
-constexpr uint32_t kTmemX = 384;           // row maxima (2 parities x 2 halves) and row sums (2 halves)
+constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 512;        // S/P of tiles A and B, then O of A and B, 128 columns each
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
+constexpr int kRegsLaunch = 168;           // registers per thread at launch (384 threads, 1 CTA/SM)
+constexpr int kRegsIO = 120, kRegsSoftmax = 192;
+static_assert(128 * kRegsIO + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 struct PrefillParams {
     void *out;
@@ -201,21 +230,70 @@ struct PrefillParams {
     int num_seqs;
     int num_q_heads;
     int group;          // num_q_heads / num_kv_heads
-    int heads_per_cta;  // query heads of one kv head that share a CTA (<= 16)
+    int heads_per_cta;  // query heads of one kv head that share a tile (<= 16)
     int head_tiles;     // group / heads_per_cta
-    int rows_per_head;  // query tokens per CTA (multiple of 8)
-    int q_tiles;        // ceil(max_seqlen_q / rows_per_head)
+    int rows_per_head;  // query tokens per tile (multiple of 8)
+    int q_pairs;        // ceil(ceil(max_seqlen_q / rows_per_head) / 2)
     int num_blocks;
     int block_size;
     int total_q;
     int max_len;        // max_blocks_per_seq * block_size
+    int num_kv_heads;
+    int num_units;      // q_pairs * num_seqs * num_kv_heads * head_tiles
     float scale_log2;   // scale * log2(e)
 };
 
+// One work unit: the two adjacent query tiles A = 2 qp and B = 2 qp + 1 of
+// head tile ht of kv head h of sequence s. They share every K/V tile (B's
+// queries come later, so B sees at least as many tiles as A). Units are
+// numbered heaviest first: u = ((qr * num_seqs + s) * num_kv_heads + h) *
+// head_tiles + ht with qp = q_pairs - 1 - qr.
+struct Unit {
+    int s, h, ht, q0, q_len, L;
+    int t0[2];       // first query token of tile A / B
+    int n[2];        // K/V tiles tile A / B sees (0: the tile has no queries)
+};
+
+// Decode unit u; false when tile A has no query rows or the sequence has bad
+// offsets or lengths (flagged once, by the unit of the sequence's first
+// heads and last query pair, when `flag`).
+__device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, bool flag)
+{
+    const int ht = u % p.head_tiles;
+    int r = u / p.head_tiles;
+    const int h = r % p.num_kv_heads;
+    r /= p.num_kv_heads;
+    const int s = r % p.num_seqs;
+    const int qr = r / p.num_seqs;
+    const int q0 = p.cu_q[s], q_len = p.cu_q[s + 1] - q0, L = p.seq_lens[s];
+    if (q_len < 0 || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len) {
+        if (flag && h == 0 && ht == 0 && qr == 0)
+            prefill_raise(PA_DEVERR_SEQ_LEN);
+        return false;
+    }
+    const int T = p.rows_per_head;
+    const int ta = 2 * (p.q_pairs - 1 - qr) * T;
+    if (ta >= q_len)
+        return false;
+    w.s = s;
+    w.h = h;
+    w.ht = ht;
+    w.q0 = q0;
+    w.q_len = q_len;
+    w.L = L;
+    for (int x = 0; x < 2; ++x) {
+        w.t0[x] = ta + x * T;
+        const int t_end = min(q_len, w.t0[x] + T);
+        w.n[x] = w.t0[x] < q_len ? (L - q_len + t_end + kN - 1) / kN : 0;  // tiles its last query sees
+    }
+    return true;
+}
+
 struct PrefillBars {
-    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], p_full, pv_done;
-    uint64_t xch[4];  // per row quarter: the two half-row warps exchanged their values
+    uint64_t q_full, q_empty, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    // Per query tile x: s_full[x] its S is in TMEM, p_full[x] its P is,
+    // pv_done[x] its O += P V is done (one phase per K/V tile).
+    uint64_t s_full[2], p_full[2], pv_done[2];
     uint32_t tmem_base;
     int fail;
 };
@@ -229,42 +307,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ PrefillBars bars;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = blockIdx.z, h = blockIdx.y;
-    const int ht = blockIdx.x % p.head_tiles;
-    const int qt = (p.q_tiles - 1) - blockIdx.x / p.head_tiles;  // heaviest tiles start first
     const int T = p.rows_per_head, HPC = p.heads_per_cta;
-
-    // The unit (uniform across the CTA); bad offsets or lengths are flagged
-    // by the first CTA of the sequence and skipped.
-    const int q0 = p.cu_q[s];
-    const int q_len = p.cu_q[s + 1] - q0;
-    const int L = p.seq_lens[s];
-    if (q_len < 0 || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len) {
-        if (tid == 0 && blockIdx.x == 0 && h == 0)
-            prefill_raise(PA_DEVERR_SEQ_LEN);
-        return;
-    }
-    const int t0 = qt * T;
-    if (t0 >= q_len)
-        return;
-    const int t_end = min(q_len, t0 + T);
-    const int n_tiles = (L - q_len + t_end + kN - 1) / kN;  // tiles the tile's last query sees
+    // Persistent: this CTA takes units blockIdx.x, + gridDim.x, ... in order;
+    // every role walks the same list and skips the same empty units, and the
+    // rings and barrier phases run on across unit boundaries.
+    const int u_first = blockIdx.x, u_step = gridDim.x;
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sQ = base + kOffQ, sP = base + kOffP;
+    auto sQ = [&](int x) { return base + kOffQ + x * kTileBytes; };
     auto sK = [&](int st) { return base + kOffK + st * kTileBytes; };
     auto sV = [&](int st) { return base + kOffV + st * kTileBytes; };
-    const uint32_t b_q = smem_addr(&bars.q_full), b_p = smem_addr(&bars.p_full),
-                   b_pv = smem_addr(&bars.pv_done);
+    const uint32_t b_q = smem_addr(&bars.q_full), b_qe = smem_addr(&bars.q_empty);
     auto b_kf = [&](int st) { return smem_addr(&bars.k_full[st]); };
     auto b_ke = [&](int st) { return smem_addr(&bars.k_empty[st]); };
     auto b_vf = [&](int st) { return smem_addr(&bars.v_full[st]); };
     auto b_ve = [&](int st) { return smem_addr(&bars.v_empty[st]); };
-    auto b_s = [&](int b) { return smem_addr(&bars.s_full[b]); };
+    auto b_s = [&](int x) { return smem_addr(&bars.s_full[x]); };
+    auto b_p = [&](int x) { return smem_addr(&bars.p_full[x]); };
+    auto b_pv = [&](int x) { return smem_addr(&bars.pv_done[x]); };
 
     if (tid == 0) {
         mbar_init(b_q, 1);
+        mbar_init(b_qe, 1);
         for (int st = 0; st < kKStages; ++st) {
             mbar_init(b_kf(st), 1);
             mbar_init(b_ke(st), 1);
@@ -273,12 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_vf(st), 1);
             mbar_init(b_ve(st), 1);
         }
-        mbar_init(b_s(0), 1);
-        mbar_init(b_s(1), 1);
-        mbar_init(b_p, kSoftmaxThreads);
-        mbar_init(b_pv, 1);
-        for (int i = 0; i < 4; ++i)
-            mbar_init(smem_addr(&bars.xch[i]), 64);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b_s(x), 1);
+            mbar_init(b_p(x), 128);
+            mbar_init(b_pv(x), 1);
+        }
         bars.fail = 0;
         fence_barrier_init();
     }
@@ -293,6 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
+    auto tS = [&](int x) { return tmem + 128u * x; };        // S of tile x; its P in the first 64 columns
+    auto tO = [&](int x) { return tmem + 256u + 128u * x; };  // O of tile x
 
     // Give up on a wait that runs out (recorded once per CTA); every role then
     // drains to the teardown.
@@ -304,252 +370,345 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
     };
 
-    if (warp == kWarpQK || warp == kWarpV) {
-        // ---------------------------------------------------------- TMA
-        // Warp 4 produces Q and the K tiles, warp 6 the V tiles, each at its
-        // own pace (separate warps, so that one producer's wait never holds
-        // up the other); lane i < 8 moves the 16-token box i of each tile.
-        // The block-table entry of the next tile is loaded while the current
-        // one waits for its stage.
-        const int32_t *table = p.block_tables + (long long)s * p.max_blocks_per_seq;
-        const bool is_k = warp == kWarpQK;
-        if (is_k && lane == 0) {
-            const int head0 = h * p.group + ht * HPC;
-            mbar_expect_tx(b_q, (uint32_t)(2 * HPC * T * 128));
-            for (int c = 0; c < 2; ++c)
-                for (int g = 0; g < HPC; ++g)
-                    tma_load_3d(sQ + c * kChunkBytes + g * T * 128, &q_map, b_q, c * 64, head0 + g, q0 + t0);
+    // Register split, per warpgroup (each of its four warps runs the same
+    // instruction): the K/V/MMA/Q group drops to kRegsIO, the two softmax
+    // groups rise to kRegsSoftmax; the sum stays within the launch's
+    // kThreads x kRegsLaunch.
+    if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIO));
+    if (warp == kWarpQ) {
+        // ------------------------------------------------------------ Q
+        // A unit's two query tiles go into the Q buffers once the previous
+        // unit's last S = Q K^T has completed.
+        if (lane == 0) {
+            int ui = 0;
+            for (int u = u_first; u < p.num_units; u += u_step) {
+                Unit w;
+                if (!unit_of(p, u, w, false))
+                    continue;
+                if (ui > 0 && !wait_or_fail(b_qe, (ui - 1) & 1))
+                    break;
+                const int head0 = w.h * p.group + w.ht * HPC;
+                const int tiles = w.n[1] > 0 ? 2 : 1;
+                mbar_expect_tx(b_q, (uint32_t)(tiles * 2 * HPC * T * 128));
+                for (int x = 0; x < tiles; ++x)
+                    for (int c = 0; c < 2; ++c)
+                        for (int g = 0; g < HPC; ++g)
+                            tma_load_3d(sQ(x) + c * kChunkBytes + g * T * 128, &q_map, b_q, c * 64, head0 + g,
+                                        w.q0 + w.t0[x]);
+                ++ui;
+            }
         }
+    } else if (warp == kWarpK || warp == kWarpV) {
+        // ---------------------------------------------------------- K, V
+        // Warp 8 produces the K tiles, warp 10 the V tiles, each at its own
+        // pace through its ring; lane i < 8 moves the 16-token box i of each
+        // tile. The block-table entry of the next tile is loaded while the
+        // current one waits for its stage.
+        const bool is_k = warp == kWarpK;
         if (lane < 8) {
             const int box = lane, leader = 0;
             const unsigned group_mask = 0x000000FFu;
             const int stages = is_k ? kKStages : kVStages;
-            auto lookup = [&](int j) {
-                const int kt = j * kN + kBoxTokens * box;
-                return (j < n_tiles && kt < L) ? __ldg(table + kt / p.block_size) : -1;
-            };
-            int next = lookup(0);
-            for (int j = 0; j < n_tiles; ++j) {
-                int phys = next;
-                next = lookup(j + 1);
-                const int st = j % stages;
-                if (j >= stages &&
-                    !wait_or_fail(is_k ? b_ke(st) : b_ve(st), ((j - stages) / stages) & 1))
-                    break;
-                const int kt = j * kN + kBoxTokens * box;
-                const int tib = kt % p.block_size;
-                if (phys >= p.num_blocks || (phys < 0 && kt < L)) {
-                    prefill_raise(PA_DEVERR_BLOCK_ID);
-                    phys = p.num_blocks;
+            int gc = 0;  // K (or V) tiles produced by this CTA so far
+            bool go = true;
+            for (int u = u_first; go && u < p.num_units; u += u_step) {
+                Unit w;
+                if (!unit_of(p, u, w, false))
+                    continue;
+                const int n = max(w.n[0], w.n[1]);
+                const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
+                auto lookup = [&](int j) {
+                    const int kt = j * kN + kBoxTokens * box;
+                    return (j < n && kt < w.L) ? __ldg(table + kt / p.block_size) : -1;
+                };
+                int next = lookup(0);
+                for (int j = 0; j < n; ++j, ++gc) {
+                    int phys = next;
+                    next = lookup(j + 1);
+                    const int st = gc % stages;
+                    if (gc >= stages &&
+                        !wait_or_fail(is_k ? b_ke(st) : b_ve(st), ((gc - stages) / stages) & 1)) {
+                        go = false;
+                        break;
+                    }
+                    const int kt = j * kN + kBoxTokens * box;
+                    const int tib = kt % p.block_size;
+                    if (phys >= p.num_blocks || (phys < 0 && kt < w.L)) {
+                        prefill_raise(PA_DEVERR_BLOCK_ID);
+                        phys = p.num_blocks;
+                    }
+                    if (phys < 0)
+                        phys = p.num_blocks;  // past the sequence end: outside the map, zeros
+                    const uint32_t full = is_k ? b_kf(st) : b_vf(st);
+                    if (lane == leader)
+                        mbar_expect_tx(full, kTileBytes);
+                    __syncwarp(group_mask);
+                    const uint32_t dst = (is_k ? sK(st) : sV(st)) + box * (kBoxTokens * 128);
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, w.h, tib, phys, is_k ? 0 : 1);
                 }
-                if (phys < 0)
-                    phys = p.num_blocks;  // past the sequence end: outside the map, zeros
-                const uint32_t full = is_k ? b_kf(st) : b_vf(st);
-                if (lane == leader)
-                    mbar_expect_tx(full, kTileBytes);
-                __syncwarp(group_mask);
-                const uint32_t dst = (is_k ? sK(st) : sV(st)) + box * (kBoxTokens * 128);
-                for (int c = 0; c < 2; ++c)
-                    tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, h, tib, phys, is_k ? 0 : 1);
             }
         }
     } else if (warp == kWarpMMA) {
         // ---------------------------------------------------------- MMA
+        // Per K/V tile j: S_A(0), S_B(0) up front, then for each tile x in
+        // turn O_x += P_x V_j followed by S_x(j + 1) = Q_x K_{j+1}^T, so the
+        // scores of one tile are computed while the other tile's softmax
+        // runs. S_x(j + 1) overwrites P_x(j) in TMEM: MMAs complete in issue
+        // order, so the P V that reads it is done first.
         if (lane == 0) {
             const uint32_t id_s = instr_desc(kM, kN, BF16, false);
             const uint32_t id_o = instr_desc(kM, kD, BF16, true);
-            auto issue_pv = [&](int jj) {
-                const int vs = jj % kVStages;
-                if (!wait_or_fail(b_p, jj & 1) || !wait_or_fail(b_vf(vs), (jj / kVStages) & 1))
-                    return false;
-                tc_fence_after();
-                // O += P V: A = P (K-major over tokens), B = V (MN-major:
-                // 64-dim chunks 16 KB apart, 8-token groups 1 KB apart).
-                for (int k = 0; k < kN / 16; ++k)
-                    tc_mma(tmem + kTmemO, smem_desc(sP + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
-                           smem_desc(sV(vs) + k * 2048, kChunkBytes, 1024), id_o,
-                           (jj > 0 || k > 0) ? 1u : 0u);
-                tc_commit(b_pv);
-                tc_commit(b_ve(vs));
-                return true;
-            };
-            bool go = wait_or_fail(b_q, 0);
-            for (int j = 0; go && j < n_tiles; ++j) {
-                const int ks = j % kKStages;
-                if (!wait_or_fail(b_kf(ks), (j / kKStages) & 1))
-                    break;
-                tc_fence_after();
-                // S = Q K^T over the head dimension, 16 per MMA.
-                const uint32_t tS = tmem + ((j & 1) ? kTmemS1 : kTmemS0);
+            auto issue_s = [&](int x, int ks) {
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-                    tc_mma(tS, smem_desc(sQ + off, 16, 1024), smem_desc(sK(ks) + off, 16, 1024), id_s,
+                    tc_mma(tS(x), smem_desc(sQ(x) + off, 16, 1024), smem_desc(sK(ks) + off, 16, 1024), id_s,
                            k > 0 ? 1u : 0u);
                 }
-                tc_commit(b_s(j & 1));
-                tc_commit(b_ke(ks));
-                if (j > 0)
-                    go = issue_pv(j - 1);
+                tc_commit(b_s(x));
+            };
+            int kc = 0, vc = 0, ui = 0;  // K tiles, V tiles and units consumed so far
+            int gx[2] = {0, 0};          // P V of tile x issued so far
+            bool go = true;
+            for (int u = u_first; go && u < p.num_units; u += u_step) {
+                Unit w;
+                if (!unit_of(p, u, w, false))
+                    continue;
+                const int n = max(w.n[0], w.n[1]);
+                if (!wait_or_fail(b_q, ui & 1))
+                    break;
+                ++ui;
+                tc_fence_after();
+                {
+                    const int ks = kc % kKStages;
+                    if (!wait_or_fail(b_kf(ks), (kc / kKStages) & 1))
+                        break;
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x)
+                        if (w.n[x] > 0)
+                            issue_s(x, ks);
+                    tc_commit(b_ke(ks));
+                    ++kc;
+                    if (n == 1)
+                        tc_commit(b_qe);  // Q free once the unit's last scores are done
+                }
+                for (int j = 0; go && j < n; ++j) {
+                    const int vs = vc % kVStages;
+                    if (!wait_or_fail(b_vf(vs), (vc / kVStages) & 1)) {
+                        go = false;
+                        break;
+                    }
+                    int ks_next = -1;
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= w.n[x])
+                            continue;
+                        if (!wait_or_fail(b_p(x), gx[x] & 1)) {
+                            go = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // O_x += P_x V: A = P from TMEM (8 columns per 16
+                        // tokens), B = V (MN-major: 64-dim chunks 16 KB apart,
+                        // 8-token groups 1 KB apart).
+                        for (int k = 0; k < kN / 16; ++k)
+                            tc_mma_ts(tO(x), tS(x) + k * 8, smem_desc(sV(vs) + k * 2048, kChunkBytes, 1024), id_o,
+                                      (j > 0 || k > 0) ? 1u : 0u);
+                        tc_commit(b_pv(x));
+                        ++gx[x];
+                        if (j + 1 < w.n[x]) {
+                            if (ks_next < 0) {
+                                ks_next = kc % kKStages;
+                                if (!wait_or_fail(b_kf(ks_next), (kc / kKStages) & 1)) {
+                                    go = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            issue_s(x, ks_next);
+                        }
+                    }
+                    if (!go)
+                        break;
+                    if (ks_next >= 0) {
+                        tc_commit(b_ke(ks_next));
+                        ++kc;
+                        if (j + 2 == n)
+                            tc_commit(b_qe);
+                    }
+                    tc_commit(b_ve(vs));
+                    ++vc;
+                }
             }
-            if (go)
-                issue_pv(n_tiles - 1);
         }
         __syncwarp();
-    } else if (warp < 8) {
-        // ------------------------------------------- softmax (half rows)
-        // Warps w and w + 4 share the TMEM lanes of row quarter w % 4 (a
-        // warp may only touch its quarter); warp w takes columns 0-63 of
-        // each row, warp w + 4 columns 64-127. They swap their partial row
-        // maxima (and at the end their partial row sums) through TMEM
-        // columns kTmemX.., with a per-quarter mbarrier in between, so both
-        // take identical rescaling decisions.
-        const int quarter = warp & 3, hf = warp >> 2;
+    }
+    } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    {
+        // ---------------------------------------------------- softmax rows
+        // Warpgroup x (warps 4x .. 4x + 3) owns query tile x; each thread one
+        // row (TMEM lane). Per K/V tile: read S, mask it causally, run the
+        // fp32 online softmax in base 2 (the reference maximum moves only
+        // when a score exceeds it by 2^8, so O in TMEM is rarely rescaled),
+        // and write P, rounded to the element type, over the row's first 64
+        // S columns for the P V MMA. At the end of the unit, divide O by the
+        // row sum and store.
+        const int x = warp >> 2, quarter = warp & 3;
         const int r = quarter * 32 + lane;  // this thread's TMEM lane (row)
         const int g = r / T, t = r - g * T;
-        const bool valid = g < HPC && t0 + t < q_len;
-        const int pos = valid ? L - q_len + t0 + t : -1;  // last token this row sees
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t b_x = smem_addr(&bars.xch[quarter]);
-        const int c0 = hf * 64;  // first column of this warp's half
-        float m_run = -INFINITY, l_run = 0.f;
+        const float sc = p.scale_log2;
+        const bool sc_pos = sc >= 0.f;
+        int gx = 0, vbase = 0;  // tiles of this query tile, and V tiles of the CTA, so far
         bool alive = true;
-        // Publish v in exchange column `col`, meet the partner warp (phase
-        // `ph`), return the partner's value from column `col ^ 1`.
-        auto swap = [&](uint32_t col, float v, uint32_t ph, float &other) {
-            tc_st1(tmem + lane_off + col, v);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            tc_fence_before();
-            mbar_arrive(b_x);
-            if (!__all_sync(kFull, wait_or_fail(b_x, ph)))
-                return false;
-            tc_fence_after();
-            other = tc_ld1(tmem + lane_off + (col ^ 1u));
-            return true;
-        };
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
-            if (!__all_sync(kFull, wait_or_fail(b_s(b), (j >> 1) & 1))) {
-                alive = false;
-                break;
-            }
-            tc_fence_after();
-            float sv[64];
-            {
-                const uint32_t tS = tmem + lane_off + (b ? kTmemS1 : kTmemS0) + c0;
-                uint32_t *rawv = reinterpret_cast<uint32_t *>(sv);
-                tc_ld32_async(tS, rawv);
-                tc_ld32_async(tS + 32, rawv + 32);
-                tc_wait_ld();
-            }
-            const int kbase = j * kN + c0;
-            // Scale (and mask) the half row; its maximum over 8 chains.
-            float m8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                m8[i] = -INFINITY;
-            if (kbase + 63 <= pos) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    sv[c] *= p.scale_log2;
-                    m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    sv[c] = (kbase + c <= pos) ? sv[c] * p.scale_log2 : -INFINITY;
-                    m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
-                }
-            }
-            const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            float mo;
-            if (!swap(kTmemX + 2 * b + hf, mh, b, mo)) {
-                alive = false;
-                break;
-            }
-            const float mx = fmaxf(mh, mo);
-            // The row's reference maximum moves only when a score exceeds it
-            // by more than kRescaleLog2 (P then stays <= 2^kRescaleLog2, which
-            // the element type holds with full relative precision); O and l
-            // are rescaled only then. Both halves see the same mx.
-            const bool grow = mx > m_run + kRescaleLog2;
-            const float m_new = grow ? mx : m_run;
-            const float alpha = grow ? ex2(m_run - m_new) : 1.f;
-            const float ref = m_new == -INFINITY ? 0.f : m_new;
-            // P, rounded to the element type, packed in registers; the row
-            // sum adds the same rounded values.
-            uint32_t pw[32];
-            float l8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                l8[i] = 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                pw[c] = pack2<BF16>(ex2(sv[2 * c] - ref), ex2(sv[2 * c + 1] - ref));
-                const float2 f = unpack2<BF16>(pw[c]);
-                l8[c & 7] += f.x + f.y;
-            }
-            const float ls = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-            // The previous tile's P V must be done before P is overwritten
-            // and before O is rescaled.
-            if (j > 0 && !__all_sync(kFull, wait_or_fail(b_pv, (j - 1) & 1))) {
-                alive = false;
-                break;
-            }
-            tc_fence_after();
-            if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
-                const uint32_t tO = tmem + lane_off + kTmemO + c0;
-                float o[32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tc_ld32(tO + c * 32, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] *= alpha;
-                    tc_st32(tO + c * 32, o);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            }
-            // P into its K-major 128-byte swizzled rows: this half is the
-            // 64-column chunk hf.
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                sts128(sP + hf * kChunkBytes + r * 128 + ((u ^ (r & 7)) << 4), pw[4 * u], pw[4 * u + 1],
-                       pw[4 * u + 2], pw[4 * u + 3]);
-            l_run = l_run * alpha + ls;
-            m_run = m_new;
-            // The last tile's V rows past the sequence end hold whatever the
-            // pool's padding slots hold: zero them (P is 0 there) once V lands;
-            // each half-row warp clears its 64-dim chunk of the row.
-            if (j * kN + kN > L) {
-                const int vs = j % kVStages;
-                if (!__all_sync(kFull, wait_or_fail(b_vf(vs), (j / kVStages) & 1))) {
+        for (int u = u_first; alive && u < p.num_units; u += u_step) {
+            Unit w;
+            if (!unit_of(p, u, w, tid == 0))
+                continue;
+            const int n = max(w.n[0], w.n[1]), nx = w.n[x];
+            // The K/V tile holding the sequence end (padding slots past it)
+            // is zeroed in V by the first tile that reads it.
+            const int jp = (w.L % kN) ? w.L / kN : -1;
+            const bool zeroes = jp >= 0 && jp < nx && (x == 0 || jp >= w.n[0]);
+            const bool valid = g < HPC && w.t0[x] + t < w.q_len;
+            const int pos = valid ? w.L - w.q_len + w.t0[x] + t : -1;  // last token this row sees
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nx; ++j, ++gx) {
+                if (!__all_sync(kFull, wait_or_fail(b_s(x), gx & 1))) {
                     alive = false;
                     break;
                 }
-                if (j * kN + r >= L)
-                    for (int u = 0; u < 8; ++u)
-                        sts128(sV(vs) + hf * kChunkBytes + r * 128 + u * 16, 0u, 0u, 0u, 0u);
+                tc_fence_after();
+                float sv[kN];
+                {
+                    const uint32_t ta = tS(x) + lane_off;
+                    uint32_t *rv = reinterpret_cast<uint32_t *>(sv);
+#pragma unroll
+                    for (int c = 0; c < kN / 32; ++c)
+                        tc_ld32_async(ta + c * 32, rv + c * 32);
+                    tc_wait_ld();
+                }
+                const int kb = j * kN;
+                const bool full = kb + kN - 1 <= pos;  // every token of the tile visible
+                // Row maximum in base 2: scale x the largest visible raw score
+                // (the smallest for a negative scale; rounding is monotone, so
+                // this is the largest scaled score exactly); 8 chains.
+                float e8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    e8[i] = sc_pos ? -INFINITY : INFINITY;
+                if (full) {
+                    if (sc_pos) {
+#pragma unroll
+                        for (int c = 0; c < kN; ++c)
+                            e8[c & 7] = fmaxf(e8[c & 7], sv[c]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kN; ++c)
+                            e8[c & 7] = fminf(e8[c & 7], sv[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kN; ++c)
+                        if (kb + c <= pos)
+                            e8[c & 7] = sc_pos ? fmaxf(e8[c & 7], sv[c]) : fminf(e8[c & 7], sv[c]);
+                }
+                const float e = sc_pos ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])),
+                                               fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
+                                       : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])),
+                                               fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
+                const float mx = (e == INFINITY || e == -INFINITY) ? -INFINITY : e * sc;
+                // The reference maximum moves only when a score exceeds it by
+                // more than kRescaleLog2 (P then stays <= 2^kRescaleLog2, which
+                // the element type holds with full relative precision).
+                const bool grow = mx > m_run + kRescaleLog2;
+                const float m_new = grow ? mx : m_run;
+                const float alpha = grow ? ex2(m_run - m_new) : 1.f;
+                const float ref = m_new == -INFINITY ? 0.f : m_new;
+                // P = 2^(s scale - ref), rounded to the element type, packed in
+                // pairs (the lower-indexed token in the low half); the row sum
+                // adds the same rounded values.
+                uint32_t pw[kN / 2];
+                float l8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    l8[i] = 0.f;
+                if (full) {
+#pragma unroll
+                    for (int c = 0; c < kN / 2; ++c) {
+                        pw[c] = pack2<BF16>(ex2(fmaf(sv[2 * c], sc, -ref)), ex2(fmaf(sv[2 * c + 1], sc, -ref)));
+                        l8[c & 7] = add_pair<BF16>(l8[c & 7], pw[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kN / 2; ++c) {
+                        const float p0 = kb + 2 * c <= pos ? ex2(fmaf(sv[2 * c], sc, -ref)) : 0.f;
+                        const float p1 = kb + 2 * c + 1 <= pos ? ex2(fmaf(sv[2 * c + 1], sc, -ref)) : 0.f;
+                        pw[c] = pack2<BF16>(p0, p1);
+                        l8[c & 7] = add_pair<BF16>(l8[c & 7], pw[c]);
+                    }
+                }
+                const float ls = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+                // Rescale O when the reference moved. The previous tile's
+                // O += P V is done: it was issued before this tile's S, whose
+                // completion was awaited above.
+                if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+                    const uint32_t to = tO(x) + lane_off;
+                    float o[32];
+#pragma unroll
+                    for (int c = 0; c < kD / 32; ++c) {
+                        tc_ld32(to + c * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] *= alpha;
+                        tc_st32(to + c * 32, o);
+                    }
+                }
+                // P over the row's first 64 S columns (already read).
+                tc_st32u(tS(x) + lane_off, pw);
+                tc_st32u(tS(x) + lane_off + 32, pw + 32);
+                l_run = l_run * alpha + ls;
+                m_run = m_new;
+                // The V rows past the sequence end hold whatever the pool's
+                // padding slots hold: zero them (P is 0 there) once V lands.
+                if (zeroes && j == jp) {
+                    const int vt = vbase + j, vs = vt % kVStages;
+                    if (!__all_sync(kFull, wait_or_fail(b_vf(vs), (vt / kVStages) & 1))) {
+                        alive = false;
+                        break;
+                    }
+                    if (kb + r >= w.L)
+                        for (int c = 0; c < 2; ++c)
+                            for (int i = 0; i < 8; ++i)
+                                sts128(sV(vs) + c * kChunkBytes + r * 128 + i * 16, 0u, 0u, 0u, 0u);
+                    fence_proxy_async();
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                mbar_arrive(b_p(x));
             }
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(b_p);
-        }
-        // Epilogue: the two partial row sums meet, then each warp stores its
-        // 64 output columns, O / l, for the valid rows.
-        float lo = 0.f;
-        if (alive && swap(kTmemX + 4 + hf, l_run, (uint32_t)(n_tiles & 1), lo) &&
-            __all_sync(kFull, wait_or_fail(b_pv, (n_tiles - 1) & 1))) {
+            if (!alive)
+                break;
+            vbase += n;
+            if (nx == 0)
+                continue;
+            // Unit epilogue: O / l for the valid rows. Reading O here comes
+            // before this row's first P of the next unit, and so before the
+            // next unit's first P V overwrites O.
+            if (!__all_sync(kFull, wait_or_fail(b_pv(x), (gx - 1) & 1))) {
+                alive = false;
+                break;
+            }
             tc_fence_after();
-            const float l_tot = l_run + lo;
-            const uint32_t tO = tmem + lane_off + kTmemO + c0;
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             uint16_t *out = static_cast<uint16_t *>(p.out) +
-                            ((long long)(q0 + t0 + t) * p.num_q_heads + h * p.group + ht * HPC + g) * kD + c0;
+                            ((long long)(w.q0 + w.t0[x] + t) * p.num_q_heads + w.h * p.group + w.ht * HPC + g) * kD;
+            const uint32_t to = tO(x) + lane_off;
             float o[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tc_ld32(tO + c * 32, o);
+            for (int c = 0; c < kD / 32; ++c) {
+                tc_ld32(to + c * 32, o);
                 if (valid) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -563,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    }
     }
 
     tc_fence_before();
@@ -664,8 +824,6 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
                          block_size);
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
         return set_error(PA_ERR_INVALID_ARG, "pa_prefill: bad sizes");
-    if (num_seqs > 65535 || num_kv_heads > 65535)
-        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: num_seqs and num_kv_heads must be <= 65535");
     if ((long long)max_blocks_per_seq * block_size > (1LL << 30))
         return set_error(PA_ERR_INVALID_ARG, "pa_prefill: max_blocks_per_seq * block_size too large");
     if (!std::isfinite(scale))
@@ -693,14 +851,18 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
     prm.heads_per_cta = group < 16 ? group : 16;
     prm.head_tiles = group / prm.heads_per_cta;
     prm.rows_per_head = (kM / prm.heads_per_cta) & ~7;
-    prm.q_tiles = (max_seqlen_q + prm.rows_per_head - 1) / prm.rows_per_head;
+    const int q_tiles = (max_seqlen_q + prm.rows_per_head - 1) / prm.rows_per_head;
+    prm.q_pairs = (q_tiles + 1) / 2;
     prm.num_blocks = num_blocks;
     prm.block_size = block_size;
     prm.total_q = total_q;
     prm.max_len = max_blocks_per_seq * block_size;
     prm.scale_log2 = scale * 1.4426950408889634f;
-    if ((long long)prm.q_tiles * prm.head_tiles > 0x7fffffffLL)
+    prm.num_kv_heads = num_kv_heads;
+    const long long units = (long long)prm.q_pairs * num_seqs * num_kv_heads * prm.head_tiles;
+    if (units > 0x7fffffffLL)
         return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: too many query tiles");
+    prm.num_units = (int)units;
 
     CUtensorMap kv_map, q_map;
     int rc = encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads);
@@ -712,11 +874,13 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
 
     const void *fn = dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true>)
                                       : reinterpret_cast<const void *>(&paged_prefill_kernel<false>);
-    // Raise the kernel's shared-memory limit once per device (a call being
-    // captured into a CUDA graph then makes no attribute call).
+    // Raise the kernel's shared-memory limit and read the SM count once per
+    // device (a call being captured into a CUDA graph then makes no
+    // attribute call).
     static std::mutex mu;
     static bool raised[2][64] = {};
-    int dev = 0;
+    static int sm_count[64] = {};
+    int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return set_error(PA_ERR_CUDA, "pa_prefill: cudaGetDevice: %s", cudaGetErrorString(e));
@@ -729,8 +893,18 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
                 return set_error(PA_ERR_CUDA, "pa_prefill: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             done = dev < 64;
         }
+        sms = dev < 64 ? sm_count[dev] : 0;
+        if (sms <= 0) {
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess || sms <= 0)
+                return set_error(PA_ERR_CUDA, "pa_prefill: SM count: %s", cudaGetErrorString(e));
+            if (dev < 64)
+                sm_count[dev] = sms;
+        }
     }
-    const dim3 grid((unsigned)(prm.q_tiles * prm.head_tiles), (unsigned)num_kv_heads, (unsigned)num_seqs);
+    // Persistent grid: one CTA per SM (the CTA holds 225 KB of shared
+    // memory), never more CTAs than units.
+    const dim3 grid((unsigned)std::min<long long>(units, sms));
     void *args[] = {&kv_map, &q_map, &prm};
     e = cudaLaunchKernel(fn, grid, dim3(kThreads), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
