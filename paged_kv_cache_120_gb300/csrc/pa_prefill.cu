@@ -42,6 +42,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/pa.h"
@@ -51,6 +52,12 @@
 namespace pa {
 
 __device__ int g_prefill_error;  // PA_DEVERR_* bits of the prefill kernels
+
+// Work-unit counters of in-flight prefill launches: {next unit, CTAs done}
+// per slot; a launch takes slot (launch number % 64), the last CTA to finish
+// puts both back to 0.
+constexpr int kSchedSlots = 64;
+__device__ int g_prefill_sched[kSchedSlots][2];
 
 namespace {
 
@@ -164,6 +171,21 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// Three-input maximum / minimum.
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // acc + the two 16-bit elements of a packed pair (low half first), each added
 // exactly as fp32 then rounded: mixed-precision adds, no unpacking.
 template <bool BF16>
@@ -217,6 +239,8 @@ constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 512;        // S/P of tiles A and B, then O of A and B, 128 columns each
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
+constexpr int kUnitSlots = 4;              // ring of unit indices handed from the scheduler to every role
+constexpr int kUnitConsumers = 11;         // K, V and MMA warps, 8 softmax warps (one arrival each)
 constexpr int kRegsLaunch = 168;           // registers per thread at launch (384 threads, 1 CTA/SM)
 constexpr int kRegsIO = 120, kRegsSoftmax = 192;
 static_assert(128 * kRegsIO + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
@@ -240,6 +264,7 @@ struct PrefillParams {
     int max_len;        // max_blocks_per_seq * block_size
     int num_kv_heads;
     int num_units;      // q_pairs * num_seqs * num_kv_heads * head_tiles
+    int sched_slot;     // this launch's row of g_prefill_sched
     float scale_log2;   // scale * log2(e)
 };
 
@@ -294,6 +319,8 @@ struct PrefillBars {
     // Per query tile x: s_full[x] its S is in TMEM, p_full[x] its P is,
     // pv_done[x] its O += P V is done (one phase per K/V tile).
     uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
+    int unit_ring[kUnitSlots];  // unit index, or -1 once the launch's units are all taken
     uint32_t tmem_base;
     int fail;
 };
@@ -308,10 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = p.rows_per_head, HPC = p.heads_per_cta;
-    // Persistent: this CTA takes units blockIdx.x, + gridDim.x, ... in order;
-    // every role walks the same list and skips the same empty units, and the
-    // rings and barrier phases run on across unit boundaries.
-    const int u_first = blockIdx.x, u_step = gridDim.x;
+    // Persistent: the Q warp takes the next unit from the launch's counter
+    // (skipping units without queries) and hands it to every role through
+    // a small ring; the TMA rings and barrier phases run on across units.
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -326,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto b_s = [&](int x) { return smem_addr(&bars.s_full[x]); };
     auto b_p = [&](int x) { return smem_addr(&bars.p_full[x]); };
     auto b_pv = [&](int x) { return smem_addr(&bars.pv_done[x]); };
+    auto b_uf = [&](int i) { return smem_addr(&bars.unit_full[i]); };
+    auto b_ue = [&](int i) { return smem_addr(&bars.unit_empty[i]); };
 
     if (tid == 0) {
         mbar_init(b_q, 1);
@@ -342,6 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_s(x), 1);
             mbar_init(b_p(x), 128);
             mbar_init(b_pv(x), 1);
+        }
+        for (int i = 0; i < kUnitSlots; ++i) {
+            mbar_init(b_uf(i), 1);
+            mbar_init(b_ue(i), kUnitConsumers);
         }
         bars.fail = 0;
         fence_barrier_init();
@@ -369,6 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefill_raise(PA_DEVERR_TIMEOUT);
         return false;
     };
+    // The i-th unit handed to this CTA (or -1: no more). Every lane in
+    // `mask` calls it; `leader` arrives once the warp has read the slot.
+    // False if the wait ran out.
+    auto take_unit = [&](int i, unsigned mask, bool leader, int &u) {
+        const int sl = i % kUnitSlots;
+        if (!__all_sync(mask, wait_or_fail(b_uf(sl), (i / kUnitSlots) & 1)))
+            return false;
+        u = *reinterpret_cast<volatile int *>(&bars.unit_ring[sl]);
+        __syncwarp(mask);
+        if (leader)
+            mbar_arrive(b_ue(sl));
+        return true;
+    };
 
     // Register split, per warpgroup (each of its four warps runs the same
     // instruction): the K/V/MMA/Q group drops to kRegsIO, the two softmax
@@ -378,15 +423,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIO));
     if (warp == kWarpQ) {
         // ------------------------------------------------------------ Q
-        // A unit's two query tiles go into the Q buffers once the previous
-        // unit's last S = Q K^T has completed.
+        // Scheduler and Q: take the next unit that has queries from the
+        // launch's counter, hand it on, and load its two query tiles once the
+        // previous unit's last S = Q K^T has completed.
         if (lane == 0) {
-            int ui = 0;
-            for (int u = u_first; u < p.num_units; u += u_step) {
+            int* next = &g_prefill_sched[p.sched_slot][0];
+            for (int i = 0;; ++i) {
                 Unit w;
-                if (!unit_of(p, u, w, false))
-                    continue;
-                if (ui > 0 && !wait_or_fail(b_qe, (ui - 1) & 1))
+                int u;
+                do {
+                    u = atomicAdd(next, 1);
+                } while (u < p.num_units && !unit_of(p, u, w, true));
+                if (u >= p.num_units)
+                    u = -1;
+                const int sl = i % kUnitSlots;
+                if (i >= kUnitSlots && !wait_or_fail(b_ue(sl), ((i / kUnitSlots) - 1) & 1))
+                    break;
+                bars.unit_ring[sl] = u;
+                mbar_arrive(b_uf(sl));
+                if (u < 0)
+                    break;
+                if (i > 0 && !wait_or_fail(b_qe, (i - 1) & 1))
                     break;
                 const int head0 = w.h * p.group + w.ht * HPC;
                 const int tiles = w.n[1] > 0 ? 2 : 1;
@@ -396,7 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int g = 0; g < HPC; ++g)
                             tma_load_3d(sQ(x) + c * kChunkBytes + g * T * 128, &q_map, b_q, c * 64, head0 + g,
                                         w.q0 + w.t0[x]);
-                ++ui;
             }
         }
     } else if (warp == kWarpK || warp == kWarpV) {
@@ -412,10 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int stages = is_k ? kKStages : kVStages;
             int gc = 0;  // K (or V) tiles produced by this CTA so far
             bool go = true;
-            for (int u = u_first; go && u < p.num_units; u += u_step) {
+            for (int i = 0; go; ++i) {
+                int u;
+                if (!take_unit(i, group_mask, lane == leader, u) || u < 0)
+                    break;
                 Unit w;
-                if (!unit_of(p, u, w, false))
-                    continue;
+                unit_of(p, u, w, false);
                 const int n = max(w.n[0], w.n[1]);
                 const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
                 auto lookup = [&](int j) {
@@ -471,10 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int kc = 0, vc = 0, ui = 0;  // K tiles, V tiles and units consumed so far
             int gx[2] = {0, 0};          // P V of tile x issued so far
             bool go = true;
-            for (int u = u_first; go && u < p.num_units; u += u_step) {
+            for (int i = 0; go; ++i) {
+                int u;
+                if (!take_unit(i, 1u, true, u) || u < 0)
+                    break;
                 Unit w;
-                if (!unit_of(p, u, w, false))
-                    continue;
+                unit_of(p, u, w, false);
                 const int n = max(w.n[0], w.n[1]);
                 if (!wait_or_fail(b_q, ui & 1))
                     break;
@@ -562,10 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool sc_pos = sc >= 0.f;
         int gx = 0, vbase = 0;  // tiles of this query tile, and V tiles of the CTA, so far
         bool alive = true;
-        for (int u = u_first; alive && u < p.num_units; u += u_step) {
+        for (int i = 0; alive; ++i) {
+            int u;
+            if (!take_unit(i, kFull, lane == 0, u) || u < 0)
+                break;
             Unit w;
-            if (!unit_of(p, u, w, tid == 0))
-                continue;
+            unit_of(p, u, w, false);
             const int n = max(w.n[0], w.n[1]), nx = w.n[x];
             // The K/V tile holding the sequence end (padding slots past it)
             // is zeroed in V by the first tile that reads it.
@@ -601,12 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (full) {
                     if (sc_pos) {
 #pragma unroll
-                        for (int c = 0; c < kN; ++c)
-                            e8[c & 7] = fmaxf(e8[c & 7], sv[c]);
+                        for (int c = 0; c < kN; c += 2)
+                            e8[(c >> 1) & 7] = max3(e8[(c >> 1) & 7], sv[c], sv[c + 1]);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < kN; ++c)
-                            e8[c & 7] = fminf(e8[c & 7], sv[c]);
+                        for (int c = 0; c < kN; c += 2)
+                            e8[(c >> 1) & 7] = min3(e8[(c >> 1) & 7], sv[c], sv[c + 1]);
                     }
                 } else {
 #pragma unroll
@@ -728,6 +790,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Every role has left its loop, so this CTA takes no more units; the
+    // last CTA to get here resets the launch's counters for the next use.
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&g_prefill_sched[p.sched_slot][1], 1) == (int)gridDim.x - 1) {
+            g_prefill_sched[p.sched_slot][0] = 0;
+            g_prefill_sched[p.sched_slot][1] = 0;
+            __threadfence();
+        }
+    }
     if (warp == kWarpMMA)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
@@ -863,6 +935,8 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
     if (units > 0x7fffffffLL)
         return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: too many query tiles");
     prm.num_units = (int)units;
+    static std::atomic<unsigned> launches{0};
+    prm.sched_slot = (int)(launches.fetch_add(1u) % (unsigned)kSchedSlots);
 
     CUtensorMap kv_map, q_map;
     int rc = encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads);
