@@ -444,6 +444,12 @@ int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens,
  * Admission stops at the first request the free queue cannot supply (that
  * request and the rest are untouched). Returns the number admitted (0..n),
  * or a negative PA_ERR_* on bad arguments (nothing admitted).
+ * The requests' block hashes are computed first, on up to
+ * PA_PCACHE_THREADS helper threads (environment, read once per pool;
+ * default min(8, hardware threads - 1); 0 = none), sharing the hashes of the
+ * leading blocks that equal request 0's token for token; matching and
+ * allocation then run in request order. Results do not depend on the
+ * thread count.
  */
 int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const int64_t *cu_tokens, int n,
                     int flags, int max_blocks_per_seq, int32_t *seq_ids, int32_t *num_cached,

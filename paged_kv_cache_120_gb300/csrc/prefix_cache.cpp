@@ -28,9 +28,17 @@
 // for the device calls and never touches device memory.
 #include <algorithm>
 #include <array>
+#include <atomic>
+#include <chrono>
 #include <climits>
+#include <condition_variable>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <memory>
+#include <mutex>
+#include <thread>
 #include <unordered_map>
 #include <vector>
 
@@ -246,6 +254,110 @@ uint64_t digest_key(const Digest &d)
     return x;
 }
 
+// A small persistent pool: run(n, fn) calls fn(0..n-1) on the workers and
+// the calling thread and returns when every call has finished. A worker
+// polls for the next job for kPollUs after finishing one (admission waves
+// come back to back; waking a sleeping thread costs tens of microseconds),
+// then sleeps on a condition variable.
+class WorkPool {
+  public:
+    explicit WorkPool(int threads)
+    {
+        for (int i = 0; i < threads; ++i)
+            workers_.emplace_back([this] { loop(); });
+    }
+    ~WorkPool()
+    {
+        {
+            std::lock_guard<std::mutex> l(m_);
+            stop_ = true;
+            stop_pub_.store(true, std::memory_order_release);
+        }
+        cv_.notify_all();
+        for (auto &t : workers_)
+            t.join();
+    }
+    void run(int n, const std::function<void(int)> &fn)
+    {
+        {
+            std::lock_guard<std::mutex> l(m_);
+            job_ = &fn;
+            count_ = n;
+            next_.store(0);
+            done_ = 0;
+            ++gen_;
+            gen_pub_.store(gen_, std::memory_order_release);
+        }
+        cv_.notify_all();
+        work();
+        std::unique_lock<std::mutex> l(m_);
+        done_cv_.wait(l, [&] { return done_ == count_; });
+        job_ = nullptr;
+    }
+
+  private:
+    void work()
+    {
+        for (;;) {
+            const std::function<void(int)> *job;
+            int count;
+            {
+                std::lock_guard<std::mutex> l(m_);
+                job = job_;
+                count = count_;
+            }
+            if (!job)
+                return;
+            const int i = next_.fetch_add(1);
+            if (i >= count)
+                return;
+            (*job)(i);
+            std::lock_guard<std::mutex> l(m_);
+            if (++done_ == count_)
+                done_cv_.notify_all();
+        }
+    }
+    void loop()
+    {
+        uint64_t seen = 0;
+        for (;;) {
+            const auto t0 = std::chrono::steady_clock::now();
+            while (gen_pub_.load(std::memory_order_acquire) == seen && !stop_pub_.load(std::memory_order_acquire) &&
+                   std::chrono::steady_clock::now() - t0 < std::chrono::microseconds(kPollUs)) {
+            }
+            {
+                std::unique_lock<std::mutex> l(m_);
+                cv_.wait(l, [&] { return stop_ || gen_ != seen; });
+                if (stop_)
+                    return;
+                seen = gen_;
+            }
+            work();
+        }
+    }
+    std::vector<std::thread> workers_;
+    std::mutex m_;
+    std::condition_variable cv_, done_cv_;
+    const std::function<void(int)> *job_ = nullptr;
+    int count_ = 0, done_ = 0;
+    std::atomic<int> next_{0};
+    uint64_t gen_ = 0;
+    bool stop_ = false;
+    std::atomic<uint64_t> gen_pub_{0};  // gen_, readable without the lock
+    std::atomic<bool> stop_pub_{false};
+    static constexpr int kPollUs = 200;
+};
+
+// Hashing threads of a pool: PA_PCACHE_THREADS if set (0 = none), else
+// min(8, hardware threads - 1).
+int hash_threads()
+{
+    if (const char *e = std::getenv("PA_PCACHE_THREADS"))
+        return std::max(0, std::min(64, std::atoi(e)));
+    const int hw = (int)std::thread::hardware_concurrency();
+    return std::max(0, std::min(8, hw - 1));
+}
+
 }  // namespace
 
 struct pa_prefix_cache {
@@ -272,6 +384,8 @@ struct pa_prefix_cache {
     };
     std::unordered_map<int, Seq> seqs;
     int next_id = 0;
+    std::unique_ptr<WorkPool> pool;  // hashes a wave's requests in parallel (created on first use)
+    bool pool_tried = false;
 
     // free queue
     void unlink(int32_t b)
@@ -302,7 +416,7 @@ struct pa_prefix_cache {
     }
     // Digest of a full block: from the memo when a recorded block has the
     // same parent hash and token ids, else SHA-256.
-    Digest digest(const Digest &parent, const int32_t *tokens)
+    Digest digest(const Digest &parent, const int32_t *tokens) const
     {
         const int B = block_size;
         for (int32_t b = memo.first(memo_key(parent, tokens, B)); b >= 0; b = memo.next(b))
@@ -401,25 +515,68 @@ namespace {
 // prompt neither matches nor records: every block is fresh and unhashed.
 // Returns PA_OK or PA_ERR_OUT_OF_BLOCKS, the latter with the pool unchanged
 // and no error text set.
+// The chained hashes of a prompt's full blocks (reads the pool, writes
+// nothing: safe to run for several prompts at once).
+void chain_digests(const pa_prefix_cache *c, const int32_t *tokens, int num_tokens, std::vector<Digest> &out)
+{
+    const int B = c->block_size, full = num_tokens / B;
+    out.clear();
+    out.reserve(full);
+    Digest parent{};
+    for (int i = 0; i < full; ++i) {
+        parent = c->digest(parent, tokens + (size_t)i * B);
+        out.push_back(parent);
+    }
+}
+
+// chain_digests of a prompt whose first `k` full blocks hold the same tokens
+// as those of a prompt with hashes `base`: chained, those hashes are equal,
+// so they are copied and hashing resumes after them.
+void chain_digests_from(const pa_prefix_cache *c, const int32_t *tokens, int num_tokens,
+                        const std::vector<Digest> &base, int k, std::vector<Digest> &out)
+{
+    const int B = c->block_size, full = num_tokens / B;
+    out.assign(base.begin(), base.begin() + k);
+    out.reserve(full);
+    Digest parent = k > 0 ? base[k - 1] : Digest{};
+    for (int i = k; i < full; ++i) {
+        parent = c->digest(parent, tokens + (size_t)i * B);
+        out.push_back(parent);
+    }
+}
+
+// `pre`, if given, holds the prompt's chain_digests (computed beforehand).
+// `prev`, if given, is the sequence admitted just before: while this
+// prompt's chained hashes equal its hashes, the lookup target of each is the
+// block `prev` holds at that index (it matched it, or recorded it as the
+// first block with that hash), so no index lookup is needed.
 int admit_one(pa_prefix_cache *c, const int32_t *tokens, int num_tokens, bool cache, int *seq_id,
-              int *num_cached_tokens, int *need_out, int *avail_out)
+              int *num_cached_tokens, int *need_out, int *avail_out, std::vector<Digest> *pre = nullptr,
+              const pa_prefix_cache::Seq *prev = nullptr)
 {
     const int B = c->block_size;
     const int full = cache ? num_tokens / B : 0, nblk = (num_tokens + B - 1) / B;
     std::vector<Digest> hashes;
-    hashes.reserve(full);
-    Digest parent{};
-    for (int i = 0; i < full; ++i) {
-        parent = c->digest(parent, tokens + (size_t)i * B);
-        hashes.push_back(parent);
-    }
+    if (cache && pre)
+        hashes = std::move(*pre);
+    else if (cache)
+        chain_digests(c, tokens, num_tokens, hashes);
     std::vector<int32_t> hits;
+    hits.reserve(full);
+    const int same = (prev && prev->cache) ? (int)std::min(prev->hashes.size(), hashes.size()) : 0;
+    bool with_prev = same > 0;
     for (int i = 0; i < full; ++i) {
         if ((long long)(i + 1) * B > num_tokens - 1)
             break;
-        const int32_t b = c->lookup(hashes[i]);
-        if (b < 0)
-            break;
+        int32_t b;
+        if (with_prev && i < same && hashes[i] == prev->hashes[i]) {
+            b = prev->table[i];
+        } else {
+            with_prev = false;  // chained: once they differ they differ from here on
+            b = c->lookup(hashes[i]);
+            if (b < 0)
+                break;
+        }
         hits.push_back(b);
     }
     int touched_free = 0;
@@ -495,15 +652,55 @@ extern "C" int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const 
     if (n > 0 && cu_tokens[n] > INT32_MAX)
         return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: more than 2^31 - 1 prompt tokens");
     const bool cache = !(flags & PA_PCACHE_NO_CACHE);
+    // Phase 1: every request's hash chain (reads only). Request 0's first;
+    // the others copy the hashes of the full blocks they share with it
+    // token for token from the start, and hash the rest in parallel.
+    std::vector<std::vector<Digest>> pre;
+    if (cache && n > 1) {
+        pre.resize(n);
+        const int32_t *t0 = tokens;
+        const int full0 = (int)(cu_tokens[1] / B);
+        chain_digests(c, t0, (int)cu_tokens[1], pre[0]);
+        std::vector<int> common(n, 0);
+        for (int r = 1; r < n; ++r) {
+            const int32_t *tr = tokens + cu_tokens[r];
+            const int fr = (int)((cu_tokens[r + 1] - cu_tokens[r]) / B);
+            int k = 0;
+            while (k < fr && k < full0 &&
+                   std::memcmp(tr + (size_t)k * B, t0 + (size_t)k * B, sizeof(int32_t) * (size_t)B) == 0)
+                ++k;
+            common[r] = k;
+        }
+        auto one = [&](int r) {
+            if (r > 0)
+                chain_digests_from(c, tokens + cu_tokens[r], (int)(cu_tokens[r + 1] - cu_tokens[r]), pre[0],
+                                   common[r], pre[r]);
+        };
+        if (!c->pool_tried) {
+            c->pool_tried = true;
+            const int t = hash_threads();
+            if (t > 0)
+                c->pool.reset(new WorkPool(t));
+        }
+        if (c->pool && n >= 4)
+            c->pool->run(n, one);
+        else
+            for (int r = 0; r < n; ++r)
+                one(r);
+    }
+    // Phase 2: match, allocate and record in request order.
     cu_seqlens_q[0] = 0;
     int32_t q = 0;
     int admitted = 0;
+    const pa_prefix_cache::Seq *prev = nullptr;
     for (; admitted < n; ++admitted) {
         const int len = (int)(cu_tokens[admitted + 1] - cu_tokens[admitted]);
         int sid = 0, hit = 0, need = 0, avail = 0;
-        if (admit_one(c, tokens + cu_tokens[admitted], len, cache, &sid, &hit, &need, &avail) != PA_OK)
+        if (admit_one(c, tokens + cu_tokens[admitted], len, cache, &sid, &hit, &need, &avail,
+                      pre.empty() ? nullptr : &pre[admitted], prev) != PA_OK)
             break;
-        const auto &table = c->seqs.find(sid)->second.table;
+        prev = &c->seqs.find(sid)->second;  // element addresses survive later insertions
+        const auto &table = prev->table;
         seq_ids[admitted] = sid;
         num_cached[admitted] = hit;
         seq_lens[admitted] = len;
