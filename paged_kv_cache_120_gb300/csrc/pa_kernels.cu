@@ -1084,32 +1084,48 @@ __global__ void __launch_bounds__(kReduceWarps * 32) paged_decode_reduce_kernel(
 
 // ------------------------------------------------------- reshape and copy
 
-// Grid (token, row chunk): the token's K row [num_kv_heads][head_size] and
-// V row are contiguous both in the input and in the pool, so each CTA copies
-// one 16-byte element of each per thread.
-constexpr int kReshapeThreads = 256;
+// One CTA per token: the token's K row [num_kv_heads][head_size] and V row
+// are contiguous both in the input and in the pool. Each thread moves
+// kReshapeVecs 16-byte elements of each, all loads issued before the stores
+// (so that many bytes are in flight); the block is sized to the row.
+constexpr int kReshapeVecs = 4;
+constexpr int kReshapeMaxThreads = 256;
 
-__global__ void __launch_bounds__(kReshapeThreads)
+__global__ void __launch_bounds__(kReshapeMaxThreads)
     reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                              uint4 *__restrict__ kv, const int32_t *__restrict__ slots,
                              int row_vecs, long long num_slots, long long half_vecs)
 {
     grid_launch_dependents();  // the decode that follows may start its prologue
     const int t = blockIdx.x;
-    const int i = blockIdx.y * kReshapeThreads + threadIdx.x;
     const long long slot = slots[t];
     if (slot < 0)
         return;
     if (slot >= num_slots) {
-        if (threadIdx.x == 0 && blockIdx.y == 0)
+        if (threadIdx.x == 0)
             raise_error(PA_DEVERR_SLOT);
         return;
     }
-    if (i < row_vecs) {
-        const uint4 k = __ldg(key + (long long)t * row_vecs + i);
-        const uint4 v = __ldg(value + (long long)t * row_vecs + i);
-        kv[slot * row_vecs + i] = k;
-        kv[half_vecs + slot * row_vecs + i] = v;
+    const uint4 *ksrc = key + (long long)t * row_vecs, *vsrc = value + (long long)t * row_vecs;
+    uint4 *kdst = kv + slot * row_vecs, *vdst = kv + half_vecs + slot * row_vecs;
+    for (int base = threadIdx.x; base < row_vecs; base += blockDim.x * kReshapeVecs) {
+        uint4 k[kReshapeVecs], v[kReshapeVecs];
+#pragma unroll
+        for (int u = 0; u < kReshapeVecs; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < row_vecs) {
+                k[u] = __ldg(ksrc + i);
+                v[u] = __ldg(vsrc + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeVecs; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < row_vecs) {
+                kdst[i] = k[u];
+                vdst[i] = v[u];
+            }
+        }
     }
 }
 
@@ -1140,8 +1156,10 @@ __device__ __forceinline__ uint2 quantize8(const uint4 x, float scale)
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
-// FP8 write path, grid (token, row chunk) as above: each thread quantises 8
-// elements of the token's K row and 8 of its V row (16 bytes in, 8 out).
+// FP8 write path, grid (token, chunk of kReshapeThreads vectors of the row):
+// each thread quantises 8 elements of the token's K row and 8 of its V row
+// (16 bytes in, 8 out).
+constexpr int kReshapeThreads = 256;
 template <bool BF16>
 __global__ void __launch_bounds__(kReshapeThreads)
     reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
@@ -1634,8 +1652,11 @@ extern "C" int pa_reshape_and_cache(const void *key, const void *value, void *kv
     const long long row_vecs = row_elems * 2 / 16;
     const long long num_slots = (long long)num_blocks * block_size;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const dim3 grid(num_tokens, (unsigned)((row_vecs + kReshapeThreads - 1) / kReshapeThreads));
-    reshape_and_cache_kernel<<<grid, kReshapeThreads, 0, s>>>(
+    // Threads: a multiple of 32 covering the row in kReshapeVecs passes, at
+    // most kReshapeMaxThreads (longer rows loop).
+    const long long per = (row_vecs + kReshapeVecs - 1) / kReshapeVecs;
+    const int threads = (int)std::min<long long>(kReshapeMaxThreads, (per + 31) / 32 * 32);
+    reshape_and_cache_kernel<<<num_tokens, threads, 0, s>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(kv_cache), slot_mapping, (int)row_vecs, num_slots, num_slots * row_vecs);
     cudaError_t e = cudaGetLastError();
