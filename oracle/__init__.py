@@ -88,6 +88,8 @@ def _load():
                                               c_i32p, d, i, i, i, i, i, i, d, d]
     lib.oracle_prefill.argtypes = [c_dp, c_u16p, c_u16p, c_i32p, i, c_i32p, c_i32p, i, d,
                                    i, i, i, i, i, i]
+    lib.oracle_prefill_fp8.argtypes = [c_dp, c_u16p, c_u8p, c_i32p, i, c_i32p, c_i32p, i, d,
+                                       i, i, i, i, i, i, d, d]
     _lib = lib
     return lib
 
@@ -294,4 +296,23 @@ def prefill(query, pool, block_tables, cu_seqlens_q, seq_lens, scale, num_q_head
                            _p(cu, ctypes.c_int32), _p(sl, ctypes.c_int32), num_seqs,
                            float(scale), num_q_heads, num_kv_heads, head_size, num_blocks,
                            block_size, dtype)
+    return out
+
+
+def prefill_fp8(query, pool, block_tables, cu_seqlens_q, seq_lens, scale, num_q_heads,
+                num_kv_heads, head_size, num_blocks, block_size, dtype, k_scale, v_scale) -> np.ndarray:
+    """Causal chunked prefill over an E4M3 pool -> [total_q, num_q_heads, head_size]
+    float64 (rows as in prefill, each the FP8 decode over its causal prefix)."""
+    q, kv = _u16(query), _u8(pool)
+    bt, cu, sl = _i32(block_tables), _i32(cu_seqlens_q), _i32(seq_lens)
+    num_seqs = sl.shape[0]
+    assert cu.shape[0] == num_seqs + 1
+    total_q = int(cu[-1])
+    max_blocks = bt.shape[1] if bt.ndim == 2 else 0
+    out = np.zeros((total_q, num_q_heads, head_size), dtype=np.float64)
+    _load().oracle_prefill_fp8(_p(out, ctypes.c_double), _p(q, ctypes.c_uint16),
+                               _p(kv, ctypes.c_uint8), _p(bt, ctypes.c_int32), max_blocks,
+                               _p(cu, ctypes.c_int32), _p(sl, ctypes.c_int32), num_seqs,
+                               float(scale), num_q_heads, num_kv_heads, head_size, num_blocks,
+                               block_size, dtype, float(k_scale), float(v_scale))
     return out

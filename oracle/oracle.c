@@ -467,6 +467,31 @@ void oracle_prefill(double *out, const uint16_t *query, const uint16_t *pool,
     }
 }
 
+/* Chunked prefill over an E4M3 pool: the same rows as oracle_prefill, each
+ * the FP8 decode definition (oracle_decode_fp8_one) over its first p + 1
+ * tokens. */
+void oracle_prefill_fp8(double *out, const uint16_t *query, const uint8_t *pool,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
+                        double scale, int num_q_heads, int num_kv_heads, int head_size,
+                        int num_blocks, int block_size, int dtype, double k_scale, double v_scale)
+{
+    for (int s = 0; s < num_seqs; ++s) {
+        int q0 = cu_seqlens_q[s];
+        int q_len = cu_seqlens_q[s + 1] - q0;
+        const int32_t *table = block_tables + (long long)s * max_blocks_per_seq;
+        for (int i = 0; i < q_len; ++i) {
+            int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */
+            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;
+            for (int hq = 0; hq < num_q_heads; ++hq)
+                oracle_decode_fp8_one(out + ((long long)(q0 + i) * num_q_heads + hq) * head_size, q_row,
+                                      pool, table, max_blocks_per_seq, &visible, 0, hq, scale,
+                                      num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                                      dtype, k_scale, v_scale);
+        }
+    }
+}
+
 /* ---- the online-softmax recurrence [P1 §4.6] ----
  * The same attention, computed the way the method streams it: the logical
  * tokens are cut into consecutive parts of `part_len` tokens; each part

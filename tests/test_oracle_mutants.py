@@ -27,6 +27,10 @@ _GATHER8 = (_GATHER % (("double",) * 6)) + """    double *q = (double *)malloc(s
         int b = table[{1}];"""
 
 # (file, original text, planted slip, pin file expected to catch it)
+# the query-row and call lines that follow the visible length in oracle_prefill
+_PREFILL16 = ("\n            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;"
+              "\n            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_one(")
+
 MUTANTS = [
     ("oracle/oracle.c", "expo - 25);", "expo - 24);", "test_oracle_pins.py"),          # f16 bias
     ("oracle/oracle.c", "ldexp((double)frac, -24)", "ldexp((double)frac, -25)", "test_oracle_pins.py"),
@@ -74,13 +78,27 @@ MUTANTS = [
     ("oracle/oracle.c", "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * v_scale;",
      "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * k_scale;",
      "test_oracle_fp8_pins.py"),                                                      # decode scale swap
-    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1;",
-     "int32_t visible = seq_lens[s] - q_len + i + 2;", "test_oracle_prefill_pins.py"),  # sees p+1
-    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1;",
-     "int32_t visible = seq_lens[s] - q_len + 1;", "test_oracle_prefill_pins.py"),      # not causal in i
-    ("oracle/oracle.c", "const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;",
-     "const uint16_t *q_row = query + (long long)(q0) * num_q_heads * head_size;",
-     "test_oracle_prefill_pins.py"),                                                      # wrong query row
+    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */" + _PREFILL16,
+     "int32_t visible = seq_lens[s] - q_len + i + 2; /* tokens 0..p */" + _PREFILL16,
+     "test_oracle_prefill_pins.py"),                                                  # sees p+1
+    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */" + _PREFILL16,
+     "int32_t visible = seq_lens[s] - q_len + 1; /* tokens 0..p */" + _PREFILL16,
+     "test_oracle_prefill_pins.py"),                                                  # not causal in i
+    ("oracle/oracle.c", "const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;"
+     "\n            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_one(",
+     "const uint16_t *q_row = query + (long long)(q0) * num_q_heads * head_size;"
+     "\n            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_one(",
+     "test_oracle_prefill_pins.py"),                                                  # wrong query row
+    ("oracle/oracle.c", "dtype, k_scale, v_scale);\n        }\n    }\n}\n\n/* ---- the online-softmax",
+     "dtype, v_scale, k_scale);\n        }\n    }\n}\n\n/* ---- the online-softmax",
+     "test_oracle_prefill_pins.py"),                                                  # FP8 prefill scales swapped
+    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */\n"
+     "            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;\n"
+     "            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_fp8_one(",
+     "int32_t visible = seq_lens[s] - q_len + i + 2; /* tokens 0..p */\n"
+     "            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;\n"
+     "            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_fp8_one(",
+     "test_oracle_prefill_pins.py"),                                                  # FP8 prefill row sees one more
     ("oracle/prefix_cache.py", "if (i + 1) * B > n - 1 or h not in self.cached:",
      "if (i + 1) * B > n or h not in self.cached:", "test_prefix_cache_model.py"),   # hit limit
     ("oracle/prefix_cache.py", "                    self.free.append(b)",

@@ -126,3 +126,40 @@ def test_empty_chunks_write_nothing():
                         np.array([18, 19, 20], np.int32), c["scale"], c["Hq"], c["Hkv"], c["D"],
                         c["nb"], c["B"], oracle.F16)
     assert np.array_equal(got, ref)
+
+
+# ----------------------------------------------------------- FP8 cache
+
+def _fp8_case(rng, ctx, qlens, B=16, Hq=4, Hkv=2, D=16, spare=3):
+    c = _case(rng, ctx, qlens, B, Hq, Hkv, D, spare)
+    codes = rng.integers(0, 254, c["pool"].shape).astype(np.uint8)
+    c["codes"] = np.where(codes >= 0x7F, codes + 1, codes).astype(np.uint8)  # every finite code
+    return c
+
+
+def test_fp8_single_query_chunks_are_the_pinned_fp8_decode():
+    rng = np.random.default_rng(11)
+    c = _fp8_case(rng, [5, 40, 16, 1], [1, 1, 1, 1])
+    got = oracle.prefill_fp8(c["q"], c["codes"], c["bt"], c["cu"], c["sl"], c["scale"], c["Hq"], c["Hkv"],
+                             c["D"], c["nb"], c["B"], oracle.F16, 0.02, 0.05)
+    ref = oracle.decode_fp8(c["q"], c["codes"], c["bt"], c["sl"], c["scale"], c["Hq"], c["Hkv"], c["D"],
+                            c["nb"], c["B"], oracle.F16, 0.02, 0.05)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_prefill_equals_16bit_prefill_on_the_dequantized_pool():
+    """Power-of-two scales (different for K and V) make every dequantised
+    value an fp16 value: the FP8 prefill must equal the pinned 16-bit prefill
+    on a pool holding those values, row for row, bit for bit."""
+    rng = np.random.default_rng(12)
+    c = _fp8_case(rng, [7, 35, 20, 64], [3, 35, 6, 17])
+    ks, vs = 0.25, 2.0
+    vals = np.vectorize(oracle.e4m3_to_double)(c["codes"])
+    vals[0] *= ks
+    vals[1] *= vs
+    pool16 = vals.astype(np.float16)
+    assert np.array_equal(pool16.astype(np.float64), vals)
+    got = oracle.prefill_fp8(c["q"], c["codes"], c["bt"], c["cu"], c["sl"], c["scale"], c["Hq"], c["Hkv"],
+                             c["D"], c["nb"], c["B"], oracle.F16, ks, vs)
+    ref = _run(c, pool=pool16.view(np.uint16))
+    assert np.array_equal(got, ref)
