@@ -289,6 +289,25 @@ int pa_prefill(void *out, const void *query, const void *kv_cache,
                int num_blocks, int block_size, int dtype, pa_stream_t stream);
 
 /*
+ * pa_prefill_fp8 — pa_prefill over an FP8 (E4M3) pool written by
+ * pa_reshape_and_cache_fp8 ([book] §4.8's lower-precision cache, with the
+ * FP8 conventions above): a cached K element stands for e4m3(code) * k_scale
+ * and a V element for e4m3(code) * v_scale. kv_cache is the byte pool
+ * (2, num_blocks, block_size, num_kv_heads, head_size); dtype is the type of
+ * query and out (PA_F16 or PA_BF16). The codes are widened exactly to that
+ * type on the way to the tensor cores; k_scale joins the score scale and
+ * v_scale the final normalisation. Same shapes, limits and error behaviour
+ * as pa_prefill; k_scale and v_scale must be finite and > 0.
+ */
+int pa_prefill_fp8(void *out, const void *query, const void *kv_cache,
+                   const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
+                   int total_q, int max_seqlen_q, float scale,
+                   int num_q_heads, int num_kv_heads, int head_size,
+                   int num_blocks, int block_size, int dtype, float k_scale, float v_scale,
+                   pa_stream_t stream);
+
+/*
  * pa_copy_blocks — copy-on-write clones of whole physical blocks
  * ([digest] "写时复制": a shared block is cloned before a write and the
  * writer's table retargeted; [lecture] §4.3 steps: allocate Q, copy P into

@@ -51,6 +51,8 @@ SIGNATURES = [
     ("pa_decode_fp8", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _f, _f,
                            _vp, _sz, _u, _vp]),
     ("pa_prefill", _i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _i, _i, _i, _vp]),
+    ("pa_prefill_fp8", _i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _i, _i, _i, _f, _f,
+                            _vp]),
     ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_get_device_error", _i, [_ip]),
     ("pa_alloc_create", _vp, [_i, _i, _i32p]),
@@ -281,6 +283,20 @@ def pa_prefill(out, query, kv_cache, block_tables, cu_seqlens_q, seq_lens, scale
         _dev(cu_seqlens_q, "cu_seqlens_q"), _dev(seq_lens, "seq_lens"), int(seq_lens.shape[0]),
         total_q, int(max_seqlen_q), float(scale), hq, hkv, d, nb, bs, _dtype_code(kv_cache),
         _stream(stream)))
+
+
+def pa_prefill_fp8(out, query, kv_cache, block_tables, cu_seqlens_q, seq_lens, scale, max_seqlen_q,
+                   k_scale, v_scale, stream=None) -> None:
+    """pa_prefill over an E4M3 byte pool (2, NB, B, Hkv, D) uint8; out/query 16-bit."""
+    _fp8_pool(kv_cache, "kv_cache")
+    total_q, hq, d = query.shape
+    _, nb, bs, hkv, _ = kv_cache.shape
+    _check(lib().pa_prefill_fp8(
+        _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
+        _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
+        _dev(cu_seqlens_q, "cu_seqlens_q"), _dev(seq_lens, "seq_lens"), int(seq_lens.shape[0]),
+        total_q, int(max_seqlen_q), float(scale), hq, hkv, d, nb, bs, _dtype_code(query),
+        float(k_scale), float(v_scale), _stream(stream)))
 
 
 def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:

@@ -171,6 +171,38 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// Two E4M3 codes (the low / high 16 bits of x, the lower byte to the lower
+// half) to an fp16 pair; exact, every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3_pair_lo(uint32_t x)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(d) : "r"(x));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e4m3_pair_hi(uint32_t x)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(d) : "r"(x));
+    return d;
+}
+
+// An fp16 pair holding E4M3 values to the same values as a bf16 pair (exact:
+// three mantissa bits and exponents within bf16's range).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h)
+{
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    const __nv_bfloat162 b = __float22bfloat162_rn(f);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
 // Three-input maximum / minimum.
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
@@ -231,12 +263,15 @@ constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit operand: 32 K
 constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size is a multiple)
 constexpr int kThreads = 384;              // warps 0-3 softmax A, 4-7 softmax B, 8 K, 9 MMA, 10 V, 11 Q
 constexpr int kWarpK = 8, kWarpMMA = 9, kWarpV = 10, kWarpQ = 11;
-constexpr int kKStages = 3;                // K ring (freed when both tiles' S = Q K^T are done)
+constexpr int kKStagesMax = 3;             // K ring (freed when both tiles' S = Q K^T are done):
+constexpr int kKStages16 = 3, kKStages8 = 2;  // 3 stages, 2 with an FP8 cache (room for staging)
 constexpr int kVStages = 2;                // V ring (freed when both tiles' O += P V are done)
 constexpr int kOffQ = 0;                   // Q of tile A, then of tile B
 constexpr int kOffK = 2 * kTileBytes;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + slack to align the base to 1024
+constexpr int kStageBytes8 = 128 * 128;    // an FP8 K or V tile as loaded, before widening: 16 KB
+// 16-bit cache: Q 64 KB, K 3 x 32, V 2 x 32. FP8 cache: Q 64, K 2 x 32, V 2 x 32,
+// then one FP8 staging tile each for K and V (16 KB each). Both 224 KB.
+constexpr int kSmemBytes = 2 * kTileBytes + 3 * kTileBytes + kVStages * kTileBytes + 1024;  // + align slack
 constexpr uint32_t kTmemCols = 512;        // S/P of tiles A and B, then O of A and B, 128 columns each
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
 constexpr int kUnitSlots = 4;              // ring of unit indices handed from the scheduler to every role
@@ -265,7 +300,8 @@ struct PrefillParams {
     int num_kv_heads;
     int num_units;      // q_pairs * num_seqs * num_kv_heads * head_tiles
     int sched_slot;     // this launch's row of g_prefill_sched
-    float scale_log2;   // scale * log2(e)
+    float scale_log2;   // scale * log2(e) (* k_scale with an FP8 cache)
+    float v_scale;      // 1, or the FP8 cache's V scale
 };
 
 // One work unit: the two adjacent query tiles A = 2 qp and B = 2 qp + 1 of
@@ -315,7 +351,8 @@ __device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, 
 }
 
 struct PrefillBars {
-    uint64_t q_full, q_empty, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t q_full, q_empty, k_full[kKStagesMax], k_empty[kKStagesMax], v_full[kVStages], v_empty[kVStages];
+    uint64_t stg_full[2];  // FP8 cache: the K / V staging tile has landed
     // Per query tile x: s_full[x] its S is in TMEM, p_full[x] its P is,
     // pv_done[x] its O += P V is done (one phase per K/V tile).
     uint64_t s_full[2], p_full[2], pv_done[2];
@@ -325,7 +362,7 @@ struct PrefillBars {
     int fail;
 };
 
-template <bool BF16>
+template <bool BF16, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap kv_map,
                          const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
@@ -342,6 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     auto sQ = [&](int x) { return base + kOffQ + x * kTileBytes; };
+    constexpr int kKStages = FP8 ? kKStages8 : kKStages16;
+    constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // FP8: K then V staging tile
     auto sK = [&](int st) { return base + kOffK + st * kTileBytes; };
     auto sV = [&](int st) { return base + kOffV + st * kTileBytes; };
     const uint32_t b_q = smem_addr(&bars.q_full), b_qe = smem_addr(&bars.q_empty);
@@ -371,6 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_p(x), 128);
             mbar_init(b_pv(x), 1);
         }
+        mbar_init(smem_addr(&bars.stg_full[0]), 1);
+        mbar_init(smem_addr(&bars.stg_full[1]), 1);
         for (int i = 0; i < kUnitSlots; ++i) {
             mbar_init(b_uf(i), 1);
             mbar_init(b_ue(i), kUnitConsumers);
@@ -457,54 +499,132 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWarpK || warp == kWarpV) {
         // ---------------------------------------------------------- K, V
-        // Warp 8 produces the K tiles, warp 10 the V tiles, each at its own
-        // pace through its ring; lane i < 8 moves the 16-token box i of each
-        // tile. The block-table entry of the next tile is loaded while the
-        // current one waits for its stage.
         const bool is_k = warp == kWarpK;
-        if (lane < 8) {
-            const int box = lane, leader = 0;
-            const unsigned group_mask = 0x000000FFu;
+        if constexpr (FP8) {
+            // FP8 cache: lanes 0-7 bring each tile's 16-token boxes of codes
+            // into a staging tile (TMA, 128-byte swizzle), then the whole warp
+            // widens them, exactly, into the 16-bit ring stage in the MMA's
+            // layout (rows past the sequence end as zeros) and marks the
+            // stage full; the next tile's codes are requested as soon as the
+            // staging tile has been read.
+            const uint32_t stg = base + kOffStage + (is_k ? 0 : kStageBytes8);
+            const uint32_t b_stg = smem_addr(&bars.stg_full[is_k ? 0 : 1]);
             const int stages = is_k ? kKStages : kVStages;
-            int gc = 0;  // K (or V) tiles produced by this CTA so far
+            int gc = 0;  // tiles produced by this CTA so far
             bool go = true;
             for (int i = 0; go; ++i) {
                 int u;
-                if (!take_unit(i, group_mask, lane == leader, u) || u < 0)
+                if (!take_unit(i, kFull, lane == 0, u) || u < 0)
                     break;
                 Unit w;
                 unit_of(p, u, w, false);
                 const int n = max(w.n[0], w.n[1]);
                 const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
-                auto lookup = [&](int j) {
-                    const int kt = j * kN + kBoxTokens * box;
-                    return (j < n && kt < w.L) ? __ldg(table + kt / p.block_size) : -1;
+                auto issue = [&](int j) {
+                    if (lane < 8) {
+                        const int kt = j * kN + kBoxTokens * lane;
+                        int phys = kt < w.L ? __ldg(table + kt / p.block_size) : -1;
+                        if (phys >= p.num_blocks || (phys < 0 && kt < w.L)) {
+                            prefill_raise(PA_DEVERR_BLOCK_ID);
+                            phys = p.num_blocks;
+                        }
+                        if (phys < 0)
+                            phys = p.num_blocks;  // past the sequence end: outside the map, zeros
+                        if (lane == 0)
+                            mbar_expect_tx(b_stg, kStageBytes8);
+                        __syncwarp(0xFFu);
+                        tma_load_5d(stg + lane * (kBoxTokens * 128), &kv_map, b_stg, 0, w.h, kt % p.block_size,
+                                    phys, is_k ? 0 : 1);
+                    }
                 };
-                int next = lookup(0);
+                issue(0);
                 for (int j = 0; j < n; ++j, ++gc) {
-                    int phys = next;
-                    next = lookup(j + 1);
                     const int st = gc % stages;
-                    if (gc >= stages &&
-                        !wait_or_fail(is_k ? b_ke(st) : b_ve(st), ((gc - stages) / stages) & 1)) {
+                    if (!__all_sync(kFull, wait_or_fail(b_stg, gc & 1)) ||
+                        (gc >= stages && !__all_sync(kFull, wait_or_fail(is_k ? b_ke(st) : b_ve(st),
+                                                                         ((gc - stages) / stages) & 1)))) {
                         go = false;
                         break;
                     }
-                    const int kt = j * kN + kBoxTokens * box;
-                    const int tib = kt % p.block_size;
-                    if (phys >= p.num_blocks || (phys < 0 && kt < w.L)) {
-                        prefill_raise(PA_DEVERR_BLOCK_ID);
-                        phys = p.num_blocks;
+                    const uint32_t dst = is_k ? sK(st) : sV(st);
+#pragma unroll 1
+                    for (int rr = 0; rr < kN / 32; ++rr) {
+                        const int r = lane + 32 * rr;
+                        const bool pad = j * kN + r >= w.L;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint4 c = pad ? make_uint4(0u, 0u, 0u, 0u) : lds128(stg + r * 128 + ((q ^ (r & 7)) << 4));
+                            uint32_t h[8] = {e4m3_pair_lo(c.x), e4m3_pair_hi(c.x), e4m3_pair_lo(c.y), e4m3_pair_hi(c.y),
+                                             e4m3_pair_lo(c.z), e4m3_pair_hi(c.z), e4m3_pair_lo(c.w), e4m3_pair_hi(c.w)};
+                            if constexpr (BF16) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    h[e] = f16x2_to_bf16x2(h[e]);
+                            }
+                            // dims 16q .. 16q + 15: chunk q / 4, 16-byte units 2 (q % 4) and + 1
+                            const uint32_t row = dst + (q >> 2) * kChunkBytes + r * 128;
+                            const int u0 = 2 * (q & 3);
+                            sts128(row + ((u0 ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+                            sts128(row + (((u0 + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+                        }
                     }
-                    if (phys < 0)
-                        phys = p.num_blocks;  // past the sequence end: outside the map, zeros
-                    const uint32_t full = is_k ? b_kf(st) : b_vf(st);
-                    if (lane == leader)
-                        mbar_expect_tx(full, kTileBytes);
-                    __syncwarp(group_mask);
-                    const uint32_t dst = (is_k ? sK(st) : sV(st)) + box * (kBoxTokens * 128);
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, w.h, tib, phys, is_k ? 0 : 1);
+                    fence_proxy_async();  // the widened tile for the MMA; the staging reads before its reuse
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(is_k ? b_kf(st) : b_vf(st));
+                    if (j + 1 < n)
+                        issue(j + 1);
+                }
+            }
+        } else {
+            // Warp 8 produces the K tiles, warp 10 the V tiles, each at its own
+            // pace through its ring; lane i < 8 moves the 16-token box i of each
+            // tile. The block-table entry of the next tile is loaded while the
+            // current one waits for its stage.
+            if (lane < 8) {
+                const int box = lane, leader = 0;
+                const unsigned group_mask = 0x000000FFu;
+                const int stages = is_k ? kKStages : kVStages;
+                int gc = 0;  // K (or V) tiles produced by this CTA so far
+                bool go = true;
+                for (int i = 0; go; ++i) {
+                    int u;
+                    if (!take_unit(i, group_mask, lane == leader, u) || u < 0)
+                        break;
+                    Unit w;
+                    unit_of(p, u, w, false);
+                    const int n = max(w.n[0], w.n[1]);
+                    const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
+                    auto lookup = [&](int j) {
+                        const int kt = j * kN + kBoxTokens * box;
+                        return (j < n && kt < w.L) ? __ldg(table + kt / p.block_size) : -1;
+                    };
+                    int next = lookup(0);
+                    for (int j = 0; j < n; ++j, ++gc) {
+                        int phys = next;
+                        next = lookup(j + 1);
+                        const int st = gc % stages;
+                        if (gc >= stages &&
+                            !wait_or_fail(is_k ? b_ke(st) : b_ve(st), ((gc - stages) / stages) & 1)) {
+                            go = false;
+                            break;
+                        }
+                        const int kt = j * kN + kBoxTokens * box;
+                        const int tib = kt % p.block_size;
+                        if (phys >= p.num_blocks || (phys < 0 && kt < w.L)) {
+                            prefill_raise(PA_DEVERR_BLOCK_ID);
+                            phys = p.num_blocks;
+                        }
+                        if (phys < 0)
+                            phys = p.num_blocks;  // past the sequence end: outside the map, zeros
+                        const uint32_t full = is_k ? b_kf(st) : b_vf(st);
+                        if (lane == leader)
+                            mbar_expect_tx(full, kTileBytes);
+                        __syncwarp(group_mask);
+                        const uint32_t dst = (is_k ? sK(st) : sV(st)) + box * (kBoxTokens * 128);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, w.h, tib, phys, is_k ? 0 : 1);
+                    }
                 }
             }
         }
@@ -632,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The K/V tile holding the sequence end (padding slots past it)
             // is zeroed in V by the first tile that reads it.
             const int jp = (w.L % kN) ? w.L / kN : -1;
-            const bool zeroes = jp >= 0 && jp < nx && (x == 0 || jp >= w.n[0]);
+            const bool zeroes = !FP8 && jp >= 0 && jp < nx && (x == 0 || jp >= w.n[0]);
             const bool valid = g < HPC && w.t0[x] + t < w.q_len;
             const int pos = valid ? w.L - w.q_len + w.t0[x] + t : -1;  // last token this row sees
             float m_run = -INFINITY, l_run = 0.f;
@@ -763,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
             uint16_t *out = static_cast<uint16_t *>(p.out) +
                             ((long long)(w.q0 + w.t0[x] + t) * p.num_q_heads + w.h * p.group + w.ht * HPC + g) * kD;
             const uint32_t to = tO(x) + lane_off;
@@ -840,6 +960,22 @@ int encode_kv_map(CUtensorMap *m, const void *kv, int num_blocks, int block_size
     return r == CUDA_SUCCESS ? PA_OK : set_error(PA_ERR_CUDA, "pa_prefill: K/V tensor map (%d)", (int)r);
 }
 
+// An FP8 pool as rank 5 (head_size bytes, kv_heads, block slots, blocks,
+// K|V), box of the 128 codes of one head x 16 slots: 2 KB, 128-byte swizzle.
+int encode_kv_map_fp8(CUtensorMap *m, const void *kv, int num_blocks, int block_size, int num_kv_heads)
+{
+    cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks, 2};
+    cuuint64_t strides[4] = {kD, (cuuint64_t)num_kv_heads * kD, (cuuint64_t)block_size * num_kv_heads * kD,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * kD};
+    cuuint32_t box[5] = {(cuuint32_t)kD, 1, (cuuint32_t)kBoxTokens, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(kv), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : set_error(PA_ERR_CUDA, "pa_prefill_fp8: K/V tensor map (%d)", (int)r);
+}
+
 // Queries as rank 3 (head_size, q_heads, tokens), box of 64 dims x one head x
 // rows_per_head tokens.
 int encode_q_map(CUtensorMap *m, const void *q, int total_q, int num_q_heads, int rows)
@@ -873,41 +1009,43 @@ int prefill_take_device_error(int *bits)
 
 using namespace pa;
 
-extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
-                          int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
-                          int num_seqs, int total_q, int max_seqlen_q, float scale, int num_q_heads,
-                          int num_kv_heads, int head_size, int num_blocks, int block_size, int dtype,
-                          pa_stream_t stream)
+namespace {
+
+int prefill_impl(const char *who, void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
+                 int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
+                 int total_q, int max_seqlen_q, float scale, int num_q_heads, int num_kv_heads, int head_size,
+                 int num_blocks, int block_size, int dtype, bool fp8, float k_scale, float v_scale,
+                 pa_stream_t stream)
 {
     if (dtype != PA_F16 && dtype != PA_BF16)
-        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: dtype %d (want PA_F16 or PA_BF16)", dtype);
+        return set_error(PA_ERR_UNSUPPORTED, "%s: dtype %d (want PA_F16 or PA_BF16)", who, dtype);
     if (head_size != kD)
-        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: head_size %d (built: 128)", head_size);
+        return set_error(PA_ERR_UNSUPPORTED, "%s: head_size %d (built: 128)", who, head_size);
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return set_error(PA_ERR_INVALID_ARG,
-                         "pa_prefill: num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                         "%s: num_q_heads %d must be a positive multiple of num_kv_heads %d", who,
                          num_q_heads, num_kv_heads);
     const int group = num_q_heads / num_kv_heads;
     if (group > 16 && group % 16 != 0)
-        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: query group %d (want <= 16 or a multiple of 16)",
+        return set_error(PA_ERR_UNSUPPORTED, "%s: query group %d (want <= 16 or a multiple of 16)", who,
                          group);
     if (block_size < kBoxTokens || block_size % kBoxTokens != 0)
-        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: block_size %d must be a positive multiple of 16",
+        return set_error(PA_ERR_INVALID_ARG, "%s: block_size %d must be a positive multiple of 16", who,
                          block_size);
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
-        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: bad sizes");
+        return set_error(PA_ERR_INVALID_ARG, "%s: bad sizes", who);
     if ((long long)max_blocks_per_seq * block_size > (1LL << 30))
-        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: max_blocks_per_seq * block_size too large");
+        return set_error(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq * block_size too large", who);
     if (!std::isfinite(scale))
-        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: scale is not finite");
+        return set_error(PA_ERR_INVALID_ARG, "%s: scale is not finite", who);
     if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0)
         return PA_OK;
     if (!out || !query || !kv_cache || !block_tables || !cu_seqlens_q || !seq_lens)
-        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: null pointer argument");
+        return set_error(PA_ERR_INVALID_ARG, "%s: null pointer argument", who);
     if (!aligned16(out) || !aligned16(query) || !aligned16(kv_cache) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3) || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3))
-        return set_error(PA_ERR_INVALID_ARG, "pa_prefill: misaligned pointer (query/out/pool 16 B)");
+        return set_error(PA_ERR_INVALID_ARG, "%s: misaligned pointer (query/out/pool 16 B)", who);
     if (!encoder())
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
 
@@ -929,49 +1067,53 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
     prm.block_size = block_size;
     prm.total_q = total_q;
     prm.max_len = max_blocks_per_seq * block_size;
-    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
+    prm.v_scale = fp8 ? v_scale : 1.f;
     prm.num_kv_heads = num_kv_heads;
     const long long units = (long long)prm.q_pairs * num_seqs * num_kv_heads * prm.head_tiles;
     if (units > 0x7fffffffLL)
-        return set_error(PA_ERR_UNSUPPORTED, "pa_prefill: too many query tiles");
+        return set_error(PA_ERR_UNSUPPORTED, "%s: too many query tiles", who);
     prm.num_units = (int)units;
     static std::atomic<unsigned> launches{0};
     prm.sched_slot = (int)(launches.fetch_add(1u) % (unsigned)kSchedSlots);
 
     CUtensorMap kv_map, q_map;
-    int rc = encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads);
+    int rc = fp8 ? encode_kv_map_fp8(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads)
+                 : encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads);
     if (rc != PA_OK)
         return rc;
     rc = encode_q_map(&q_map, query, total_q, num_q_heads, prm.rows_per_head);
     if (rc != PA_OK)
         return rc;
 
-    const void *fn = dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true>)
-                                      : reinterpret_cast<const void *>(&paged_prefill_kernel<false>);
+    const void *fn = fp8 ? (dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, true>)
+                                             : reinterpret_cast<const void *>(&paged_prefill_kernel<false, true>))
+                         : (dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, false>)
+                                             : reinterpret_cast<const void *>(&paged_prefill_kernel<false, false>));
     // Raise the kernel's shared-memory limit and read the SM count once per
     // device (a call being captured into a CUDA graph then makes no
     // attribute call).
     static std::mutex mu;
-    static bool raised[2][64] = {};
+    static bool raised[4][64] = {};
     static int sm_count[64] = {};
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
-        return set_error(PA_ERR_CUDA, "pa_prefill: cudaGetDevice: %s", cudaGetErrorString(e));
+        return set_error(PA_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
     {
         std::lock_guard<std::mutex> lock(mu);
-        bool &done = raised[dtype == PA_BF16][dev & 63];
+        bool &done = raised[(dtype == PA_BF16) + 2 * fp8][dev & 63];
         if (!done) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess)
-                return set_error(PA_ERR_CUDA, "pa_prefill: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+                return set_error(PA_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", who, cudaGetErrorString(e));
             done = dev < 64;
         }
         sms = dev < 64 ? sm_count[dev] : 0;
         if (sms <= 0) {
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess || sms <= 0)
-                return set_error(PA_ERR_CUDA, "pa_prefill: SM count: %s", cudaGetErrorString(e));
+                return set_error(PA_ERR_CUDA, "%s: SM count: %s", who, cudaGetErrorString(e));
             if (dev < 64)
                 sm_count[dev] = sms;
         }
@@ -982,6 +1124,32 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
     void *args[] = {&kv_map, &q_map, &prm};
     e = cudaLaunchKernel(fn, grid, dim3(kThreads), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
-        return set_error(PA_ERR_CUDA, "pa_prefill: launch: %s", cudaGetErrorString(e));
+        return set_error(PA_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                          int num_seqs, int total_q, int max_seqlen_q, float scale, int num_q_heads,
+                          int num_kv_heads, int head_size, int num_blocks, int block_size, int dtype,
+                          pa_stream_t stream)
+{
+    return prefill_impl("pa_prefill", out, query, kv_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
+                        seq_lens, num_seqs, total_q, max_seqlen_q, scale, num_q_heads, num_kv_heads, head_size,
+                        num_blocks, block_size, dtype, false, 1.f, 1.f, stream);
+}
+
+extern "C" int pa_prefill_fp8(void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                              int num_seqs, int total_q, int max_seqlen_q, float scale, int num_q_heads,
+                              int num_kv_heads, int head_size, int num_blocks, int block_size, int dtype,
+                              float k_scale, float v_scale, pa_stream_t stream)
+{
+    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return set_error(PA_ERR_INVALID_ARG, "pa_prefill_fp8: k_scale and v_scale must be finite and > 0");
+    return prefill_impl("pa_prefill_fp8", out, query, kv_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
+                        seq_lens, num_seqs, total_q, max_seqlen_q, scale, num_q_heads, num_kv_heads, head_size,
+                        num_blocks, block_size, dtype, true, k_scale, v_scale, stream);
 }

@@ -87,6 +87,26 @@ def test_prefill_host_side_validation_without_a_gpu(lib):
     assert call(maxq=0) == binding.PA_OK
 
 
+def test_prefill_fp8_host_side_validation_without_a_gpu(lib):
+    null = None
+    ok_args = dict(maxb=4, S=2, total=10, maxq=8, scale=0.1, hq=8, hkv=2, d=128, nb=16, bs=16, dt=0,
+                   ks=0.02, vs=0.05)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.pa_prefill_fp8(null, null, null, null, a["maxb"], null, null, a["S"], a["total"], a["maxq"],
+                                  a["scale"], a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["dt"], a["ks"],
+                                  a["vs"], null)
+    assert call(ks=0.0) == binding.PA_ERR_INVALID_ARG
+    assert call(vs=float("nan")) == binding.PA_ERR_INVALID_ARG
+    assert call(ks=-1.0) == binding.PA_ERR_INVALID_ARG
+    assert call(d=64) == binding.PA_ERR_UNSUPPORTED
+    assert call(dt=binding.PA_FP8_E4M3) == binding.PA_ERR_UNSUPPORTED  # dtype is the query's type
+    assert call(bs=24) == binding.PA_ERR_INVALID_ARG
+    assert call() == binding.PA_ERR_INVALID_ARG                          # null pointers
+    assert call(S=0) == binding.PA_OK
+
+
 def test_fp8_host_side_validation_without_a_gpu(lib):
     null = None
     args = (null, null, null, null, 1, null, 4, 1.0, 8, 8, 128, 10, 16)
