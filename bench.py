@@ -92,6 +92,7 @@ KERNEL_SOURCES = {
     "decode": ("pa_kernels.cu", "pa_device.cuh"),
     "decode_fp8": ("pa_kernels.cu", "pa_device.cuh"),
     "prefill": ("pa_prefill.cu", "pa_device.cuh"),
+    "prefill_fp8": ("pa_prefill.cu", "pa_device.cuh"),
 }
 
 
@@ -562,7 +563,7 @@ def prefill_config(name, plan):
                   % (2 * int(plan.seq_lens.sum()) * w.num_kv_heads * w.head_size * 2 / 1e6)}
 
 
-def oracle_prefill_sample(name, plan, pool_bits, q_bits, budget_s: float, start: int = 0):
+def oracle_prefill_sample(name, plan, pool_bits, q_bits, budget_s: float, start: int = 0, fp8_scales=None):
     """The oracle on prefill rows (every query head of one chunk row at a
     time, round-robin over rows) for about budget_s. Returns (seconds, flops
     covered, rows, next start)."""
@@ -579,10 +580,16 @@ def oracle_prefill_sample(name, plan, pool_bits, q_bits, budget_s: float, start:
         i = row - int(plan.cu_seqlens_q[s])
         vis = int(plan.seq_lens[s]) - int(plan.chunk_lens[s]) + i + 1
         t0 = time.perf_counter()
-        oracle.decode_sampled(np.zeros(w.num_q_heads, np.int32), heads, q_bits[row:row + 1], pool_bits,
-                              plan.block_tables[s:s + 1], np.array([vis], np.int32), w.scale,
-                              w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks, w.block_size,
-                              w.dtype)
+        if fp8_scales is None:
+            oracle.decode_sampled(np.zeros(w.num_q_heads, np.int32), heads, q_bits[row:row + 1], pool_bits,
+                                  plan.block_tables[s:s + 1], np.array([vis], np.int32), w.scale,
+                                  w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks, w.block_size,
+                                  w.dtype)
+        else:
+            oracle.decode_fp8_sampled(np.zeros(w.num_q_heads, np.int32), heads, q_bits[row:row + 1], pool_bits,
+                                      plan.block_tables[s:s + 1], np.array([vis], np.int32), w.scale,
+                                      w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks,
+                                      w.block_size, w.dtype, *fp8_scales)
         t += time.perf_counter() - t0
         flops += 4 * w.head_size * w.num_q_heads * vis
         n += 1
@@ -600,7 +607,7 @@ def run_prefill(args, rank, local_rank, world):
     w = workloads.PREFILL_WORKLOADS[name]
     seed = args.seed + 1000 * rank
     plan = stepmod.plan_prefill(name, seed)
-    st = stepmod.PrefillStep(name, plan, seed, dev)
+    st = stepmod.PrefillStep(name, plan, seed, dev, args.kv_cache)
     flops = stepmod.prefill_flops(plan, w.num_q_heads, w.head_size)
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
@@ -658,9 +665,10 @@ def run_prefill(args, rank, local_rank, world):
     peak, peak_note = measured_tensor_peak()
     achieved = flops / (pre_ms / 1e3) / 1e12
     value = world * flops * K / t_s / 1e12
-    pool_bits = st.pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    pool_bits = (st.pool.cpu().numpy() if st.fp8 else st.pool.view(torch.int16).cpu().numpy().view(np.uint16))
     q_bits = st.query.view(torch.int16).cpu().numpy().view(np.uint16)
-    ot, of, on, _ = oracle_prefill_sample(name, plan, pool_bits, q_bits, args.cpu_budget)
+    ot, of, on, _ = oracle_prefill_sample(name, plan, pool_bits, q_bits, args.cpu_budget, 0,
+                                          (st.k_scale, st.v_scale) if st.fp8 else None)
     del pool_bits
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -668,11 +676,12 @@ def run_prefill(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
         "data": "synthetic (seeded N(0,1) values, seeded block placement)",
-        "config": prefill_config(name, plan),
+        "config": dict(prefill_config(name, plan), kv_cache="fp8_e4m3" if st.fp8 else "16bit"),
         "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) * K / t_s,
         "prefill_only": {"ms": pre_ms, "tflops": achieved, "sampled_launches": len(ev)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic_record("prefill", name), "kernel": "pa_prefill (paged_prefill_kernel)",
+                     "frac": achieved / peak, "traffic": traffic_record("prefill_fp8" if st.fp8 else "prefill", name),
+                     "kernel": ("pa_prefill_fp8" if st.fp8 else "pa_prefill") + " (paged_prefill_kernel)",
                      "peak_source": peak_note, "flops_per_launch": flops},
         "e2e": {"value": world * flops * ke / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3 / ke},
@@ -888,17 +897,18 @@ def run_prefill_reference(args, rank, world):
     w = workloads.PREFILL_WORKLOADS[name]
     plan = stepmod.plan_prefill(name, args.seed)
     dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
-    st = stepmod.PrefillStep(name, plan, args.seed, dev)
-    pool_bits = st.pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    st = stepmod.PrefillStep(name, plan, args.seed, dev, args.kv_cache)
+    pool_bits = (st.pool.cpu().numpy() if st.fp8 else st.pool.view(torch.int16).cpu().numpy().view(np.uint16))
     q_bits = st.query.view(torch.int16).cpu().numpy().view(np.uint16)
+    scales = (st.k_scale, st.v_scale) if st.fp8 else None
     del st
     per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
     nxt = 0
     for _ in range(args.warmup):
-        _, _, _, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt)
+        _, _, _, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt, scales)
     tt, tf, tn = 0.0, 0, 0
     for _ in range(args.steps):
-        a, b, c, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt)
+        a, b, c, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt, scales)
         tt, tf, tn = tt + a, tf + b, tn + c
     v = tf / tt / 1e12
     sample = f"{tn} query rows x {w.num_q_heads} heads of the {name} batch, about {per_step:.2f} s per step"
@@ -906,7 +916,8 @@ def run_prefill_reference(args, rank, world):
                       "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                       "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True, "scaling": "weak",
                       "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                      "config": prefill_config(name, plan),
+                      "config": dict(prefill_config(name, plan),
+                                     kv_cache="fp8_e4m3" if scales else "16bit"),
                       "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                                        "sample": sample},
                       "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -950,8 +961,6 @@ def main():
             dist.destroy_process_group()
         return
     prefill = args.workload in workloads.PREFILL_WORKLOADS
-    if prefill and args.kv_cache != "16bit":
-        ap.error("--kv-cache fp8 applies to the decode workloads")
     if args.impl == "reference":
         (run_prefill_reference(args, rank, world) if prefill else run_reference(args, rank, world))
     else:

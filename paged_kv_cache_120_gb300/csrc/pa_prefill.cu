@@ -261,7 +261,10 @@ constexpr int kN = 128;                    // cached tokens per K/V tile
 constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
 constexpr int kTileBytes = 2 * kChunkBytes;  // a 128 x 128 16-bit operand: 32 KB
 constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size is a multiple)
-constexpr int kThreads = 384;              // warps 0-3 softmax A, 4-7 softmax B, 8 K, 9 MMA, 10 V, 11 Q
+// Warps 0-3 softmax A, 4-7 softmax B, 8 K, 9 MMA, 10 V, 11 Q; with an FP8
+// cache also 12-15, which widen the codes (8 and 10 then stay idle).
+constexpr int kThreads16 = 384, kThreads8 = 512;
+__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? kThreads8 : kThreads16; }
 constexpr int kWarpK = 8, kWarpMMA = 9, kWarpV = 10, kWarpQ = 11;
 constexpr int kKStagesMax = 3;             // K ring (freed when both tiles' S = Q K^T are done):
 constexpr int kKStages16 = 3, kKStages8 = 2;  // 3 stages, 2 with an FP8 cache (room for staging)
@@ -275,10 +278,15 @@ constexpr int kSmemBytes = 2 * kTileBytes + 3 * kTileBytes + kVStages * kTileByt
 constexpr uint32_t kTmemCols = 512;        // S/P of tiles A and B, then O of A and B, 128 columns each
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
 constexpr int kUnitSlots = 4;              // ring of unit indices handed from the scheduler to every role
-constexpr int kUnitConsumers = 11;         // K, V and MMA warps, 8 softmax warps (one arrival each)
-constexpr int kRegsLaunch = 168;           // registers per thread at launch (384 threads, 1 CTA/SM)
-constexpr int kRegsIO = 120, kRegsSoftmax = 192;
-static_assert(128 * kRegsIO + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
+// Unit consumers (one arrival each): K, V and MMA warps and the 8 softmax
+// warps; with an FP8 cache the 4 widening warps instead of K and V.
+__host__ __device__ constexpr int unit_consumers(bool fp8) { return fp8 ? 13 : 11; }
+// Registers per thread at launch (65536 / threads, one CTA per SM) and the
+// per-warpgroup split; the sum stays within the launch's total.
+constexpr int kRegsSoftmax16 = 192, kRegsIO16 = 120;  // 384 threads, 168 each at launch
+constexpr int kRegsSoftmax8 = 184, kRegsIO8 = 72;     // 512 threads, 128 each (I/O and widening groups)
+static_assert(128 * kRegsIO16 + 256 * kRegsSoftmax16 <= kThreads16 * 168, "register split exceeds the launch");
+static_assert(256 * kRegsIO8 + 256 * kRegsSoftmax8 <= kThreads8 * 128, "register split exceeds the launch");
 
 struct PrefillParams {
     void *out;
@@ -352,7 +360,7 @@ __device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, 
 
 struct PrefillBars {
     uint64_t q_full, q_empty, k_full[kKStagesMax], k_empty[kKStagesMax], v_full[kVStages], v_empty[kVStages];
-    uint64_t stg_full[2];  // FP8 cache: the K / V staging tile has landed
+    uint64_t stg_full[2][2];  // FP8 cache: K / V staging half 0 / 1 has landed
     // Per query tile x: s_full[x] its S is in TMEM, p_full[x] its P is,
     // pv_done[x] its O += P V is done (one phase per K/V tile).
     uint64_t s_full[2], p_full[2], pv_done[2];
@@ -363,7 +371,7 @@ struct PrefillBars {
 };
 
 template <bool BF16, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(FP8), 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap kv_map,
                          const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
 {
@@ -399,11 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(b_q, 1);
         mbar_init(b_qe, 1);
         for (int st = 0; st < kKStages; ++st) {
-            mbar_init(b_kf(st), 1);
+            mbar_init(b_kf(st), FP8 ? 2 : 1);  // FP8: the two widening warps of the tile
             mbar_init(b_ke(st), 1);
         }
         for (int st = 0; st < kVStages; ++st) {
-            mbar_init(b_vf(st), 1);
+            mbar_init(b_vf(st), FP8 ? 2 : 1);
             mbar_init(b_ve(st), 1);
         }
         for (int x = 0; x < 2; ++x) {
@@ -411,11 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_p(x), 128);
             mbar_init(b_pv(x), 1);
         }
-        mbar_init(smem_addr(&bars.stg_full[0]), 1);
-        mbar_init(smem_addr(&bars.stg_full[1]), 1);
+        for (int i = 0; i < 4; ++i)
+            mbar_init(smem_addr(&bars.stg_full[i >> 1][i & 1]), 1);
         for (int i = 0; i < kUnitSlots; ++i) {
             mbar_init(b_uf(i), 1);
-            mbar_init(b_ue(i), kUnitConsumers);
+            mbar_init(b_ue(i), unit_consumers(FP8));
         }
         bars.fail = 0;
         fence_barrier_init();
@@ -458,11 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // Register split, per warpgroup (each of its four warps runs the same
-    // instruction): the K/V/MMA/Q group drops to kRegsIO, the two softmax
-    // groups rise to kRegsSoftmax; the sum stays within the launch's
-    // kThreads x kRegsLaunch.
+    // instruction): the K/V/MMA/Q group (and with an FP8 cache the widening
+    // group) drops to kRegsIO16 / kRegsIO8, the two softmax groups rise to
+    // kRegsSoftmax16 / kRegsSoftmax8; the sum stays within the launch's total.
     if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIO));
+    if constexpr (FP8)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIO8));
+    else
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIO16));
     if (warp == kWarpQ) {
         // ------------------------------------------------------------ Q
         // Scheduler and Q: take the next unit that has queries from the
@@ -500,83 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpK || warp == kWarpV) {
         // ---------------------------------------------------------- K, V
         const bool is_k = warp == kWarpK;
-        if constexpr (FP8) {
-            // FP8 cache: lanes 0-7 bring each tile's 16-token boxes of codes
-            // into a staging tile (TMA, 128-byte swizzle), then the whole warp
-            // widens them, exactly, into the 16-bit ring stage in the MMA's
-            // layout (rows past the sequence end as zeros) and marks the
-            // stage full; the next tile's codes are requested as soon as the
-            // staging tile has been read.
-            const uint32_t stg = base + kOffStage + (is_k ? 0 : kStageBytes8);
-            const uint32_t b_stg = smem_addr(&bars.stg_full[is_k ? 0 : 1]);
-            const int stages = is_k ? kKStages : kVStages;
-            int gc = 0;  // tiles produced by this CTA so far
-            bool go = true;
-            for (int i = 0; go; ++i) {
-                int u;
-                if (!take_unit(i, kFull, lane == 0, u) || u < 0)
-                    break;
-                Unit w;
-                unit_of(p, u, w, false);
-                const int n = max(w.n[0], w.n[1]);
-                const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
-                auto issue = [&](int j) {
-                    if (lane < 8) {
-                        const int kt = j * kN + kBoxTokens * lane;
-                        int phys = kt < w.L ? __ldg(table + kt / p.block_size) : -1;
-                        if (phys >= p.num_blocks || (phys < 0 && kt < w.L)) {
-                            prefill_raise(PA_DEVERR_BLOCK_ID);
-                            phys = p.num_blocks;
-                        }
-                        if (phys < 0)
-                            phys = p.num_blocks;  // past the sequence end: outside the map, zeros
-                        if (lane == 0)
-                            mbar_expect_tx(b_stg, kStageBytes8);
-                        __syncwarp(0xFFu);
-                        tma_load_5d(stg + lane * (kBoxTokens * 128), &kv_map, b_stg, 0, w.h, kt % p.block_size,
-                                    phys, is_k ? 0 : 1);
-                    }
-                };
-                issue(0);
-                for (int j = 0; j < n; ++j, ++gc) {
-                    const int st = gc % stages;
-                    if (!__all_sync(kFull, wait_or_fail(b_stg, gc & 1)) ||
-                        (gc >= stages && !__all_sync(kFull, wait_or_fail(is_k ? b_ke(st) : b_ve(st),
-                                                                         ((gc - stages) / stages) & 1)))) {
-                        go = false;
-                        break;
-                    }
-                    const uint32_t dst = is_k ? sK(st) : sV(st);
-#pragma unroll 1
-                    for (int rr = 0; rr < kN / 32; ++rr) {
-                        const int r = lane + 32 * rr;
-                        const bool pad = j * kN + r >= w.L;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const uint4 c = pad ? make_uint4(0u, 0u, 0u, 0u) : lds128(stg + r * 128 + ((q ^ (r & 7)) << 4));
-                            uint32_t h[8] = {e4m3_pair_lo(c.x), e4m3_pair_hi(c.x), e4m3_pair_lo(c.y), e4m3_pair_hi(c.y),
-                                             e4m3_pair_lo(c.z), e4m3_pair_hi(c.z), e4m3_pair_lo(c.w), e4m3_pair_hi(c.w)};
-                            if constexpr (BF16) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    h[e] = f16x2_to_bf16x2(h[e]);
-                            }
-                            // dims 16q .. 16q + 15: chunk q / 4, 16-byte units 2 (q % 4) and + 1
-                            const uint32_t row = dst + (q >> 2) * kChunkBytes + r * 128;
-                            const int u0 = 2 * (q & 3);
-                            sts128(row + ((u0 ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
-                            sts128(row + (((u0 + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
-                        }
-                    }
-                    fence_proxy_async();  // the widened tile for the MMA; the staging reads before its reuse
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(is_k ? b_kf(st) : b_vf(st));
-                    if (j + 1 < n)
-                        issue(j + 1);
-                }
-            }
-        } else {
+        if constexpr (!FP8) {
             // Warp 8 produces the K tiles, warp 10 the V tiles, each at its own
             // pace through its ring; lane i < 8 moves the 16-token box i of each
             // tile. The block-table entry of the next tile is loaded while the
@@ -626,6 +561,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, w.h, tib, phys, is_k ? 0 : 1);
                     }
                 }
+            }
+        }
+    } else if (FP8 && warp >= 12) {
+        // ------------------------------------------------- FP8 widening
+        // Warps 12-15: K rows 0-63, K rows 64-127, V rows 0-63, V rows
+        // 64-127 of every tile. Lanes 0-3 bring the half tile's four 16-token
+        // boxes of codes into this warp's 8 KB staging buffer (TMA, 128-byte
+        // swizzle); the whole warp widens them, exactly, into the 16-bit ring
+        // stage in the MMA's layout (rows past the sequence end as zeros),
+        // arrives on the stage's full barrier (two arrivals make it full)
+        // and requests its half of the next tile.
+        const int cw = warp - 12, part = cw & 1;
+        const bool is_k = cw < 2;
+        const uint32_t stg = base + kOffStage + cw * (kStageBytes8 / 2);
+        const uint32_t b_stg = smem_addr(&bars.stg_full[cw >> 1][part]);
+        const int stages = is_k ? kKStages : kVStages;
+        int gc = 0;  // tiles produced by this CTA so far
+        bool go = true;
+        for (int i = 0; go; ++i) {
+            int u;
+            if (!take_unit(i, kFull, lane == 0, u) || u < 0)
+                break;
+            Unit w;
+            unit_of(p, u, w, false);
+            const int n = max(w.n[0], w.n[1]);
+            const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
+            auto issue = [&](int j) {
+                if (lane < 4) {
+                    const int kt = j * kN + part * (kN / 2) + kBoxTokens * lane;
+                    int phys = kt < w.L ? __ldg(table + kt / p.block_size) : -1;
+                    if (phys >= p.num_blocks || (phys < 0 && kt < w.L)) {
+                        prefill_raise(PA_DEVERR_BLOCK_ID);
+                        phys = p.num_blocks;
+                    }
+                    if (phys < 0)
+                        phys = p.num_blocks;  // past the sequence end: outside the map, zeros
+                    if (lane == 0)
+                        mbar_expect_tx(b_stg, kStageBytes8 / 2);
+                    __syncwarp(0xFu);
+                    tma_load_5d(stg + lane * (kBoxTokens * 128), &kv_map, b_stg, 0, w.h, kt % p.block_size, phys,
+                                is_k ? 0 : 1);
+                }
+            };
+            issue(0);
+            for (int j = 0; j < n; ++j, ++gc) {
+                const int st = gc % stages;
+                if (!__all_sync(kFull, wait_or_fail(b_stg, gc & 1)) ||
+                    (gc >= stages && !__all_sync(kFull, wait_or_fail(is_k ? b_ke(st) : b_ve(st),
+                                                                     ((gc - stages) / stages) & 1)))) {
+                    go = false;
+                    break;
+                }
+                const uint32_t dst = is_k ? sK(st) : sV(st);
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int rh = lane + 32 * rr;          // row within the half
+                    const int r = part * (kN / 2) + rh;    // row within the tile
+                    const bool pad = j * kN + r >= w.L;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 c = pad ? make_uint4(0u, 0u, 0u, 0u) : lds128(stg + rh * 128 + ((q ^ (rh & 7)) << 4));
+                        uint32_t h[8] = {e4m3_pair_lo(c.x), e4m3_pair_hi(c.x), e4m3_pair_lo(c.y), e4m3_pair_hi(c.y),
+                                         e4m3_pair_lo(c.z), e4m3_pair_hi(c.z), e4m3_pair_lo(c.w), e4m3_pair_hi(c.w)};
+                        if constexpr (BF16) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                h[e] = f16x2_to_bf16x2(h[e]);
+                        }
+                        // dims 16q .. 16q + 15: chunk q / 4, 16-byte units 2 (q % 4) and + 1
+                        const uint32_t row = dst + (q >> 2) * kChunkBytes + r * 128;
+                        const int u0 = 2 * (q & 3);
+                        sts128(row + ((u0 ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+                        sts128(row + (((u0 + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+                    }
+                }
+                fence_proxy_async();  // widened rows for the MMA; staging reads before its reuse
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(is_k ? b_kf(st) : b_vf(st));
+                if (j + 1 < n)
+                    issue(j + 1);
             }
         }
     } else if (warp == kWarpMMA) {
@@ -724,7 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
     } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    if constexpr (FP8)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax8));
+    else
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax16));
     {
         // ---------------------------------------------------- softmax rows
         // Warpgroup x (warps 4x .. 4x + 3) owns query tile x; each thread one
@@ -1122,7 +1141,7 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     // memory), never more CTAs than units.
     const dim3 grid((unsigned)std::min<long long>(units, sms));
     void *args[] = {&kv_map, &q_map, &prm};
-    e = cudaLaunchKernel(fn, grid, dim3(kThreads), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
+    e = cudaLaunchKernel(fn, grid, dim3(threads_for(fp8)), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return set_error(PA_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
     return PA_OK;

@@ -284,12 +284,19 @@ class PrefillStep:
     by slot (pa_reshape_and_cache), then pa_prefill reads the whole causal
     context of every query through the block table."""
 
-    def __init__(self, name: str, plan: PrefillPlan, seed: int, device):
+    def __init__(self, name: str, plan: PrefillPlan, seed: int, device, kv_cache: str = "16bit"):
         import torch
         self.w = w = workloads.PREFILL_WORKLOADS[name]
         total = int(plan.cu_seqlens_q[-1])
-        self.pool = workloads.normal_values(
-            (2, plan.num_blocks, w.block_size, w.num_kv_heads, w.head_size), w.dtype, seed + 20, device)
+        self.fp8 = kv_cache == "fp8"
+        shape = (plan.num_blocks, w.block_size, w.num_kv_heads, w.head_size)
+        if self.fp8:
+            self.k_scale, self.v_scale = workloads.FP8_K_SCALE, workloads.FP8_V_SCALE
+            self.pool = torch.empty((2,) + shape, dtype=torch.uint8, device=device)
+            self.pool[0] = workloads.fp8_codes(shape, self.k_scale, seed + 20, device)
+            self.pool[1] = workloads.fp8_codes(shape, self.v_scale, seed + 24, device)
+        else:
+            self.pool = workloads.normal_values((2,) + shape, w.dtype, seed + 20, device)
         self.query = workloads.normal_values((total, w.num_q_heads, w.head_size), w.dtype, seed + 21, device)
         self.key_new = workloads.normal_values((total, w.num_kv_heads, w.head_size), w.dtype, seed + 22, device)
         self.value_new = workloads.normal_values((total, w.num_kv_heads, w.head_size), w.dtype, seed + 23,
@@ -308,11 +315,20 @@ class PrefillStep:
         self.prefill(stream)
 
     def reshape(self, stream=None) -> None:
-        binding.pa_reshape_and_cache(self.key_new, self.value_new, self.pool, self.slot_mapping, stream)
+        if self.fp8:
+            binding.pa_reshape_and_cache_fp8(self.key_new, self.value_new, self.pool, self.slot_mapping,
+                                             self.k_scale, self.v_scale, stream)
+        else:
+            binding.pa_reshape_and_cache(self.key_new, self.value_new, self.pool, self.slot_mapping, stream)
 
     def prefill(self, stream=None) -> None:
-        binding.pa_prefill(self.out, self.query, self.pool, self.block_tables, self.cu_seqlens_q,
-                           self.seq_lens, self.w.scale, self.max_seqlen_q, stream)
+        if self.fp8:
+            binding.pa_prefill_fp8(self.out, self.query, self.pool, self.block_tables, self.cu_seqlens_q,
+                                   self.seq_lens, self.w.scale, self.max_seqlen_q, self.k_scale, self.v_scale,
+                                   stream)
+        else:
+            binding.pa_prefill(self.out, self.query, self.pool, self.block_tables, self.cu_seqlens_q,
+                               self.seq_lens, self.w.scale, self.max_seqlen_q, stream)
 
     def run_host(self, host: dict, out_host, stream=None) -> None:
         """The step from pinned host buffers (query, key_new, value_new,
