@@ -9,30 +9,31 @@
 // attends to tokens 0..p through the block table, with the online softmax
 // of §4.6.
 //
-// How it is computed (a work unit = 128 query rows of one (sequence, kv
-// head); one persistent CTA per SM walks its share of the units, heaviest
-// first, with its TMA rings and barrier phases running on across units):
-//  * Rows are (query head of the kv head's group, query token) pairs, so the
-//    heads that share a kv head share every K/V tile. A TMEM lane per row.
-//  * Warp 8 loads Q once and the K tiles, warp 10 the V tiles, by TMA
-//    (16-token boxes looked up through the block table, 128-byte swizzle),
-//    into rings of three K and two V stages, each at its own pace. One
-//    thread of warp 9 issues the MMAs: S = Q K^T into one of two TMEM
-//    buffers, then O += P V (V read as an MN-major operand) into a third,
-//    so the next tile's scores overlap this tile's softmax.
-//  * Warps 0-7 run the softmax, two warps per row: warp w and w + 4 share
-//    the TMEM lanes of row quarter w % 4 and take the row's columns 0-63 and
-//    64-127. Each scales and masks its half causally, the two swap partial
-//    maxima through TMEM, and both run the same fp32 online softmax in base
-//    2 (the reference maximum moves only when a score exceeds it by 2^8, so
-//    O in TMEM is rarely rescaled and the next tile's softmax need not wait
-//    for this tile's P V), writing their half of P (rounded to the element
-//    type) to shared memory in the MMA's swizzled layout. Two warps per
-//    row keep two softmax warps issuing on every SM sub-partition. At the
-//    end the partial row sums meet, and each warp divides and stores its
-//    half of O.
-//  * Every wait is bounded; the K/V rows past a sequence's end (padding slots
-//    of its last block, possibly NaN) are zeroed before P V reads them.
+// How it is computed:
+//  * Work units. A unit is two adjacent 128-row query tiles (A and B) of
+//    one (sequence, kv head, head tile); rows are (query head of the group,
+//    query token) pairs, so the heads sharing a kv head, and both tiles,
+//    share every K/V tile. One persistent CTA per SM takes units from a
+//    per-launch counter (warp 11, which also loads each unit's Q) and hands
+//    them to every role through a small ring; TMA rings and barrier phases
+//    run on across units.
+//  * Loads. Warp 8 brings the K tiles and warp 10 the V tiles by TMA
+//    (16-token boxes through the block table, 128-byte swizzle) into rings
+//    of three K and two V stages. With an FP8 cache, warps 12-15 instead
+//    bring the codes into staging buffers and widen them exactly into the
+//    16-bit ring stages (two K stages then).
+//  * Tensor memory holds S_A, S_B, O_A and O_B; P is written over the first
+//    64 columns of its S as 16-bit pairs. One thread of warp 9 issues, per
+//    K/V tile j, O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1)
+//    (tcgen05, P read from tensor memory, V as an MN-major operand), so one
+//    tile's matrix work overlaps the other tile's softmax.
+//  * Softmax. Warpgroup x owns tile x, a full row per thread: read S, mask
+//    causally, row maximum as scale x raw extremum, P = 2^(s scale - ref)
+//    rounded to the element type (the reference maximum moves only when a
+//    score exceeds it by 2^8, so O is rarely rescaled), row sum of the
+//    rounded values, P into tensor memory. At the unit's end, O / l.
+//  * Every wait is bounded; K/V rows past a sequence's end (padding slots,
+//    possibly NaN) are zeroed before P V reads them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
