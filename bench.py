@@ -680,7 +680,8 @@ def run_prefill(args, rank, local_rank, world):
         "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) * K / t_s,
         "prefill_only": {"ms": pre_ms, "tflops": achieved, "sampled_launches": len(ev)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic_record("prefill_fp8" if st.fp8 else "prefill", name),
+                     "frac": achieved / peak, "traffic": traffic_record("prefill_fp8" if st.fp8 else "prefill",
+                                                                    name[len("prefill_"):]),
                      "kernel": ("pa_prefill_fp8" if st.fp8 else "pa_prefill") + " (paged_prefill_kernel)",
                      "peak_source": peak_note, "flops_per_launch": flops},
         "e2e": {"value": world * flops * ke / e2e_s / 1e12, "unit": "TFLOP/s",
