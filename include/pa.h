@@ -272,7 +272,7 @@ int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
  *   total_q        rows of query / out (host int)
  *   max_seqlen_q   host int >= every q_len (sizes the list of work units; larger
  *                  is only slower)
- *   head_size      128; the group num_q_heads / num_kv_heads must be <= 16
+ *   head_size      64 or 128; the group num_q_heads / num_kv_heads must be <= 16
  *                  or a multiple of 16
  * Rows of sequences whose offsets or lengths are inconsistent are not
  * written and set PA_DEVERR_SEQ_LEN; block ids outside the pool read as
@@ -297,7 +297,8 @@ int pa_prefill(void *out, const void *query, const void *kv_cache,
  * query and out (PA_F16 or PA_BF16). The codes are widened exactly to that
  * type on the way to the tensor cores; k_scale joins the score scale and
  * v_scale the final normalisation. Same shapes, limits and error behaviour
- * as pa_prefill; k_scale and v_scale must be finite and > 0.
+ * as pa_prefill, except that head_size must be 128; k_scale and v_scale
+ * must be finite and > 0.
  */
 int pa_prefill_fp8(void *out, const void *query, const void *kv_cache,
                    const int32_t *block_tables, int max_blocks_per_seq,

@@ -256,7 +256,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 
 // ----------------------------------------------------------------- layout
 
-constexpr int kD = 128;                    // head size (the one built)
+constexpr int kD = 128;                    // largest head size built (64 and 128; the FP8 cache: 128)
 constexpr int kM = 128;                    // query rows per tile (TMEM lanes)
 constexpr int kN = 128;                    // cached tokens per K/V tile
 constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
@@ -371,7 +371,7 @@ struct PrefillBars {
     int fail;
 };
 
-template <bool BF16, bool FP8>
+template <bool BF16, bool FP8, int D>
 __global__ void __launch_bounds__(threads_for(FP8), 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap kv_map,
                          const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
@@ -388,6 +388,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     auto sQ = [&](int x) { return base + kOffQ + x * kTileBytes; };
+    static_assert(D == 64 || D == 128, "head size 64 or 128");
+    static_assert(!FP8 || D == 128, "the FP8-cache path is built for head size 128");
+    constexpr int kChunks = D / 64;  // 64-dim, 128-byte-row chunks of a Q/K/V row
     constexpr int kKStages = FP8 ? kKStages8 : kKStages16;
     constexpr int kOffV = kOffK + kKStages * kTileBytes;
     constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // FP8: K then V staging tile
@@ -501,9 +504,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     break;
                 const int head0 = w.h * p.group + w.ht * HPC;
                 const int tiles = w.n[1] > 0 ? 2 : 1;
-                mbar_expect_tx(b_q, (uint32_t)(tiles * 2 * HPC * T * 128));
+                mbar_expect_tx(b_q, (uint32_t)(tiles * kChunks * HPC * T * 128));
                 for (int x = 0; x < tiles; ++x)
-                    for (int c = 0; c < 2; ++c)
+                    for (int c = 0; c < kChunks; ++c)
                         for (int g = 0; g < HPC; ++g)
                             tma_load_3d(sQ(x) + c * kChunkBytes + g * T * 128, &q_map, b_q, c * 64, head0 + g,
                                         w.q0 + w.t0[x]);
@@ -555,10 +558,10 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                             phys = p.num_blocks;  // past the sequence end: outside the map, zeros
                         const uint32_t full = is_k ? b_kf(st) : b_vf(st);
                         if (lane == leader)
-                            mbar_expect_tx(full, kTileBytes);
+                            mbar_expect_tx(full, kChunks * kChunkBytes);
                         __syncwarp(group_mask);
                         const uint32_t dst = (is_k ? sK(st) : sV(st)) + box * (kBoxTokens * 128);
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < kChunks; ++c)
                             tma_load_5d(dst + c * kChunkBytes, &kv_map, full, c * 64, w.h, tib, phys, is_k ? 0 : 1);
                     }
                 }
@@ -654,9 +657,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         // order, so the P V that reads it is done first.
         if (lane == 0) {
             const uint32_t id_s = instr_desc(kM, kN, BF16, false);
-            const uint32_t id_o = instr_desc(kM, kD, BF16, true);
+            const uint32_t id_o = instr_desc(kM, D, BF16, true);
             auto issue_s = [&](int x, int ks) {
-                for (int k = 0; k < kD / 16; ++k) {
+                for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
                     tc_mma(tS(x), smem_desc(sQ(x) + off, 16, 1024), smem_desc(sK(ks) + off, 16, 1024), id_s,
                            k > 0 ? 1u : 0u);
@@ -859,7 +862,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     const uint32_t to = tO(x) + lane_off;
                     float o[32];
 #pragma unroll
-                    for (int c = 0; c < kD / 32; ++c) {
+                    for (int c = 0; c < D / 32; ++c) {
                         tc_ld32(to + c * 32, o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
@@ -881,7 +884,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         break;
                     }
                     if (kb + r >= w.L)
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < kChunks; ++c)
                             for (int i = 0; i < 8; ++i)
                                 sts128(sV(vs) + c * kChunkBytes + r * 128 + i * 16, 0u, 0u, 0u, 0u);
                     fence_proxy_async();
@@ -905,11 +908,11 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
             tc_fence_after();
             const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
             uint16_t *out = static_cast<uint16_t *>(p.out) +
-                            ((long long)(w.q0 + w.t0[x] + t) * p.num_q_heads + w.h * p.group + w.ht * HPC + g) * kD;
+                            ((long long)(w.q0 + w.t0[x] + t) * p.num_q_heads + w.h * p.group + w.ht * HPC + g) * D;
             const uint32_t to = tO(x) + lane_off;
             float o[32];
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 tc_ld32(to + c * 32, o);
                 if (valid) {
 #pragma unroll
@@ -964,14 +967,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
 
 // Pool as rank 5 (head_size, kv_heads, block slots, blocks, K|V), box of 64
 // dims x one head x 16 slots x one block x one of K/V: 2 KB, 128-byte swizzle.
-int encode_kv_map(CUtensorMap *m, const void *kv, int num_blocks, int block_size, int num_kv_heads)
+int encode_kv_map(CUtensorMap *m, const void *kv, int num_blocks, int block_size, int num_kv_heads, int d)
 {
-    const cuuint64_t e = 2;
-    cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
-                          (cuuint64_t)num_blocks, 2};
-    cuuint64_t strides[4] = {kD * e, (cuuint64_t)num_kv_heads * kD * e,
-                             (cuuint64_t)block_size * num_kv_heads * kD * e,
-                             (cuuint64_t)num_blocks * block_size * num_kv_heads * kD * e};
+    const cuuint64_t e = 2, hd = (cuuint64_t)d;
+    cuuint64_t dims[5] = {hd, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size, (cuuint64_t)num_blocks, 2};
+    cuuint64_t strides[4] = {hd * e, (cuuint64_t)num_kv_heads * hd * e,
+                             (cuuint64_t)block_size * num_kv_heads * hd * e,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * hd * e};
     cuuint32_t box[5] = {64, 1, (cuuint32_t)kBoxTokens, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void *>(kv), dims, strides, box,
@@ -998,11 +1000,11 @@ int encode_kv_map_fp8(CUtensorMap *m, const void *kv, int num_blocks, int block_
 
 // Queries as rank 3 (head_size, q_heads, tokens), box of 64 dims x one head x
 // rows_per_head tokens.
-int encode_q_map(CUtensorMap *m, const void *q, int total_q, int num_q_heads, int rows)
+int encode_q_map(CUtensorMap *m, const void *q, int total_q, int num_q_heads, int rows, int d)
 {
-    const cuuint64_t e = 2;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
-    cuuint64_t strides[2] = {kD * e, (cuuint64_t)num_q_heads * kD * e};
+    const cuuint64_t e = 2, hd = (cuuint64_t)d;
+    cuuint64_t dims[3] = {hd, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {hd * e, (cuuint64_t)num_q_heads * hd * e};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(q), dims, strides, box,
@@ -1039,8 +1041,9 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
 {
     if (dtype != PA_F16 && dtype != PA_BF16)
         return set_error(PA_ERR_UNSUPPORTED, "%s: dtype %d (want PA_F16 or PA_BF16)", who, dtype);
-    if (head_size != kD)
-        return set_error(PA_ERR_UNSUPPORTED, "%s: head_size %d (built: 128)", who, head_size);
+    if (head_size != kD && !(head_size == 64 && !fp8))
+        return set_error(PA_ERR_UNSUPPORTED, "%s: head_size %d (built: %s)", who, head_size,
+                         fp8 ? "128" : "64 and 128");
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return set_error(PA_ERR_INVALID_ARG,
                          "%s: num_q_heads %d must be a positive multiple of num_kv_heads %d", who,
@@ -1099,22 +1102,26 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
 
     CUtensorMap kv_map, q_map;
     int rc = fp8 ? encode_kv_map_fp8(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads)
-                 : encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads);
+                 : encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads, head_size);
     if (rc != PA_OK)
         return rc;
-    rc = encode_q_map(&q_map, query, total_q, num_q_heads, prm.rows_per_head);
+    rc = encode_q_map(&q_map, query, total_q, num_q_heads, prm.rows_per_head, head_size);
     if (rc != PA_OK)
         return rc;
 
-    const void *fn = fp8 ? (dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, true>)
-                                             : reinterpret_cast<const void *>(&paged_prefill_kernel<false, true>))
-                         : (dtype == PA_BF16 ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, false>)
-                                             : reinterpret_cast<const void *>(&paged_prefill_kernel<false, false>));
+    const bool bf = dtype == PA_BF16, d64 = head_size == 64;
+    const void *fn =
+        fp8 ? (bf ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 128>)
+                  : reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 128>))
+        : d64 ? (bf ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 64>)
+                    : reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 64>))
+              : (bf ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 128>)
+                    : reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 128>));
     // Raise the kernel's shared-memory limit and read the SM count once per
     // device (a call being captured into a CUDA graph then makes no
     // attribute call).
     static std::mutex mu;
-    static bool raised[4][64] = {};
+    static bool raised[6][64] = {};
     static int sm_count[64] = {};
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1122,7 +1129,7 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
         return set_error(PA_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
     {
         std::lock_guard<std::mutex> lock(mu);
-        bool &done = raised[(dtype == PA_BF16) + 2 * fp8][dev & 63];
+        bool &done = raised[bf + 2 * (fp8 ? 2 : d64 ? 1 : 0)][dev & 63];
         if (!done) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess)

@@ -75,7 +75,8 @@ def test_prefill_host_side_validation_without_a_gpu(lib):
         return lib.pa_prefill(null, null, null, a["bt"], a["maxb"], a["cu"], a["sl"], a["S"], a["total"],
                               a["maxq"], a["scale"], a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["dt"],
                               null)
-    assert call(d=64) == binding.PA_ERR_UNSUPPORTED
+    assert call(d=96) == binding.PA_ERR_UNSUPPORTED
+    assert call(d=64) == binding.PA_ERR_INVALID_ARG              # head size 64 is built: null pointers
     assert call(dt=2) == binding.PA_ERR_UNSUPPORTED
     assert call(hq=40, hkv=2) == binding.PA_ERR_UNSUPPORTED      # group 20
     assert call(hkv=3) == binding.PA_ERR_INVALID_ARG

@@ -219,3 +219,48 @@ def test_prefill_sampled_rows_at_llama13b_shape(dev):
     got = oracle.decode_elems(u16(out), workloads.F16)[rows, hq]
     assert max_abs_err(got, want) <= TOL[workloads.F16]
     assert binding.pa_get_device_error() == 0
+
+
+def test_prefill_replayed_from_a_cuda_graph_is_bit_identical(dev):
+    """The work-unit counter a launch uses is fixed when it is captured; the
+    last CTA of every run resets it, so replays (interleaved with eager
+    launches that use other counters) give the eager outputs bit for bit."""
+    import torch
+    c = PrefillCase(dev, workloads.BF16, 16, 2, 16, [300, 129, 517, 64], [150, 129, 200, 64], seed=77)
+    eager = c.gpu()
+    c.check(eager)
+    ref = eager.clone()
+    out = torch.full_like(c.q, float("nan"))
+    q = c.q.contiguous()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        binding.pa_prefill(out, q, c.pool, c.bt_d, c.cu_d, c.sl_d, c.scale, c.max_q)   # warm-up on s
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        binding.pa_prefill(out, q, c.pool, c.bt_d, c.cu_d, c.sl_d, c.scale, c.max_q)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        again = c.prefill(c.pool, c.bt_d)          # an eager launch between replays
+        assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
+    assert binding.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
+@pytest.mark.parametrize("heads", [(4, 4), (8, 2), (16, 1), (32, 1)])
+def test_prefill_head_size_64(dev, dtype, heads):
+    """Head size 64: one 64-dim chunk per row, four score MMAs per tile,
+    P V with N = 64; same cases as the head-size-128 grid."""
+    Hq, Hkv = heads
+    c = PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=900 + Hq + Hkv + dtype, D=64)
+    c.check(c.gpu())
+
+
+def test_prefill_head_size_64_nan_padding_and_large_blocks(dev):
+    c = PrefillCase(dev, workloads.BF16, 8, 2, 32, [33, 250, 7, 600], [33, 100, 7, 300], seed=93, poison=True, D=64)
+    c.check(c.gpu())
