@@ -297,8 +297,8 @@ int pa_prefill(void *out, const void *query, const void *kv_cache,
  * query and out (PA_F16 or PA_BF16). The codes are widened exactly to that
  * type on the way to the tensor cores; k_scale joins the score scale and
  * v_scale the final normalisation. Same shapes, limits and error behaviour
- * as pa_prefill, except that head_size must be 128; k_scale and v_scale
- * must be finite and > 0.
+ * as pa_prefill (head_size 64 or 128); k_scale and v_scale must be finite
+ * and > 0.
  */
 int pa_prefill_fp8(void *out, const void *query, const void *kv_cache,
                    const int32_t *block_tables, int max_blocks_per_seq,

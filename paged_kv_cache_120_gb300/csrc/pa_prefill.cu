@@ -256,7 +256,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 
 // ----------------------------------------------------------------- layout
 
-constexpr int kD = 128;                    // largest head size built (64 and 128; the FP8 cache: 128)
+constexpr int kD = 128;                    // largest head size built (64 and 128)
 constexpr int kM = 128;                    // query rows per tile (TMEM lanes)
 constexpr int kN = 128;                    // cached tokens per K/V tile
 constexpr int kChunkBytes = 128 * 128;     // a 64-column, 128-row swizzled chunk: 16 KB
@@ -389,7 +389,6 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     auto sQ = [&](int x) { return base + kOffQ + x * kTileBytes; };
     static_assert(D == 64 || D == 128, "head size 64 or 128");
-    static_assert(!FP8 || D == 128, "the FP8-cache path is built for head size 128");
     constexpr int kChunks = D / 64;  // 64-dim, 128-byte-row chunks of a Q/K/V row
     constexpr int kKStages = FP8 ? kKStages8 : kKStages16;
     constexpr int kOffV = kOffK + kKStages * kTileBytes;
@@ -571,8 +570,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         // ------------------------------------------------- FP8 widening
         // Warps 12-15: K rows 0-63, K rows 64-127, V rows 0-63, V rows
         // 64-127 of every tile. Lanes 0-3 bring the half tile's four 16-token
-        // boxes of codes into this warp's 8 KB staging buffer (TMA, 128-byte
-        // swizzle); the whole warp widens them, exactly, into the 16-bit ring
+        // boxes of codes into this warp's staging buffer (TMA; 128-byte rows
+        // with the 128-byte swizzle at head size 128, plain 64-byte rows at
+        // 64); the whole warp widens them, exactly, into the 16-bit ring
         // stage in the MMA's layout (rows past the sequence end as zeros),
         // arrives on the stage's full barrier (two arrivals make it full)
         // and requests its half of the next tile.
@@ -602,9 +602,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     if (phys < 0)
                         phys = p.num_blocks;  // past the sequence end: outside the map, zeros
                     if (lane == 0)
-                        mbar_expect_tx(b_stg, kStageBytes8 / 2);
+                        mbar_expect_tx(b_stg, (kN / 2) * D);
                     __syncwarp(0xFu);
-                    tma_load_5d(stg + lane * (kBoxTokens * 128), &kv_map, b_stg, 0, w.h, kt % p.block_size, phys,
+                    tma_load_5d(stg + lane * (kBoxTokens * D), &kv_map, b_stg, 0, w.h, kt % p.block_size, phys,
                                 is_k ? 0 : 1);
                 }
             };
@@ -624,8 +624,18 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     const int r = part * (kN / 2) + rh;    // row within the tile
                     const bool pad = j * kN + r >= w.L;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 c = pad ? make_uint4(0u, 0u, 0u, 0u) : lds128(stg + rh * 128 + ((q ^ (rh & 7)) << 4));
+                    for (int qi = 0; qi < D / 16; ++qi) {
+                        // The 16-byte unit q of codes (dims 16q .. 16q + 15).
+                        // At head size 64 the rows are 64 bytes, unswizzled:
+                        // lane pairs take the units in the order q = qi ^ h(a),
+                        // a = (row / 2) % 4, h = multiplication by a generator
+                        // of GF(4) (0, 2, 3, 1), so that both h(a) and
+                        // h(a) ^ a run over all four units and neither these
+                        // loads nor the swizzled stores below meet a bank
+                        // conflict within a quarter warp.
+                        const int q = D == 128 ? qi : qi ^ ((0x78 >> (2 * ((rh >> 1) & 3))) & 3);
+                        const uint32_t src = D == 128 ? stg + rh * 128 + ((q ^ (rh & 7)) << 4) : stg + rh * 64 + (q << 4);
+                        const uint4 c = pad ? make_uint4(0u, 0u, 0u, 0u) : lds128(src);
                         uint32_t h[8] = {e4m3_pair_lo(c.x), e4m3_pair_hi(c.x), e4m3_pair_lo(c.y), e4m3_pair_hi(c.y),
                                          e4m3_pair_lo(c.z), e4m3_pair_hi(c.z), e4m3_pair_lo(c.w), e4m3_pair_hi(c.w)};
                         if constexpr (BF16) {
@@ -983,17 +993,19 @@ int encode_kv_map(CUtensorMap *m, const void *kv, int num_blocks, int block_size
 }
 
 // An FP8 pool as rank 5 (head_size bytes, kv_heads, block slots, blocks,
-// K|V), box of the 128 codes of one head x 16 slots: 2 KB, 128-byte swizzle.
-int encode_kv_map_fp8(CUtensorMap *m, const void *kv, int num_blocks, int block_size, int num_kv_heads)
+// K|V), box of the d codes of one head x 16 slots: 128-byte rows with the
+// 128-byte swizzle at d = 128 (2 KB), plain 64-byte rows at d = 64 (1 KB).
+int encode_kv_map_fp8(CUtensorMap *m, const void *kv, int num_blocks, int block_size, int num_kv_heads, int d)
 {
-    cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
-                          (cuuint64_t)num_blocks, 2};
-    cuuint64_t strides[4] = {kD, (cuuint64_t)num_kv_heads * kD, (cuuint64_t)block_size * num_kv_heads * kD,
-                             (cuuint64_t)num_blocks * block_size * num_kv_heads * kD};
-    cuuint32_t box[5] = {(cuuint32_t)kD, 1, (cuuint32_t)kBoxTokens, 1, 1};
+    const cuuint64_t hd = (cuuint64_t)d;
+    cuuint64_t dims[5] = {hd, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size, (cuuint64_t)num_blocks, 2};
+    cuuint64_t strides[4] = {hd, (cuuint64_t)num_kv_heads * hd, (cuuint64_t)block_size * num_kv_heads * hd,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * hd};
+    cuuint32_t box[5] = {(cuuint32_t)d, 1, (cuuint32_t)kBoxTokens, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(kv), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           d == kD ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : set_error(PA_ERR_CUDA, "pa_prefill_fp8: K/V tensor map (%d)", (int)r);
 }
@@ -1041,9 +1053,8 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
 {
     if (dtype != PA_F16 && dtype != PA_BF16)
         return set_error(PA_ERR_UNSUPPORTED, "%s: dtype %d (want PA_F16 or PA_BF16)", who, dtype);
-    if (head_size != kD && !(head_size == 64 && !fp8))
-        return set_error(PA_ERR_UNSUPPORTED, "%s: head_size %d (built: %s)", who, head_size,
-                         fp8 ? "128" : "64 and 128");
+    if (head_size != kD && head_size != 64)
+        return set_error(PA_ERR_UNSUPPORTED, "%s: head_size %d (built: 64 and 128)", who, head_size);
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return set_error(PA_ERR_INVALID_ARG,
                          "%s: num_q_heads %d must be a positive multiple of num_kv_heads %d", who,
@@ -1101,7 +1112,7 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     prm.sched_slot = (int)(launches.fetch_add(1u) % (unsigned)kSchedSlots);
 
     CUtensorMap kv_map, q_map;
-    int rc = fp8 ? encode_kv_map_fp8(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads)
+    int rc = fp8 ? encode_kv_map_fp8(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads, head_size)
                  : encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads, head_size);
     if (rc != PA_OK)
         return rc;
@@ -1110,18 +1121,23 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
         return rc;
 
     const bool bf = dtype == PA_BF16, d64 = head_size == 64;
-    const void *fn =
-        fp8 ? (bf ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 128>)
-                  : reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 128>))
-        : d64 ? (bf ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 64>)
-                    : reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 64>))
-              : (bf ? reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 128>)
-                    : reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 128>));
+    // Instances by (FP8 cache, head size 64, bf16).
+    static const void *const kernels[8] = {
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 128>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 128>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 64>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 64>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 128>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 128>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 64>),
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 64>)};
+    const int variant = (fp8 ? 4 : 0) + (d64 ? 2 : 0) + (bf ? 1 : 0);
+    const void *fn = kernels[variant];
     // Raise the kernel's shared-memory limit and read the SM count once per
     // device (a call being captured into a CUDA graph then makes no
     // attribute call).
     static std::mutex mu;
-    static bool raised[6][64] = {};
+    static bool raised[8][64] = {};
     static int sm_count[64] = {};
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1129,7 +1145,7 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
         return set_error(PA_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
     {
         std::lock_guard<std::mutex> lock(mu);
-        bool &done = raised[bf + 2 * (fp8 ? 2 : d64 ? 1 : 0)][dev & 63];
+        bool &done = raised[variant][dev & 63];
         if (!done) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess)

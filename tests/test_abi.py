@@ -101,7 +101,8 @@ def test_prefill_fp8_host_side_validation_without_a_gpu(lib):
     assert call(ks=0.0) == binding.PA_ERR_INVALID_ARG
     assert call(vs=float("nan")) == binding.PA_ERR_INVALID_ARG
     assert call(ks=-1.0) == binding.PA_ERR_INVALID_ARG
-    assert call(d=64) == binding.PA_ERR_UNSUPPORTED
+    assert call(d=96) == binding.PA_ERR_UNSUPPORTED
+    assert call(d=64) == binding.PA_ERR_INVALID_ARG                      # built; null pointers
     assert call(dt=binding.PA_FP8_E4M3) == binding.PA_ERR_UNSUPPORTED  # dtype is the query's type
     assert call(bs=24) == binding.PA_ERR_INVALID_ARG
     assert call() == binding.PA_ERR_INVALID_ARG                          # null pointers

@@ -42,9 +42,8 @@ class Fp8PrefillCase:
     """As the 16-bit prefill case, on a byte pool: the prefix is E4M3 codes of
     N(0,1)-sized values, the chunk's K/V go in by pa_reshape_and_cache_fp8."""
 
-    def __init__(self, dev, dtype, Hq, Hkv, B, ctx, qlen, seed, spare=8, poison=False, ks=KS, vs=VS):
+    def __init__(self, dev, dtype, Hq, Hkv, B, ctx, qlen, seed, spare=8, poison=False, ks=KS, vs=VS, D=128):
         import torch
-        D = 128
         self.dtype, self.Hq, self.Hkv, self.B, self.D, self.ks, self.vs = dtype, Hq, Hkv, B, D, ks, vs
         self.scale = 1.0 / math.sqrt(D)
         rng = np.random.default_rng(seed)
@@ -186,3 +185,19 @@ def test_prefill_fp8_llama13b_shaped_batch_sampled(dev):
                                          c.B, c.dtype, c.ks, c.vs)
         assert max_abs_err(got[r, heads], want) <= TOL[c.dtype], f"row {r}"
     assert binding.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
+@pytest.mark.parametrize("heads", [(4, 4), (8, 2), (16, 1), (12, 3)])
+def test_prefill_fp8_head_size_64(dev, dtype, heads):
+    """Head size 64 over an FP8 cache: 64-byte code rows staged without a
+    swizzle and widened into one 64-dim chunk per row."""
+    Hq, Hkv = heads
+    c = Fp8PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=950 + Hq + Hkv + dtype, D=64)
+    c.check(c.gpu())
+
+
+def test_prefill_fp8_head_size_64_nan_padding_and_large_blocks(dev):
+    c = Fp8PrefillCase(dev, workloads.BF16, 8, 2, 32, [33, 250, 7, 600], [33, 100, 7, 300], seed=97,
+                       poison=True, D=64)
+    c.check(c.gpu())
