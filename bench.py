@@ -389,24 +389,21 @@ def run_ours(args, rank, local_rank, world):
     if dev_err:
         raise RuntimeError(f"device error word {dev_err} set during the timed region")
 
-    # End to end through the public step API with pinned host buffers.
-    host = {n: t.cpu().pin_memory() for n, t in
-            (("query", st.query), ("key_new", st.key_new), ("value_new", st.value_new),
-             ("slot_mapping", st.slot_mapping), ("block_tables", st.block_tables),
-             ("seq_lens", st.seq_lens))}
-    if st.cow_pairs is not None:
-        host["cow_pairs"] = st.cow_pairs.cpu().pin_memory()
-    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    # End to end through the public step API from pinned host memory: every
+    # step copies all of its inputs (one packed buffer) to the device, runs
+    # the libpa calls and reads the output back before the next step starts.
+    host = st.pin_host()
+    out_host = host.pop("out")
+    h2d = st.pinned_bytes()
     d2h = out_host.numel() * out_host.element_size()
     for _ in range(3):
-        st.run_host(host, out_host)
+        st.run_pinned()
     dist_barrier(world, dev)
     torch.cuda.synchronize(dev)
     ke = max(1, min(K, 500))
     t0 = time.perf_counter()
     for _ in range(ke):
-        st.run_host(host, out_host)
+        st.run_pinned()
     e2e_s = time.perf_counter() - t0
     e2e_s = dist_max(e2e_s, world, dev)
     dist_barrier(world, dev)
@@ -645,19 +642,20 @@ def run_prefill(args, rank, local_rank, world):
     if dev_err:
         raise RuntimeError(f"device error word {dev_err} set during the timed region")
 
-    host = {n: getattr(st, n).cpu().pin_memory() for n in
-            ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens", "cu_seqlens_q")}
-    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    # End to end from pinned host memory, as for decode: every step copies
+    # its packed inputs in and its output back.
+    host = st.pin_host()
+    out_host = host.pop("out")
+    h2d = st.pinned_bytes()
     d2h = out_host.numel() * out_host.element_size()
     for _ in range(3):
-        st.run_host(host, out_host)
+        st.run_pinned()
     dist_barrier(world, dev)
     torch.cuda.synchronize(dev)
     ke = max(1, min(K, 200))
     t0 = time.perf_counter()
     for _ in range(ke):
-        st.run_host(host, out_host)
+        st.run_pinned()
     e2e_s = dist_max(time.perf_counter() - t0, world, dev)
     dist_barrier(world, dev)
     if rank != 0:

@@ -101,7 +101,75 @@ def plan_step(name: str, seed: int, variant: str = "literal") -> StepPlan:
     return _finish(alloc, ids, slots, pairs, w.block_size)
 
 
-class DecodeStep:
+class PinnedHostStep:
+    """A step that can run from one packed pinned host buffer. The class
+    names its device inputs in ``_INPUTS`` and runs its libpa calls in
+    ``run()``; ``out`` is its output tensor."""
+
+    def pin_host(self) -> dict:
+        """Stage the step's inputs through one packed pinned host buffer.
+
+        The step's device inputs become views of one device buffer, and the
+        returned dict holds pinned host views of the same layout, filled with
+        the current inputs, plus a pinned ``out``. A caller writes the next
+        step's inputs into those views and calls run_pinned(). The libpa calls
+        are then replayed from a CUDA graph recorded on the first
+        run_pinned(), which holds this batch's launch configuration: call
+        pin_host() again when the batch's shape or lengths change."""
+        import torch
+        names = [n for n in self._INPUTS if getattr(self, n, None) is not None]
+        offs, size = {}, 0
+        for n in names:
+            t = getattr(self, n)
+            size = (size + 255) & ~255
+            offs[n] = size
+            size += t.numel() * t.element_size()
+        dev_buf = torch.empty(size, dtype=torch.uint8, device=self.out.device)
+        host_buf = torch.empty(size, dtype=torch.uint8).pin_memory()
+        views = {}
+        for n in names:
+            t = getattr(self, n)
+            nbytes = t.numel() * t.element_size()
+            d = dev_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+            d.copy_(t)
+            setattr(self, n, d)
+            views[n] = host_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+            views[n].copy_(t)
+        views["out"] = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        torch.cuda.synchronize(self.out.device)
+        self._pinned = (host_buf, dev_buf, views["out"])
+        self._pinned_graph = None
+        return views
+
+    def pinned_bytes(self) -> int:
+        """Bytes one run_pinned() copies to the device (the packed inputs)."""
+        return self._pinned[0].numel()
+
+    def run_pinned(self) -> None:
+        """One step from the buffers of pin_host(): one host-to-device copy
+        of the packed inputs, the step's libpa calls (graph replay), one
+        device-to-host copy of the output; returns once the output is on the
+        host."""
+        import torch
+        host_buf, dev_buf, out_host = self._pinned
+        if self._pinned_graph is None:
+            self.run()  # first calls set up kernel attributes and tensor maps
+            torch.cuda.synchronize(self.out.device)
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                    self.run()
+            torch.cuda.current_stream().wait_stream(s)
+            self._pinned_graph = g
+        dev_buf.copy_(host_buf, non_blocking=True)
+        self._pinned_graph.replay()
+        out_host.copy_(self.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+
+class DecodeStep(PinnedHostStep):
     """Device buffers of one step and the three libpa calls that run it."""
 
     def __init__(self, name: str, plan: StepPlan, pool, query, key_new, value_new, device,
@@ -157,6 +225,8 @@ class DecodeStep:
         self.run(stream)
         out_host.copy_(self.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
+
+    _INPUTS = ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens", "cow_pairs")
 
     def decode(self, stream=None) -> None:
         if self.fp8:
@@ -279,7 +349,7 @@ def plan_prefill(name: str, seed: int) -> PrefillPlan:
                        allocator=alloc)
 
 
-class PrefillStep:
+class PrefillStep(PinnedHostStep):
     """Device buffers of one chunked-prefill step: the chunk's K/V are written
     by slot (pa_reshape_and_cache), then pa_prefill reads the whole causal
     context of every query through the block table."""
@@ -306,6 +376,8 @@ class PrefillStep:
         self.cu_seqlens_q, self.slot_mapping = t(plan.cu_seqlens_q), t(plan.slot_mapping)
         self.max_seqlen_q = int(plan.chunk_lens.max())
         self.out = torch.empty_like(self.query)
+
+    _INPUTS = ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens", "cu_seqlens_q")
 
     def launches_per_step(self) -> int:
         return 2  # reshape_and_cache + prefill

@@ -111,3 +111,55 @@ def test_model_step_over_layer_pools_and_graph_replay(dev, name, variant, kv):
     for a, p in zip(pools_after, ms.pools):
         assert torch.equal(a.view(torch.uint8) if fp8 else a.view(torch.int16),
                            p.view(torch.uint8) if fp8 else p.view(torch.int16))
+
+
+@pytest.mark.parametrize("name,variant", [("llama13b", "literal"), ("prefix_cow", "fork")])
+def test_pinned_host_step_matches_the_eager_step(dev, name, variant):
+    """The packed pinned-host path (one copy each way, the libpa calls
+    replayed from a CUDA graph) leaves the pool and the output bit for bit
+    as the eager step does, and a new query written into the host view is
+    the one the next step attends with."""
+    import torch
+    w = workloads.WORKLOADS[name]
+    plan = step.plan_step(name, 3, variant)
+    pool, q, k, v = step.make_device_inputs(name, plan, 3, dev)
+    eager = step.DecodeStep(name, plan, pool.clone(), q.clone(), k.clone(), v.clone(), dev)
+    pinned = step.DecodeStep(name, plan, pool, q, k, v, dev)
+    host = pinned.pin_host()
+    out = host.pop("out")
+    assert pinned.pinned_bytes() >= sum(t.numel() * t.element_size() for t in host.values())
+    eager.run()
+    pinned.run_pinned()
+    assert torch.equal(out.view(torch.int16), eager.out.cpu().view(torch.int16))
+    assert torch.equal(pinned.pool.view(torch.int16), eager.pool.view(torch.int16))
+    first = out.clone()
+    q2 = workloads.normal_values(tuple(q.shape), w.dtype, 77, dev)
+    eager.query.copy_(q2)
+    host["query"].copy_(q2.cpu())
+    eager.run()
+    pinned.run_pinned()
+    assert torch.equal(out.view(torch.int16), eager.out.cpu().view(torch.int16))
+    assert not torch.equal(out.view(torch.int16), first.view(torch.int16))
+    assert binding.pa_get_device_error() == 0
+
+
+def test_host_step_paths_agree_for_prefill(dev):
+    """The chunked-prefill step (GQA-8B shapes, 8 x 1024-token chunks) gives
+    the same output bits eagerly, from separate pinned host tensors
+    (run_host) and from the packed pinned buffer (run_pinned)."""
+    import torch
+    plan = step.plan_prefill("prefill_gqa8b", 5)
+    st = step.PrefillStep("prefill_gqa8b", plan, 5, dev)
+    loose = {n: getattr(st, n).cpu().pin_memory() for n in st._INPUTS}
+    st.run()
+    torch.cuda.synchronize()
+    want = st.out.cpu().view(torch.int16).clone()
+    out_loose = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    st.run_host(loose, out_loose)
+    assert torch.equal(out_loose.view(torch.int16), want)
+    host = st.pin_host()
+    out = host.pop("out")
+    st.run_pinned()
+    st.run_pinned()
+    assert torch.equal(out.view(torch.int16), want)
+    assert binding.pa_get_device_error() == 0
