@@ -264,3 +264,56 @@ def test_prefill_head_size_64(dev, dtype, heads):
 def test_prefill_head_size_64_nan_padding_and_large_blocks(dev):
     c = PrefillCase(dev, workloads.BF16, 8, 2, 32, [33, 250, 7, 600], [33, 100, 7, 300], seed=93, poison=True, D=64)
     c.check(c.gpu())
+
+
+@pytest.mark.parametrize("kv", ["16bit", "fp8"])
+@pytest.mark.parametrize("name", ["prefill_llama13b", "prefill_gqa8b"])
+def test_prefill_workload_full_size(dev, name, kv):
+    """The prefill step bench.py times (same plan, seed and launch: 8 x
+    1024-token chunks after seeded prefixes), run once: the allocator's plan
+    against the block-manager model, the chunk's K/V writes bit-exact against
+    the oracle over the whole pool, and 96 sampled (row, head) outputs, the
+    last row of every chunk among them, against the oracle's decode over the
+    row's causal prefix."""
+    import torch
+    from paged_kv_cache_120_gb300 import step
+    w = workloads.PREFILL_WORKLOADS[name]
+    seed = 0
+    plan = step.plan_prefill(name, seed)
+    model = BlockManagerModel(plan.num_blocks, w.block_size, workloads.free_order(plan.num_blocks, seed))
+    pref = workloads.prefill_prefixes(name, seed)
+    ids = [model.add_seq(int(p)) for p in pref]
+    slots = [model.append_token(sid)[0] for sid in ids for _ in range(w.chunk)]
+    assert np.array_equal(np.asarray(slots, np.int32), plan.slot_mapping)
+    for k, sid in enumerate(ids):
+        t = model.table(sid)
+        assert list(plan.block_tables[k, :len(t)]) == list(t)
+    st = step.PrefillStep(name, plan, seed, dev, kv)
+    fp8 = kv == "fp8"
+    pool_bits = st.pool.cpu().numpy().copy() if fp8 else u16(st.pool).copy()
+    k_bits, v_bits, q_bits = u16(st.key_new), u16(st.value_new), u16(st.query)
+    st.run()
+    torch.cuda.synchronize()
+    assert binding.pa_get_device_error() == 0
+    geo = (plan.num_blocks, w.block_size, w.num_kv_heads, w.head_size)
+    if fp8:
+        n = oracle.reshape_and_cache_fp8(k_bits, v_bits, pool_bits, plan.slot_mapping, *geo, w.dtype,
+                                         st.k_scale, st.v_scale)
+        assert np.array_equal(st.pool.cpu().numpy(), pool_bits)
+    else:
+        n = oracle.reshape_and_cache(k_bits, v_bits, pool_bits, plan.slot_mapping, *geo)
+        assert np.array_equal(u16(st.pool), pool_bits)
+    assert n == len(plan.slot_mapping)
+    rng = np.random.default_rng(11)
+    S, m = len(pref), 96
+    s = rng.integers(0, S, size=m)
+    i = rng.integers(0, w.chunk, size=m)
+    s[:S], i[:S] = np.arange(S), w.chunk - 1
+    hq = rng.integers(0, w.num_q_heads, size=m).astype(np.int32)
+    rows = plan.cu_seqlens_q[s] + i
+    vis = (plan.seq_lens[s] - w.chunk + i + 1).astype(np.int32)
+    args = (np.arange(m, dtype=np.int32), hq, q_bits[rows], pool_bits, plan.block_tables[s], vis, w.scale,
+            w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks, w.block_size, w.dtype)
+    want = (oracle.decode_fp8_sampled(*args, st.k_scale, st.v_scale) if fp8 else oracle.decode_sampled(*args))
+    got = oracle.decode_elems(u16(st.out)[rows, hq], w.dtype)
+    assert max_abs_err(got, want) <= TOL[w.dtype]
