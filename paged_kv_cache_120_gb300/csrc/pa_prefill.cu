@@ -20,8 +20,10 @@
 //  * Loads. Warp 8 brings the K tiles and warp 10 the V tiles by TMA
 //    (16-token boxes through the block table, 128-byte swizzle) into rings
 //    of three K and two V stages. With an FP8 cache, warps 12-15 instead
-//    bring the codes into staging buffers and widen them exactly into the
-//    16-bit ring stages (two K stages then).
+//    bring the codes into staging buffers and widen them exactly into fp16
+//    ring stages (two K stages then); the MMAs then run in fp16, and bf16
+//    queries are moved to fp16 row by row under a power-of-two scale that
+//    joins the row's score factor.
 //  * Tensor memory holds S_A, S_B, O_A and O_B; P is written over the first
 //    64 columns of its S as 16-bit pairs. One thread of warp 9 issues, per
 //    K/V tile j, O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1)
@@ -45,6 +47,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/pa.h"
 #include "pa_device.cuh"
@@ -186,15 +189,6 @@ __device__ __forceinline__ uint32_t e4m3_pair_hi(uint32_t x)
     uint32_t d;
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(d) : "r"(x));
     return d;
-}
-
-// An fp16 pair holding E4M3 values to the same values as a bf16 pair (exact:
-// three mantissa bits and exponents within bf16's range).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h)
-{
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    const __nv_bfloat162 b = __float22bfloat162_rn(f);
-    return *reinterpret_cast<const uint32_t *>(&b);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
@@ -361,6 +355,7 @@ __device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, 
 
 struct PrefillBars {
     uint64_t q_full, q_empty, k_full[kKStagesMax], k_empty[kKStagesMax], v_full[kVStages], v_empty[kVStages];
+    uint64_t q_ready;  // FP8 cache, bf16 queries: the softmax threads have moved Q to fp16
     uint64_t stg_full[2][2];  // FP8 cache: K / V staging half 0 / 1 has landed
     // Per query tile x: s_full[x] its S is in TMEM, p_full[x] its P is,
     // pv_done[x] its O += P V is done (one phase per K/V tile).
@@ -390,12 +385,18 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     auto sQ = [&](int x) { return base + kOffQ + x * kTileBytes; };
     static_assert(D == 64 || D == 128, "head size 64 or 128");
     constexpr int kChunks = D / 64;  // 64-dim, 128-byte-row chunks of a Q/K/V row
+    // The MMAs' element type: the query type, except over an FP8 cache, where
+    // the codes widen to fp16 in one instruction per pair and bf16 queries
+    // are moved to fp16 (kQToF16) by the softmax threads, row by row.
+    constexpr bool kMmaBF16 = BF16 && !FP8;
+    constexpr bool kQToF16 = BF16 && FP8;
     constexpr int kKStages = FP8 ? kKStages8 : kKStages16;
     constexpr int kOffV = kOffK + kKStages * kTileBytes;
     constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // FP8: K then V staging tile
     auto sK = [&](int st) { return base + kOffK + st * kTileBytes; };
     auto sV = [&](int st) { return base + kOffV + st * kTileBytes; };
     const uint32_t b_q = smem_addr(&bars.q_full), b_qe = smem_addr(&bars.q_empty);
+    const uint32_t b_qr = smem_addr(&bars.q_ready);
     auto b_kf = [&](int st) { return smem_addr(&bars.k_full[st]); };
     auto b_ke = [&](int st) { return smem_addr(&bars.k_empty[st]); };
     auto b_vf = [&](int st) { return smem_addr(&bars.v_full[st]); };
@@ -408,6 +409,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
 
     if (tid == 0) {
         mbar_init(b_q, 1);
+        mbar_init(b_qr, 256);  // the 8 softmax warps
         mbar_init(b_qe, 1);
         for (int st = 0; st < kKStages; ++st) {
             mbar_init(b_kf(st), FP8 ? 2 : 1);  // FP8: the two widening warps of the tile
@@ -636,13 +638,11 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         const int q = D == 128 ? qi : qi ^ ((0x78 >> (2 * ((rh >> 1) & 3))) & 3);
                         const uint32_t src = D == 128 ? stg + rh * 128 + ((q ^ (rh & 7)) << 4) : stg + rh * 64 + (q << 4);
                         const uint4 c = pad ? make_uint4(0u, 0u, 0u, 0u) : lds128(src);
-                        uint32_t h[8] = {e4m3_pair_lo(c.x), e4m3_pair_hi(c.x), e4m3_pair_lo(c.y), e4m3_pair_hi(c.y),
-                                         e4m3_pair_lo(c.z), e4m3_pair_hi(c.z), e4m3_pair_lo(c.w), e4m3_pair_hi(c.w)};
-                        if constexpr (BF16) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                h[e] = f16x2_to_bf16x2(h[e]);
-                        }
+                        // fp16 whatever the query type: the MMAs of the FP8
+                        // path run in fp16 (bf16 queries are moved to fp16).
+                        const uint32_t h[8] = {e4m3_pair_lo(c.x), e4m3_pair_hi(c.x), e4m3_pair_lo(c.y),
+                                               e4m3_pair_hi(c.y), e4m3_pair_lo(c.z), e4m3_pair_hi(c.z),
+                                               e4m3_pair_lo(c.w), e4m3_pair_hi(c.w)};
                         // dims 16q .. 16q + 15: chunk q / 4, 16-byte units 2 (q % 4) and + 1
                         const uint32_t row = dst + (q >> 2) * kChunkBytes + r * 128;
                         const int u0 = 2 * (q & 3);
@@ -666,8 +666,8 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         // runs. S_x(j + 1) overwrites P_x(j) in TMEM: MMAs complete in issue
         // order, so the P V that reads it is done first.
         if (lane == 0) {
-            const uint32_t id_s = instr_desc(kM, kN, BF16, false);
-            const uint32_t id_o = instr_desc(kM, D, BF16, true);
+            const uint32_t id_s = instr_desc(kM, kN, kMmaBF16, false);
+            const uint32_t id_o = instr_desc(kM, D, kMmaBF16, true);
             auto issue_s = [&](int x, int ks) {
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 Unit w;
                 unit_of(p, u, w, false);
                 const int n = max(w.n[0], w.n[1]);
-                if (!wait_or_fail(b_q, ui & 1))
+                if (!wait_or_fail(kQToF16 ? b_qr : b_q, ui & 1))
                     break;
                 ++ui;
                 tc_fence_after();
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         const int r = quarter * 32 + lane;  // this thread's TMEM lane (row)
         const int g = r / T, t = r - g * T;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const float sc = p.scale_log2;
+        float sc = p.scale_log2;  // this row's score factor (base 2)
         const bool sc_pos = sc >= 0.f;
         int gx = 0, vbase = 0;  // tiles of this query tile, and V tiles of the CTA, so far
         bool alive = true;
@@ -788,6 +788,46 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
             const bool zeroes = !FP8 && jp >= 0 && jp < nx && (x == 0 || jp >= w.n[0]);
             const bool valid = g < HPC && w.t0[x] + t < w.q_len;
             const int pos = valid ? w.L - w.q_len + w.t0[x] + t : -1;  // last token this row sees
+            if constexpr (kQToF16) {
+                // Move Q row r of this tile to fp16 in place, scaled by 2^-e
+                // so that the row's largest magnitude lies in [2^14, 2^15):
+                // exact for every element within 2^31 of that maximum, and
+                // no overflow. This thread also owns score row r, so 2^e
+                // joins its score factor. A row holding Inf or NaN keeps
+                // e = 0 (and yields NaN, as the definition does).
+                if (!__all_sync(kFull, wait_or_fail(b_q, i & 1))) {
+                    alive = false;
+                    break;
+                }
+                sc = p.scale_log2;
+                if (nx > 0) {
+                    const uint32_t row = sQ(x) + r * 128;
+                    uint4 qv[kChunks * 8];
+                    uint32_t mag = 0;  // largest |q| as bf16 bits, per half
+#pragma unroll
+                    for (int k = 0; k < kChunks * 8; ++k) {
+                        qv[k] = lds128(row + (k >> 3) * kChunkBytes + (((k & 7) ^ (r & 7)) << 4));
+                        mag = __vmaxu2(mag, __vmaxu2(qv[k].x & 0x7FFF7FFFu, qv[k].y & 0x7FFF7FFFu));
+                        mag = __vmaxu2(mag, __vmaxu2(qv[k].z & 0x7FFF7FFFu, qv[k].w & 0x7FFF7FFFu));
+                    }
+                    mag = max(mag & 0xFFFFu, mag >> 16);
+                    const int field = (int)(mag >> 7);  // biased exponent (0: zero or subnormal)
+                    const int e = field == 255 ? 0 : field == 0 ? (mag ? -120 : 0) : max(field - 141, -120);
+                    const float down = __int_as_float((127 - e) << 23);  // 2^-e
+                    sc = p.scale_log2 * __int_as_float((127 + e) << 23);
+                    auto to_f16 = [&](uint32_t b) {
+                        const __half2 h = __floats2half2_rn(__uint_as_float(b << 16) * down,
+                                                            __uint_as_float(b & 0xFFFF0000u) * down);
+                        return *reinterpret_cast<const uint32_t *>(&h);
+                    };
+#pragma unroll
+                    for (int k = 0; k < kChunks * 8; ++k)
+                        sts128(row + (k >> 3) * kChunkBytes + (((k & 7) ^ (r & 7)) << 4), to_f16(qv[k].x),
+                               to_f16(qv[k].y), to_f16(qv[k].z), to_f16(qv[k].w));
+                }
+                fence_proxy_async();  // the fp16 rows, for the score MMAs
+                mbar_arrive(b_qr);
+            }
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nx; ++j, ++gx) {
                 if (!__all_sync(kFull, wait_or_fail(b_s(x), gx & 1))) {
@@ -833,7 +873,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                                                fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
                                        : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])),
                                                fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
-                const float mx = (e == INFINITY || e == -INFINITY) ? -INFINITY : e * sc;
+                const float mx = (e == INFINITY || e == -INFINITY) ? -INFINITY : __fmul_rn(e, sc);
                 // The reference maximum moves only when a score exceeds it by
                 // more than kRescaleLog2 (P then stays <= 2^kRescaleLog2, which
                 // the element type holds with full relative precision).
@@ -843,27 +883,45 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 const float ref = m_new == -INFINITY ? 0.f : m_new;
                 // P = 2^(s scale - ref), rounded to the element type, packed in
                 // pairs (the lower-indexed token in the low half); the row sum
-                // adds the same rounded values.
+                // adds the same rounded values. The argument is one fused
+                // multiply-add while |ref| < 2^20: its residual against the
+                // rounded maximum is then below 2^-4, so P <= 2^8.1. A warp
+                // holding a larger reference rounds each product before the
+                // subtraction, as for the maximum, so that the largest
+                // score's argument is exactly mx - ref <= 2^8 however large
+                // the scores (a fused residual can reach half an ulp of them).
                 uint32_t pw[kN / 2];
                 float l8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     l8[i] = 0.f;
-                if (full) {
+                auto fill = [&](auto fused) {
+                    auto p_of = [&](float s) {
+                        if constexpr (decltype(fused)::value)
+                            return ex2(fmaf(s, sc, -ref));
+                        else
+                            return ex2(__fmul_rn(s, sc) - ref);
+                    };
+                    if (full) {
 #pragma unroll
-                    for (int c = 0; c < kN / 2; ++c) {
-                        pw[c] = pack2<BF16>(ex2(fmaf(sv[2 * c], sc, -ref)), ex2(fmaf(sv[2 * c + 1], sc, -ref)));
-                        l8[c & 7] = add_pair<BF16>(l8[c & 7], pw[c]);
-                    }
-                } else {
+                        for (int c = 0; c < kN / 2; ++c) {
+                            pw[c] = pack2<kMmaBF16>(p_of(sv[2 * c]), p_of(sv[2 * c + 1]));
+                            l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
+                        }
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < kN / 2; ++c) {
-                        const float p0 = kb + 2 * c <= pos ? ex2(fmaf(sv[2 * c], sc, -ref)) : 0.f;
-                        const float p1 = kb + 2 * c + 1 <= pos ? ex2(fmaf(sv[2 * c + 1], sc, -ref)) : 0.f;
-                        pw[c] = pack2<BF16>(p0, p1);
-                        l8[c & 7] = add_pair<BF16>(l8[c & 7], pw[c]);
+                        for (int c = 0; c < kN / 2; ++c) {
+                            const float p0 = kb + 2 * c <= pos ? p_of(sv[2 * c]) : 0.f;
+                            const float p1 = kb + 2 * c + 1 <= pos ? p_of(sv[2 * c + 1]) : 0.f;
+                            pw[c] = pack2<kMmaBF16>(p0, p1);
+                            l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
+                        }
                     }
-                }
+                };
+                if (__all_sync(kFull, fabsf(ref) < 0x1p20f))
+                    fill(std::true_type{});
+                else
+                    fill(std::false_type{});
                 const float ls = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
                 // Rescale O when the reference moved. The previous tile's
                 // O += P V is done: it was issued before this tile's S, whose

@@ -14,7 +14,7 @@ import oracle
 from oracle.block_manager import BlockManagerModel
 from paged_kv_cache_120_gb300 import binding, build, workloads
 
-from harness import TOL, max_abs_err, u16
+from harness import TOL, max_abs_err, max_abs_err_bf16_large, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -317,3 +317,23 @@ def test_prefill_workload_full_size(dev, name, kv):
     want = (oracle.decode_fp8_sampled(*args, st.k_scale, st.v_scale) if fp8 else oracle.decode_sampled(*args))
     got = oracle.decode_elems(u16(st.out)[rows, hq], w.dtype)
     assert max_abs_err(got, want) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_bf16_queries_with_huge_scores(dev, D):
+    """bf16 query rows scaled by 2^100 and 2^-100 over a 16-bit cache:
+    scores far beyond 2^32 in base 2 give one-hot rows, not overflow (the
+    exponent argument rounds the product before subtracting the reference,
+    so the largest score's P stays 2^0 .. 2^8)."""
+    import torch
+    c = PrefillCase(dev, workloads.BF16, 8, 2, 16, [200, 77, 300], [200, 77, 150], seed=63, D=D)
+    q = c.q.float()
+    q[0::3] *= 2.0 ** 100
+    q[1::3] *= 2.0 ** -100
+    c.q = q.to(torch.bfloat16)
+    c.q_bits = u16(c.q)
+    out = c.gpu()
+    assert torch.isfinite(out.float()).all()
+    want = c.oracle()
+    assert max_abs_err_bf16_large(oracle.decode_elems(u16(out), c.dtype), want) <= TOL[c.dtype]
+    assert binding.pa_get_device_error() == 0

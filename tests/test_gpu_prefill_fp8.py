@@ -16,7 +16,7 @@ import oracle
 from oracle.block_manager import BlockManagerModel
 from paged_kv_cache_120_gb300 import binding, build, workloads
 
-from harness import TOL, max_abs_err, u16
+from harness import TOL, max_abs_err, max_abs_err_bf16_large, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -201,3 +201,29 @@ def test_prefill_fp8_head_size_64_nan_padding_and_large_blocks(dev):
     c = Fp8PrefillCase(dev, workloads.BF16, 8, 2, 32, [33, 250, 7, 600], [33, 100, 7, 300], seed=97,
                        poison=True, D=64)
     c.check(c.gpu())
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_fp8_bf16_queries_beyond_the_fp16_range(dev, D):
+    """bf16 query rows scaled by 2^24, 2^-24 and 2^100, and rows with one
+    huge and many tiny elements: the FP8-cache kernel moves each row to
+    fp16 under its own power-of-two scale, so none overflows and the outputs
+    stay within the bf16 tolerance of the oracle."""
+    import torch
+    c = Fp8PrefillCase(dev, workloads.BF16, 8, 2, 16, [200, 77, 300], [200, 77, 150], seed=61, D=D)
+    q = c.q.float()
+    q[0::5] *= 2.0 ** 24
+    q[1::5] *= 2.0 ** -24
+    q[2::5] *= 2.0 ** 100
+    q[3::5, :, 0] = 3.0e5
+    q[3::5, :, 1:] *= 2.0 ** -30
+    c.q = q.to(torch.bfloat16)
+    c.q_bits = u16(c.q)
+    assert np.isfinite(oracle.decode_elems(c.q_bits, c.dtype)).all()
+    out = c.gpu()
+    want = c.oracle()
+    assert np.array_equal(u8(c.pool), c.pool_bits)
+    # Most rows are one-hot (the output is one V row): bf16 outputs >= 4 are
+    # held to the oracle rounded to bf16.
+    assert max_abs_err_bf16_large(oracle.decode_elems(u16(out), c.dtype), want) <= TOL[c.dtype]
+    assert binding.pa_get_device_error() == 0
