@@ -15,7 +15,7 @@ import oracle
 from oracle.block_manager import BlockManagerModel
 from paged_kv_cache_120_gb300 import binding, build, step, workloads
 
-from harness import TOL, max_abs_err, oracle_plan, u16
+from harness import TOL, max_abs_err, max_abs_err_bf16_large, oracle_plan, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -346,3 +346,23 @@ def test_fp8_workload_full_size(dev, name):
     idx = torch.tensor(sorted(touched), device=dev)
     assert np.array_equal(u8(pool[:, idx]), pool_bits[:, sorted(touched)])
     assert binding.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("heads", [(8, 2), (16, 1), (4, 4)])
+@pytest.mark.parametrize("D", [128, 64])
+def test_fp8_decode_bf16_queries_with_huge_scores(dev, heads, D):
+    """As for the 16-bit cache: bf16 query rows scaled by 2^100 and 2^-100
+    over an FP8 cache (each query column moved to fp16 under its own power
+    of two) give one-hot or uniform rows, within the bf16 tolerance."""
+    import torch
+    Hq, Hkv = heads
+    c = Fp8Case(dev, workloads.BF16, D, Hq, Hkv, 16, LENS, seed=73 + Hq + D)
+    q = c.q.float()
+    q[0::3] *= 2.0 ** 100
+    q[1::3] *= 2.0 ** -100
+    c.q = q.to(torch.bfloat16).contiguous()
+    c.q_bits = u16(c.q)
+    out = c.gpu()
+    want = c.oracle()
+    got = oracle.decode_elems(u16(out), workloads.BF16)
+    assert max_abs_err_bf16_large(got, want) <= TOL[workloads.BF16]

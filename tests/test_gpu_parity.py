@@ -13,7 +13,7 @@ import oracle
 from oracle.block_manager import BlockManagerModel
 from paged_kv_cache_120_gb300 import binding, build, step, workloads
 
-from harness import TOL, max_abs_err, oracle_plan, oracle_step, u16
+from harness import TOL, max_abs_err, max_abs_err_bf16_large, oracle_plan, oracle_step, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -429,3 +429,23 @@ def test_cow_leaves_other_sharers_unchanged(dev):
     bt = alloc.block_tables(sibs, 70)
     want = oracle.decode(q_bits, pool_bits, bt, alloc.seq_lens(sibs), scale, Hq, H, D, nb, B, dt)
     assert max_abs_err(oracle.decode_elems(u16(after), dt), want) <= TOL[dt]
+
+
+@pytest.mark.parametrize("heads", [(8, 2), (16, 1), (4, 4)])
+@pytest.mark.parametrize("D", [128, 64])
+def test_decode_bf16_queries_with_huge_scores(dev, heads, D):
+    """bf16 query rows scaled by 2^100 and 2^-100: scores far beyond 2^32 in
+    base 2 give one-hot rows (bf16 outputs >= 4 held to the oracle rounded
+    to bf16), near-zero scores give the mean of V; nothing overflows."""
+    import torch
+    Hq, Hkv = heads
+    c = Case(dev, workloads.BF16, D, Hq, Hkv, 16, LENS, seed=71 + Hq + D)
+    q = c.q.float()
+    q[0::3] *= 2.0 ** 100
+    q[1::3] *= 2.0 ** -100
+    c.q = q.to(torch.bfloat16).contiguous()
+    c.q_bits = u16(c.q)
+    out = c.gpu()
+    want = c.oracle()
+    got = oracle.decode_elems(u16(out), workloads.BF16)
+    assert max_abs_err_bf16_large(got, want) <= TOL[workloads.BF16]
