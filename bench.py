@@ -720,14 +720,19 @@ def run_prefix_cache(args, rank, local_rank, world):
     pc = binding.PrefixCache(nb, B)
     flags = 0 if use_cache else binding.PA_PCACHE_NO_CACHE
     maxb = (cfg["system"] + cfg["suffix_hi"] + B - 1) // B
-    pin = lambda n: torch.empty(n, dtype=torch.int32).pin_memory()
-    host = {"seq_ids": torch.empty(R, dtype=torch.int32), "num_cached": torch.empty(R, dtype=torch.int32),
-            "cu_seqlens_q": pin(R + 1), "seq_lens": pin(R), "slot_mapping": pin(max_tok),
-            "block_tables": pin(R * maxb)}
-    d_slots = torch.empty(max_tok, dtype=torch.int32, device=dev)
-    d_bt = torch.empty(R, maxb, dtype=torch.int32, device=dev)
-    d_cu = torch.empty(R + 1, dtype=torch.int32, device=dev)
-    d_sl = torch.empty(R, dtype=torch.int32, device=dev)
+    # The admission writes the wave's device inputs into one pinned staging
+    # buffer (cu_seqlens_q, seq_lens, slot_mapping, block tables), moved to
+    # the device with one copy into views of the same layout.
+    parts = (("cu_seqlens_q", R + 1), ("seq_lens", R), ("slot_mapping", max_tok), ("block_tables", R * maxb))
+    stage = torch.empty(sum(n for _, n in parts), dtype=torch.int32).pin_memory()
+    d_stage = torch.empty(stage.numel(), dtype=torch.int32, device=dev)
+    host = {"seq_ids": torch.empty(R, dtype=torch.int32), "num_cached": torch.empty(R, dtype=torch.int32)}
+    dview, off = {}, 0
+    for name, n in parts:
+        host[name], dview[name] = stage[off:off + n], d_stage[off:off + n]
+        off += n
+    d_cu, d_sl, d_slots = dview["cu_seqlens_q"], dview["seq_lens"], dview["slot_mapping"]
+    d_bt = dview["block_tables"].view(R, maxb)
     copied = torch.cuda.Event()
     copied.record()
     scale = D ** -0.5
@@ -735,7 +740,8 @@ def run_prefix_cache(args, rank, local_rank, world):
     events = None
 
     def wave(w, times):
-        """One wave (tokens, cu_tokens, prompt tokens); returns (tokens computed, flops)."""
+        """One wave (tokens, cu_tokens, prompt tokens); returns (tokens computed, cached tokens per
+        request, new tokens per request)."""
         tokens, cu_tokens, served = w
         copied.synchronize()        # the previous wave's pinned inputs are on the device
         t0 = time.perf_counter()
@@ -745,10 +751,7 @@ def run_prefix_cache(args, rank, local_rank, world):
         cu = host["cu_seqlens_q"].numpy()
         news = int(cu[R])
         t1 = time.perf_counter()
-        d_slots[:news].copy_(host["slot_mapping"][:news], non_blocking=True)
-        d_bt.view(-1).copy_(host["block_tables"], non_blocking=True)
-        d_cu.copy_(host["cu_seqlens_q"], non_blocking=True)
-        d_sl.copy_(host["seq_lens"], non_blocking=True)
+        d_stage.copy_(stage, non_blocking=True)
         copied.record()
         binding.pa_reshape_and_cache(k[:news], v[:news], pool, d_slots[:news])
         if events is not None:
@@ -760,10 +763,7 @@ def run_prefix_cache(args, rank, local_rank, world):
         t2 = time.perf_counter()
         pc.free_seqs(host["seq_ids"])
         times[0] += (t1 - t0) + (time.perf_counter() - t2)
-        hits = host["num_cached"].numpy().astype(np.int64)
-        n_new = np.diff(cu).astype(np.int64)
-        flops = int((4 * D * Hq * ((2 * hits + 1 + n_new) * n_new // 2)).sum())
-        return news, flops
+        return news, host["num_cached"].numpy().copy(), np.diff(cu)
 
     def prompts_for_wave():
         prompts = [np.concatenate([system, g.integers(0, cfg["vocab"], size=int(g.integers(
@@ -774,6 +774,10 @@ def run_prefix_cache(args, rank, local_rank, world):
     # 64 distinct waves, cycled: a wave's private blocks are long evicted
     # (about 20 waves of allocation refill the pool) before it comes round again
     waves = [prompts_for_wave() for _ in range(64)]
+    def wave_flops(hits, n_new):
+        hits, n_new = hits.astype(np.int64), n_new.astype(np.int64)
+        return int((4 * D * Hq * ((2 * hits + 1 + n_new) * n_new // 2)).sum())
+
     host_s = [0.0]
     for i in range(max(3, args.warmup)):
         wave(waves[i % len(waves)], host_s)
@@ -787,15 +791,17 @@ def run_prefix_cache(args, rank, local_rank, world):
         clocks.start()
     dist_barrier(world, dev)
     torch.cuda.synchronize(dev)
-    computed = served = flops = 0
-    events = []
+    computed = served = 0
+    events, counts = [], []
     t0 = time.perf_counter()
     for i in range(K):
         w = waves[(args.warmup + i) % len(waves)]
-        a, c = wave(w, host_s)
-        computed, served, flops = computed + a, served + w[2], flops + c
+        a, hits, n_new = wave(w, host_s)
+        computed, served = computed + a, served + w[2]
+        counts.append((hits, n_new))
     torch.cuda.synchronize(dev)
     t_s = dist_max(time.perf_counter() - t0, world, dev)
+    flops = sum(wave_flops(h, n) for h, n in counts)
     dist_barrier(world, dev)
     if clocks:
         clocks.stop()

@@ -64,21 +64,29 @@ constexpr uint32_t kRound[64] = {
 
 inline uint32_t rotr(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
 
-// One 512-bit block into the eight working variables.
-void sha256_compress(uint32_t st[8], const uint8_t *blk)
+inline uint32_t bswap32(uint32_t x)
 {
-    uint32_t w[64];
+    return (x >> 24) | ((x >> 8) & 0xff00u) | ((x << 8) & 0xff0000u) | (x << 24);
+}
+
+// One 512-bit block, given as its 16 big-endian words, into the eight
+// working variables; the message schedule is kept as a rolling window of
+// 16 words.
+void sha256_compress(uint32_t st[8], const uint32_t m[16])
+{
+    uint32_t w[16];
     for (int t = 0; t < 16; ++t)
-        w[t] = (uint32_t)blk[4 * t] << 24 | (uint32_t)blk[4 * t + 1] << 16 | (uint32_t)blk[4 * t + 2] << 8 |
-               (uint32_t)blk[4 * t + 3];
-    for (int t = 16; t < 64; ++t) {
-        const uint32_t s0 = rotr(w[t - 15], 7) ^ rotr(w[t - 15], 18) ^ (w[t - 15] >> 3);
-        const uint32_t s1 = rotr(w[t - 2], 17) ^ rotr(w[t - 2], 19) ^ (w[t - 2] >> 10);
-        w[t] = w[t - 16] + s0 + w[t - 7] + s1;
-    }
+        w[t] = m[t];
     uint32_t a = st[0], b = st[1], c = st[2], d = st[3], e = st[4], f = st[5], g = st[6], h = st[7];
+#pragma GCC unroll 64
     for (int t = 0; t < 64; ++t) {
-        const uint32_t t1 = h + (rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25)) + ((e & f) ^ (~e & g)) + kRound[t] + w[t];
+        uint32_t wt = w[t & 15];
+        if (t >= 16) {
+            const uint32_t x = w[(t + 1) & 15], y = w[(t + 14) & 15];
+            wt += (rotr(x, 7) ^ rotr(x, 18) ^ (x >> 3)) + w[(t + 9) & 15] + (rotr(y, 17) ^ rotr(y, 19) ^ (y >> 10));
+            w[t & 15] = wt;
+        }
+        const uint32_t t1 = h + (rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25)) + ((e & f) ^ (~e & g)) + kRound[t] + wt;
         const uint32_t t2 = (rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22)) + ((a & b) ^ (a & c) ^ (b & c));
         h = g;
         g = f;
@@ -100,38 +108,38 @@ void sha256_compress(uint32_t st[8], const uint8_t *blk)
 }
 
 // Hash of a full block: SHA-256(parent hash || token ids as little-endian
-// int32). The message is staged 64 bytes at a time; padding is a 1 bit,
-// zeros, and the 64-bit big-endian bit length.
+// int32). Every part of the message (and its padding: a 1 bit, zeros, the
+// 64-bit big-endian bit length) is 4-byte aligned, so its big-endian words
+// are formed directly: a parent word as read, a token byte-swapped.
 Digest block_hash(const Digest &parent, const int32_t *tokens, int n)
 {
     uint32_t st[8] = {0x6a09e667, 0xbb67ae85, 0x3c6ef372, 0xa54ff53a, 0x510e527f, 0x9b05688c, 0x1f83d9ab,
                       0x5be0cd19};
-    uint8_t blk[64];
-    std::memcpy(blk, parent.data(), 32);
-    int used = 32;
+    uint32_t m[16];
+    for (int i = 0; i < 8; ++i)
+        m[i] = (uint32_t)parent[4 * i] << 24 | (uint32_t)parent[4 * i + 1] << 16 | (uint32_t)parent[4 * i + 2] << 8 |
+               (uint32_t)parent[4 * i + 3];
+    int used = 8;  // words of m filled
     for (int i = 0; i < n; ++i) {
-        const uint32_t t = (uint32_t)tokens[i];
-        blk[used] = (uint8_t)t;
-        blk[used + 1] = (uint8_t)(t >> 8);
-        blk[used + 2] = (uint8_t)(t >> 16);
-        blk[used + 3] = (uint8_t)(t >> 24);
-        used += 4;
-        if (used == 64) {
-            sha256_compress(st, blk);
+        m[used++] = bswap32((uint32_t)tokens[i]);
+        if (used == 16) {
+            sha256_compress(st, m);
             used = 0;
         }
     }
     const uint64_t bits = (32 + 4 * (uint64_t)n) * 8;
-    blk[used++] = 0x80;
-    if (used > 56) {
-        std::memset(blk + used, 0, 64 - used);
-        sha256_compress(st, blk);
+    m[used++] = 0x80000000u;
+    if (used > 14) {
+        while (used < 16)
+            m[used++] = 0;
+        sha256_compress(st, m);
         used = 0;
     }
-    std::memset(blk + used, 0, 56 - used);
-    for (int i = 0; i < 8; ++i)
-        blk[56 + i] = (uint8_t)(bits >> (56 - 8 * i));
-    sha256_compress(st, blk);
+    while (used < 14)
+        m[used++] = 0;
+    m[14] = (uint32_t)(bits >> 32);
+    m[15] = (uint32_t)bits;
+    sha256_compress(st, m);
     Digest d;
     for (int i = 0; i < 8; ++i)
         for (int j = 0; j < 4; ++j)
@@ -652,16 +660,18 @@ extern "C" int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const 
     if (n > 0 && cu_tokens[n] > INT32_MAX)
         return set_error(PA_ERR_INVALID_ARG, "pa_pcache_admit: more than 2^31 - 1 prompt tokens");
     const bool cache = !(flags & PA_PCACHE_NO_CACHE);
-    // Phase 1: every request's hash chain (reads only). Request 0's first;
-    // the others copy the hashes of the full blocks they share with it
-    // token for token from the start, and hash the rest in parallel.
+    // Phase 1: every request's hash chain (reads only). The full blocks a
+    // request shares token for token with request 0 from the start have
+    // request 0's hashes: those (up to the longest such run) are chained
+    // first, then every request hashes the rest of its chain in parallel,
+    // request 0 included.
     std::vector<std::vector<Digest>> pre;
     if (cache && n > 1) {
         pre.resize(n);
         const int32_t *t0 = tokens;
         const int full0 = (int)(cu_tokens[1] / B);
-        chain_digests(c, t0, (int)cu_tokens[1], pre[0]);
         std::vector<int> common(n, 0);
+        int shared = 0;  // longest run of leading full blocks another request shares with request 0
         for (int r = 1; r < n; ++r) {
             const int32_t *tr = tokens + cu_tokens[r];
             const int fr = (int)((cu_tokens[r + 1] - cu_tokens[r]) / B);
@@ -670,11 +680,13 @@ extern "C" int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const 
                    std::memcmp(tr + (size_t)k * B, t0 + (size_t)k * B, sizeof(int32_t) * (size_t)B) == 0)
                 ++k;
             common[r] = k;
+            shared = std::max(shared, k);
         }
+        std::vector<Digest> head;  // request 0's first `shared` chained hashes
+        chain_digests(c, t0, shared * B, head);
         auto one = [&](int r) {
-            if (r > 0)
-                chain_digests_from(c, tokens + cu_tokens[r], (int)(cu_tokens[r + 1] - cu_tokens[r]), pre[0],
-                                   common[r], pre[r]);
+            chain_digests_from(c, tokens + cu_tokens[r], (int)(cu_tokens[r + 1] - cu_tokens[r]), head,
+                               r > 0 ? common[r] : shared, pre[r]);
         };
         if (!c->pool_tried) {
             c->pool_tried = true;
