@@ -168,6 +168,21 @@ def _host_addr(a) -> int:
     return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
 
 
+_TORCH_DTYPE_NAMES = {np.dtype(np.int32): "torch.int32", np.dtype(np.int64): "torch.int64"}
+
+
+def _host_ptr_size(a, dtype, name):
+    """(address, element count) of a contiguous host array of the given dtype:
+    numpy, or a CPU tensor checked and addressed directly (no numpy view)."""
+    if hasattr(a, "is_cuda"):
+        if a.is_cuda or not a.is_contiguous() or str(a.dtype) != _TORCH_DTYPE_NAMES.get(np.dtype(dtype)):
+            raise PAError(PA_ERR_INVALID_ARG, f"{name}: needs a contiguous host {np.dtype(dtype).name} tensor")
+        return a.data_ptr(), a.numel()
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags.c_contiguous:
+        raise PAError(PA_ERR_INVALID_ARG, f"{name}: needs a contiguous {np.dtype(dtype).name} array")
+    return a.ctypes.data, a.size
+
+
 def pa_version() -> int:
     return lib().pa_version()
 
@@ -432,7 +447,8 @@ class PrefixCache:
         cu_tokens int64 (numpy or CPU tensors); out maps the six output names
         to int32 host buffers (numpy or CPU tensors, e.g. pinned), allocated
         here when not given."""
-        tok, cu = _host_array(tokens, np.int32, "tokens"), _host_array(cu_tokens, np.int64, "cu_tokens")
+        tok_ptr, _ = _host_ptr_size(tokens, np.int32, "tokens")
+        cu = _host_array(cu_tokens, np.int64, "cu_tokens")
         n = len(cu) - 1
         total = int(cu[-1]) if n > 0 else 0
         sizes = {"seq_ids": n, "num_cached": n, "cu_seqlens_q": n + 1, "seq_lens": n,
@@ -442,18 +458,19 @@ class PrefixCache:
             out["block_tables"] = out["block_tables"].reshape(n, max_blocks_per_seq)
         ptrs = []
         for k in self._ADMIT_OUT:
-            a = _host_array(out[k], np.int32, k)
-            if a.size < sizes[k]:
-                raise PAError(PA_ERR_INVALID_ARG, f"admit: {k} holds {a.size} < {sizes[k]}")
-            ptrs.append(_host_addr(out[k]))
-        slot_cap = _host_array(out["slot_mapping"], np.int32, "slot_mapping").size
-        count = _check(lib().pa_pcache_admit(self._h, _host_addr(tokens), _host_addr(cu_tokens), n, flags,
+            ptr, size = _host_ptr_size(out[k], np.int32, k)
+            if size < sizes[k]:
+                raise PAError(PA_ERR_INVALID_ARG, f"admit: {k} holds {size} < {sizes[k]}")
+            ptrs.append(ptr)
+            if k == "slot_mapping":
+                slot_cap = size
+        count = _check(lib().pa_pcache_admit(self._h, tok_ptr, _host_addr(cu), n, flags,
                                              max_blocks_per_seq, *ptrs[:5], slot_cap, ptrs[5]))
         return count, out
 
     def free_seqs(self, seqs) -> None:
-        ids = _host_array(seqs, np.int32, "seqs")
-        _check(lib().pa_pcache_free_seqs(self._h, _host_addr(seqs), len(ids)))
+        ptr, n = _host_ptr_size(seqs, np.int32, "seqs")
+        _check(lib().pa_pcache_free_seqs(self._h, ptr, n))
 
     def append_token(self, seq: int, token: int) -> int:
         slot = ctypes.c_int32(0)
