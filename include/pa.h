@@ -466,7 +466,7 @@ int pa_pcache_add_seq(pa_prefix_cache *c, const int32_t *tokens, int num_tokens,
  * or a negative PA_ERR_* on bad arguments (nothing admitted).
  * The requests' block hashes are computed first, on up to
  * PA_PCACHE_THREADS helper threads (environment, read once per pool;
- * default min(8, hardware threads - 1); 0 = none), sharing the hashes of the
+ * default min(16, hardware threads - 1); 0 = none), sharing the hashes of the
  * leading blocks that equal request 0's token for token; matching and
  * allocation then run in request order. Results do not depend on the
  * thread count.

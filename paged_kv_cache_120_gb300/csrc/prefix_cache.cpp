@@ -357,13 +357,13 @@ class WorkPool {
 };
 
 // Hashing threads of a pool: PA_PCACHE_THREADS if set (0 = none), else
-// min(8, hardware threads - 1).
+// min(16, hardware threads - 1).
 int hash_threads()
 {
     if (const char *e = std::getenv("PA_PCACHE_THREADS"))
         return std::max(0, std::min(64, std::atoi(e)));
     const int hw = (int)std::thread::hardware_concurrency();
-    return std::max(0, std::min(8, hw - 1));
+    return std::max(0, std::min(16, hw - 1));
 }
 
 }  // namespace
@@ -716,8 +716,13 @@ extern "C" int pa_pcache_admit(pa_prefix_cache *c, const int32_t *tokens, const 
         seq_ids[admitted] = sid;
         num_cached[admitted] = hit;
         seq_lens[admitted] = len;
-        for (int pos = hit; pos < len; ++pos)
-            slot_mapping[q++] = table[pos / B] * B + pos % B;
+        // Slots of the uncached tokens, block by block (no division per token).
+        for (int j = hit / B, pos = hit; pos < len; ++j) {
+            const int32_t base = table[j] * B;
+            const int end = std::min(len, (j + 1) * B);
+            for (int o = pos - j * B; pos < end; ++pos, ++o)
+                slot_mapping[q++] = base + o;
+        }
         cu_seqlens_q[admitted + 1] = q;
         int32_t *row = block_tables + (size_t)admitted * max_blocks_per_seq;
         for (int j = 0; j < max_blocks_per_seq; ++j)
