@@ -271,7 +271,8 @@ int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
  *   seq_lens       device, [num_seqs] int32, >= the sequence's q_len
  *   total_q        rows of query / out (host int)
  *   max_seqlen_q   host int >= every q_len (sizes the list of work units; larger
- *                  is only slower)
+ *                  is only slower; a chunk longer than it is an inconsistent
+ *                  length, below)
  *   head_size      64 or 128; the group num_q_heads / num_kv_heads must be <= 16
  *                  or a multiple of 16
  * Rows of sequences whose offsets or lengths are inconsistent are not

@@ -296,6 +296,7 @@ struct PrefillParams {
     int head_tiles;     // group / heads_per_cta
     int rows_per_head;  // query tokens per tile (multiple of 8)
     int q_pairs;        // ceil(ceil(max_seqlen_q / rows_per_head) / 2)
+    int max_q;          // max_seqlen_q: a longer chunk is inconsistent (flagged, not written)
     int num_blocks;
     int block_size;
     int total_q;
@@ -330,7 +331,7 @@ __device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, 
     const int s = r % p.num_seqs;
     const int qr = r / p.num_seqs;
     const int q0 = p.cu_q[s], q_len = p.cu_q[s + 1] - q0, L = p.seq_lens[s];
-    if (q_len < 0 || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len) {
+    if (q_len < 0 || q_len > p.max_q || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len) {
         if (flag && h == 0 && ht == 0 && qr == 0)
             prefill_raise(PA_DEVERR_SEQ_LEN);
         return false;
@@ -1155,6 +1156,7 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     prm.rows_per_head = (kM / prm.heads_per_cta) & ~7;
     const int q_tiles = (max_seqlen_q + prm.rows_per_head - 1) / prm.rows_per_head;
     prm.q_pairs = (q_tiles + 1) / 2;
+    prm.max_q = max_seqlen_q;
     prm.num_blocks = num_blocks;
     prm.block_size = block_size;
     prm.total_q = total_q;

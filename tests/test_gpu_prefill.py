@@ -191,6 +191,13 @@ def test_prefill_rows_outside_chunks_are_untouched_and_bad_inputs_flagged(dev):
     bt[0, 1] = c.nb + 3
     binding.pa_prefill(out, c.q, c.pool, torch.from_numpy(bt).to(dev), c.cu_d, c.sl_d, c.scale, c.max_q)
     assert binding.pa_get_device_error() & binding.PA_DEVERR_BLOCK_ID
+    # a chunk longer than the max_seqlen_q hint: that sequence is skipped and
+    # flagged, not written in part
+    out = torch.full_like(c.q, float("nan"))
+    binding.pa_prefill(out, c.q, c.pool, c.bt_d, c.cu_d, c.sl_d, c.scale, 15)
+    torch.cuda.synchronize()
+    assert binding.pa_get_device_error() == binding.PA_DEVERR_SEQ_LEN
+    assert torch.isnan(out[10:].float()).all() and not torch.isnan(out[:10].float()).any()
 
 
 def test_prefill_sampled_rows_at_llama13b_shape(dev):
