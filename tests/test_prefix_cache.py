@@ -226,3 +226,37 @@ def test_admit_stops_at_the_first_request_that_does_not_fit(lib):
     assert count2 == len(want2) == 2
     assert out2["seq_ids"].tolist() == [w[0] for w in want2]
     _same(pc, m, [w[0] for w in want2])
+
+
+def test_admit_into_host_tensors_and_their_checks(lib):
+    """admit and free_seqs take CPU tensors (int32, contiguous) as well as
+    numpy arrays, addressed in place: a wrong dtype, a strided view or a
+    too-small buffer is an argument error and admits nothing."""
+    import torch
+    pc = binding.PrefixCache(32, 16)
+    toks = torch.arange(40, dtype=torch.int32)
+    cu = np.array([0, 17, 40], np.int64)
+    out = {k: torch.full((64,), -7, dtype=torch.int32) for k in binding.PrefixCache._ADMIT_OUT}
+    count, got = pc.admit(toks, cu, 4, 0, out)
+    assert count == 2 and got is out
+    want_count, want = binding.PrefixCache(32, 16).admit(toks.numpy(), cu, 4)
+    assert want_count == 2
+    for k in ("seq_ids", "num_cached", "cu_seqlens_q", "seq_lens"):
+        n = len(want[k])
+        assert out[k][:n].tolist() == want[k].tolist(), k
+    assert out["slot_mapping"][:40].tolist() == want["slot_mapping"].tolist()
+    assert out["block_tables"][:8].tolist() == want["block_tables"].ravel().tolist()
+    pc.free_seqs(out["seq_ids"][:2].clone())
+    free = pc.num_free()
+    bad = [dict(out, seq_ids=torch.zeros(64, dtype=torch.int64)),          # dtype
+           dict(out, slot_mapping=torch.zeros(128, dtype=torch.int32)[::2]),  # strided
+           dict(out, slot_mapping=torch.zeros(39, dtype=torch.int32))]       # too small for 40 tokens
+    for o in bad:
+        with pytest.raises(binding.PAError) as e:
+            pc.admit(toks, cu, 4, 0, o)
+        assert e.value.code == binding.PA_ERR_INVALID_ARG
+    with pytest.raises(binding.PAError):
+        pc.admit(toks.to(torch.int64), cu, 4, 0, out)
+    with pytest.raises(binding.PAError):
+        pc.free_seqs(out["seq_ids"][:2].to(torch.int64))
+    assert pc.num_free() == free
