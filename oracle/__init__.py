@@ -31,14 +31,19 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c with gcc (plain -O2, IEEE semantics, no fast-math)."""
+    """Compile oracle.c with gcc (plain -O2, IEEE semantics, no fast-math),
+    with OpenMP for the row-parallel batch functions when the compiler has
+    it (the results are the same either way)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
-                           "-fno-fast-math", _SRC, "-o", tmp, "-lm"])
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", _SRC, "-o", tmp]
+    try:
+        subprocess.check_call(base + ["-fopenmp", "-lm"], stderr=subprocess.DEVNULL)
+    except subprocess.CalledProcessError:
+        subprocess.check_call(base + ["-lm"])
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -52,6 +57,10 @@ def _load():
     c_i32p = ctypes.POINTER(ctypes.c_int32)
     c_dp = ctypes.POINTER(ctypes.c_double)
     i, d, ll = ctypes.c_int, ctypes.c_double, ctypes.c_longlong
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads.restype = None
+    lib.oracle_threads.argtypes = []
+    lib.oracle_threads.restype = ctypes.c_int
     lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_to_double.restype = d
     lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -111,6 +120,18 @@ def _i32(a) -> np.ndarray:
 
 def _p(a, ct):
     return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def set_threads(n: int) -> None:
+    """Threads for the batch-level calls (decode, decode_sampled, their FP8
+    forms, prefill); each output row is still computed by one thread with the
+    same arithmetic, so results do not depend on n."""
+    _load().oracle_set_threads(int(n))
+
+
+def threads() -> int:
+    """Threads the next batch-level call will use (1 if built without OpenMP)."""
+    return int(_load().oracle_threads())
 
 
 def f16_to_double(bits: int) -> float:

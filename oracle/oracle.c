@@ -37,8 +37,51 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+#ifdef __GLIBC__
+#include <malloc.h>
+#endif
 
 enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+
+/* ---- threads ----
+ * The batch-level functions below (decode, its sampled and FP8 forms, and
+ * prefill) hand whole output rows, one (sequence or query row, q-head) at a
+ * time, to OpenMP threads. Each row is computed by the same single-threaded
+ * code whatever the thread count, so results do not depend on it. Built
+ * without OpenMP, everything runs on the calling thread. */
+void oracle_set_threads(int n)
+{
+#ifdef __GLIBC__
+    /* Rows allocate their gathered K/V (up to tens of MB) and free them again.
+     * Served by mmap, every row would fault its pages in afresh, and the
+     * threads would queue on the kernel's memory map; from the heap the
+     * memory is reused. This changes only where the buffers come from. */
+    static int heap_set = 0;
+    if (!heap_set) {
+        mallopt(M_MMAP_THRESHOLD, 1 << 30);
+        mallopt(M_TRIM_THRESHOLD, 1 << 30);
+        heap_set = 1;
+    }
+#endif
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
+
+/* Threads the next batch-level call will use (1 without OpenMP). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ---- exact 16-bit float decoders (IEEE 754 binary16, bfloat16) ---- */
 
@@ -345,6 +388,7 @@ void oracle_decode(double *out, const uint16_t *query, const uint16_t *pool,
                    double scale, int num_q_heads, int num_kv_heads, int head_size,
                    int num_blocks, int block_size, int dtype)
 {
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int s = 0; s < num_seqs; ++s)
         for (int hq = 0; hq < num_q_heads; ++hq)
             oracle_decode_one(out + ((long long)s * num_q_heads + hq) * head_size, query, pool,
@@ -360,6 +404,7 @@ void oracle_decode_sampled(double *out, const int32_t *seq_ids, const int32_t *q
                            int num_kv_heads, int head_size, int num_blocks, int block_size,
                            int dtype)
 {
+#pragma omp parallel for schedule(dynamic, 1)
     for (int i = 0; i < n; ++i)
         oracle_decode_one(out + (long long)i * head_size, query, pool, block_tables,
                           max_blocks_per_seq, seq_lens, seq_ids[i], q_heads[i], scale,
@@ -412,6 +457,7 @@ void oracle_decode_fp8(double *out, const uint16_t *query, const uint8_t *pool,
                        double scale, int num_q_heads, int num_kv_heads, int head_size,
                        int num_blocks, int block_size, int dtype, double k_scale, double v_scale)
 {
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int s = 0; s < num_seqs; ++s)
         for (int hq = 0; hq < num_q_heads; ++hq)
             oracle_decode_fp8_one(out + ((long long)s * num_q_heads + hq) * head_size, query, pool,
@@ -428,6 +474,7 @@ void oracle_decode_fp8_sampled(double *out, const int32_t *seq_ids, const int32_
                                int num_kv_heads, int head_size, int num_blocks, int block_size,
                                int dtype, double k_scale, double v_scale)
 {
+#pragma omp parallel for schedule(dynamic, 1)
     for (int i = 0; i < n; ++i)
         oracle_decode_fp8_one(out + (long long)i * head_size, query, pool, block_tables,
                               max_blocks_per_seq, seq_lens, seq_ids[i], q_heads[i], scale,
@@ -451,19 +498,23 @@ void oracle_prefill(double *out, const uint16_t *query, const uint16_t *pool,
                     double scale, int num_q_heads, int num_kv_heads, int head_size,
                     int num_blocks, int block_size, int dtype)
 {
-    for (int s = 0; s < num_seqs; ++s) {
+    int total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < total_q; ++r) {
+        int s = 0;
+        while (cu_seqlens_q[s + 1] <= r) /* the sequence whose chunk holds row r */
+            ++s;
         int q0 = cu_seqlens_q[s];
         int q_len = cu_seqlens_q[s + 1] - q0;
+        int i = r - q0;
         const int32_t *table = block_tables + (long long)s * max_blocks_per_seq;
-        for (int i = 0; i < q_len; ++i) {
-            int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */
-            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;
-            for (int hq = 0; hq < num_q_heads; ++hq)
-                oracle_decode_one(out + ((long long)(q0 + i) * num_q_heads + hq) * head_size, q_row,
-                                  pool, table, max_blocks_per_seq, &visible, 0, hq, scale,
-                                  num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
-                                  dtype);
-        }
+        int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */
+        const uint16_t *q_row = query + (long long)r * num_q_heads * head_size;
+        for (int hq = 0; hq < num_q_heads; ++hq)
+            oracle_decode_one(out + ((long long)r * num_q_heads + hq) * head_size, q_row,
+                              pool, table, max_blocks_per_seq, &visible, 0, hq, scale,
+                              num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                              dtype);
     }
 }
 
@@ -476,19 +527,23 @@ void oracle_prefill_fp8(double *out, const uint16_t *query, const uint8_t *pool,
                         double scale, int num_q_heads, int num_kv_heads, int head_size,
                         int num_blocks, int block_size, int dtype, double k_scale, double v_scale)
 {
-    for (int s = 0; s < num_seqs; ++s) {
+    int total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < total_q; ++r) {
+        int s = 0;
+        while (cu_seqlens_q[s + 1] <= r) /* the sequence whose chunk holds row r */
+            ++s;
         int q0 = cu_seqlens_q[s];
         int q_len = cu_seqlens_q[s + 1] - q0;
+        int i = r - q0;
         const int32_t *table = block_tables + (long long)s * max_blocks_per_seq;
-        for (int i = 0; i < q_len; ++i) {
-            int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */
-            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;
-            for (int hq = 0; hq < num_q_heads; ++hq)
-                oracle_decode_fp8_one(out + ((long long)(q0 + i) * num_q_heads + hq) * head_size, q_row,
-                                      pool, table, max_blocks_per_seq, &visible, 0, hq, scale,
-                                      num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
-                                      dtype, k_scale, v_scale);
-        }
+        int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */
+        const uint16_t *q_row = query + (long long)r * num_q_heads * head_size;
+        for (int hq = 0; hq < num_q_heads; ++hq)
+            oracle_decode_fp8_one(out + ((long long)r * num_q_heads + hq) * head_size, q_row,
+                                  pool, table, max_blocks_per_seq, &visible, 0, hq, scale,
+                                  num_q_heads, num_kv_heads, head_size, num_blocks, block_size,
+                                  dtype, k_scale, v_scale);
     }
 }
 

@@ -27,9 +27,18 @@ _GATHER8 = (_GATHER % (("double",) * 6)) + """    double *q = (double *)malloc(s
         int b = table[{1}];"""
 
 # (file, original text, planted slip, pin file expected to catch it)
-# the query-row and call lines that follow the visible length in oracle_prefill
-_PREFILL16 = ("\n            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;"
-              "\n            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_one(")
+# the query-row and call lines that follow the visible length in the prefill
+# row loops (16-bit and FP8; they differ only in the call)
+_ROW_TAIL = ("\n        const uint16_t *q_row = query + (long long)r * num_q_heads * head_size;"
+             "\n        for (int hq = 0; hq < num_q_heads; ++hq)\n            %s(")
+_PREFILL16 = _ROW_TAIL % "oracle_decode_one"
+_PREFILL8 = _ROW_TAIL % "oracle_decode_fp8_one"
+_VISIBLE = "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */"
+# the row -> sequence search that opens each prefill row
+_ROW_SEARCH = ("while (cu_seqlens_q[s + 1] <= r) /* the sequence whose chunk holds row r */\n"
+               "            ++s;\n        int q0 = cu_seqlens_q[s];\n"
+               "        int q_len = cu_seqlens_q[s + 1] - q0;\n        int i = r - q0;\n"
+               "        const int32_t *table = block_tables + (long long)s * max_blocks_per_seq;\n        ")
 
 MUTANTS = [
     ("oracle/oracle.c", "expo - 25);", "expo - 24);", "test_oracle_pins.py"),          # f16 bias
@@ -78,26 +87,19 @@ MUTANTS = [
     ("oracle/oracle.c", "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * v_scale;",
      "v[(long long)i * head_size + d] = oracle_e4m3_to_double(vc) * k_scale;",
      "test_oracle_fp8_pins.py"),                                                      # decode scale swap
-    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */" + _PREFILL16,
-     "int32_t visible = seq_lens[s] - q_len + i + 2; /* tokens 0..p */" + _PREFILL16,
+    ("oracle/oracle.c", _VISIBLE + _PREFILL16, _VISIBLE.replace("i + 1;", "i + 2;") + _PREFILL16,
      "test_oracle_prefill_pins.py"),                                                  # sees p+1
-    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */" + _PREFILL16,
-     "int32_t visible = seq_lens[s] - q_len + 1; /* tokens 0..p */" + _PREFILL16,
+    ("oracle/oracle.c", _VISIBLE + _PREFILL16, _VISIBLE.replace("i + 1;", "1;") + _PREFILL16,
      "test_oracle_prefill_pins.py"),                                                  # not causal in i
-    ("oracle/oracle.c", "const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;"
-     "\n            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_one(",
-     "const uint16_t *q_row = query + (long long)(q0) * num_q_heads * head_size;"
-     "\n            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_one(",
+    ("oracle/oracle.c", _PREFILL16, _PREFILL16.replace("(long long)r *", "(long long)i *"),
      "test_oracle_prefill_pins.py"),                                                  # wrong query row
-    ("oracle/oracle.c", "dtype, k_scale, v_scale);\n        }\n    }\n}\n\n/* ---- the online-softmax",
-     "dtype, v_scale, k_scale);\n        }\n    }\n}\n\n/* ---- the online-softmax",
+    ("oracle/oracle.c", _ROW_SEARCH + _VISIBLE + _PREFILL16,
+     _ROW_SEARCH.replace("<= r)", "< r)") + _VISIBLE + _PREFILL16,
+     "test_oracle_prefill_pins.py"),                                                  # row -> sequence off by one
+    ("oracle/oracle.c", "dtype, k_scale, v_scale);\n    }\n}\n\n/* ---- the online-softmax",
+     "dtype, v_scale, k_scale);\n    }\n}\n\n/* ---- the online-softmax",
      "test_oracle_prefill_pins.py"),                                                  # FP8 prefill scales swapped
-    ("oracle/oracle.c", "int32_t visible = seq_lens[s] - q_len + i + 1; /* tokens 0..p */\n"
-     "            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;\n"
-     "            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_fp8_one(",
-     "int32_t visible = seq_lens[s] - q_len + i + 2; /* tokens 0..p */\n"
-     "            const uint16_t *q_row = query + (long long)(q0 + i) * num_q_heads * head_size;\n"
-     "            for (int hq = 0; hq < num_q_heads; ++hq)\n                oracle_decode_fp8_one(",
+    ("oracle/oracle.c", _VISIBLE + _PREFILL8, _VISIBLE.replace("i + 1;", "i + 2;") + _PREFILL8,
      "test_oracle_prefill_pins.py"),                                                  # FP8 prefill row sees one more
     ("oracle/prefix_cache.py", "if (i + 1) * B > n - 1 or h not in self.cached:",
      "if (i + 1) * B > n or h not in self.cached:", "test_prefix_cache_model.py"),   # hit limit
