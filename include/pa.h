@@ -73,6 +73,12 @@ typedef struct CUstream_st *pa_stream_t;
 #define PA_DECODE_SHARED_BLOCKS 1u  /* some physical block appears in more than one
                                        sequence's table (prefix sharing, parallel
                                        sampling): keep K/V at normal L2 priority */
+#define PA_DECODE_LENS_READY    2u  /* the caller guarantees that seq_lens already
+                                       holds its final values when the kernel
+                                       enqueued just before this call starts (it was
+                                       copied from the host, or written by an
+                                       earlier kernel): the decode may then read it
+                                       while that kernel finishes */
 
 /* Bits of the device error word. */
 #define PA_DEVERR_BLOCK_ID  1   /* a block table entry outside [0, num_blocks) */
@@ -122,9 +128,9 @@ int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
 
 /*
  * pa_decode — one query token per sequence attends over all its cached
- * tokens through the block table ([book] §4.5 step 2 and the read loop
- * "for logical_block in used_blocks: phys = block_table[row, logical_block]";
- * §4.4.1 block table; [digest] "注意力内核为何能正常工作").
+ * tokens through the block table ([book] §4.5 step 2: each logical block's
+ * physical id is looked up in the sequence's table row before its K/V are
+ * read; §4.4.1 block table; [digest] "注意力内核为何能正常工作").
  *
  *   out            device, [num_seqs][num_q_heads][head_size], dtype
  *   query          device, [num_seqs][num_q_heads][head_size], dtype
@@ -148,18 +154,27 @@ int pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  *                  initialisation and are not preserved. Calls that share a
  *                  workspace must not overlap on the GPU.
  *
- *   flags          0 or PA_DECODE_SHARED_BLOCKS. Without it the K/V tiles
- *                  are streamed with an L2 evict-first hint (each byte is
- *                  read once per call, and the split-K records and tables
- *                  stay in L2); with it they keep normal priority so that
- *                  sequences sharing blocks hit L2. Results are identical
- *                  either way; only the speed differs.
+ *   flags          a bitwise OR of:
+ *                  PA_DECODE_SHARED_BLOCKS: without it the K/V tiles are
+ *                  streamed with an L2 evict-first hint (each byte is read
+ *                  once per call, and the split-K records and tables stay
+ *                  in L2); with it they keep normal priority so that
+ *                  sequences sharing blocks hit L2.
+ *                  PA_DECODE_LENS_READY: seq_lens is final before the kernel
+ *                  enqueued just before this call starts (see Launch).
+ *                  Results are identical under every combination; only the
+ *                  speed differs.
  *
  * Launch: two kernels (the stream and the split-K merge), both with
  * programmatic dependent launch. The first may start while the preceding
  * kernel in the stream is finishing (typically this step's
- * pa_reshape_and_cache); before waiting for that kernel it reads only
- * seq_lens, and it reads the pool and writes anything only after the wait.
+ * pa_reshape_and_cache). By default it waits for that kernel before it
+ * reads anything, so seq_lens may be written by the kernel just before
+ * this call (a scheduler or length-update kernel). With PA_DECODE_LENS_READY
+ * it reads seq_lens and plans its split while that kernel finishes, and
+ * waits only before it reads the pool or writes anything; seq_lens must then
+ * not be written by that kernel (host copies and earlier kernels are fine:
+ * they complete before it starts).
  *
  * Result: out[s][hq] = sum_i softmax_i(scale * q.k_i) v_i over the
  * seq_lens[s] logical tokens, computed with fp32 dot products, an fp32

@@ -27,6 +27,7 @@ PA_F16 = 0
 PA_BF16 = 1
 PA_FP8_E4M3 = 2
 PA_DECODE_SHARED_BLOCKS = 1
+PA_DECODE_LENS_READY = 2
 PA_PCACHE_NO_CACHE = 1
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SLOT = 2
@@ -221,7 +222,7 @@ def pa_decode(out, query, kv_cache, block_tables, seq_lens, scale, workspace,
               flags=0, stream=None) -> None:
     """out/query [S, Hq, D]; kv_cache (2, NB, B, Hkv, D); block_tables [S, maxblk] int32;
     seq_lens [S] int32; workspace: uint8 CUDA tensor (see decode_workspace);
-    flags: 0 or PA_DECODE_SHARED_BLOCKS."""
+    flags: an OR of PA_DECODE_SHARED_BLOCKS and PA_DECODE_LENS_READY (0 = none)."""
     s, hq, d = query.shape
     _, nb, bs, hkv, _ = kv_cache.shape
     _check(lib().pa_decode(

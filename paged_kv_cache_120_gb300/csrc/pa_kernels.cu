@@ -236,6 +236,7 @@ struct DecodeParams {
     float scale_log2;     // scale * log2(e) (* k_scale for an FP8 cache): scores in base 2
     float v_scale;        // FP8 cache: value of a V code's unit; 1 otherwise
     int kv_stream;        // 1: stream K/V with the L2 evict-first hint (no block shared)
+    int lens_early;       // 1: seq_lens may be read before the preceding kernel has finished
     int total_warps;      // grid * warps per CTA
 };
 
@@ -348,6 +349,12 @@ __global__ void __launch_bounds__(decode_warps<NT, FP8>() * 32)
     const int segs_per_seq = p.num_kv_heads * p.qtiles;
     const int max_len = p.max_blocks_per_seq * p.block_size;
 
+    // Unless the caller vouched that seq_lens is final before the preceding
+    // kernel in the stream started, that kernel may still be writing it:
+    // wait for it before the first read.
+    if (!p.lens_early)
+        grid_dependency_wait();
+
     // 1. Sequence lengths and the exclusive prefix of units (tiles x segments).
     {
         const int per = (S + blockDim.x - 1) / blockDim.x;
@@ -392,9 +399,10 @@ __global__ void __launch_bounds__(decode_warps<NT, FP8>() * 32)
 
     // Let the reduce kernel start launching; it waits for this grid anyway.
     grid_launch_dependents();
-    // Everything above read only inputs the caller produced (lengths). The
-    // pool may still be being written by the preceding kernel (this step's
-    // reshape_and_cache): wait for it before any pool read or global write.
+    // Everything above read only the lengths. The pool may still be being
+    // written by the preceding kernel (this step's reshape_and_cache): wait
+    // for it before any pool read or global write (a no-op if the wait above
+    // already ran).
     grid_dependency_wait();
 
     const long long N = prefix[S];
@@ -1517,7 +1525,7 @@ int decode_impl(const char *fn, void *out, const void *query, const void *kv_cac
         return set_error(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq * block_size too large", fn);
     if (!std::isfinite(scale))
         return set_error(PA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
-    if (flags & ~PA_DECODE_SHARED_BLOCKS)
+    if (flags & ~(PA_DECODE_SHARED_BLOCKS | PA_DECODE_LENS_READY))
         return set_error(PA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
     if (!aligned(kv_cache, 16) || !aligned(query, 16) || !aligned(out, 16) ||
         !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
@@ -1558,6 +1566,7 @@ int decode_impl(const char *fn, void *out, const void *query, const void *kv_cac
     prm.scale_log2 = (fp8 ? scale * k_scale : scale) * 1.4426950408889634f;
     prm.v_scale = fp8 ? v_scale : 1.f;
     prm.kv_stream = (flags & PA_DECODE_SHARED_BLOCKS) ? 0 : 1;
+    prm.lens_early = (flags & PA_DECODE_LENS_READY) ? 1 : 0;
     prm.total_warps = pl.total_warps;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

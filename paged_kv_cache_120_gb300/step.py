@@ -192,6 +192,9 @@ class DecodeStep(PinnedHostStep):
         # then K/V keep normal L2 priority, else they are streamed.
         ids = plan.block_tables[plan.block_tables >= 0]
         self.flags = binding.PA_DECODE_SHARED_BLOCKS if len(np.unique(ids)) < len(ids) else 0
+        # seq_lens only ever arrives by a host-to-device copy, which completes
+        # before the reshape kernel that precedes the decode starts.
+        self.flags |= binding.PA_DECODE_LENS_READY
 
     def launches_per_step(self) -> int:
         # copy_blocks (if any COW pairs) + reshape_and_cache + decode (stream + merge)

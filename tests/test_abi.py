@@ -33,6 +33,20 @@ def test_every_declared_function_is_exported(lib):
     assert sorted(n for n, _, _ in binding.SIGNATURES) == names
 
 
+def test_exported_set_is_exactly_the_declared_set(lib):
+    """No pa_* function leaves the library without a declaration in pa.h."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines()
+                       if line.split() and line.split()[-1].startswith("pa_") and " T " in line})
+    assert exported == _declared_functions()
+
+
 def test_version(lib):
     assert binding.pa_version() == 10000
 

@@ -213,6 +213,58 @@ def test_shared_blocks_flag_changes_speed_not_results(dev):
     assert e.value.code == binding.PA_ERR_INVALID_ARG
 
 
+def test_lengths_written_by_the_kernel_just_before_the_decode(dev):
+    """Book §4.5: this step's lengths (its token included) are final before
+    attention reads them. A serving loop may compute them on the device, in
+    the kernel enqueued just before pa_decode; by default the decode waits for
+    that kernel before its first read of seq_lens, so the output is that of
+    the new lengths, not of what the buffer held before."""
+    import torch
+    lens = [2000, 1500, 37, 900, 16, 1, 1200, 640, 333, 1999, 64, 700, 5, 1024, 17, 300]
+    c = Case(dev, workloads.BF16, 128, 32, 8, 16, lens, seed=41)
+    want = c.oracle()
+    t = lambda a: torch.from_numpy(a).to(dev)
+    binding.pa_reshape_and_cache(c.k, c.v, c.pool, t(c.slots))
+    bt = t(c.bt)
+    sl = torch.empty(len(lens), dtype=torch.int32, device=dev)
+    # A slow kernel (a row sum over 256 MB) whose outputs are the lengths.
+    big = torch.zeros((len(lens), 1 << 22), dtype=torch.int32, device=dev)
+    big[:, 0] = t(c.seq_lens)
+    ws = binding.decode_workspace(c.q, c.pool)
+    for _ in range(3):
+        out = torch.full_like(c.q, float("nan"))
+        sl.fill_(1)                                             # stale lengths
+        torch.cuda.synchronize()
+        torch.sum(big, dim=1, dtype=torch.int32, out=sl)       # the kernel just before the decode
+        binding.pa_decode(out, c.q, c.pool, bt, sl, c.scale, ws)
+        torch.cuda.synchronize()
+        assert sl.cpu().numpy().tolist() == lens
+        err = max_abs_err(oracle.decode_elems(u16(out), c.dtype), want)
+        assert err <= TOL[c.dtype], f"max abs err {err}"
+    # With PA_DECODE_LENS_READY the lengths come from a host copy (complete
+    # before the kernel ahead of the decode starts): the same bits.
+    host = torch.from_numpy(c.seq_lens).pin_memory()
+    out2 = torch.empty_like(c.q)
+    sl.fill_(1)
+    sl.copy_(host, non_blocking=True)
+    binding.pa_reshape_and_cache(c.k, c.v, c.pool, t(c.slots))
+    binding.pa_decode(out2, c.q, c.pool, bt, sl, c.scale, ws, flags=binding.PA_DECODE_LENS_READY)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    assert binding.pa_get_device_error() == 0
+
+
+def test_unknown_decode_flags_are_rejected(dev):
+    import torch
+    c = Case(dev, workloads.F16, 64, 4, 4, 16, [20], seed=9)
+    out = torch.empty_like(c.q)
+    ws = binding.decode_workspace(c.q, c.pool)
+    with pytest.raises(binding.PAError) as e:
+        binding.pa_decode(out, c.q, c.pool, torch.from_numpy(c.bt).to(dev),
+                          torch.from_numpy(c.seq_lens).to(dev), c.scale, ws, flags=4)
+    assert e.value.code == binding.PA_ERR_INVALID_ARG
+
+
 def test_copy_blocks_bit_exact_and_conflicts_rejected(dev):
     import torch
     rng = np.random.default_rng(4)
@@ -355,12 +407,14 @@ def test_workload_toy_worked_example(dev):
 
 @pytest.mark.parametrize("name", ["llama13b", "gqa8b", "longctx"])
 def test_workload_full_size(dev, name):
-    _run_workload(dev, name, seed=1, n_sample=16 if name == "longctx" else 48)
+    """The whole step at full size; every (sequence, head) output row against
+    the oracle, element by element."""
+    _run_workload(dev, name, seed=1, n_sample=None)
 
 
 @pytest.mark.parametrize("variant", ["literal", "fork"])
 def test_workload_prefix_sharing_cow(dev, variant):
-    st, plan, *_ = _run_workload(dev, "prefix_cow", seed=2, variant=variant, n_sample=64)
+    st, plan, *_ = _run_workload(dev, "prefix_cow", seed=2, variant=variant, n_sample=None)
     if variant == "fork":
         assert len(plan.cow_pairs) == workloads.PREFIX_GROUPS * (workloads.PREFIX_GROUP_SIZE - 1)
     else:
