@@ -5,10 +5,11 @@ whose caching allocator owns every byte of device memory, a plugin held to a
 fixed memory budget, or a latency-critical loop where an allocation (which
 can synchronise the device) is forbidden. For them the library offers an
 entry point whose split-K scratch is a static device array inside the
-library. These tests call it through the C ABI and require the same outputs
-as pa_decode with a caller workspace, on two calls in a row (the second call
-finds the previous call's contents in the shared array), and a clear refusal
-for a shape whose scratch would not fit.
+library. These tests call it through the C ABI and require the same output
+bits as pa_decode with a caller workspace, on two calls in a row that follow
+a call of another shape (each call finds the previous call's contents in the
+shared array), no change in free device memory across the second call, and a
+clear refusal for a shape whose scratch would not fit.
 
 This file is collected last on purpose, and it also passes on its own in a
 fresh process (its first call does the one-time address lookup).
@@ -63,16 +64,25 @@ def test_static_scratch_matches_workspace_decode_on_two_calls(dev, dtype, Hq, Hk
     pool, q, bt, sl, scale = _case(dev, dtype, Hq, Hkv, D, lens, seed=31 + Hq)
     ref = torch.empty_like(q)
     binding.pa_decode(ref, q, pool, bt, sl, scale, binding.decode_workspace(q, pool))
+    # Leave a different shape's records in the shared array first: a later
+    # call must not pick any of them up.
+    o_pool, o_q, o_bt, o_sl, _ = _case(dev, dtype, Hq, Hkv, D, [30000, 70, 5000], seed=77)
+    binding.pa_decode_static_scratch(torch.empty_like(o_q), o_q, o_pool, o_bt, o_sl, 0.3)
+    outs = [torch.full_like(q, float("nan")) for _ in range(2)]
     torch.cuda.synchronize()
-    ref_v = ref.float().cpu().numpy()
-    for call in range(2):
-        out = torch.full_like(q, float("nan"))
+    for call, out in enumerate(outs):
+        free_before = torch.cuda.mem_get_info(dev)[0]
         binding.pa_decode_static_scratch(out, q, pool, bt, sl, scale)
         torch.cuda.synchronize()
-        got = out.float().cpu().numpy()
-        assert np.all(np.isfinite(got)), f"call {call}: non-finite output"
-        err = float(np.max(np.abs(got - ref_v)))
-        assert err <= TOL[dtype], f"call {call}: max abs err {err} vs pa_decode"
+        if call == 1:
+            # the array was set up by the earlier calls; this call allocates nothing
+            assert torch.cuda.mem_get_info(dev)[0] == free_before
+        # the same kernels and the same split as pa_decode: the same bits
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"call {call}"
+    # (so within the tests' decode tolerance of it too)
+    got = outs[1].float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert float(np.max(np.abs(got - ref.float().cpu().numpy()))) <= TOL[dtype]
     assert binding.pa_get_device_error() == 0
 
 
