@@ -1,22 +1,29 @@
 #!/usr/bin/env python3
-"""Benchmark of one PagedAttention decode step on GB300.
+"""Benchmark of the PagedAttention hot path on GB300.
 
-A step is one pass of the whole hot path over one batch:
+A decode step is one pass of the whole hot path over one batch:
     pa_copy_blocks (COW pairs, if the workload has any)
     -> pa_reshape_and_cache (one new token per sequence)
-    -> pa_decode (main kernel + split-K reduce)
+    -> pa_decode (stream kernel + split-K merge kernel)
 Default workload: the Llama-2-13B layer (64 sequences, 40/40 heads,
 head_dim 128, fp16, lengths uniform in [1, 2048], 9000-block pool).
 
 Prints one JSON line (rank 0). ``value`` is the step's algorithmic HBM bytes
-per second (GB/s); ``seq_steps_per_s`` is sequences decoded per second.
-``--kv-cache fp8`` runs the same step on a cache of E4M3 codes (one byte per
-K/V element, per-tensor scales): pa_reshape_and_cache_fp8 and pa_decode_fp8.
+per second (GB/s) over exactly --steps timed steps; ``seq_steps_per_s`` is
+sequences decoded per second. Each kernel family is also timed alone: a
+block of back-to-back launches (at least 50), every launch bracketed by CUDA
+events, summarised by its median; the roofline fraction comes from that
+median. The default run adds a ``configs`` record with the same measurements
+for every other large workload: GQA-8B, long context, prefix sharing with
+copy-on-write (L2 flushed between iterations and not), the FP8 (E4M3) cache
+on the three decode shapes, and chunked prefill.
+
+``--kv-cache fp8`` runs a step on a cache of E4M3 codes (one byte per K/V
+element, per-tensor scales): pa_reshape_and_cache_fp8 and pa_decode_fp8.
 ``--workload prefill_llama13b|prefill_gqa8b`` times a chunked-prefill step
-instead (pa_reshape_and_cache of each sequence's 1024-token chunk, then the
-tcgen05 pa_prefill): ``value`` is causal attention TFLOP/s and the roofline is
-the tensor-core one.
-``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+(pa_reshape_and_cache of each sequence's 1024-token chunk, then the tcgen05
+pa_prefill): ``value`` is causal attention TFLOP/s against the tensor-core
+roofline. ``--impl reference`` times the fp64 CPU oracle on the host cores.
 Under torchrun every rank runs its own replica of the workload (weak
 scaling: sequences are independent, no collective on the data path).
 """
@@ -24,7 +31,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -42,6 +48,10 @@ from paged_kv_cache_120_gb300 import workloads  # noqa: E402
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
+METRIC = "paged-decode attention achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+PREFILL_METRIC = "paged chunked-prefill causal attention TFLOP/s"
+# Launches per kernel in a per-launch timing block (each bracketed by events).
+LAUNCHES = 200
 
 
 # ------------------------------------------------------------ bytes of a step
@@ -88,6 +98,18 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
 
 
+def measured_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (the prefill kernel runs inside long
+    loops); fp16 runs at the same nominal rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS)"
+    except Exception:
+        return 1700.0, "fallback 1.7 PFLOP/s sustained (MEASURED_PEAKS.json absent)"
+
+
 KERNEL_SOURCES = {
     "decode": ("pa_kernels.cu", "pa_device.cuh"),
     "decode_fp8": ("pa_kernels.cu", "pa_device.cuh"),
@@ -128,7 +150,8 @@ def traffic_record(tag: str, workload: str):
 # ------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi in the background; samples are filtered to the timed window."""
+    """nvidia-smi sampling in the background for the whole run; summaries
+    are taken over the windows in which GPU work was timed."""
 
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -144,25 +167,20 @@ class ClockSampler:
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        self.t0 = self.t1 = None
 
-    def start(self):
-        time.sleep(0.3)
-        self.t0 = time.time()
-
-    def stop(self):
-        self.t1 = time.time()
-        time.sleep(0.15)
+    def close(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        try:
+            os.unlink(self.file.name)
+        except OSError:
+            pass
 
-    def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+    def _rows(self):
         self.file.flush()
         rows = []
         with open(self.file.name) as f:
@@ -176,8 +194,16 @@ class ClockSampler:
                     rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
                 except Exception:
                     continue
-        os.unlink(self.file.name)
-        inside = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        return rows
+
+    def summary(self, t0: float, t1: float):
+        """Median SM clock, max clock and active throttle reasons of the
+        samples taken in [t0, t1] (all samples so far if none fell inside)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)   # let the sampler write the window's last line
+        rows = self._rows()
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
         use = inside if inside else rows
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
@@ -185,7 +211,8 @@ class ClockSampler:
         reasons = sorted({n for r in use for n, v in zip(names, r[3]) if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
                 "reasons": reasons, "samples": len(inside),
-                "window": "timed region" if inside else "whole run (timed region too short to sample)"}
+                "window": ("timed steps, per-launch blocks and e2e steps" if inside
+                           else "whole run (timed window too short to sample)")}
 
 
 # --------------------------------------------------------------- distributed
@@ -220,93 +247,227 @@ def dist_barrier(world: int, device=None):
             dist.barrier()
 
 
+# -------------------------------------------------------------- GPU timing
+
+def gpu_lead(dev):
+    """Keep the GPU busy for about a millisecond (a spin kernel, outside any
+    timed interval) so that the host has enqueued the first timed launches
+    before the start event is reached: the interval then holds device time
+    only, not the host's first launch latency."""
+    import torch
+    torch.cuda._sleep(2_000_000)
+
+
+def timed_steps(fn, K: int, world: int, dev) -> float:
+    """Exactly K calls of fn between two events, bracketed by a barrier and a
+    device synchronisation on both sides; milliseconds, max over ranks."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    gpu_lead(dev)
+    start.record(stream)
+    for _ in range(K):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world, dev)
+    return dist_max(start.elapsed_time(end), world, dev)
+
+
+def per_launch(fn, n: int, world: int, dev, before=None) -> dict:
+    """n calls of fn, each bracketed by its own pair of events (``before``,
+    if given, runs outside the events ahead of each call). Returns the
+    median, mean and spread in ms (median max over ranks)."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    gpu_lead(dev)
+    for a, b in ev:
+        if before is not None:
+            before()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(world, dev)
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    q = lambda f: ms[min(len(ms) - 1, int(f * len(ms)))]
+    return {"median_ms": dist_max(statistics.median(ms), world, dev), "mean_ms": statistics.mean(ms),
+            "p10_ms": q(0.1), "p90_ms": q(0.9), "launches": n}
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2, evicting whatever the previous
+    launch left there (a torch fill kernel, run outside the timed events)."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+        self.i = 0
+
+    def __call__(self):
+        self.i += 1
+        self.buf.fill_(self.i)
+
+
+def check_device_error(where: str):
+    from paged_kv_cache_120_gb300 import binding
+    err = binding.pa_get_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err} set during {where}")
+
+
 # ------------------------------------------------------------ oracle timing
 
-def oracle_sample_time(name, plan, pool_bits, q_bits, budget_s: float, start_seq: int = 0,
-                       kv_cache: str = "16bit"):
-    """Time the oracle's decode on whole sequences (round-robin from
-    start_seq) until about budget_s of CPU time is spent. Returns
-    (seconds, algorithmic bytes covered, sequences, next start)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def pool_host_bits(t):
+    """Host copy of a tensor's bits: uint16 patterns, or the E4M3 bytes."""
+    import torch
+    if t.dtype == torch.uint8:
+        return t.cpu().numpy()
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def compact_decode_inputs(w, plan, pool, query, cap_bytes: float, kv_elem: int) -> dict:
+    """The oracle's host inputs for the first sequences of a batch (in order,
+    until their K/V bytes reach cap_bytes): their blocks gathered into a
+    small pool (shared blocks once), their tables renumbered into it, their
+    queries. The oracle then walks exactly the blocks the GPU walks."""
+    import torch
+    B = w.block_size
+    L = np.asarray(plan.seq_lens, dtype=np.int64)
+    take, tot = [], 0
+    for s in range(len(L)):
+        take.append(s)
+        tot += int(2 * L[s] * w.num_kv_heads * w.head_size * kv_elem)
+        if tot >= cap_bytes:
+            break
+    nblk = [int((L[s] + B - 1) // B) for s in take]
+    ids = np.concatenate([plan.block_tables[s, :n] for s, n in zip(take, nblk)]).astype(np.int64)
+    uniq, inv = np.unique(ids, return_inverse=True)
+    bt = np.full((len(take), max(1, max(nblk))), -1, dtype=np.int32)
+    o = 0
+    for i, n in enumerate(nblk):
+        bt[i, :n] = inv[o:o + n]
+        o += n
+    idx = torch.from_numpy(uniq).to(pool.device)
+    sub = pool.index_select(1, idx)
+    sel = torch.tensor(take, dtype=torch.long, device=query.device)
+    return {"pool": pool_host_bits(sub), "q": pool_host_bits(query.index_select(0, sel)), "bt": bt,
+            "lens": L[take].astype(np.int32), "num_blocks": int(len(uniq)), "seqs": len(take),
+            "seq_bytes": [algorithmic_bytes(w, [L[s]], 0, 0, kv_elem)["decode"] for s in take]}
+
+
+def oracle_decode_rate(w, h, fp8: bool, budget_s: float, threads: int, batch: int, start: int = 0):
+    """Time the oracle's decode on (sequence, q-head) rows of the compacted
+    inputs h, ``batch`` rows per call, cycling through them, until about
+    budget_s of wall time. A row is credited 1/Hq of its sequence's
+    algorithmic bytes. Returns (seconds, bytes, rows, next start)."""
     import oracle
-    w = workloads.WORKLOADS[name]
-    S = len(plan.seq_lens)
-    done_bytes, n, t = 0, 0, 0.0
-    s = start_seq % S
-    fp8 = kv_cache == "fp8"
-    while t < budget_s and n < S:
-        seqs = np.full(w.num_q_heads, s, dtype=np.int32)
-        heads = np.arange(w.num_q_heads, dtype=np.int32)
+    oracle.set_threads(threads)
+    Hq = w.num_q_heads
+    P = h["seqs"] * Hq
+    t, b, n, k = 0.0, 0.0, 0, start
+    while t < budget_s:
+        r = (np.arange(k, k + batch) % P)
+        seqs, heads = (r // Hq).astype(np.int32), (r % Hq).astype(np.int32)
         t0 = time.perf_counter()
         if fp8:
-            oracle.decode_fp8_sampled(seqs, heads, q_bits, pool_bits, plan.block_tables,
-                                      plan.seq_lens, w.scale, w.num_q_heads, w.num_kv_heads,
-                                      w.head_size, w.num_blocks, w.block_size, w.dtype,
+            oracle.decode_fp8_sampled(seqs, heads, h["q"], h["pool"], h["bt"], h["lens"], w.scale, Hq,
+                                      w.num_kv_heads, w.head_size, h["num_blocks"], w.block_size, w.dtype,
                                       workloads.FP8_K_SCALE, workloads.FP8_V_SCALE)
         else:
-            oracle.decode_sampled(seqs, heads, q_bits, pool_bits, plan.block_tables,
-                                  plan.seq_lens, w.scale, w.num_q_heads, w.num_kv_heads,
-                                  w.head_size, w.num_blocks, w.block_size, w.dtype)
+            oracle.decode_sampled(seqs, heads, h["q"], h["pool"], h["bt"], h["lens"], w.scale, Hq,
+                                  w.num_kv_heads, w.head_size, h["num_blocks"], w.block_size, w.dtype)
         t += time.perf_counter() - t0
-        done_bytes += algorithmic_bytes(w, [plan.seq_lens[s]], 0, 0, 1 if fp8 else 2)["decode"]
-        n += 1
-        s = (s + 1) % S
-    return t, done_bytes, n, s
+        b += sum(h["seq_bytes"][s] for s in seqs) / Hq
+        n += batch
+        k += batch
+    return t, b, n, k
 
 
-def pool_host_bits(pool):
-    """Host copy of a pool's bits: uint16 patterns, or the E4M3 bytes."""
-    import torch
-    if pool.dtype == torch.uint8:
-        return pool.cpu().numpy()
-    return pool.view(torch.int16).cpu().numpy().view(np.uint16)
+def decode_cpu_baseline(w, h, fp8: bool, budget_s: float) -> dict:
+    """The oracle as it stands, on the machine's host cores: single-threaded and
+    on every core (rows spread over OpenMP threads), GB/s of the metric."""
+    import oracle
+    cores = host_cores()
+    t1, b1, n1, _ = oracle_decode_rate(w, h, fp8, budget_s / 2, 1, 1)
+    tn, bn, nn, _ = oracle_decode_rate(w, h, fp8, budget_s / 2, cores, 4 * cores)
+    oracle.set_threads(cores)
+    what = (f"(sequence, q-head) rows of the first {h['seqs']} sequences of the same batch, "
+            f"each credited 1/{w.num_q_heads} of its sequence's bytes")
+    return {"value": bn / tn / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nn} {what} ({tn:.1f} s on {cores} threads, fp64 C with OpenMP over rows)",
+            "single_thread": {"value": b1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} rows ({t1:.1f} s)"},
+            "host_cores": cores}
 
 
-def host_inputs(name, plan, seed, kv_cache="16bit"):
-    """The oracle's host copies of the step's inputs (bit patterns)."""
-    import torch
-    from paged_kv_cache_120_gb300 import step as stepmod
-    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
-    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev, kv_cache)
-    pool_bits, q_bits = pool_host_bits(pool), pool_host_bits(q)
-    del pool
-    return pool_bits, q_bits
+def prefill_rows_inputs(plan, pool, query) -> dict:
+    """Host copies for the prefill oracle: the pool, the queries and, per
+    chunk row, its sequence and number of visible tokens."""
+    cu = plan.cu_seqlens_q
+    rows = int(cu[-1])
+    seq = (np.searchsorted(cu, np.arange(rows), side="right") - 1).astype(np.int64)
+    vis = (plan.seq_lens[seq] - plan.chunk_lens[seq] + (np.arange(rows) - cu[seq]) + 1).astype(np.int32)
+    return {"pool": pool_host_bits(pool), "q": pool_host_bits(query), "seq": seq, "vis": vis, "rows": rows}
 
 
-def run_reference(args, rank, world):
-    """The reference arm: the fp64 oracle on the host cores."""
-    if rank != 0:
-        return
-    from paged_kv_cache_120_gb300 import step as stepmod
-    name = args.workload
-    w = workloads.WORKLOADS[name]
-    plan = stepmod.plan_step(name, args.seed)
-    pool_bits, q_bits = host_inputs(name, plan, args.seed, args.kv_cache)
-    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    nxt = 0
-    for _ in range(args.warmup):
-        _, _, _, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt,
-                                          args.kv_cache)
-    tot_t, tot_b, tot_n = 0.0, 0, 0
-    for _ in range(args.steps):
-        t, b, n, nxt = oracle_sample_time(name, plan, pool_bits, q_bits, per_step, nxt,
-                                          args.kv_cache)
-        tot_t, tot_b, tot_n = tot_t + t, tot_b + b, tot_n + n
-    gbs = tot_b / tot_t / 1e9
-    sample = (f"{tot_n} whole sequences (all {w.num_q_heads} q heads each) of the {name} batch, "
-              f"about {per_step:.2f} s of oracle time per step")
-    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic",
-            "config": workload_config(name, plan, args.kv_cache),
-            "seq_steps_per_s": tot_n / tot_t,
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
-            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+def oracle_prefill_rate(w, plan, h, fp8_scales, budget_s: float, threads: int, batch: int, start: int = 0):
+    """Time the oracle on prefill query rows (all heads of each row; a row is
+    the decode definition over its visible tokens), ``batch`` rows per call,
+    rows visited in a scattered fixed order. Returns (seconds, flops, rows,
+    next start)."""
+    import oracle
+    oracle.set_threads(threads)
+    Hq = w.num_q_heads
+    t, fl, n, k = 0.0, 0, 0, start
+    while t < budget_s:
+        r = (np.arange(k, k + batch) * 7919) % h["rows"]
+        bt = plan.block_tables[h["seq"][r]]
+        vis = h["vis"][r]
+        seqs = np.repeat(np.arange(batch, dtype=np.int32), Hq)
+        heads = np.tile(np.arange(Hq, dtype=np.int32), batch)
+        t0 = time.perf_counter()
+        if fp8_scales is None:
+            oracle.decode_sampled(seqs, heads, h["q"][r], h["pool"], bt, vis, w.scale, Hq, w.num_kv_heads,
+                                  w.head_size, plan.num_blocks, w.block_size, w.dtype)
+        else:
+            oracle.decode_fp8_sampled(seqs, heads, h["q"][r], h["pool"], bt, vis, w.scale, Hq,
+                                      w.num_kv_heads, w.head_size, plan.num_blocks, w.block_size, w.dtype,
+                                      *fp8_scales)
+        t += time.perf_counter() - t0
+        fl += int(4 * w.head_size * Hq * vis.astype(np.int64).sum())
+        n += batch
+        k += batch
+    return t, fl, n, k
 
 
-METRIC = "paged-decode attention achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+def prefill_cpu_baseline(w, plan, h, fp8_scales, budget_s: float) -> dict:
+    import oracle
+    cores = host_cores()
+    t1, f1, n1, _ = oracle_prefill_rate(w, plan, h, fp8_scales, budget_s / 2, 1, 1)
+    tn, fn, nn, _ = oracle_prefill_rate(w, plan, h, fp8_scales, budget_s / 2, cores, cores)
+    oracle.set_threads(cores)
+    return {"value": fn / tn / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nn} query rows x {w.num_q_heads} heads of the same batch ({tn:.1f} s on {cores} "
+                      "threads, fp64 C with OpenMP over rows)",
+            "single_thread": {"value": f1 / t1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"{n1} rows ({t1:.1f} s)"},
+            "host_cores": cores}
 
+
+# -------------------------------------------------------------- configs
 
 def workload_config(name, plan, kv_cache="16bit"):
     w = workloads.WORKLOADS[name]
@@ -325,69 +486,72 @@ def workload_config(name, plan, kv_cache="16bit"):
                    % (ab["kv"] / 1e9))}
 
 
-# -------------------------------------------------------------------- ours
+def prefill_config(name, plan, kv_cache="16bit"):
+    w = workloads.PREFILL_WORKLOADS[name]
+    kvb = 2 * int(plan.seq_lens.sum()) * w.num_kv_heads * w.head_size * (1 if kv_cache == "fp8" else 2)
+    return {"workload": f"{name}: {w.description}", "num_seqs": w.num_seqs,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
+            "block_size": w.block_size, "num_blocks": int(plan.num_blocks),
+            "seq_lens": [int(x) for x in plan.seq_lens], "chunk": w.chunk,
+            "kv_cache": "fp8_e4m3" if kv_cache == "fp8" else "16bit",
+            "l2": "inputs larger than L2: %.0f MB of K/V read per step vs 129 MB L2, no flush" % (kvb / 1e6)}
 
-def run_ours(args, rank, local_rank, world):
+
+def dtype_name(w) -> str:
+    return "f16" if w.dtype == workloads.F16 else "bf16"
+
+
+# ------------------------------------------------------------------ decode
+
+def measure_decode(args, rank, world, dev, clocks, name, kv_cache="16bit", variant="literal",
+                   cpu_budget=0.0, l2_variants=False) -> dict:
+    """One decode workload: exactly args.steps timed steps, then per-launch
+    blocks (the decode alone, the reshape alone, the decode right behind its
+    reshape), then steps end to end from pinned host memory, then (rank 0)
+    the oracle on the host cores. With l2_variants the steps and the decode
+    are also timed with L2 flushed before every iteration."""
     import torch
-    from paged_kv_cache_120_gb300 import binding, build, step as stepmod
-    build.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    name = args.workload
+    from paged_kv_cache_120_gb300 import step as stepmod
     w = workloads.WORKLOADS[name]
     seed = args.seed + 1000 * rank
-    plan = stepmod.plan_step(name, seed, args.variant)
-    if args.layers > 1:
-        return run_model_step(args, rank, world, dev, name, plan, seed)
-    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev, args.kv_cache)
+    plan = stepmod.plan_step(name, seed, variant)
+    pool, q, k, v = stepmod.make_device_inputs(name, plan, seed, dev, kv_cache)
     st = stepmod.DecodeStep(name, plan, pool, q, k, v, dev)
+    kv_elem = 1 if st.fp8 else 2
     n_tokens = int((plan.slot_mapping >= 0).sum())
-    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens,
-                           1 if st.fp8 else 2)
-    stream = torch.cuda.current_stream(dev)
+    ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens, kv_elem)
+    kv_u = unique_kv_bytes(w, plan.seq_lens, plan.block_tables, kv_elem)
+    roof_bytes = ab["decode"] - ab["kv"] + kv_u
+    K = args.steps
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize(dev)
-    if binding.pa_get_device_error() != 0:
-        raise RuntimeError("device error word set during warm-up")
+    check_device_error("warm-up")
 
-    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    K = args.steps
-    # Every EV_EVERY-th step brackets its pa_decode with events (for the
-    # roofline's per-launch duration). An event between reshape and decode
-    # stops the decode from starting under the reshape's tail, so sampling
-    # keeps that cost out of most steps.
-    EV_EVERY = 8
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range((K + EV_EVERY - 1) // EV_EVERY)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if clocks:
-        clocks.start()
-    dist_barrier(world, dev)
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for i in range(K):
+    def before_decode():
         if st.cow_pairs is not None:
+            from paged_kv_cache_120_gb300 import binding
             binding.pa_copy_blocks([st.pool], st.cow_pairs)
         st.reshape()
-        if i % EV_EVERY == 0:
-            ev[i // EV_EVERY][0].record(stream)
-            st.decode()
-            ev[i // EV_EVERY][1].record(stream)
-        else:
-            st.decode()
-    end.record(stream)
+
+    w0 = time.time()
+    step_ms = timed_steps(st.run, K, world, dev) / K
+    dec = per_launch(st.decode, LAUNCHES, world, dev)
+    resh = per_launch(st.reshape, LAUNCHES, world, dev)
+    in_step = per_launch(st.decode, 50, world, dev, before=before_decode)
+    flushed = None
+    if l2_variants:
+        fl = L2Flush(dev)
+        st_fl = per_launch(st.run, max(K, 50), world, dev, before=fl)
+        dec_fl = per_launch(st.decode, LAUNCHES, world, dev, before=fl)
+        del fl
+        flushed = {"step_ms": st_fl["mean_ms"], "steps": st_fl["launches"],
+                   "value": world * ab["step"] / (st_fl["mean_ms"] / 1e3) / 1e9,
+                   "decode_only": dict(dec_fl, gbs=ab["decode"] / (dec_fl["median_ms"] / 1e3) / 1e9),
+                   "roofline_achieved_gbs": roof_bytes / (dec_fl["median_ms"] / 1e3) / 1e9}
     torch.cuda.synchronize(dev)
-    dist_barrier(world, dev)
-    if clocks:
-        clocks.stop()
-    t_ms = start.elapsed_time(end)
-    decode_ms = [a.elapsed_time(b) for a, b in ev]
-    t_s = dist_max(t_ms / 1e3, world, dev)
-    dev_err = binding.pa_get_device_error()
-    if dev_err:
-        raise RuntimeError(f"device error word {dev_err} set during the timed region")
+    check_device_error("the timed region")
 
     # End to end through the public step API from pinned host memory: every
     # step copies all of its inputs (one packed buffer) to the device, runs
@@ -400,107 +564,223 @@ def run_ours(args, rank, local_rank, world):
         st.run_pinned()
     dist_barrier(world, dev)
     torch.cuda.synchronize(dev)
-    ke = max(1, min(K, 500))
+    ke = max(1, min(K, 200))
     t0 = time.perf_counter()
     for _ in range(ke):
         st.run_pinned()
-    e2e_s = time.perf_counter() - t0
-    e2e_s = dist_max(e2e_s, world, dev)
+    e2e_s = dist_max(time.perf_counter() - t0, world, dev)
+    w1 = time.time()
     dist_barrier(world, dev)
-
     if rank != 0:
-        return
+        return {}
+
     peak, peak_note = measured_peak()
-    dec_ms = statistics.mean(decode_ms)
-    # shared blocks: the HBM minimum counts each physical block once
-    kv_u = unique_kv_bytes(w, plan.seq_lens, plan.block_tables, 1 if st.fp8 else 2)
-    roof_bytes = ab["decode"] - ab["kv"] + kv_u
+    dec_ms = dec["median_ms"]
     achieved = roof_bytes / (dec_ms / 1e3) / 1e9
-    value = world * ab["step"] * K / t_s / 1e9
-    seq_steps = world * len(plan.seq_lens) * K / t_s
-    traffic = traffic_record("decode_fp8" if args.kv_cache == "fp8" else "decode", name)
-
-    # CPU baseline: the oracle, single-threaded, on a bounded sample.
-    pool_bits, q_bits = pool_host_bits(st.pool), pool_host_bits(st.query)
-    ot, ob, on, _ = oracle_sample_time(name, plan, pool_bits, q_bits, args.cpu_budget, 0,
-                                       args.kv_cache)
-    del pool_bits
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": t_s * 1e3 / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
-        "data": "synthetic (seeded N(0,1) values, seeded block placement)",
-        "config": dict(workload_config(name, plan, args.kv_cache),
-                       kv_l2_policy="normal (blocks shared)" if st.flags else "evict-first (no block shared)"),
-        "seq_steps_per_s": seq_steps,
+    value = world * ab["step"] / (step_ms / 1e3) / 1e9
+    tag = "decode_fp8" if st.fp8 else "decode"
+    rec = {
+        "value": value, "unit": "GB/s", "steps": K, "ms_per_step": step_ms,
+        "dtype": dtype_name(w),
+        "config": workload_config(name, plan, kv_cache),
+        "seq_steps_per_s": world * len(plan.seq_lens) / (step_ms / 1e3),
         "pct_of_nominal_8TBps": 100.0 * value / NOMINAL_HBM_GBS,
         "pct_of_measured_peak": 100.0 * value / peak,
-        "decode_only": {"ms": dec_ms, "gbs": ab["decode"] / (dec_ms / 1e3) / 1e9,
-                        "seq_steps_per_s": len(plan.seq_lens) / (dec_ms / 1e3),
-                        "sampled_launches": len(decode_ms)},
+        "decode_only": dict(dec, gbs=ab["decode"] / (dec_ms / 1e3) / 1e9,
+                            pct_of_nominal_8TBps=100.0 * ab["decode"] / (dec_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                            seq_steps_per_s=len(plan.seq_lens) / (dec_ms / 1e3)),
+        "reshape_only": resh,
+        "decode_in_step": dict(in_step, note="decode launches each bracketed right behind this step's "
+                                             "reshape: the event between them stops the decode's prologue "
+                                             "from overlapping the reshape"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": traffic_record(tag, name + ("_fork" if variant == "fork" else "")),
                      "kernel": ("pa_decode_fp8" if st.fp8 else "pa_decode")
                                + " (paged_decode_kernel + paged_decode_reduce_kernel)",
+                     "duration": f"median of {dec['launches']} back-to-back launches, CUDA events",
                      "peak_source": peak_note, "bytes_per_launch": roof_bytes,
                      "bytes_basis": ("unique physical blocks (shared blocks once); logical "
                                      f"{ab['decode']} B per launch") if kv_u < ab["kv"] else "logical = unique"},
+        "kv_l2_policy": "normal (blocks shared)" if st.flags & 1 else "evict-first (no block shared)",
         "e2e": {"value": world * ab["step"] * ke / e2e_s / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s * 1e3 / ke},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3 / ke,
+                "steps": ke},
         "gpu_launches": st.launches_per_step() * K,
-        "cpu_baseline": {"value": ob / ot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{on} whole sequences x {w.num_q_heads} q heads of the same batch "
-                                   f"({ot:.1f} s, single-threaded fp64 C)"},
-        "clocks": clocks.summary() if clocks else None,
+        "clocks": clocks.summary(w0, w1) if clocks else None,
     }
-    print(json.dumps(line), flush=True)
+    if flushed is not None:
+        rec["config"]["l2"] = ("unflushed: the shared prompt's K/V (64 MB) stay in L2 across steps; "
+                               "see l2_flushed for the same step with L2 flushed before every iteration")
+        rec["l2_flushed"] = dict(flushed, note="a 258 MB buffer written before every iteration, outside the events")
+    if cpu_budget > 0:
+        h = compact_decode_inputs(w, plan, st.pool, st.query, 1.0e9, kv_elem)
+        rec["cpu_baseline"] = decode_cpu_baseline(w, h, st.fp8, cpu_budget)
+    return rec
+
+
+# ----------------------------------------------------------------- prefill
+
+def measure_prefill(args, rank, world, dev, clocks, name, kv_cache="16bit", cpu_budget=0.0) -> dict:
+    """One chunked-prefill workload: exactly args.steps timed steps
+    (reshape + prefill), a per-launch block of the prefill alone, steps end
+    to end from pinned host memory, then (rank 0) the oracle."""
+    import torch
+    from paged_kv_cache_120_gb300 import step as stepmod
+    w = workloads.PREFILL_WORKLOADS[name]
+    seed = args.seed + 1000 * rank
+    plan = stepmod.plan_prefill(name, seed)
+    st = stepmod.PrefillStep(name, plan, seed, dev, kv_cache)
+    flops = stepmod.prefill_flops(plan, w.num_q_heads, w.head_size)
+    K = args.steps
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize(dev)
+    check_device_error("warm-up")
+    w0 = time.time()
+    step_ms = timed_steps(st.run, K, world, dev) / K
+    pre = per_launch(st.prefill, LAUNCHES, world, dev)
+    torch.cuda.synchronize(dev)
+    check_device_error("the timed region")
+    host = st.pin_host()
+    out_host = host.pop("out")
+    h2d = st.pinned_bytes()
+    d2h = out_host.numel() * out_host.element_size()
+    for _ in range(3):
+        st.run_pinned()
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ke = max(1, min(K, 200))
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        st.run_pinned()
+    e2e_s = dist_max(time.perf_counter() - t0, world, dev)
+    w1 = time.time()
+    dist_barrier(world, dev)
+    if rank != 0:
+        return {}
+    peak, peak_note = measured_tensor_peak()
+    achieved = flops / (pre["median_ms"] / 1e3) / 1e12
+    value = world * flops / (step_ms / 1e3) / 1e12
+    tag = "prefill_fp8" if st.fp8 else "prefill"
+    rec = {
+        "value": value, "unit": "TFLOP/s", "steps": K, "ms_per_step": step_ms, "dtype": dtype_name(w),
+        "config": prefill_config(name, plan, kv_cache),
+        "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) / (step_ms / 1e3),
+        "prefill_only": dict(pre, tflops=achieved),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic_record(tag, name[len("prefill_"):]),
+                     "kernel": ("pa_prefill_fp8" if st.fp8 else "pa_prefill") + " (paged_prefill_kernel)",
+                     "duration": f"median of {pre['launches']} back-to-back launches, CUDA events",
+                     "peak_source": peak_note, "flops_per_launch": flops},
+        "e2e": {"value": world * flops * ke / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3 / ke,
+                "steps": ke},
+        "gpu_launches": st.launches_per_step() * K,
+        "clocks": clocks.summary(w0, w1) if clocks else None,
+    }
+    if cpu_budget > 0:
+        h = prefill_rows_inputs(plan, st.pool, st.query)
+        rec["cpu_baseline"] = prefill_cpu_baseline(w, plan, h, (st.k_scale, st.v_scale) if st.fp8 else None,
+                                                   cpu_budget)
+    return rec
+
+
+# The default run's other workloads: (key, kind, workload, cache, variant, L2 variants).
+EXTRA_CONFIGS = (
+    ("gqa8b", "decode", "gqa8b", "16bit", "literal", False),
+    ("longctx", "decode", "longctx", "16bit", "literal", False),
+    ("prefix_cow", "decode", "prefix_cow", "16bit", "literal", True),
+    ("prefix_cow_fork", "decode", "prefix_cow", "16bit", "fork", True),
+    ("llama13b_fp8", "decode", "llama13b", "fp8", "literal", False),
+    ("gqa8b_fp8", "decode", "gqa8b", "fp8", "literal", False),
+    ("longctx_fp8", "decode", "longctx", "fp8", "literal", False),
+    ("prefill_llama13b", "prefill", "prefill_llama13b", "16bit", None, False),
+    ("prefill_gqa8b", "prefill", "prefill_gqa8b", "16bit", None, False),
+    ("prefill_llama13b_fp8", "prefill", "prefill_llama13b", "fp8", None, False),
+    ("prefill_gqa8b_fp8", "prefill", "prefill_gqa8b", "fp8", None, False),
+)
+
+
+def top_line(rec: dict, args, world, metric, data) -> dict:
+    """The contract's JSON line around a measured record."""
+    line = {"metric": metric, "value": rec["value"], "unit": rec["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": rec["dtype"],
+            "data": data, "config": rec["config"]}
+    for k, v in rec.items():
+        if k not in line and k not in ("steps",):
+            line[k] = v
+    return line
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    from paged_kv_cache_120_gb300 import build
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    try:
+        if args.layers > 1:
+            from paged_kv_cache_120_gb300 import step as stepmod
+            plan = stepmod.plan_step(args.workload, args.seed + 1000 * rank, args.variant)
+            return run_model_step(args, rank, world, dev, clocks, args.workload, plan, args.seed + 1000 * rank)
+        prefill = args.workload in workloads.PREFILL_WORKLOADS
+        if prefill:
+            rec = measure_prefill(args, rank, world, dev, clocks, args.workload, args.kv_cache, args.cpu_budget)
+            metric, data = PREFILL_METRIC, "synthetic (seeded N(0,1) values, seeded block placement)"
+        else:
+            rec = measure_decode(args, rank, world, dev, clocks, args.workload, args.kv_cache, args.variant,
+                                 args.cpu_budget, l2_variants=args.workload == "prefix_cow")
+            metric, data = METRIC, "synthetic (seeded N(0,1) values, seeded block placement)"
+        configs = {}
+        default_run = (args.workload == "llama13b" and args.kv_cache == "16bit" and args.variant == "literal"
+                       and not args.no_configs)
+        if default_run:
+            for key, kind, name, kv, variant, l2v in EXTRA_CONFIGS:
+                torch.cuda.empty_cache()
+                budget = args.cpu_budget * 0.4
+                if kind == "decode":
+                    configs[key] = measure_decode(args, rank, world, dev, clocks, name, kv, variant, budget, l2v)
+                else:
+                    configs[key] = measure_prefill(args, rank, world, dev, clocks, name, kv, budget)
+        if rank == 0:
+            line = top_line(rec, args, world, metric, data)
+            if configs:
+                line["configs"] = configs
+            print(json.dumps(line), flush=True)
+    finally:
+        if clocks:
+            clocks.close()
 
 
 # ------------------------------------------------------------- model step
 
-def run_model_step(args, rank, world, dev, name, plan, seed):
+def run_model_step(args, rank, world, dev, clocks, name, plan, seed):
     """A decode step of a whole model: COW copies in every layer pool (one
     pa_copy_blocks call), then reshape_and_cache + decode for each of
     args.layers layers, eagerly or replayed from a CUDA graph (--graph)."""
     import torch
-    from paged_kv_cache_120_gb300 import binding, step as stepmod
+    from paged_kv_cache_120_gb300 import step as stepmod
     w = workloads.WORKLOADS[name]
     ms = stepmod.ModelStep(name, plan, args.layers, seed, dev, args.kv_cache)
     fp8 = ms.layers[0].fp8
     n_tokens = int((plan.slot_mapping >= 0).sum())
     ab = algorithmic_bytes(w, plan.seq_lens, len(plan.cow_pairs), n_tokens, 1 if fp8 else 2)
     step_bytes = args.layers * ab["step"]
-    for _ in range(max(3, args.warmup)):
+    for _ in range(args.warmup):
         ms.run()
     if args.graph:
         ms.capture()
         for _ in range(3):
             ms.run()
     torch.cuda.synchronize(dev)
-    if binding.pa_get_device_error() != 0:
-        raise RuntimeError("device error word set during warm-up")
-    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    K = max(1, args.steps // args.layers)
-    stream = torch.cuda.current_stream(dev)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if clocks:
-        clocks.start()
-    dist_barrier(world, dev)
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for _ in range(K):
-        ms.run()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    dist_barrier(world, dev)
-    if clocks:
-        clocks.stop()
-    t_s = dist_max(start.elapsed_time(end) / 1e3, world, dev)
-    if binding.pa_get_device_error():
-        raise RuntimeError("device error word set during the timed region")
+    check_device_error("warm-up")
+    K = args.steps
+    w0 = time.time()
+    t_s = timed_steps(ms.run, K, world, dev) / 1e3
+    w1 = time.time()
+    check_device_error("the timed region")
     if rank != 0:
         return
     peak, peak_note = measured_peak()
@@ -511,8 +791,7 @@ def run_model_step(args, rank, world, dev, name, plan, seed):
     line = {
         "metric": METRIC, "value": world * step_bytes * K / t_s / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": t_s * 1e3 / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(w),
         "data": "synthetic (seeded N(0,1) values per layer, seeded block placement)",
         "config": dict(workload_config(name, plan, args.kv_cache), layers=args.layers,
                        launch="CUDA graph replay" if args.graph else "eager",
@@ -528,167 +807,7 @@ def run_model_step(args, rank, world, dev, name, plan, seed):
                      "bytes_basis": ("unique physical blocks (shared blocks once); logical "
                                      f"{step_bytes} B per step") if kv_u < ab["kv"] else "logical = unique"},
         "gpu_launches": ms.launches_per_step() * K,
-        "clocks": clocks.summary() if clocks else None,
-    }
-    print(json.dumps(line), flush=True)
-
-
-# ------------------------------------------------------------------ prefill
-
-PREFILL_METRIC = "paged chunked-prefill causal attention TFLOP/s"
-
-
-def measured_tensor_peak():
-    """Sustained dense bf16 TFLOP/s (the prefill step is timed inside a long
-    loop); fp16 runs at the same nominal rate."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            d = json.load(f)
-        return float(d["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS)"
-    except Exception:
-        return 1700.0, "fallback 1.7 PFLOP/s sustained (MEASURED_PEAKS.json absent)"
-
-
-def prefill_config(name, plan):
-    w = workloads.PREFILL_WORKLOADS[name]
-    return {"workload": f"{name}: {w.description}", "num_seqs": w.num_seqs,
-            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
-            "block_size": w.block_size, "num_blocks": int(plan.num_blocks),
-            "seq_lens": [int(x) for x in plan.seq_lens], "chunk": w.chunk,
-            "l2": "K/V of all sequences read per step (~%.0f MB) and reused across query tiles; no flush"
-                  % (2 * int(plan.seq_lens.sum()) * w.num_kv_heads * w.head_size * 2 / 1e6)}
-
-
-def oracle_prefill_sample(name, plan, pool_bits, q_bits, budget_s: float, start: int = 0, fp8_scales=None):
-    """The oracle on prefill rows (every query head of one chunk row at a
-    time, round-robin over rows) for about budget_s. Returns (seconds, flops
-    covered, rows, next start)."""
-    import oracle
-    w = workloads.PREFILL_WORKLOADS[name]
-    S = len(plan.seq_lens)
-    rows = int(plan.cu_seqlens_q[-1])
-    t, flops, n = 0.0, 0, 0
-    k = start
-    heads = np.arange(w.num_q_heads, dtype=np.int32)
-    while t < budget_s and n < rows:
-        row = (k * 7919) % rows
-        s = int(np.searchsorted(plan.cu_seqlens_q, row, side="right") - 1)
-        i = row - int(plan.cu_seqlens_q[s])
-        vis = int(plan.seq_lens[s]) - int(plan.chunk_lens[s]) + i + 1
-        t0 = time.perf_counter()
-        if fp8_scales is None:
-            oracle.decode_sampled(np.zeros(w.num_q_heads, np.int32), heads, q_bits[row:row + 1], pool_bits,
-                                  plan.block_tables[s:s + 1], np.array([vis], np.int32), w.scale,
-                                  w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks, w.block_size,
-                                  w.dtype)
-        else:
-            oracle.decode_fp8_sampled(np.zeros(w.num_q_heads, np.int32), heads, q_bits[row:row + 1], pool_bits,
-                                      plan.block_tables[s:s + 1], np.array([vis], np.int32), w.scale,
-                                      w.num_q_heads, w.num_kv_heads, w.head_size, plan.num_blocks,
-                                      w.block_size, w.dtype, *fp8_scales)
-        t += time.perf_counter() - t0
-        flops += 4 * w.head_size * w.num_q_heads * vis
-        n += 1
-        k += 1
-    return t, flops, n, k
-
-
-def run_prefill(args, rank, local_rank, world):
-    import torch
-    from paged_kv_cache_120_gb300 import binding, build, step as stepmod
-    build.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    name = args.workload
-    w = workloads.PREFILL_WORKLOADS[name]
-    seed = args.seed + 1000 * rank
-    plan = stepmod.plan_prefill(name, seed)
-    st = stepmod.PrefillStep(name, plan, seed, dev, args.kv_cache)
-    flops = stepmod.prefill_flops(plan, w.num_q_heads, w.head_size)
-    stream = torch.cuda.current_stream(dev)
-    for _ in range(max(3, args.warmup)):
-        st.run()
-    torch.cuda.synchronize(dev)
-    if binding.pa_get_device_error() != 0:
-        raise RuntimeError("device error word set during warm-up")
-    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    K = args.steps
-    EV_EVERY = 8
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range((K + EV_EVERY - 1) // EV_EVERY)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if clocks:
-        clocks.start()
-    dist_barrier(world, dev)
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for i in range(K):
-        st.reshape()
-        if i % EV_EVERY == 0:
-            ev[i // EV_EVERY][0].record(stream)
-            st.prefill()
-            ev[i // EV_EVERY][1].record(stream)
-        else:
-            st.prefill()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    dist_barrier(world, dev)
-    if clocks:
-        clocks.stop()
-    t_s = dist_max(start.elapsed_time(end) / 1e3, world, dev)
-    pre_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    dev_err = binding.pa_get_device_error()
-    if dev_err:
-        raise RuntimeError(f"device error word {dev_err} set during the timed region")
-
-    # End to end from pinned host memory, as for decode: every step copies
-    # its packed inputs in and its output back.
-    host = st.pin_host()
-    out_host = host.pop("out")
-    h2d = st.pinned_bytes()
-    d2h = out_host.numel() * out_host.element_size()
-    for _ in range(3):
-        st.run_pinned()
-    dist_barrier(world, dev)
-    torch.cuda.synchronize(dev)
-    ke = max(1, min(K, 200))
-    t0 = time.perf_counter()
-    for _ in range(ke):
-        st.run_pinned()
-    e2e_s = dist_max(time.perf_counter() - t0, world, dev)
-    dist_barrier(world, dev)
-    if rank != 0:
-        return
-    peak, peak_note = measured_tensor_peak()
-    achieved = flops / (pre_ms / 1e3) / 1e12
-    value = world * flops * K / t_s / 1e12
-    pool_bits = (st.pool.cpu().numpy() if st.fp8 else st.pool.view(torch.int16).cpu().numpy().view(np.uint16))
-    q_bits = st.query.view(torch.int16).cpu().numpy().view(np.uint16)
-    ot, of, on, _ = oracle_prefill_sample(name, plan, pool_bits, q_bits, args.cpu_budget, 0,
-                                          (st.k_scale, st.v_scale) if st.fp8 else None)
-    del pool_bits
-    line = {
-        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": t_s * 1e3 / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if w.dtype == workloads.F16 else "bf16",
-        "data": "synthetic (seeded N(0,1) values, seeded block placement)",
-        "config": dict(prefill_config(name, plan), kv_cache="fp8_e4m3" if st.fp8 else "16bit"),
-        "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) * K / t_s,
-        "prefill_only": {"ms": pre_ms, "tflops": achieved, "sampled_launches": len(ev)},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic_record("prefill_fp8" if st.fp8 else "prefill",
-                                                                    name[len("prefill_"):]),
-                     "kernel": ("pa_prefill_fp8" if st.fp8 else "pa_prefill") + " (paged_prefill_kernel)",
-                     "peak_source": peak_note, "flops_per_launch": flops},
-        "e2e": {"value": world * flops * ke / e2e_s / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3 / ke},
-        "gpu_launches": st.launches_per_step() * K,
-        "cpu_baseline": {"value": of / ot / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{on} query rows x {w.num_q_heads} heads of the same batch "
-                                   f"({ot:.1f} s, single-threaded fp64 C)"},
-        "clocks": clocks.summary() if clocks else None,
+        "clocks": clocks.summary(w0, w1) if clocks else None,
     }
     print(json.dumps(line), flush=True)
 
@@ -779,7 +898,7 @@ def run_prefix_cache(args, rank, local_rank, world):
         return int((4 * D * Hq * ((2 * hits + 1 + n_new) * n_new // 2)).sum())
 
     host_s = [0.0]
-    for i in range(max(3, args.warmup)):
+    for i in range(args.warmup):
         wave(waves[i % len(waves)], host_s)
     torch.cuda.synchronize(dev)
     if binding.pa_get_device_error() != 0:
@@ -787,8 +906,7 @@ def run_prefix_cache(args, rank, local_rank, world):
     host_s = [0.0]
     K = args.steps
     clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    if clocks:
-        clocks.start()
+    w0 = time.time()
     dist_barrier(world, dev)
     torch.cuda.synchronize(dev)
     computed = served = 0
@@ -803,10 +921,12 @@ def run_prefix_cache(args, rank, local_rank, world):
     t_s = dist_max(time.perf_counter() - t0, world, dev)
     flops = sum(wave_flops(h, n) for h, n in counts)
     dist_barrier(world, dev)
-    if clocks:
-        clocks.stop()
+    w1 = time.time()
     if binding.pa_get_device_error():
         raise RuntimeError("device error word set during the timed region")
+    if clocks:
+        summary = clocks.summary(w0, w1)
+        clocks.close()
     if rank != 0:
         return
     pre_ms = sum(a.elapsed_time(b) for a, b in events) / K
@@ -832,7 +952,7 @@ def run_prefix_cache(args, rank, local_rank, world):
                      "peak_source": peak_note, "flops_per_launch": flops / K},
         "cpu_baseline": cpu,
         "gpu_launches": 2 * K,
-        "clocks": clocks.summary() if clocks else None,
+        "clocks": summary,
     }
     print(json.dumps(line), flush=True)
 
@@ -868,6 +988,8 @@ def prefix_wave_cpu_baseline(args, cfg, waves, host, pool, q, maxb, scale):
     sl = host["seq_lens"].numpy().copy()
     bt = host["block_tables"].numpy().reshape(R, maxb).copy()
     heads = np.arange(Hq, dtype=np.int32)
+    cores = host_cores()
+    oracle.set_threads(cores)
     rows = int(cu[R])
     t_att, fl, n, k = 0.0, 0, 0, 0
     while t_att < budget * 2 / 3 and n < rows:
@@ -886,47 +1008,66 @@ def prefix_wave_cpu_baseline(args, cfg, waves, host, pool, q, maxb, scale):
     last_flops = float((4 * D * Hq * ((2 * hits + 1 + n_new) * n_new // 2)).sum())
     served = float(sl.astype(np.int64).sum())
     wave_s = t_adm / n_adm + last_flops / (fl / t_att)
-    return {"value": served / wave_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"pool model over {n_adm} whole waves ({1e3 * t_adm / n_adm:.1f} ms/wave) + attention "
-                      f"oracle on {n} query rows of the last wave x {Hq} heads ({fl / t_att / 1e9:.2f} GFLOP/s), "
-                      f"scaled to that wave's {last_flops / 1e9:.1f} GFLOP"}
+    return {"value": served / wave_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"pool model (one thread) over {n_adm} whole waves ({1e3 * t_adm / n_adm:.1f} ms/wave) + "
+                      f"attention oracle (heads of a row over {cores} threads) on {n} query rows of the last "
+                      f"wave x {Hq} heads ({fl / t_att / 1e9:.2f} GFLOP/s), scaled to that wave's "
+                      f"{last_flops / 1e9:.1f} GFLOP"}
 
 
-def run_prefill_reference(args, rank, world):
-    """The reference arm for a prefill workload: the oracle on sampled rows."""
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on the host cores (every core,
+    rows over OpenMP threads), each step a bounded sample of the workload."""
     if rank != 0:
         return
     import torch
     from paged_kv_cache_120_gb300 import step as stepmod
     name = args.workload
-    w = workloads.PREFILL_WORKLOADS[name]
-    plan = stepmod.plan_prefill(name, args.seed)
-    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
-    st = stepmod.PrefillStep(name, plan, args.seed, dev, args.kv_cache)
-    pool_bits = (st.pool.cpu().numpy() if st.fp8 else st.pool.view(torch.int16).cpu().numpy().view(np.uint16))
-    q_bits = st.query.view(torch.int16).cpu().numpy().view(np.uint16)
-    scales = (st.k_scale, st.v_scale) if st.fp8 else None
-    del st
     per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
+    cores = host_cores()
+    if name in workloads.PREFILL_WORKLOADS:
+        w = workloads.PREFILL_WORKLOADS[name]
+        plan = stepmod.plan_prefill(name, args.seed)
+        st = stepmod.PrefillStep(name, plan, args.seed, dev, args.kv_cache)
+        h = prefill_rows_inputs(plan, st.pool, st.query)
+        scales = (st.k_scale, st.v_scale) if st.fp8 else None
+        del st
+        rate = lambda b, k: oracle_prefill_rate(w, plan, h, scales, b, cores, cores, k)
+        metric, unit, scale_unit = PREFILL_METRIC, "TFLOP/s", 1e12
+        config = prefill_config(name, plan, args.kv_cache)
+        what = f"query rows x {w.num_q_heads} heads of the {name} batch"
+    else:
+        w = workloads.WORKLOADS[name]
+        plan = stepmod.plan_step(name, args.seed, args.variant)
+        pool, q, _, _ = stepmod.make_device_inputs(name, plan, args.seed, dev, args.kv_cache)
+        fp8 = args.kv_cache == "fp8"
+        h = compact_decode_inputs(w, plan, pool, q, 1.0e9, 1 if fp8 else 2)
+        del pool, q
+        rate = lambda b, k: oracle_decode_rate(w, h, fp8, b, cores, 4 * cores, k)
+        metric, unit, scale_unit = METRIC, "GB/s", 1e9
+        config = workload_config(name, plan, args.kv_cache)
+        what = (f"(sequence, q-head) rows of the first {h['seqs']} sequences of the {name} batch, each "
+                f"credited 1/{w.num_q_heads} of its sequence's bytes")
     nxt = 0
     for _ in range(args.warmup):
-        _, _, _, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt, scales)
-    tt, tf, tn = 0.0, 0, 0
+        _, _, _, nxt = rate(per_step, nxt)
+    tot_t, tot_x, tot_n = 0.0, 0.0, 0
     for _ in range(args.steps):
-        a, b, c, nxt = oracle_prefill_sample(name, plan, pool_bits, q_bits, per_step, nxt, scales)
-        tt, tf, tn = tt + a, tf + b, tn + c
-    v = tf / tt / 1e12
-    sample = f"{tn} query rows x {w.num_q_heads} heads of the {name} batch, about {per_step:.2f} s per step"
-    print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "TFLOP/s",
-                      "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-                      "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True, "scaling": "weak",
-                      "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                      "config": dict(prefill_config(name, plan),
-                                     kv_cache="fp8_e4m3" if scales else "16bit"),
-                      "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                                       "sample": sample},
-                      "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
-                              "d2h_bytes_per_step": 0}}), flush=True)
+        t, x, n, nxt = rate(per_step, nxt)
+        tot_t, tot_x, tot_n = tot_t + t, tot_x + x, tot_n + n
+    v = tot_x / tot_t / scale_unit
+    sample = (f"{tot_n} {what}, about {per_step:.2f} s per step on {cores} threads "
+              "(fp64 C, OpenMP over rows)")
+    line = {"impl": "reference", "metric": metric, "value": v, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
 
 
 def main():
@@ -947,9 +1088,11 @@ def main():
                     help="decode workloads: layers per model step (one pool per layer)")
     ap.add_argument("--graph", action="store_true",
                     help="with --layers: replay the model step from a CUDA graph")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default workload: skip the records of the other workloads")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-budget", type=float, default=15.0,
-                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the main cpu_baseline (0.4x for each other config)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -961,15 +1104,10 @@ def main():
                                   "bookkeeping plus pa_prefill; its oracle arm is the prefill one"}))
         else:
             run_prefix_cache(args, rank, local_rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-    prefill = args.workload in workloads.PREFILL_WORKLOADS
-    if args.impl == "reference":
-        (run_prefill_reference(args, rank, world) if prefill else run_reference(args, rank, world))
+    elif args.impl == "reference":
+        run_reference(args, rank, world)
     else:
-        (run_prefill(args, rank, local_rank, world) if prefill else run_ours(args, rank, local_rank, world))
+        run_ours(args, rank, local_rank, world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
