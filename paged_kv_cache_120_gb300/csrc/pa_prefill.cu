@@ -229,6 +229,74 @@ __device__ __forceinline__ float add_pair(float acc, uint32_t w)
     return acc;
 }
 
+// Two fp32 lanes at once (the packed .f32x2 forms: one instruction each).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpk2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// 2^x0, 2^x1 on the FMA pipe, without the MUFU unit that ex2 uses: x = j + f
+// with j = round(x) (adding and subtracting 1.5 * 2^23 rounds to an integer
+// in fp32 for |x| < 2^22) and f in [-1/2, 1/2] exact, then p(f) ~ 2^f by the
+// minimax polynomial of degree DEG (coefficients from a Remez exchange fit of
+// the relative error, printed by paged_kv_cache_120_gb300/exp2_poly.py; max
+// relative error 7.5e-5 at degree 3, 2.7e-6 at degree 4), then j added to
+// p's exponent field. Inputs below -126 are clamped there (2^-126 or less
+// rounds to zero or to a negligible subnormal in the 16-bit P); NaN stays
+// NaN (max.NaN keeps it, and the exponent add leaves NaN bits NaN).
+template <int DEG>
+__device__ __forceinline__ void exp2_poly2(uint64_t x2, float &y0, float &y1)
+{
+    float x0, x1;
+    unpk2(x2, x0, x1);
+    asm("max.NaN.f32 %0, %0, 0fC2FC0000;" : "+f"(x0));  // -126
+    asm("max.NaN.f32 %0, %0, 0fC2FC0000;" : "+f"(x1));
+    const uint64_t xv = pk2(x0, x1);
+    const uint64_t magic = pk2(12582912.f, 12582912.f), nmagic = pk2(-12582912.f, -12582912.f);
+    const uint64_t j = add2(xv, magic);           // round(x) in the low mantissa bits
+    const uint64_t t = add2(j, nmagic);           // round(x) as a float
+    uint64_t f;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(f) : "l"(xv), "l"(t));
+    uint64_t p;
+    if constexpr (DEG == 4) {
+        p = fma2(pk2(0x1.3997d6p-7f, 0x1.3997d6p-7f), f, pk2(0x1.ca1440p-5f, 0x1.ca1440p-5f));
+        p = fma2(p, f, pk2(0x1.ec06dap-3f, 0x1.ec06dap-3f));
+        p = fma2(p, f, pk2(0x1.62e0dcp-1f, 0x1.62e0dcp-1f));
+        p = fma2(p, f, pk2(0x1.ffffe8p-1f, 0x1.ffffe8p-1f));
+    } else {
+        static_assert(DEG == 3, "degree 3 or 4");
+        p = fma2(pk2(0x1.c3f760p-5f, 0x1.c3f760p-5f), f, pk2(0x1.f0de1ap-3f, 0x1.f0de1ap-3f));
+        p = fma2(p, f, pk2(0x1.62f31ap-1f, 0x1.62f31ap-1f));
+        p = fma2(p, f, pk2(0x1.fff692p-1f, 0x1.fff692p-1f));
+    }
+    float p0, p1, j0, j1;
+    unpk2(p, p0, p1);
+    unpk2(j, j0, j1);
+    y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(j0) << 23));
+    y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(j1) << 23));
+}
+
 // 32 consecutive 32-bit columns of this thread's TMEM lane from raw words.
 __device__ __forceinline__ void tc_st32u(uint32_t taddr, const uint32_t *v)
 {
@@ -272,6 +340,15 @@ constexpr int kStageBytes8 = 128 * 128;    // an FP8 K or V tile as loaded, befo
 constexpr int kSmemBytes = 2 * kTileBytes + 3 * kTileBytes + kVStages * kTileBytes + 1024;  // + align slack
 constexpr uint32_t kTmemCols = 512;        // S/P of tiles A and B, then O of A and B, 128 columns each
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
+// If > 0: in a full score tile, every kPolyEvery-th pair of exponentials is
+// computed by a polynomial on the FMA pipe instead of the MUFU unit. Off: on
+// GB300 the softmax is bound by instruction latency, not by the MUFU unit,
+// and the extra instructions cost more than they relieve (measured: every
+// 3rd pair made the Llama-2-13B-shaped prefill 12% slower).
+#ifndef PA_PREFILL_POLY_EVERY
+#define PA_PREFILL_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = PA_PREFILL_POLY_EVERY;
 constexpr int kUnitSlots = 4;              // ring of unit indices handed from the scheduler to every role
 // Unit consumers (one arrival each): K, V and MMA warps and the 8 softmax
 // warps; with an FP8 cache the 4 widening warps instead of K and V.
@@ -669,11 +746,16 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         if (lane == 0) {
             const uint32_t id_s = instr_desc(kM, kN, kMmaBF16, false);
             const uint32_t id_o = instr_desc(kM, D, kMmaBF16, true);
+            // Descriptors are built once per operand tile; each k step adds
+            // its byte offset / 16 to the start-address field (bits 0-13,
+            // which cannot carry: shared memory ends below 256 KB).
             auto issue_s = [&](int x, int ks) {
+                const uint64_t dq = smem_desc(sQ(x), 16, 1024), dk = smem_desc(sK(ks), 16, 1024);
+                const uint32_t ts = tS(x);
+#pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-                    tc_mma(tS(x), smem_desc(sQ(x) + off, 16, 1024), smem_desc(sK(ks) + off, 16, 1024), id_s,
-                           k > 0 ? 1u : 0u);
+                    const uint64_t off = (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4);
+                    tc_mma(ts, dq + off, dk + off, id_s, k > 0 ? 1u : 0u);
                 }
                 tc_commit(b_s(x));
             };
@@ -722,8 +804,11 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         // O_x += P_x V: A = P from TMEM (8 columns per 16
                         // tokens), B = V (MN-major: 64-dim chunks 16 KB apart,
                         // 8-token groups 1 KB apart).
+                        const uint64_t dv = smem_desc(sV(vs), kChunkBytes, 1024);
+                        const uint32_t to = tO(x), ts = tS(x);
+#pragma unroll
                         for (int k = 0; k < kN / 16; ++k)
-                            tc_mma_ts(tO(x), tS(x) + k * 8, smem_desc(sV(vs) + k * 2048, kChunkBytes, 1024), id_o,
+                            tc_mma_ts(to, ts + k * 8, dv + (uint64_t)(k * (2048 >> 4)), id_o,
                                       (j > 0 || k > 0) ? 1u : 0u);
                         tc_commit(b_pv(x));
                         ++gx[x];
@@ -903,7 +988,29 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         else
                             return ex2(__fmul_rn(s, sc) - ref);
                     };
-                    if (full) {
+                    if (full && decltype(fused)::value) {
+                        // The common case, two columns per step: the argument
+                        // by one packed fused multiply-add (the same value as
+                        // fmaf), then 2^x from the MUFU unit (or, every
+                        // kPolyEvery-th pair if enabled, from the FMA-pipe
+                        // polynomial).
+                        const uint64_t sc2 = pk2(sc, sc), nref2 = pk2(-ref, -ref);
+#pragma unroll
+                        for (int c = 0; c < kN / 2; ++c) {
+                            const uint64_t x2 = fma2(pk2(sv[2 * c], sv[2 * c + 1]), sc2, nref2);
+                            float p0, p1;
+                            if (kPolyEvery > 0 && c % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1) {
+                                exp2_poly2<kMmaBF16 ? 3 : 4>(x2, p0, p1);
+                            } else {
+                                float x0, x1;
+                                unpk2(x2, x0, x1);
+                                p0 = ex2(x0);
+                                p1 = ex2(x1);
+                            }
+                            pw[c] = pack2<kMmaBF16>(p0, p1);
+                            l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
+                        }
+                    } else if (full) {
 #pragma unroll
                         for (int c = 0; c < kN / 2; ++c) {
                             pw[c] = pack2<kMmaBF16>(p_of(sv[2 * c]), p_of(sv[2 * c + 1]));
