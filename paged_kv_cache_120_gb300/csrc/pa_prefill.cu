@@ -19,7 +19,8 @@
 //    run on across units.
 //  * Loads. Warp 8 brings the K tiles and warp 10 the V tiles by TMA
 //    (16-token boxes through the block table, 128-byte swizzle) into rings
-//    of three K and two V stages. With an FP8 cache, warps 12-15 instead
+//    of two K and three V stages (a V stage is released as soon as its last
+//    P V is issued). With an FP8 cache (two and two), warps 12-15 instead
 //    bring the codes into staging buffers and widen them exactly into fp16
 //    ring stages (two K stages then); the MMAs then run in fp16, and bf16
 //    queries are moved to fp16 row by row under a power-of-two scale that
@@ -329,15 +330,22 @@ constexpr int kBoxTokens = 16;             // tokens per K/V TMA box (block_size
 constexpr int kThreads16 = 384, kThreads8 = 512;
 __host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? kThreads8 : kThreads16; }
 constexpr int kWarpK = 8, kWarpMMA = 9, kWarpV = 10, kWarpQ = 11;
-constexpr int kKStagesMax = 3;             // K ring (freed when both tiles' S = Q K^T are done):
-constexpr int kKStages16 = 3, kKStages8 = 2;  // 3 stages, 2 with an FP8 cache (room for staging)
-constexpr int kVStages = 2;                // V ring (freed when both tiles' O += P V are done)
+// K ring (a stage is freed when both tiles' S = Q K^T are done) and V ring
+// (freed when both tiles' O += P V are done). The V tile is needed first
+// in a K/V step and K one half step later, so V gets the deeper ring: 2 K
+// and 3 V stages with a 16-bit cache, 2 and 2 with an FP8 cache (whose
+// staging buffers take the rest of shared memory).
+constexpr int kKStagesMax = 2, kVStagesMax = 3;
+constexpr int kKStages16 = 2, kKStages8 = 2;
+constexpr int kVStages16 = 3, kVStages8 = 2;
 constexpr int kOffQ = 0;                   // Q of tile A, then of tile B
 constexpr int kOffK = 2 * kTileBytes;
 constexpr int kStageBytes8 = 128 * 128;    // an FP8 K or V tile as loaded, before widening: 16 KB
-// 16-bit cache: Q 64 KB, K 3 x 32, V 2 x 32. FP8 cache: Q 64, K 2 x 32, V 2 x 32,
+// 16-bit cache: Q 64 KB, K 2 x 32, V 3 x 32. FP8 cache: Q 64, K 2 x 32, V 2 x 32,
 // then one FP8 staging tile each for K and V (16 KB each). Both 224 KB.
-constexpr int kSmemBytes = 2 * kTileBytes + 3 * kTileBytes + kVStages * kTileBytes + 1024;  // + align slack
+constexpr int kSmemBytes = 2 * kTileBytes + 5 * kTileBytes + 1024;  // + align slack
+static_assert((kKStages16 + kVStages16) * kTileBytes <= 5 * kTileBytes &&
+              (kKStages8 + kVStages8) * kTileBytes + 2 * kStageBytes8 <= 5 * kTileBytes, "shared memory plan");
 constexpr uint32_t kTmemCols = 512;        // S/P of tiles A and B, then O of A and B, 128 columns each
 constexpr float kRescaleLog2 = 8.f;        // reference-maximum slack (base 2)
 // If > 0: in a full score tile, every kPolyEvery-th pair of exponentials is
@@ -432,7 +440,7 @@ __device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, 
 }
 
 struct PrefillBars {
-    uint64_t q_full, q_empty, k_full[kKStagesMax], k_empty[kKStagesMax], v_full[kVStages], v_empty[kVStages];
+    uint64_t q_full, q_empty, k_full[kKStagesMax], k_empty[kKStagesMax], v_full[kVStagesMax], v_empty[kVStagesMax];
     uint64_t q_ready;  // FP8 cache, bf16 queries: the softmax threads have moved Q to fp16
     uint64_t stg_full[2][2];  // FP8 cache: K / V staging half 0 / 1 has landed
     // Per query tile x: s_full[x] its S is in TMEM, p_full[x] its P is,
@@ -469,6 +477,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     constexpr bool kMmaBF16 = BF16 && !FP8;
     constexpr bool kQToF16 = BF16 && FP8;
     constexpr int kKStages = FP8 ? kKStages8 : kKStages16;
+    constexpr int kVStages = FP8 ? kVStages8 : kVStages16;
     constexpr int kOffV = kOffK + kKStages * kTileBytes;
     constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // FP8: K then V staging tile
     auto sK = [&](int st) { return base + kOffK + st * kTileBytes; };
@@ -812,6 +821,11 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                                       (j > 0 || k > 0) ? 1u : 0u);
                         tc_commit(b_pv(x));
                         ++gx[x];
+                        // The tile's last O += P V is issued: V's stage is
+                        // free once it completes (tile B, if it reads V_j,
+                        // comes after tile A).
+                        if (x == 1 || j >= w.n[1])
+                            tc_commit(b_ve(vs));
                         if (j + 1 < w.n[x]) {
                             if (ks_next < 0) {
                                 ks_next = kc % kKStages;
@@ -832,7 +846,6 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         if (j + 2 == n)
                             tc_commit(b_qe);
                     }
-                    tc_commit(b_ve(vs));
                     ++vc;
                 }
             }
@@ -931,7 +944,18 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     tc_wait_ld();
                 }
                 const int kb = j * kN;
-                const bool full = kb + kN - 1 <= pos;  // every token of the tile visible
+                // Causal mask: a score this row must not see becomes -inf
+                // (+inf for a negative scale): neutral for the extremum
+                // below, and its weight 2^(s scale - ref) is exactly 0, so
+                // the tile then runs the same branch-free code as a full one.
+                // Padding slots past the sequence end (whatever they hold,
+                // NaN included) are masked the same way.
+                if (kb + kN - 1 > pos) {
+                    const float masked = sc_pos ? -INFINITY : INFINITY;
+#pragma unroll
+                    for (int c = 0; c < kN; ++c)
+                        sv[c] = kb + c <= pos ? sv[c] : masked;
+                }
                 // Row maximum in base 2: scale x the largest visible raw score
                 // (the smallest for a negative scale; rounding is monotone, so
                 // this is the largest scaled score exactly); 8 chains.
@@ -939,21 +963,14 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     e8[i] = sc_pos ? -INFINITY : INFINITY;
-                if (full) {
-                    if (sc_pos) {
+                if (sc_pos) {
 #pragma unroll
-                        for (int c = 0; c < kN; c += 2)
-                            e8[(c >> 1) & 7] = max3(e8[(c >> 1) & 7], sv[c], sv[c + 1]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < kN; c += 2)
-                            e8[(c >> 1) & 7] = min3(e8[(c >> 1) & 7], sv[c], sv[c + 1]);
-                    }
+                    for (int c = 0; c < kN; c += 2)
+                        e8[(c >> 1) & 7] = max3(e8[(c >> 1) & 7], sv[c], sv[c + 1]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < kN; ++c)
-                        if (kb + c <= pos)
-                            e8[c & 7] = sc_pos ? fmaxf(e8[c & 7], sv[c]) : fminf(e8[c & 7], sv[c]);
+                    for (int c = 0; c < kN; c += 2)
+                        e8[(c >> 1) & 7] = min3(e8[(c >> 1) & 7], sv[c], sv[c + 1]);
                 }
                 const float e = sc_pos ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])),
                                                fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
@@ -988,12 +1005,11 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         else
                             return ex2(__fmul_rn(s, sc) - ref);
                     };
-                    if (full && decltype(fused)::value) {
-                        // The common case, two columns per step: the argument
-                        // by one packed fused multiply-add (the same value as
-                        // fmaf), then 2^x from the MUFU unit (or, every
-                        // kPolyEvery-th pair if enabled, from the FMA-pipe
-                        // polynomial).
+                    if constexpr (decltype(fused)::value) {
+                        // Two columns per step: the argument by one packed
+                        // fused multiply-add (the same value as fmaf), then
+                        // 2^x from the MUFU unit (or, every kPolyEvery-th
+                        // pair if enabled, from the FMA-pipe polynomial).
                         const uint64_t sc2 = pk2(sc, sc), nref2 = pk2(-ref, -ref);
 #pragma unroll
                         for (int c = 0; c < kN / 2; ++c) {
@@ -1010,18 +1026,10 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                             pw[c] = pack2<kMmaBF16>(p0, p1);
                             l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
                         }
-                    } else if (full) {
-#pragma unroll
-                        for (int c = 0; c < kN / 2; ++c) {
-                            pw[c] = pack2<kMmaBF16>(p_of(sv[2 * c]), p_of(sv[2 * c + 1]));
-                            l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
-                        }
                     } else {
 #pragma unroll
                         for (int c = 0; c < kN / 2; ++c) {
-                            const float p0 = kb + 2 * c <= pos ? p_of(sv[2 * c]) : 0.f;
-                            const float p1 = kb + 2 * c + 1 <= pos ? p_of(sv[2 * c + 1]) : 0.f;
-                            pw[c] = pack2<kMmaBF16>(p0, p1);
+                            pw[c] = pack2<kMmaBF16>(p_of(sv[2 * c]), p_of(sv[2 * c + 1]));
                             l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
                         }
                     }
@@ -1030,6 +1038,19 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     fill(std::true_type{});
                 else
                     fill(std::false_type{});
+                if (sc == 0.f && kb + kN - 1 > pos) {
+                    // Scale 0: a masked score would have given 0 x inf = NaN.
+                    // Every visible token weighs 2^-ref, every masked one 0.
+                    const float pv = ex2(-ref);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        l8[i] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kN / 2; ++c) {
+                        pw[c] = pack2<kMmaBF16>(kb + 2 * c <= pos ? pv : 0.f, kb + 2 * c + 1 <= pos ? pv : 0.f);
+                        l8[c & 7] = add_pair<kMmaBF16>(l8[c & 7], pw[c]);
+                    }
+                }
                 const float ls = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
                 // Rescale O when the reference moved. The previous tile's
                 // O += P V is done: it was issued before this tile's S, whose

@@ -344,3 +344,15 @@ def test_prefill_bf16_queries_with_huge_scores(dev, D):
     want = c.oracle()
     assert max_abs_err_bf16_large(oracle.decode_elems(u16(out), c.dtype), want) <= TOL[c.dtype]
     assert binding.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3, 2.0])
+@pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
+def test_prefill_zero_negative_and_large_scales(dev, scale, dtype):
+    """Causally masked scores must weigh exactly nothing whatever the scale:
+    0 (every visible token weighs the same), negative (the row minimum is
+    the reference), and large; padding slots hold NaN."""
+    c = PrefillCase(dev, dtype, 8, 2, 16, [300, 129, 77, 1], [200, 129, 40, 1], seed=61, poison=True)
+    c.scale = scale
+    out = c.gpu()
+    c.check(out)
