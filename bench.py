@@ -1090,12 +1090,20 @@ def main():
                     help="with --layers: replay the model step from a CUDA graph")
     ap.add_argument("--no-configs", action="store_true",
                     help="default workload: skip the records of the other workloads")
+    ap.add_argument("--pool-blocks", type=int, default=0,
+                    help="decode workloads: pool of this many blocks instead of the workload's (the same "
+                         "sequences and lengths, placement drawn from fewer blocks): small profiling cases")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the main cpu_baseline (0.4x for each other config)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.pool_blocks > 0 and args.workload in workloads.WORKLOADS:
+        import dataclasses
+        w = workloads.WORKLOADS[args.workload]
+        workloads.WORKLOADS[args.workload] = dataclasses.replace(w, num_blocks=args.pool_blocks)
+        args.no_configs = True
     rank, local_rank, world = dist_setup()
     if args.workload == "prefix_cache_prefill":
         if args.impl == "reference":
