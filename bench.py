@@ -639,6 +639,13 @@ def measure_prefill(args, rank, world, dev, clocks, name, kv_cache="16bit", cpu_
     w0 = time.time()
     step_ms = timed_steps(st.run, K, world, dev) / K
     pre = per_launch(st.prefill, LAUNCHES, world, dev)
+    whole = None
+    if st.workspace is not None:
+        # Few work units: the step splits K/V ranges across the SMs. The same
+        # launches with each unit's range whole, for comparison.
+        ws, st.workspace = st.workspace, None
+        whole = per_launch(st.prefill, LAUNCHES, world, dev)
+        st.workspace = ws
     torch.cuda.synchronize(dev)
     check_device_error("the timed region")
     host = st.pin_host()
@@ -667,6 +674,10 @@ def measure_prefill(args, rank, world, dev, clocks, name, kv_cache="16bit", cpu_
         "config": prefill_config(name, plan, kv_cache),
         "tokens_per_s": world * int(plan.cu_seqlens_q[-1]) / (step_ms / 1e3),
         "prefill_only": dict(pre, tflops=achieved),
+        "kv_split": None if whole is None else {
+            "whole_units": dict(whole, tflops=flops / (whole["median_ms"] / 1e3) / 1e12),
+            "speedup": whole["median_ms"] / pre["median_ms"],
+            "workspace_bytes": st.workspace.numel()},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_record(tag, name[len("prefill_"):]),
                      "kernel": ("pa_prefill_fp8" if st.fp8 else "pa_prefill") + " (paged_prefill_kernel)",
@@ -698,6 +709,8 @@ EXTRA_CONFIGS = (
     ("prefill_gqa8b", "prefill", "prefill_gqa8b", "16bit", None, False),
     ("prefill_llama13b_fp8", "prefill", "prefill_llama13b", "fp8", None, False),
     ("prefill_gqa8b_fp8", "prefill", "prefill_gqa8b", "fp8", None, False),
+    ("prefill_longctx_llama13b", "prefill", "prefill_longctx_llama13b", "16bit", None, False),
+    ("prefill_longctx_gqa8b", "prefill", "prefill_longctx_gqa8b", "16bit", None, False),
 )
 
 

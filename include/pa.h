@@ -290,19 +290,44 @@ int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
  *                  length, below)
  *   head_size      64 or 128; the group num_q_heads / num_kv_heads must be <= 16
  *                  or a multiple of 16
+ *   workspace      device, NULL or >= pa_prefill_workspace_size(...) bytes,
+ *                  256-byte aligned; workspace_bytes its size. With few work
+ *                  units (a unit: up to 256 query rows of one sequence and kv
+ *                  head; at most 4 per SM, e.g. a few long sequences with
+ *                  short chunks) and a workspace, the units' K/V ranges are
+ *                  split into equal shares across all SMs and the pieces
+ *                  merged with the rule of [book] §4.6 (partial max, sum and
+ *                  output over disjoint token ranges). NULL: each unit's range
+ *                  stays whole (same result up to fp32 rounding). Its contents
+ *                  need no initialisation and are not preserved; calls that
+ *                  share it must not overlap on the GPU. A non-NULL workspace
+ *                  that is too small or misaligned when a split is planned
+ *                  gives PA_ERR_WORKSPACE.
  * Rows of sequences whose offsets or lengths are inconsistent are not
  * written and set PA_DEVERR_SEQ_LEN; block ids outside the pool read as
  * zeros and set PA_DEVERR_BLOCK_ID. Computed on the tcgen05 tensor cores:
  * S = Q K^T and O = P V in fp32 (tensor memory), an fp32 online softmax in
- * base 2 with P rounded once to dtype, one rounding of O / l at the end.
- * Allocates nothing and needs no workspace. Returns PA_OK or a PA_ERR_* code.
+ * base 2 with P rounded once to dtype, split pieces combined in fp32 in a
+ * fixed order, one rounding of O / l at the end. For a given device, shape
+ * and workspace choice the result is deterministic. Allocates nothing.
+ * Returns PA_OK or a PA_ERR_* code.
  */
 int pa_prefill(void *out, const void *query, const void *kv_cache,
                const int32_t *block_tables, int max_blocks_per_seq,
                const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
                int total_q, int max_seqlen_q, float scale,
                int num_q_heads, int num_kv_heads, int head_size,
-               int num_blocks, int block_size, int dtype, pa_stream_t stream);
+               int num_blocks, int block_size, int dtype,
+               void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_prefill_workspace_size — bytes of workspace with which pa_prefill and
+ * pa_prefill_fp8 split the K/V ranges of this shape on the current device
+ * (it depends on the SM count); 0 when they would not split (many work
+ * units). Same shape arguments as the calls. Writes *bytes.
+ */
+int pa_prefill_workspace_size(int num_seqs, int max_seqlen_q, int num_q_heads,
+                              int num_kv_heads, int head_size, size_t *bytes);
 
 /*
  * pa_prefill_fp8 — pa_prefill over an FP8 (E4M3) pool written by
@@ -313,8 +338,8 @@ int pa_prefill(void *out, const void *query, const void *kv_cache,
  * query and out (PA_F16 or PA_BF16). The codes are widened exactly to that
  * type on the way to the tensor cores; k_scale joins the score scale and
  * v_scale the final normalisation. Same shapes, limits and error behaviour
- * as pa_prefill (head_size 64 or 128); k_scale and v_scale must be finite
- * and > 0.
+ * as pa_prefill (head_size 64 or 128, the same workspace rules and size);
+ * k_scale and v_scale must be finite and > 0.
  */
 int pa_prefill_fp8(void *out, const void *query, const void *kv_cache,
                    const int32_t *block_tables, int max_blocks_per_seq,
@@ -322,7 +347,7 @@ int pa_prefill_fp8(void *out, const void *query, const void *kv_cache,
                    int total_q, int max_seqlen_q, float scale,
                    int num_q_heads, int num_kv_heads, int head_size,
                    int num_blocks, int block_size, int dtype, float k_scale, float v_scale,
-                   pa_stream_t stream);
+                   void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_copy_blocks — copy-on-write clones of whole physical blocks

@@ -51,9 +51,11 @@ SIGNATURES = [
     ("pa_decode_fp8_workspace_size", _i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     ("pa_decode_fp8", _i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _f, _i, _i, _i, _i, _i, _i, _f, _f,
                            _vp, _sz, _u, _vp]),
-    ("pa_prefill", _i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _i, _i, _i, _vp]),
+    ("pa_prefill", _i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _i, _i, _i,
+                        _vp, _sz, _vp]),
+    ("pa_prefill_workspace_size", _i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     ("pa_prefill_fp8", _i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _i, _i, _i, _f, _f,
-                            _vp]),
+                            _vp, _sz, _vp]),
     ("pa_copy_blocks", _i, [ctypes.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     ("pa_get_device_error", _i, [_ip]),
     ("pa_alloc_create", _vp, [_i, _i, _i32p]),
@@ -287,32 +289,58 @@ def pa_decode_fp8(out, query, kv_cache, block_tables, seq_lens, scale, k_scale, 
         workspace.numel() * workspace.element_size(), int(flags), _stream(stream)))
 
 
+def _workspace_args(workspace):
+    if workspace is None:
+        return ctypes.c_void_p(None), 0
+    return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def pa_prefill_workspace_size(num_seqs, max_seqlen_q, num_q_heads, num_kv_heads, head_size) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pa_prefill_workspace_size(int(num_seqs), int(max_seqlen_q), num_q_heads, num_kv_heads,
+                                           head_size, ctypes.byref(out)))
+    return out.value
+
+
+def prefill_workspace(query, kv_cache, num_seqs, max_seqlen_q):
+    """A uint8 workspace tensor with which pa_prefill / pa_prefill_fp8 split
+    the K/V ranges of this shape, or None when they would not split."""
+    import torch
+    _, hq, d = query.shape
+    hkv = kv_cache.shape[3]
+    n = pa_prefill_workspace_size(num_seqs, max_seqlen_q, hq, hkv, d)
+    return torch.empty(n, dtype=torch.uint8, device=query.device) if n else None
+
+
 def pa_prefill(out, query, kv_cache, block_tables, cu_seqlens_q, seq_lens, scale, max_seqlen_q,
-               stream=None) -> None:
+               workspace=None, stream=None) -> None:
     """out/query [total_q, Hq, D]; kv_cache (2, NB, B, Hkv, D); block_tables [S, maxblk] int32;
-    cu_seqlens_q [S + 1] int32; seq_lens [S] int32 (chunk included); max_seqlen_q: host int."""
+    cu_seqlens_q [S + 1] int32; seq_lens [S] int32 (chunk included); max_seqlen_q: host int;
+    workspace: None (no K/V split) or a uint8 CUDA tensor (see prefill_workspace)."""
     total_q, hq, d = query.shape
     _, nb, bs, hkv, _ = kv_cache.shape
+    ws, ws_bytes = _workspace_args(workspace)
     _check(lib().pa_prefill(
         _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
         _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
         _dev(cu_seqlens_q, "cu_seqlens_q"), _dev(seq_lens, "seq_lens"), int(seq_lens.shape[0]),
         total_q, int(max_seqlen_q), float(scale), hq, hkv, d, nb, bs, _dtype_code(kv_cache),
-        _stream(stream)))
+        ws, ws_bytes, _stream(stream)))
 
 
 def pa_prefill_fp8(out, query, kv_cache, block_tables, cu_seqlens_q, seq_lens, scale, max_seqlen_q,
-                   k_scale, v_scale, stream=None) -> None:
+                   k_scale, v_scale, workspace=None, stream=None) -> None:
     """pa_prefill over an E4M3 byte pool (2, NB, B, Hkv, D) uint8; out/query 16-bit."""
     _fp8_pool(kv_cache, "kv_cache")
     total_q, hq, d = query.shape
     _, nb, bs, hkv, _ = kv_cache.shape
+    ws, ws_bytes = _workspace_args(workspace)
     _check(lib().pa_prefill_fp8(
         _dev(out, "out"), _dev(query, "query"), _dev(kv_cache, "kv_cache"),
         _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
         _dev(cu_seqlens_q, "cu_seqlens_q"), _dev(seq_lens, "seq_lens"), int(seq_lens.shape[0]),
         total_q, int(max_seqlen_q), float(scale), hq, hkv, d, nb, bs, _dtype_code(query),
-        float(k_scale), float(v_scale), _stream(stream)))
+        float(k_scale), float(v_scale), ws, ws_bytes, _stream(stream)))
 
 
 def pa_copy_blocks(kv_caches, src_dst_pairs, stream=None) -> None:

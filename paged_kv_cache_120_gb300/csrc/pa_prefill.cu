@@ -64,6 +64,13 @@ __device__ int g_prefill_error;  // PA_DEVERR_* bits of the prefill kernels
 constexpr int kSchedSlots = 64;
 __device__ int g_prefill_sched[kSchedSlots][2];
 
+// Stream-K launches (few work units, below): per slot, one arrival counter
+// per (unit, query tile, warp of the tile's softmax group), counting the
+// pieces of the unit whose partial rows have been written. The last CTA of
+// the launch puts the slot's counters back to 0.
+constexpr int kMaxSplitUnits = 1024;
+__device__ int g_prefill_fix[kSchedSlots][kMaxSplitUnits * 8];
+
 namespace {
 
 __device__ __forceinline__ void prefill_raise(int bit) { atomicOr(&g_prefill_error, bit); }
@@ -388,35 +395,75 @@ struct PrefillParams {
     int max_len;        // max_blocks_per_seq * block_size
     int num_kv_heads;
     int num_units;      // q_pairs * num_seqs * num_kv_heads * head_tiles
-    int sched_slot;     // this launch's row of g_prefill_sched
+    int sched_slot;     // this launch's row of g_prefill_sched (and g_prefill_fix)
+    float *part_o;      // stream-K: partial O rows [CTA][slot 2][tile 2][128][D] fp32
+    float2 *part_ml;    // stream-K: partial (reference maximum, row sum) [CTA][slot 2][tile 2][128]
     float scale_log2;   // scale * log2(e) (* k_scale with an FP8 cache)
     float v_scale;      // 1, or the FP8 cache's V scale
 };
 
 // One work unit: the two adjacent query tiles A = 2 qp and B = 2 qp + 1 of
 // head tile ht of kv head h of sequence s. They share every K/V tile (B's
-// queries come later, so B sees at least as many tiles as A). Units are
-// numbered heaviest first: u = ((qr * num_seqs + s) * num_kv_heads + h) *
-// head_tiles + ht with qp = q_pairs - 1 - qr.
+// queries come later, so B sees at least as many tiles as A). With qp =
+// q_pairs - 1 - qr, units are numbered heaviest first, u = ((qr * num_seqs
+// + s) * num_kv_heads + h) * head_tiles + ht, when each CTA takes whole
+// units from a counter; sequence-major, u = ((s * num_kv_heads + h) *
+// head_tiles + ht) * q_pairs + qr, when CTAs take equal shares of the
+// tiles (stream-K), so that a sequence's units lie side by side.
 struct Unit {
     int s, h, ht, q0, q_len, L;
     int t0[2];       // first query token of tile A / B
     int n[2];        // K/V tiles tile A / B sees (0: the tile has no queries)
 };
 
+// What a CTA is handed: K/V tiles j0 <= j < j1 of unit u. CTAs clo..chi
+// hold the unit's pieces; clo == chi: the item is the whole unit.
+struct Item {
+    int u, j0, j1, clo, chi;
+};
+
 // Decode unit u; false when tile A has no query rows or the sequence has bad
 // offsets or lengths (flagged once, by the unit of the sequence's first
 // heads and last query pair, when `flag`).
+// A sequence's offsets and length are consistent.
+__device__ __forceinline__ bool seq_ok(const PrefillParams &p, int q0, int q_len, int L)
+{
+    return !(q_len < 0 || q_len > p.max_q || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len);
+}
+
+// K/V tiles the unit of query pair qr of a sequence reads (those its tile
+// B's last query sees, or tile A's when B has no queries); 0 when tile A
+// has no queries.
+__device__ __forceinline__ int pair_tiles(const PrefillParams &p, int q_len, int L, int qr)
+{
+    const int ta = 2 * (p.q_pairs - 1 - qr) * p.rows_per_head;
+    if (ta >= q_len)
+        return 0;
+    return (L - q_len + min(q_len, ta + 2 * p.rows_per_head) + kN - 1) / kN;
+}
+
+// SK: the stream-K numbering (sequence-major).
+template <bool SK>
 __device__ __forceinline__ bool unit_of(const PrefillParams &p, int u, Unit &w, bool flag)
 {
-    const int ht = u % p.head_tiles;
-    int r = u / p.head_tiles;
-    const int h = r % p.num_kv_heads;
-    r /= p.num_kv_heads;
-    const int s = r % p.num_seqs;
-    const int qr = r / p.num_seqs;
+    int ht, h, s, qr;
+    if constexpr (SK) {
+        qr = u % p.q_pairs;
+        int r = u / p.q_pairs;
+        ht = r % p.head_tiles;
+        r /= p.head_tiles;
+        h = r % p.num_kv_heads;
+        s = r / p.num_kv_heads;
+    } else {
+        ht = u % p.head_tiles;
+        int r = u / p.head_tiles;
+        h = r % p.num_kv_heads;
+        r /= p.num_kv_heads;
+        s = r % p.num_seqs;
+        qr = r / p.num_seqs;
+    }
     const int q0 = p.cu_q[s], q_len = p.cu_q[s + 1] - q0, L = p.seq_lens[s];
-    if (q_len < 0 || q_len > p.max_q || q0 < 0 || q0 + q_len > p.total_q || L < q_len || L > p.max_len) {
+    if (!seq_ok(p, q0, q_len, L)) {
         if (flag && h == 0 && ht == 0 && qr == 0)
             prefill_raise(PA_DEVERR_SEQ_LEN);
         return false;
@@ -450,9 +497,15 @@ struct PrefillBars {
     int unit_ring[kUnitSlots];  // unit index, or -1 once the launch's units are all taken
     uint32_t tmem_base;
     int fail;
+    // Stream-K: the rest of each work item (first and end K/V tile, first
+    // and last CTA holding a piece of the unit; equal: the whole unit).
+    int item_ext[kUnitSlots][4];
+    int cta_last;
 };
 
-template <bool BF16, bool FP8, int D>
+// SPLIT: the stream-K instance (few units, K/V ranges shared out evenly);
+// otherwise whole units from a counter.
+template <bool BF16, bool FP8, int D, bool SPLIT>
 __global__ void __launch_bounds__(threads_for(FP8), 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap kv_map,
                          const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
@@ -543,14 +596,25 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
             prefill_raise(PA_DEVERR_TIMEOUT);
         return false;
     };
-    // The i-th unit handed to this CTA (or -1: no more). Every lane in
+    // The i-th item handed to this CTA (unit -1: no more). Every lane in
     // `mask` calls it; `leader` arrives once the warp has read the slot.
     // False if the wait ran out.
-    auto take_unit = [&](int i, unsigned mask, bool leader, int &u) {
+    auto take_unit = [&](int i, unsigned mask, bool leader, Item &it) {
         const int sl = i % kUnitSlots;
         if (!__all_sync(mask, wait_or_fail(b_uf(sl), (i / kUnitSlots) & 1)))
             return false;
-        u = *reinterpret_cast<volatile int *>(&bars.unit_ring[sl]);
+        it.u = *reinterpret_cast<volatile int *>(&bars.unit_ring[sl]);
+        if constexpr (SPLIT) {
+            const volatile int *e = bars.item_ext[sl];
+            it.j0 = e[0];
+            it.j1 = e[1];
+            it.clo = e[2];
+            it.chi = e[3];
+        } else {
+            it.j0 = 0;
+            it.j1 = 0x7fffffff;
+            it.clo = it.chi = 0;
+        }
         __syncwarp(mask);
         if (leader)
             mbar_arrive(b_ue(sl));
@@ -568,25 +632,141 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIO16));
     if (warp == kWarpQ) {
         // ------------------------------------------------------------ Q
-        // Scheduler and Q: take the next unit that has queries from the
-        // launch's counter, hand it on, and load its two query tiles once the
-        // previous unit's last S = Q K^T has completed.
+        // Scheduler and Q: find this CTA's next work item, hand it on, and
+        // load its two query tiles once the previous item's last S = Q K^T
+        // has completed. Whole units come from the launch's counter; under
+        // stream-K, CTA c takes tiles [c W / G, (c + 1) W / G) of the W K/V
+        // tiles of all units laid end to end (G CTAs), cut at unit ends.
+        const int H = p.num_kv_heads * p.head_tiles;  // units of one query pair of a sequence
+        auto seq_tiles = [&](int s, bool flag) {     // K/V tiles of one head tile of sequence s
+            const int q0 = p.cu_q[s], q_len = p.cu_q[s + 1] - q0, L = p.seq_lens[s];
+            if (!seq_ok(p, q0, q_len, L)) {
+                if (flag)
+                    prefill_raise(PA_DEVERR_SEQ_LEN);
+                return 0LL;
+            }
+            long long a = 0;
+            for (int qr = 0; qr < p.q_pairs; ++qr)
+                a += pair_tiles(p, q_len, L, qr);
+            return a;
+        };
+        long long lo = 0, hi = 0, W = 0, Ts = 0;  // this CTA's tiles [lo, hi); sequence ws starts at tile Ts
+        long long G = 1;                           // CTAs sharing the tiles: at most one per tile, so that
+        int ws = 0;                                // every share is non-empty
+        if constexpr (SPLIT) {
+            long long part = 0;
+            for (int s = lane; s < p.num_seqs; s += 32)
+                part += H * seq_tiles(s, true);
+            for (int o = 16; o > 0; o >>= 1)
+                part += __shfl_xor_sync(kFull, part, o);
+            W = part;
+            G = min((long long)gridDim.x, max(W, 1LL));
+            if (blockIdx.x < G) {
+                lo = (long long)blockIdx.x * W / G;
+                hi = ((long long)blockIdx.x + 1) * W / G;
+            }
+            long long done = 0;  // tiles of the sequences before this group of 32
+            for (int s0 = 0; lo < hi && s0 < p.num_seqs; s0 += 32) {
+                const int s = s0 + lane;
+                const long long wq = s < p.num_seqs ? H * seq_tiles(s, false) : 0;
+                long long incl = wq;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long v = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o)
+                        incl += v;
+                }
+                const long long start = done + incl - wq;
+                const unsigned hit = __ballot_sync(kFull, wq > 0 && start <= lo && lo < start + wq);
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    ws = s0 + src;
+                    Ts = __shfl_sync(kFull, start, src);
+                    break;
+                }
+                done += __shfl_sync(kFull, incl, 31);
+            }
+        }
         if (lane == 0) {
             int* next = &g_prefill_sched[p.sched_slot][0];
+            // Stream-K walk: unit (ws, hh, qr) holds tiles [Tu, Tu + nu).
+            int hh = 0, qr = 0, wq_len = 0, wL = 0, nu = 0;
+            bool wok = false;
+            long long Tu = 0, pos = lo;
+            auto enter_seq = [&]() {
+                const int q0 = p.cu_q[ws];
+                wq_len = p.cu_q[ws + 1] - q0;
+                wL = p.seq_lens[ws];
+                wok = seq_ok(p, q0, wq_len, wL);
+            };
+            auto tiles_here = [&]() { return wok ? pair_tiles(p, wq_len, wL, qr) : 0; };
+            if (SPLIT && lo < hi) {
+                enter_seq();
+                const long long a = seq_tiles(ws, false);
+                hh = a > 0 ? (int)((lo - Ts) / a) : 0;
+                Tu = Ts + hh * a;
+                nu = tiles_here();
+                while (Tu + nu <= lo && qr + 1 < p.q_pairs) {
+                    Tu += nu;
+                    ++qr;
+                    nu = tiles_here();
+                }
+            }
+            auto cta_of = [&](long long t) { return (int)(((t + 1) * G - 1) / W); };
             for (int i = 0;; ++i) {
                 Unit w;
-                int u;
-                do {
-                    u = atomicAdd(next, 1);
-                } while (u < p.num_units && !unit_of(p, u, w, true));
-                if (u >= p.num_units)
-                    u = -1;
+                Item it = {-1, 0, 0, 0, 0};
+                if constexpr (SPLIT) {
+                    if (pos < hi && nu > 0 && Tu <= pos && pos < Tu + nu) {
+                        it.u = ((ws * H) + hh) * p.q_pairs + qr;
+                        const long long end = min(Tu + nu, hi);
+                        it.j0 = (int)(pos - Tu);
+                        it.j1 = (int)(end - Tu);
+                        it.clo = cta_of(Tu);
+                        it.chi = cta_of(Tu + nu - 1);
+                        pos = end;
+                        // On to the next unit with tiles (bounded: every step
+                        // moves (ws, hh, qr) forward).
+                        while (pos < hi) {
+                            Tu += nu;
+                            nu = 0;
+                            if (++qr == p.q_pairs) {
+                                qr = 0;
+                                if (++hh == H) {
+                                    hh = 0;
+                                    if (++ws >= p.num_seqs)
+                                        break;
+                                    enter_seq();
+                                }
+                            }
+                            nu = tiles_here();
+                            if (nu > 0)
+                                break;
+                        }
+                        if (!unit_of<true>(p, it.u, w, false))
+                            it.u = -1;
+                    }
+                } else {
+                    int u;
+                    do {
+                        u = atomicAdd(next, 1);
+                    } while (u < p.num_units && !unit_of<false>(p, u, w, true));
+                    if (u < p.num_units) {
+                        it.u = u;
+                        it.j1 = 0x7fffffff;
+                    }
+                }
                 const int sl = i % kUnitSlots;
                 if (i >= kUnitSlots && !wait_or_fail(b_ue(sl), ((i / kUnitSlots) - 1) & 1))
                     break;
-                bars.unit_ring[sl] = u;
+                bars.unit_ring[sl] = it.u;
+                if constexpr (SPLIT) {
+                    bars.item_ext[sl][0] = it.j0;
+                    bars.item_ext[sl][1] = it.j1;
+                    bars.item_ext[sl][2] = it.clo;
+                    bars.item_ext[sl][3] = it.chi;
+                }
                 mbar_arrive(b_uf(sl));
-                if (u < 0)
+                if (it.u < 0)
                     break;
                 if (i > 0 && !wait_or_fail(b_qe, (i - 1) & 1))
                     break;
@@ -615,19 +795,19 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 int gc = 0;  // K (or V) tiles produced by this CTA so far
                 bool go = true;
                 for (int i = 0; go; ++i) {
-                    int u;
-                    if (!take_unit(i, group_mask, lane == leader, u) || u < 0)
+                    Item it;
+                    if (!take_unit(i, group_mask, lane == leader, it) || it.u < 0)
                         break;
                     Unit w;
-                    unit_of(p, u, w, false);
-                    const int n = max(w.n[0], w.n[1]);
+                    unit_of<SPLIT>(p, it.u, w, false);
+                    const int n = SPLIT ? min(max(w.n[0], w.n[1]), it.j1) : max(w.n[0], w.n[1]);
                     const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
                     auto lookup = [&](int j) {
                         const int kt = j * kN + kBoxTokens * box;
                         return (j < n && kt < w.L) ? __ldg(table + kt / p.block_size) : -1;
                     };
-                    int next = lookup(0);
-                    for (int j = 0; j < n; ++j, ++gc) {
+                    int next = lookup(it.j0);
+                    for (int j = it.j0; j < n; ++j, ++gc) {
                         int phys = next;
                         next = lookup(j + 1);
                         const int st = gc % stages;
@@ -673,12 +853,12 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         int gc = 0;  // tiles produced by this CTA so far
         bool go = true;
         for (int i = 0; go; ++i) {
-            int u;
-            if (!take_unit(i, kFull, lane == 0, u) || u < 0)
+            Item it;
+            if (!take_unit(i, kFull, lane == 0, it) || it.u < 0)
                 break;
             Unit w;
-            unit_of(p, u, w, false);
-            const int n = max(w.n[0], w.n[1]);
+            unit_of<SPLIT>(p, it.u, w, false);
+            const int n = SPLIT ? min(max(w.n[0], w.n[1]), it.j1) : max(w.n[0], w.n[1]);
             const int32_t *table = p.block_tables + (long long)w.s * p.max_blocks_per_seq;
             auto issue = [&](int j) {
                 if (lane < 4) {
@@ -697,8 +877,8 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                                 is_k ? 0 : 1);
                 }
             };
-            issue(0);
-            for (int j = 0; j < n; ++j, ++gc) {
+            issue(it.j0);
+            for (int j = it.j0; j < n; ++j, ++gc) {
                 const int st = gc % stages;
                 if (!__all_sync(kFull, wait_or_fail(b_stg, gc & 1)) ||
                     (gc >= stages && !__all_sync(kFull, wait_or_fail(is_k ? b_ke(st) : b_ve(st),
@@ -772,12 +952,16 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
             int gx[2] = {0, 0};          // P V of tile x issued so far
             bool go = true;
             for (int i = 0; go; ++i) {
-                int u;
-                if (!take_unit(i, 1u, true, u) || u < 0)
+                Item it;
+                if (!take_unit(i, 1u, true, it) || it.u < 0)
                     break;
                 Unit w;
-                unit_of(p, u, w, false);
-                const int n = max(w.n[0], w.n[1]);
+                unit_of<SPLIT>(p, it.u, w, false);
+                // Tiles j0 <= j < j1 of the unit; tile x reads those below its ne[x].
+                const int j0 = SPLIT ? it.j0 : 0;
+                const int j1 = SPLIT ? min(max(w.n[0], w.n[1]), it.j1) : max(w.n[0], w.n[1]);
+                const int ne_piece[2] = {min(w.n[0], j1), min(w.n[1], j1)};
+                const int *ne = SPLIT ? ne_piece : w.n;
                 if (!wait_or_fail(kQToF16 ? b_qr : b_q, ui & 1))
                     break;
                 ++ui;
@@ -788,14 +972,14 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         break;
                     tc_fence_after();
                     for (int x = 0; x < 2; ++x)
-                        if (w.n[x] > 0)
+                        if (ne[x] > j0)
                             issue_s(x, ks);
                     tc_commit(b_ke(ks));
                     ++kc;
-                    if (n == 1)
-                        tc_commit(b_qe);  // Q free once the unit's last scores are done
+                    if (j1 - j0 == 1)
+                        tc_commit(b_qe);  // Q free once the item's last scores are done
                 }
-                for (int j = 0; go && j < n; ++j) {
+                for (int j = j0; go && j < j1; ++j) {
                     const int vs = vc % kVStages;
                     if (!wait_or_fail(b_vf(vs), (vc / kVStages) & 1)) {
                         go = false;
@@ -803,7 +987,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     }
                     int ks_next = -1;
                     for (int x = 0; x < 2; ++x) {
-                        if (j >= w.n[x])
+                        if (j >= ne[x])
                             continue;
                         if (!wait_or_fail(b_p(x), gx[x] & 1)) {
                             go = false;
@@ -818,15 +1002,15 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
 #pragma unroll
                         for (int k = 0; k < kN / 16; ++k)
                             tc_mma_ts(to, ts + k * 8, dv + (uint64_t)(k * (2048 >> 4)), id_o,
-                                      (j > 0 || k > 0) ? 1u : 0u);
+                                      (j > j0 || k > 0) ? 1u : 0u);
                         tc_commit(b_pv(x));
                         ++gx[x];
                         // The tile's last O += P V is issued: V's stage is
                         // free once it completes (tile B, if it reads V_j,
                         // comes after tile A).
-                        if (x == 1 || j >= w.n[1])
+                        if (x == 1 || j >= ne[1])
                             tc_commit(b_ve(vs));
-                        if (j + 1 < w.n[x]) {
+                        if (j + 1 < ne[x]) {
                             if (ks_next < 0) {
                                 ks_next = kc % kKStages;
                                 if (!wait_or_fail(b_kf(ks_next), (kc / kKStages) & 1)) {
@@ -843,7 +1027,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     if (ks_next >= 0) {
                         tc_commit(b_ke(ks_next));
                         ++kc;
-                        if (j + 2 == n)
+                        if (j + 2 == j1)
                             tc_commit(b_qe);
                     }
                     ++vc;
@@ -875,16 +1059,19 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
         int gx = 0, vbase = 0;  // tiles of this query tile, and V tiles of the CTA, so far
         bool alive = true;
         for (int i = 0; alive; ++i) {
-            int u;
-            if (!take_unit(i, kFull, lane == 0, u) || u < 0)
+            Item it;
+            if (!take_unit(i, kFull, lane == 0, it) || it.u < 0)
                 break;
             Unit w;
-            unit_of(p, u, w, false);
-            const int n = max(w.n[0], w.n[1]), nx = w.n[x];
+            unit_of<SPLIT>(p, it.u, w, false);
+            // This tile reads K/V tiles j0 <= j < nx of the item's j0 .. j1.
+            const int j0 = SPLIT ? it.j0 : 0;
+            const int j1 = SPLIT ? min(max(w.n[0], w.n[1]), it.j1) : max(w.n[0], w.n[1]);
+            const int nx = SPLIT ? min(w.n[x], j1) : w.n[x];
             // The K/V tile holding the sequence end (padding slots past it)
             // is zeroed in V by the first tile that reads it.
             const int jp = (w.L % kN) ? w.L / kN : -1;
-            const bool zeroes = !FP8 && jp >= 0 && jp < nx && (x == 0 || jp >= w.n[0]);
+            const bool zeroes = !FP8 && jp >= j0 && jp < nx && (x == 0 || jp >= (SPLIT ? min(w.n[0], j1) : w.n[0]));
             const bool valid = g < HPC && w.t0[x] + t < w.q_len;
             const int pos = valid ? w.L - w.q_len + w.t0[x] + t : -1;  // last token this row sees
             if constexpr (kQToF16) {
@@ -899,7 +1086,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                     break;
                 }
                 sc = p.scale_log2;
-                if (nx > 0) {
+                if (nx > j0) {
                     const uint32_t row = sQ(x) + r * 128;
                     uint4 qv[kChunks * 8];
                     uint32_t mag = 0;  // largest |q| as bf16 bits, per half
@@ -928,7 +1115,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 mbar_arrive(b_qr);
             }
             float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < nx; ++j, ++gx) {
+            for (int j = j0; j < nx; ++j, ++gx) {
                 if (!__all_sync(kFull, wait_or_fail(b_s(x), gx & 1))) {
                     alive = false;
                     break;
@@ -1055,7 +1242,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 // Rescale O when the reference moved. The previous tile's
                 // O += P V is done: it was issued before this tile's S, whose
                 // completion was awaited above.
-                if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+                if (j > j0 && __any_sync(kFull, alpha != 1.f)) {
                     const uint32_t to = tO(x) + lane_off;
                     float o[32];
 #pragma unroll
@@ -1075,7 +1262,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 // The V rows past the sequence end hold whatever the pool's
                 // padding slots hold: zero them (P is 0 there) once V lands.
                 if (zeroes && j == jp) {
-                    const int vt = vbase + j, vs = vt % kVStages;
+                    const int vt = vbase + (j - j0), vs = vt % kVStages;
                     if (!__all_sync(kFull, wait_or_fail(b_vf(vs), (vt / kVStages) & 1))) {
                         alive = false;
                         break;
@@ -1092,36 +1279,109 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
             }
             if (!alive)
                 break;
-            vbase += n;
-            if (nx == 0)
-                continue;
-            // Unit epilogue: O / l for the valid rows. Reading O here comes
-            // before this row's first P of the next unit, and so before the
-            // next unit's first P V overwrites O.
-            if (!__all_sync(kFull, wait_or_fail(b_pv(x), (gx - 1) & 1))) {
-                alive = false;
-                break;
+            vbase += j1 - j0;
+            const bool whole = !SPLIT || it.clo == it.chi, work = nx > j0;
+            if (w.n[x] == 0 || (whole && !work))
+                continue;  // the tile has no queries (or, whole, no tiles)
+            // Item epilogue. Reading O here comes before this row's first P
+            // of the next item, and so before its first P V overwrites O.
+            if (work) {
+                if (!__all_sync(kFull, wait_or_fail(b_pv(x), (gx - 1) & 1))) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
             }
-            tc_fence_after();
-            const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
             uint16_t *out = static_cast<uint16_t *>(p.out) +
                             ((long long)(w.q0 + w.t0[x] + t) * p.num_q_heads + w.h * p.group + w.ht * HPC + g) * D;
             const uint32_t to = tO(x) + lane_off;
             float o[32];
+            auto store_row = [&](int c, const float *v, float inv) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                tc_ld32(to + c * 32, o);
-                if (valid) {
+                for (int q = 0; q < 4; ++q) {
+                    uint4 e;
+                    e.x = pack2<BF16>(v[8 * q + 0] * inv, v[8 * q + 1] * inv);
+                    e.y = pack2<BF16>(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
+                    e.z = pack2<BF16>(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
+                    e.w = pack2<BF16>(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
+                    reinterpret_cast<uint4 *>(out + c * 32)[q] = e;
+                }
+            };
+            if (whole) {
+                // O / l for the valid rows.
+                const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 v;
-                        v.x = pack2<BF16>(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-                        v.y = pack2<BF16>(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-                        v.z = pack2<BF16>(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-                        v.w = pack2<BF16>(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-                        reinterpret_cast<uint4 *>(out + c * 32)[q] = v;
+                for (int c = 0; c < D / 32; ++c) {
+                    tc_ld32(to + c * 32, o);
+                    if (valid)
+                        store_row(c, o, inv);
+                }
+                continue;
+            }
+            // A piece of a split unit ([book] §4.6: partial softmax states
+            // over disjoint token ranges combine exactly). Store this piece's
+            // state (O relative to 2^m, the reference maximum m, the row sum
+            // l; a tile with no K/V tile in the piece stores the empty state
+            // m = -inf, l = 0, O = 0); the warp that stores the unit's last
+            // piece of its 32 rows then combines all pieces in CTA order.
+            // Slot: CTA c holds at most two partial pieces, the unit it
+            // starts inside (slot 0) and the one it starts and leaves
+            // unfinished (slot 1), so the first CTA of a unit uses slot 1.
+            auto slot_of = [&](int c) { return ((c * 2 + (c == it.clo ? 1 : 0)) * 2 + x) * kM + r; };
+            {
+                float4 *po = reinterpret_cast<float4 *>(p.part_o + (size_t)slot_of((int)blockIdx.x) * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    if (work) {
+                        tc_ld32(to + c * 32, o);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = 0.f;
+                    }
+                    if (valid)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            po[c * 8 + q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                }
+                if (valid)
+                    p.part_ml[slot_of((int)blockIdx.x)] = work ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+            }
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0)
+                last = atomicAdd(&g_prefill_fix[p.sched_slot][(it.u * 2 + x) * 4 + quarter], 1) == it.chi - it.clo;
+            if (!__shfl_sync(kFull, last, 0) || !valid)
+                continue;
+            __threadfence();
+            float mref = -INFINITY, lsum = 0.f;
+            for (int c = it.clo; c <= it.chi; ++c)
+                mref = fmaxf(mref, __ldcg(&p.part_ml[slot_of(c)].x));
+            auto weight = [&](float m) { return m == mref ? 1.f : ex2(m - mref); };
+            for (int c = it.clo; c <= it.chi; ++c) {
+                const float2 ml = __ldcg(&p.part_ml[slot_of(c)]);
+                lsum += weight(ml.x) * ml.y;
+            }
+            const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = 0.f;
+                for (int c = it.clo; c <= it.chi; ++c) {
+                    const float wgt = weight(__ldcg(&p.part_ml[slot_of(c)].x));
+                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (size_t)slot_of(c) * D) + cc * 8;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 v = __ldcg(src + q);
+                        o[4 * q] += wgt * v.x;
+                        o[4 * q + 1] += wgt * v.y;
+                        o[4 * q + 2] += wgt * v.z;
+                        o[4 * q + 3] += wgt * v.w;
                     }
                 }
+                store_row(cc, o, inv);
             }
         }
     }
@@ -1132,7 +1392,21 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     tc_fence_after();
     // Every role has left its loop, so this CTA takes no more units; the
     // last CTA to get here resets the launch's counters for the next use.
-    if (tid == 0) {
+    if constexpr (SPLIT) {
+        // (and the slot's arrival counters)
+        if (tid == 0) {
+            __threadfence();
+            bars.cta_last = atomicAdd(&g_prefill_sched[p.sched_slot][1], 1) == (int)gridDim.x - 1;
+        }
+        __syncthreads();
+        if (bars.cta_last) {
+            if (tid == 0)
+                g_prefill_sched[p.sched_slot][1] = 0;
+            for (int i = tid; i < p.num_units * 8; i += blockDim.x)
+                g_prefill_fix[p.sched_slot][i] = 0;
+            __threadfence();
+        }
+    } else if (tid == 0) {
         __threadfence();
         if (atomicAdd(&g_prefill_sched[p.sched_slot][1], 1) == (int)gridDim.x - 1) {
             g_prefill_sched[p.sched_slot][0] = 0;
@@ -1232,14 +1506,68 @@ using namespace pa;
 
 namespace {
 
-int prefill_impl(const char *who, void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
-                 int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
-                 int total_q, int max_seqlen_q, float scale, int num_q_heads, int num_kv_heads, int head_size,
-                 int num_blocks, int block_size, int dtype, bool fp8, float k_scale, float v_scale,
-                 pa_stream_t stream)
+// A launch's work units and scheduling. With enough units, each of
+// min(units, SMs) persistent CTAs takes whole units, heaviest first, from a
+// counter. With few (at most kSplitUnitsPerSm per SM, and a workspace), the
+// units' K/V tiles are dealt out in equal contiguous shares (stream-K) to G
+// CTAs, G = min(SMs, units * kMaxPiecesPerUnit) so that no unit is cut into
+// more than about kMaxPiecesPerUnit pieces (the last piece's warp combines
+// them all).
+constexpr int kSplitUnitsPerSm = 4, kMaxPiecesPerUnit = 16;
+
+struct LaunchPlan {
+    int heads_per_cta, head_tiles, rows_per_head, q_pairs;
+    long long units;
+    int split_grid;     // G under stream-K, 0 when the launch takes whole units
+    size_t split_bytes; // workspace stream-K needs
+};
+
+LaunchPlan plan_launch(int num_seqs, int max_seqlen_q, int num_q_heads, int num_kv_heads, int head_size, int sms)
 {
-    if (dtype != PA_F16 && dtype != PA_BF16)
-        return set_error(PA_ERR_UNSUPPORTED, "%s: dtype %d (want PA_F16 or PA_BF16)", who, dtype);
+    LaunchPlan lp;
+    const int group = num_q_heads / num_kv_heads;
+    lp.heads_per_cta = group < 16 ? group : 16;
+    lp.head_tiles = group / lp.heads_per_cta;
+    lp.rows_per_head = (kM / lp.heads_per_cta) & ~7;
+    const int q_tiles = (max_seqlen_q + lp.rows_per_head - 1) / lp.rows_per_head;
+    lp.q_pairs = (q_tiles + 1) / 2;
+    lp.units = (long long)lp.q_pairs * num_seqs * num_kv_heads * lp.head_tiles;
+    lp.split_grid = 0;
+    lp.split_bytes = 0;
+    if (lp.units > 0 && lp.units <= std::min<long long>(kMaxSplitUnits, (long long)kSplitUnitsPerSm * sms)) {
+        lp.split_grid = (int)std::min<long long>(sms, lp.units * kMaxPiecesPerUnit);
+        // Per CTA two slots of two 128-row tiles: O rows (head_size fp32)
+        // and (m, l) pairs.
+        lp.split_bytes = (size_t)lp.split_grid * 2 * 2 * kM * ((size_t)head_size * 4 + 8);
+    }
+    return lp;
+}
+
+// SM count of the current device (cached per device).
+int current_sms(const char *who, int *dev_out, int *sms_out)
+{
+    static std::mutex mu;
+    static int sm_count[64] = {};
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return set_error(PA_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
+    sms = dev < 64 ? sm_count[dev] : 0;
+    if (sms <= 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess || sms <= 0)
+            return set_error(PA_ERR_CUDA, "%s: SM count: %s", who, cudaGetErrorString(e));
+        if (dev < 64)
+            sm_count[dev] = sms;
+    }
+    *dev_out = dev;
+    *sms_out = sms;
+    return PA_OK;
+}
+
+int check_heads(const char *who, int num_q_heads, int num_kv_heads, int head_size)
+{
     if (head_size != kD && head_size != 64)
         return set_error(PA_ERR_UNSUPPORTED, "%s: head_size %d (built: 64 and 128)", who, head_size);
     if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -1250,6 +1578,21 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     if (group > 16 && group % 16 != 0)
         return set_error(PA_ERR_UNSUPPORTED, "%s: query group %d (want <= 16 or a multiple of 16)", who,
                          group);
+    return PA_OK;
+}
+
+int prefill_impl(const char *who, void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
+                 int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens, int num_seqs,
+                 int total_q, int max_seqlen_q, float scale, int num_q_heads, int num_kv_heads, int head_size,
+                 int num_blocks, int block_size, int dtype, bool fp8, float k_scale, float v_scale,
+                 void *workspace, size_t workspace_bytes, pa_stream_t stream)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return set_error(PA_ERR_UNSUPPORTED, "%s: dtype %d (want PA_F16 or PA_BF16)", who, dtype);
+    int rc = check_heads(who, num_q_heads, num_kv_heads, head_size);
+    if (rc != PA_OK)
+        return rc;
+    const int group = num_q_heads / num_kv_heads;
     if (block_size < kBoxTokens || block_size % kBoxTokens != 0)
         return set_error(PA_ERR_INVALID_ARG, "%s: block_size %d must be a positive multiple of 16", who,
                          block_size);
@@ -1270,6 +1613,19 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     if (!encoder())
         return set_error(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
 
+    int dev = 0, sms = 0;
+    rc = current_sms(who, &dev, &sms);
+    if (rc != PA_OK)
+        return rc;
+    const LaunchPlan lp = plan_launch(num_seqs, max_seqlen_q, num_q_heads, num_kv_heads, head_size, sms);
+    if (lp.units > 0x7fffffffLL)
+        return set_error(PA_ERR_UNSUPPORTED, "%s: too many query tiles", who);
+    // Stream-K needs the workspace; without one the launch takes whole units.
+    const bool split = lp.split_grid > 0 && workspace != nullptr;
+    if (split && (workspace_bytes < lp.split_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+        return set_error(PA_ERR_WORKSPACE, "%s: workspace of %zu bytes at %p (need %zu, 256-byte aligned)", who,
+                         workspace_bytes, workspace, lp.split_bytes);
+
     PrefillParams prm;
     prm.out = out;
     prm.block_tables = block_tables;
@@ -1279,11 +1635,10 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     prm.num_seqs = num_seqs;
     prm.num_q_heads = num_q_heads;
     prm.group = group;
-    prm.heads_per_cta = group < 16 ? group : 16;
-    prm.head_tiles = group / prm.heads_per_cta;
-    prm.rows_per_head = (kM / prm.heads_per_cta) & ~7;
-    const int q_tiles = (max_seqlen_q + prm.rows_per_head - 1) / prm.rows_per_head;
-    prm.q_pairs = (q_tiles + 1) / 2;
+    prm.heads_per_cta = lp.heads_per_cta;
+    prm.head_tiles = lp.head_tiles;
+    prm.rows_per_head = lp.rows_per_head;
+    prm.q_pairs = lp.q_pairs;
     prm.max_q = max_seqlen_q;
     prm.num_blocks = num_blocks;
     prm.block_size = block_size;
@@ -1292,15 +1647,16 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     prm.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
     prm.v_scale = fp8 ? v_scale : 1.f;
     prm.num_kv_heads = num_kv_heads;
-    const long long units = (long long)prm.q_pairs * num_seqs * num_kv_heads * prm.head_tiles;
-    if (units > 0x7fffffffLL)
-        return set_error(PA_ERR_UNSUPPORTED, "%s: too many query tiles", who);
-    prm.num_units = (int)units;
+    prm.num_units = (int)lp.units;
+    prm.part_o = split ? static_cast<float *>(workspace) : nullptr;
+    prm.part_ml = split ? reinterpret_cast<float2 *>(static_cast<float *>(workspace) +
+                                                     (size_t)lp.split_grid * 2 * 2 * kM * head_size)
+                        : nullptr;
     static std::atomic<unsigned> launches{0};
     prm.sched_slot = (int)(launches.fetch_add(1u) % (unsigned)kSchedSlots);
 
     CUtensorMap kv_map, q_map;
-    int rc = fp8 ? encode_kv_map_fp8(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads, head_size)
+    rc = fp8 ? encode_kv_map_fp8(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads, head_size)
                  : encode_kv_map(&kv_map, kv_cache, num_blocks, block_size, num_kv_heads, head_size);
     if (rc != PA_OK)
         return rc;
@@ -1309,28 +1665,26 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
         return rc;
 
     const bool bf = dtype == PA_BF16, d64 = head_size == 64;
-    // Instances by (FP8 cache, head size 64, bf16).
-    static const void *const kernels[8] = {
-        reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 128>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 128>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 64>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 64>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 128>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 128>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 64>),
-        reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 64>)};
-    const int variant = (fp8 ? 4 : 0) + (d64 ? 2 : 0) + (bf ? 1 : 0);
+    // Instances by (stream-K, FP8 cache, head size 64, bf16).
+#define PA_PREFILL_INSTANCES(SK)                                                              \
+    reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 128, SK>),               \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 128, SK>),           \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, false, 64, SK>),           \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, false, 64, SK>),            \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 128, SK>),           \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 128, SK>),            \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<false, true, 64, SK>),            \
+        reinterpret_cast<const void *>(&paged_prefill_kernel<true, true, 64, SK>)
+    static const void *const kernels[16] = {PA_PREFILL_INSTANCES(false), PA_PREFILL_INSTANCES(true)};
+#undef PA_PREFILL_INSTANCES
+    const int variant = (split ? 8 : 0) + (fp8 ? 4 : 0) + (d64 ? 2 : 0) + (bf ? 1 : 0);
     const void *fn = kernels[variant];
-    // Raise the kernel's shared-memory limit and read the SM count once per
-    // device (a call being captured into a CUDA graph then makes no
-    // attribute call).
+    // Raise the kernel's shared-memory limit once per device (a call being
+    // captured into a CUDA graph then makes no attribute call; the SM count
+    // is cached likewise).
     static std::mutex mu;
-    static bool raised[8][64] = {};
-    static int sm_count[64] = {};
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return set_error(PA_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
+    static bool raised[16][64] = {};
+    cudaError_t e;
     {
         std::lock_guard<std::mutex> lock(mu);
         bool &done = raised[variant][dev & 63];
@@ -1340,18 +1694,10 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
                 return set_error(PA_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", who, cudaGetErrorString(e));
             done = dev < 64;
         }
-        sms = dev < 64 ? sm_count[dev] : 0;
-        if (sms <= 0) {
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess || sms <= 0)
-                return set_error(PA_ERR_CUDA, "%s: SM count: %s", who, cudaGetErrorString(e));
-            if (dev < 64)
-                sm_count[dev] = sms;
-        }
     }
     // Persistent grid: one CTA per SM (the CTA holds 225 KB of shared
-    // memory), never more CTAs than units.
-    const dim3 grid((unsigned)std::min<long long>(units, sms));
+    // memory), never more CTAs than units; G CTAs under stream-K.
+    const dim3 grid(split ? (unsigned)lp.split_grid : (unsigned)std::min<long long>(lp.units, sms));
     void *args[] = {&kv_map, &q_map, &prm};
     e = cudaLaunchKernel(fn, grid, dim3(threads_for(fp8)), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
@@ -1365,22 +1711,45 @@ extern "C" int pa_prefill(void *out, const void *query, const void *kv_cache, co
                           int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
                           int num_seqs, int total_q, int max_seqlen_q, float scale, int num_q_heads,
                           int num_kv_heads, int head_size, int num_blocks, int block_size, int dtype,
-                          pa_stream_t stream)
+                          void *workspace, size_t workspace_bytes, pa_stream_t stream)
 {
     return prefill_impl("pa_prefill", out, query, kv_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
                         seq_lens, num_seqs, total_q, max_seqlen_q, scale, num_q_heads, num_kv_heads, head_size,
-                        num_blocks, block_size, dtype, false, 1.f, 1.f, stream);
+                        num_blocks, block_size, dtype, false, 1.f, 1.f, workspace, workspace_bytes, stream);
 }
 
 extern "C" int pa_prefill_fp8(void *out, const void *query, const void *kv_cache, const int32_t *block_tables,
                               int max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
                               int num_seqs, int total_q, int max_seqlen_q, float scale, int num_q_heads,
                               int num_kv_heads, int head_size, int num_blocks, int block_size, int dtype,
-                              float k_scale, float v_scale, pa_stream_t stream)
+                              float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                              pa_stream_t stream)
 {
     if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
         return set_error(PA_ERR_INVALID_ARG, "pa_prefill_fp8: k_scale and v_scale must be finite and > 0");
     return prefill_impl("pa_prefill_fp8", out, query, kv_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
                         seq_lens, num_seqs, total_q, max_seqlen_q, scale, num_q_heads, num_kv_heads, head_size,
-                        num_blocks, block_size, dtype, true, k_scale, v_scale, stream);
+                        num_blocks, block_size, dtype, true, k_scale, v_scale, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pa_prefill_workspace_size(int num_seqs, int max_seqlen_q, int num_q_heads, int num_kv_heads,
+                                         int head_size, size_t *bytes)
+{
+    const char *who = "pa_prefill_workspace_size";
+    if (!bytes)
+        return set_error(PA_ERR_INVALID_ARG, "%s: null bytes", who);
+    *bytes = 0;
+    int rc = check_heads(who, num_q_heads, num_kv_heads, head_size);
+    if (rc != PA_OK)
+        return rc;
+    if (num_seqs < 0 || max_seqlen_q < 0)
+        return set_error(PA_ERR_INVALID_ARG, "%s: bad sizes", who);
+    if (num_seqs == 0 || max_seqlen_q == 0)
+        return PA_OK;
+    int dev = 0, sms = 0;
+    rc = current_sms(who, &dev, &sms);
+    if (rc != PA_OK)
+        return rc;
+    *bytes = plan_launch(num_seqs, max_seqlen_q, num_q_heads, num_kv_heads, head_size, sms).split_bytes;
+    return PA_OK;
 }

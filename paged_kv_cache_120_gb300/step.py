@@ -379,6 +379,8 @@ class PrefillStep(PinnedHostStep):
         self.cu_seqlens_q, self.slot_mapping = t(plan.cu_seqlens_q), t(plan.slot_mapping)
         self.max_seqlen_q = int(plan.chunk_lens.max())
         self.out = torch.empty_like(self.query)
+        # None unless the shape has few enough work units to split K/V ranges.
+        self.workspace = binding.prefill_workspace(self.query, self.pool, len(plan.seq_ids), self.max_seqlen_q)
 
     _INPUTS = ("query", "key_new", "value_new", "slot_mapping", "block_tables", "seq_lens", "cu_seqlens_q")
 
@@ -400,10 +402,10 @@ class PrefillStep(PinnedHostStep):
         if self.fp8:
             binding.pa_prefill_fp8(self.out, self.query, self.pool, self.block_tables, self.cu_seqlens_q,
                                    self.seq_lens, self.w.scale, self.max_seqlen_q, self.k_scale, self.v_scale,
-                                   stream)
+                                   self.workspace, stream)
         else:
             binding.pa_prefill(self.out, self.query, self.pool, self.block_tables, self.cu_seqlens_q,
-                               self.seq_lens, self.w.scale, self.max_seqlen_q, stream)
+                               self.seq_lens, self.w.scale, self.max_seqlen_q, self.workspace, stream)
 
     def run_host(self, host: dict, out_host, stream=None) -> None:
         """The step from pinned host buffers (query, key_new, value_new,

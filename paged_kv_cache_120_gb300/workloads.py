@@ -67,9 +67,11 @@ WORKLOADS = {
 }
 
 # Chunked-prefill workloads (many queries per sequence, causal): each
-# sequence holds a cached prefix of U[0, max_prefix] tokens and this step
-# brings a chunk of `chunk` new tokens whose K/V are written first, as the
-# varlen read of the book's §4.5 receives them.
+# sequence holds a cached prefix of U[min_prefix, max_prefix] tokens and this
+# step brings a chunk of `chunk` new tokens whose K/V are written first, as
+# the varlen read of the book's §4.5 receives them. The long-context ones are
+# few long sequences with short chunks (the late chunks of long prompts):
+# few work units, so each unit's K/V range is split across the SMs.
 @dataclasses.dataclass(frozen=True)
 class PrefillWorkload:
     name: str
@@ -83,6 +85,7 @@ class PrefillWorkload:
     chunk: int
     scale: float
     description: str
+    min_prefix: int = 0
 
 
 PREFILL_WORKLOADS = {
@@ -93,6 +96,14 @@ PREFILL_WORKLOADS = {
     "prefill_gqa8b": PrefillWorkload(
         "prefill_gqa8b", 16, 32, 8, 128, BF16, 8, 4096, 1024, 128 ** -0.5,
         "GQA 8B chunked prefill: 32/8 heads, d=128, bf16, 8 seqs, prefix U[0,4096] + 1024-token chunk"),
+    "prefill_longctx_llama13b": PrefillWorkload(
+        "prefill_longctx_llama13b", 16, 40, 40, 128, F16, 2, 16384, 512, 128 ** -0.5,
+        "Llama-2-13B layer, long context: 40/40 heads, d=128, fp16, 2 seqs, "
+        "prefix U[12288,16384] + 512-token chunk", min_prefix=12288),
+    "prefill_longctx_gqa8b": PrefillWorkload(
+        "prefill_longctx_gqa8b", 16, 32, 8, 128, BF16, 1, 65536, 2048, 128 ** -0.5,
+        "GQA 8B, long prompt: 32/8 heads, d=128, bf16, 1 seq, prefix U[57344,65536] + 2048-token chunk",
+        min_prefix=57344),
 }
 
 
@@ -112,7 +123,7 @@ def shared_prompt_tokens(seed: int):
 def prefill_prefixes(name: str, seed: int) -> np.ndarray:
     """Cached prefix length of every sequence of a prefill workload."""
     w = PREFILL_WORKLOADS[name]
-    return rng(seed + 3).integers(0, w.max_prefix + 1, size=w.num_seqs).astype(np.int32)
+    return rng(seed + 3).integers(w.min_prefix, w.max_prefix + 1, size=w.num_seqs).astype(np.int32)
 
 
 TOY_LENGTHS = (25, 47, 12)

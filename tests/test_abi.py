@@ -88,7 +88,7 @@ def test_prefill_host_side_validation_without_a_gpu(lib):
         a = dict(ok_args, **kw)
         return lib.pa_prefill(null, null, null, a["bt"], a["maxb"], a["cu"], a["sl"], a["S"], a["total"],
                               a["maxq"], a["scale"], a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["dt"],
-                              null)
+                              null, 0, null)
     assert call(d=96) == binding.PA_ERR_UNSUPPORTED
     assert call(d=64) == binding.PA_ERR_INVALID_ARG              # head size 64 is built: null pointers
     assert call(dt=2) == binding.PA_ERR_UNSUPPORTED
@@ -102,6 +102,23 @@ def test_prefill_host_side_validation_without_a_gpu(lib):
     assert call(maxq=0) == binding.PA_OK
 
 
+def test_prefill_workspace_size_validation_without_a_gpu(lib):
+    import ctypes
+    n = ctypes.c_size_t(99)
+    assert lib.pa_prefill_workspace_size(2, 64, 8, 2, 128, None) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_prefill_workspace_size(2, 64, 8, 2, 96, ctypes.byref(n)) == binding.PA_ERR_UNSUPPORTED
+    assert n.value == 0
+    assert lib.pa_prefill_workspace_size(2, 64, 8, 3, 128, ctypes.byref(n)) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_prefill_workspace_size(2, 64, 40, 2, 128, ctypes.byref(n)) == binding.PA_ERR_UNSUPPORTED
+    assert lib.pa_prefill_workspace_size(-1, 64, 8, 2, 128, ctypes.byref(n)) == binding.PA_ERR_INVALID_ARG
+    n.value = 99
+    assert lib.pa_prefill_workspace_size(0, 64, 8, 2, 128, ctypes.byref(n)) == binding.PA_OK
+    assert n.value == 0
+    n.value = 99
+    assert lib.pa_prefill_workspace_size(3, 0, 8, 2, 128, ctypes.byref(n)) == binding.PA_OK
+    assert n.value == 0
+
+
 def test_prefill_fp8_host_side_validation_without_a_gpu(lib):
     null = None
     ok_args = dict(maxb=4, S=2, total=10, maxq=8, scale=0.1, hq=8, hkv=2, d=128, nb=16, bs=16, dt=0,
@@ -111,7 +128,7 @@ def test_prefill_fp8_host_side_validation_without_a_gpu(lib):
         a = dict(ok_args, **kw)
         return lib.pa_prefill_fp8(null, null, null, null, a["maxb"], null, null, a["S"], a["total"], a["maxq"],
                                   a["scale"], a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["dt"], a["ks"],
-                                  a["vs"], null)
+                                  a["vs"], null, 0, null)
     assert call(ks=0.0) == binding.PA_ERR_INVALID_ARG
     assert call(vs=float("nan")) == binding.PA_ERR_INVALID_ARG
     assert call(ks=-1.0) == binding.PA_ERR_INVALID_ARG

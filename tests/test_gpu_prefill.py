@@ -35,9 +35,10 @@ class PrefillCase:
     step's chunk: the allocator lays out ctx - qlen tokens, then reserves the
     chunk's slots; the chunk's K/V go in by pa_reshape_and_cache."""
 
-    def __init__(self, dev, dtype, Hq, Hkv, B, ctx, qlen, seed, spare=8, poison=False, D=128):
+    def __init__(self, dev, dtype, Hq, Hkv, B, ctx, qlen, seed, spare=8, poison=False, D=128, split=False):
         import torch
         self.dtype, self.Hq, self.Hkv, self.B, self.D = dtype, Hq, Hkv, B, D
+        self.split = split
         self.scale = 1.0 / math.sqrt(D)
         rng = np.random.default_rng(seed)
         nb = sum(-(-L // B) for L in ctx) + spare
@@ -88,11 +89,19 @@ class PrefillCase:
                                          t(self.slots))
         return self.prefill(self.pool, self.bt_d)
 
-    def prefill(self, pool, bt_d):
+    def workspace(self):
+        """The K/V-split workspace for this shape, filled with NaN bytes (its
+        contents must not matter); the shape must be one that splits."""
+        ws = binding.prefill_workspace(self.q, self.pool, len(self.seq_lens), self.max_q)
+        assert ws is not None, "this shape does not split its K/V ranges"
+        return ws.fill_(0xFF)
+
+    def prefill(self, pool, bt_d, split=None):
         import torch
+        split = self.split if split is None else split
         out = torch.full_like(self.q, float("nan"))
         binding.pa_prefill(out, self.q.contiguous(), pool, bt_d, self.cu_d, self.sl_d, self.scale,
-                           self.max_q)
+                           self.max_q, self.workspace() if split else None)
         torch.cuda.synchronize()
         return out
 
@@ -120,11 +129,14 @@ QLEN = [200, 60, 1, 150, 1, 0, 40, 129, 64]
 HEADS = [(4, 4), (8, 2), (8, 1), (16, 1), (32, 1), (12, 3), (40, 8), (6, 2)]
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
 @pytest.mark.parametrize("heads", HEADS)
-def test_prefill_parity_small(dev, dtype, heads):
+def test_prefill_parity_small(dev, dtype, heads, split):
+    """Every head layout, with each unit's K/V range whole and (a
+    workspace given; these shapes have few units) split across the SMs."""
     Hq, Hkv = heads
-    c = PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=500 + Hq + Hkv + dtype)
+    c = PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=500 + Hq + Hkv + dtype, split=split)
     c.check(c.gpu())
 
 
@@ -258,13 +270,14 @@ def test_prefill_replayed_from_a_cuda_graph_is_bit_identical(dev):
     assert binding.pa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
 @pytest.mark.parametrize("heads", [(4, 4), (8, 2), (16, 1), (32, 1)])
-def test_prefill_head_size_64(dev, dtype, heads):
+def test_prefill_head_size_64(dev, dtype, heads, split):
     """Head size 64: one 64-dim chunk per row, four score MMAs per tile,
     P V with N = 64; same cases as the head-size-128 grid."""
     Hq, Hkv = heads
-    c = PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=900 + Hq + Hkv + dtype, D=64)
+    c = PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=900 + Hq + Hkv + dtype, D=64, split=split)
     c.check(c.gpu())
 
 

@@ -42,9 +42,11 @@ class Fp8PrefillCase:
     """As the 16-bit prefill case, on a byte pool: the prefix is E4M3 codes of
     N(0,1)-sized values, the chunk's K/V go in by pa_reshape_and_cache_fp8."""
 
-    def __init__(self, dev, dtype, Hq, Hkv, B, ctx, qlen, seed, spare=8, poison=False, ks=KS, vs=VS, D=128):
+    def __init__(self, dev, dtype, Hq, Hkv, B, ctx, qlen, seed, spare=8, poison=False, ks=KS, vs=VS, D=128,
+                 split=False):
         import torch
         self.dtype, self.Hq, self.Hkv, self.B, self.D, self.ks, self.vs = dtype, Hq, Hkv, B, D, ks, vs
+        self.split = split
         self.scale = 1.0 / math.sqrt(D)
         rng = np.random.default_rng(seed)
         nb = sum(-(-L // B) for L in ctx) + spare
@@ -96,11 +98,18 @@ class Fp8PrefillCase:
                                              self.ks, self.vs)
         return self.prefill(self.pool, self.bt_d)
 
-    def prefill(self, pool, bt_d):
+    def workspace(self):
+        """The K/V-split workspace for this shape, filled with NaN bytes."""
+        ws = binding.prefill_workspace(self.q, self.pool, len(self.seq_lens), self.max_q)
+        assert ws is not None, "this shape does not split its K/V ranges"
+        return ws.fill_(0xFF)
+
+    def prefill(self, pool, bt_d, split=None):
         import torch
+        split = self.split if split is None else split
         out = torch.full_like(self.q, float("nan"))
         binding.pa_prefill_fp8(out, self.q.contiguous(), pool, bt_d, self.cu_d, self.sl_d, self.scale,
-                               self.max_q, self.ks, self.vs)
+                               self.max_q, self.ks, self.vs, self.workspace() if split else None)
         torch.cuda.synchronize()
         return out
 
@@ -127,17 +136,20 @@ QLEN = [200, 60, 1, 150, 1, 0, 40, 129, 64]
 HEADS = [(4, 4), (8, 2), (8, 1), (16, 1), (32, 1), (12, 3), (40, 8)]
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
 @pytest.mark.parametrize("heads", HEADS)
-def test_prefill_fp8_parity_small(dev, dtype, heads):
+def test_prefill_fp8_parity_small(dev, dtype, heads, split):
     Hq, Hkv = heads
-    c = Fp8PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=700 + Hq + Hkv + dtype)
+    c = Fp8PrefillCase(dev, dtype, Hq, Hkv, 16, CTX, QLEN, seed=700 + Hq + Hkv + dtype, split=split)
     c.check(c.gpu())
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
-def test_prefill_fp8_nan_codes_in_padding_change_nothing(dev, dtype):
-    c = Fp8PrefillCase(dev, dtype, 8, 2, 16, [33, 250, 7], [33, 100, 7], seed=41 + dtype, poison=True)
+def test_prefill_fp8_nan_codes_in_padding_change_nothing(dev, dtype, split):
+    c = Fp8PrefillCase(dev, dtype, 8, 2, 16, [33, 250, 7], [33, 100, 7], seed=41 + dtype, poison=True,
+                       split=split)
     c.check(c.gpu())
 
 
