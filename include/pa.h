@@ -309,8 +309,9 @@ int pa_decode_fp8(void *out, const void *query, const void *kv_cache,
  * S = Q K^T and O = P V in fp32 (tensor memory), an fp32 online softmax in
  * base 2 with P rounded once to dtype, split pieces combined in fp32 in a
  * fixed order, one rounding of O / l at the end. For a given device, shape
- * and workspace choice the result is deterministic. Allocates nothing.
- * Returns PA_OK or a PA_ERR_* code.
+ * and workspace choice the result is deterministic. Launch: one persistent
+ * kernel; with a split, a second (the merge) follows with programmatic
+ * dependent launch. Allocates nothing. Returns PA_OK or a PA_ERR_* code.
  */
 int pa_prefill(void *out, const void *query, const void *kv_cache,
                const int32_t *block_tables, int max_blocks_per_seq,

@@ -64,12 +64,9 @@ __device__ int g_prefill_error;  // PA_DEVERR_* bits of the prefill kernels
 constexpr int kSchedSlots = 64;
 __device__ int g_prefill_sched[kSchedSlots][2];
 
-// Stream-K launches (few work units, below): per slot, one arrival counter
-// per (unit, query tile, warp of the tile's softmax group), counting the
-// pieces of the unit whose partial rows have been written. The last CTA of
-// the launch puts the slot's counters back to 0.
+// Stream-K launches (few work units): at most this many units.
 constexpr int kMaxSplitUnits = 1024;
-__device__ int g_prefill_fix[kSchedSlots][kMaxSplitUnits * 8];
+constexpr int kMergeRowsPerThread = 4;  // rows one merge thread combines
 
 namespace {
 
@@ -395,9 +392,12 @@ struct PrefillParams {
     int max_len;        // max_blocks_per_seq * block_size
     int num_kv_heads;
     int num_units;      // q_pairs * num_seqs * num_kv_heads * head_tiles
-    int sched_slot;     // this launch's row of g_prefill_sched (and g_prefill_fix)
+    int sched_slot;     // this launch's row of g_prefill_sched
     float *part_o;      // stream-K: partial O rows [CTA][slot 2][tile 2][128][D] fp32
     float2 *part_ml;    // stream-K: partial (reference maximum, row sum) [CTA][slot 2][tile 2][128]
+    int4 *jobs;         // stream-K: per CTA c, the split unit whose first piece c holds (kNoJob: none):
+                        // {last CTA holding a piece, first query row of tile A, query rows from there,
+                        //  first query head}
     float scale_log2;   // scale * log2(e) (* k_scale with an FP8 cache)
     float v_scale;      // 1, or the FP8 cache's V scale
 };
@@ -500,7 +500,6 @@ struct PrefillBars {
     // Stream-K: the rest of each work item (first and end K/V tile, first
     // and last CTA holding a piece of the unit; equal: the whole unit).
     int item_ext[kUnitSlots][4];
-    int cta_last;
 };
 
 // SPLIT: the stream-K instance (few units, K/V ranges shared out evenly);
@@ -712,6 +711,8 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 }
             }
             auto cta_of = [&](long long t) { return (int)(((t + 1) * G - 1) / W); };
+            if constexpr (SPLIT)
+                p.jobs[blockIdx.x] = make_int4(-1, 0, 0, 0);
             for (int i = 0;; ++i) {
                 Unit w;
                 Item it = {-1, 0, 0, 0, 0};
@@ -744,6 +745,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                         }
                         if (!unit_of<true>(p, it.u, w, false))
                             it.u = -1;
+                        else if (it.j0 == 0 && it.chi > it.clo)  // this CTA holds the unit's first piece
+                            p.jobs[blockIdx.x] = make_int4(it.chi, w.q0 + w.t0[0], w.q_len - w.t0[0],
+                                                           w.h * p.group + w.ht * HPC);
                     }
                 } else {
                     int u;
@@ -1318,18 +1322,16 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                 }
                 continue;
             }
-            // A piece of a split unit ([book] §4.6: partial softmax states
-            // over disjoint token ranges combine exactly). Store this piece's
-            // state (O relative to 2^m, the reference maximum m, the row sum
-            // l; a tile with no K/V tile in the piece stores the empty state
-            // m = -inf, l = 0, O = 0); the warp that stores the unit's last
-            // piece of its 32 rows then combines all pieces in CTA order.
+            // A piece of a split unit: store this piece's partial softmax
+            // state for paged_prefill_merge_kernel (O relative to 2^m, the
+            // reference maximum m, the row sum l; a tile with no K/V tile in
+            // the piece stores the empty state m = -inf, l = 0, O = 0).
             // Slot: CTA c holds at most two partial pieces, the unit it
             // starts inside (slot 0) and the one it starts and leaves
-            // unfinished (slot 1), so the first CTA of a unit uses slot 1.
-            auto slot_of = [&](int c) { return ((c * 2 + (c == it.clo ? 1 : 0)) * 2 + x) * kM + r; };
+            // unfinished (slot 1).
             {
-                float4 *po = reinterpret_cast<float4 *>(p.part_o + (size_t)slot_of((int)blockIdx.x) * D);
+                const int slot = (((int)blockIdx.x * 2 + ((int)blockIdx.x == it.clo ? 1 : 0)) * 2 + x) * kM + r;
+                float4 *po = reinterpret_cast<float4 *>(p.part_o + (size_t)slot * D);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     if (work) {
@@ -1345,43 +1347,7 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
                             po[c * 8 + q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                 }
                 if (valid)
-                    p.part_ml[slot_of((int)blockIdx.x)] = work ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
-            }
-            __threadfence();
-            __syncwarp();
-            int last = 0;
-            if (lane == 0)
-                last = atomicAdd(&g_prefill_fix[p.sched_slot][(it.u * 2 + x) * 4 + quarter], 1) == it.chi - it.clo;
-            if (!__shfl_sync(kFull, last, 0) || !valid)
-                continue;
-            __threadfence();
-            float mref = -INFINITY, lsum = 0.f;
-            for (int c = it.clo; c <= it.chi; ++c)
-                mref = fmaxf(mref, __ldcg(&p.part_ml[slot_of(c)].x));
-            auto weight = [&](float m) { return m == mref ? 1.f : ex2(m - mref); };
-            for (int c = it.clo; c <= it.chi; ++c) {
-                const float2 ml = __ldcg(&p.part_ml[slot_of(c)]);
-                lsum += weight(ml.x) * ml.y;
-            }
-            const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    o[i] = 0.f;
-                for (int c = it.clo; c <= it.chi; ++c) {
-                    const float wgt = weight(__ldcg(&p.part_ml[slot_of(c)].x));
-                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (size_t)slot_of(c) * D) + cc * 8;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 v = __ldcg(src + q);
-                        o[4 * q] += wgt * v.x;
-                        o[4 * q + 1] += wgt * v.y;
-                        o[4 * q + 2] += wgt * v.z;
-                        o[4 * q + 3] += wgt * v.w;
-                    }
-                }
-                store_row(cc, o, inv);
+                    p.part_ml[slot] = work ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
             }
         }
     }
@@ -1391,22 +1357,9 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     __syncthreads();
     tc_fence_after();
     // Every role has left its loop, so this CTA takes no more units; the
-    // last CTA to get here resets the launch's counters for the next use.
-    if constexpr (SPLIT) {
-        // (and the slot's arrival counters)
-        if (tid == 0) {
-            __threadfence();
-            bars.cta_last = atomicAdd(&g_prefill_sched[p.sched_slot][1], 1) == (int)gridDim.x - 1;
-        }
-        __syncthreads();
-        if (bars.cta_last) {
-            if (tid == 0)
-                g_prefill_sched[p.sched_slot][1] = 0;
-            for (int i = tid; i < p.num_units * 8; i += blockDim.x)
-                g_prefill_fix[p.sched_slot][i] = 0;
-            __threadfence();
-        }
-    } else if (tid == 0) {
+    // last CTA to get here resets the launch's counters for the next use
+    // (a stream-K launch uses none).
+    if (!SPLIT && tid == 0) {
         __threadfence();
         if (atomicAdd(&g_prefill_sched[p.sched_slot][1], 1) == (int)gridDim.x - 1) {
             g_prefill_sched[p.sched_slot][0] = 0;
@@ -1417,6 +1370,89 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
     if (warp == kWarpMMA)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
+}
+
+// Stream-K merge ([book] §4.6: partial softmax states over disjoint token
+// ranges combine exactly). For each split unit (the job record of the CTA
+// holding its first piece) and each valid row of its tiles, the pieces'
+// states (m_c, l_c, O_c) are folded in CTA order with the online rule (M the
+// running maximum, earlier terms rescaled by 2^(M_old - M_new)), so the
+// result does not depend on which piece finished first; out = O / L. A
+// thread takes 4 columns of kMergeRowsPerThread rows (loads of all its rows
+// in flight together); one block per (CTA c, tile, row block). It waits
+// for the main kernel (programmatic dependent launch).
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256) paged_prefill_merge_kernel(const PrefillParams p, int grid_main)
+{
+    constexpr int kTpr = D / 4;                            // threads per row
+    constexpr int kRows = 256 / kTpr;                      // rows per pass of the block
+    constexpr int kBlockRows = kRows * kMergeRowsPerThread;
+    constexpr int kBlocks = kM / kBlockRows;               // blocks per 128-row tile
+    const int c = blockIdx.x / (2 * kBlocks), x = (blockIdx.x / kBlocks) & 1, rb = blockIdx.x % kBlocks;
+    const int tpr = threadIdx.x % kTpr, rsub = threadIdx.x / kTpr;
+    grid_dependency_wait();
+    if (c >= grid_main)
+        return;
+    const int4 job = p.jobs[c];  // {last CTA, first row of tile A, rows from there, first head}
+    if (job.x <= c || job.x >= grid_main)
+        return;
+    const int T = p.rows_per_head;
+    float M[kMergeRowsPerThread], L[kMergeRowsPerThread], A[kMergeRowsPerThread][4];
+    int slot0[kMergeRowsPerThread];
+    bool ok[kMergeRowsPerThread];
+#pragma unroll
+    for (int k = 0; k < kMergeRowsPerThread; ++k) {
+        const int r = rb * kBlockRows + k * kRows + rsub;  // row of tile x
+        const int g = r / T, t = r - g * T;
+        ok[k] = g < p.heads_per_cta && x * T + t < job.z;
+        slot0[k] = x * kM + r;
+        M[k] = -INFINITY;
+        L[k] = 0.f;
+        A[k][0] = A[k][1] = A[k][2] = A[k][3] = 0.f;
+    }
+    for (int cc = c; cc <= job.x; ++cc) {
+        const int base = (cc * 2 + (cc == c ? 1 : 0)) * 2 * kM;  // slot (cc, 1 or 0), tile 0, row 0
+        float2 ml[kMergeRowsPerThread];
+        float4 v[kMergeRowsPerThread];
+#pragma unroll
+        for (int k = 0; k < kMergeRowsPerThread; ++k)
+            if (ok[k]) {
+                ml[k] = __ldcg(&p.part_ml[base + slot0[k]]);
+                v[k] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (size_t)(base + slot0[k]) * D) + tpr);
+            }
+#pragma unroll
+        for (int k = 0; k < kMergeRowsPerThread; ++k) {
+            if (!ok[k] || ml[k].x == -INFINITY)
+                continue;  // an empty piece (no visible token): weight 0
+            if (ml[k].x > M[k]) {
+                const float alpha = ex2(M[k] - ml[k].x);  // 0 while M is -inf
+                L[k] *= alpha;
+                A[k][0] *= alpha;
+                A[k][1] *= alpha;
+                A[k][2] *= alpha;
+                A[k][3] *= alpha;
+                M[k] = ml[k].x;
+            }
+            const float wgt = ml[k].x == M[k] ? 1.f : ex2(ml[k].x - M[k]);
+            L[k] += wgt * ml[k].y;
+            A[k][0] += wgt * v[k].x;
+            A[k][1] += wgt * v[k].y;
+            A[k][2] += wgt * v[k].z;
+            A[k][3] += wgt * v[k].w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kMergeRowsPerThread; ++k) {
+        if (!ok[k])
+            continue;
+        const int r = rb * kBlockRows + k * kRows + rsub;
+        const int g = r / T, t = r - g * T;
+        const float inv = L[k] > 0.f ? p.v_scale / L[k] : 0.f;
+        uint16_t *out = static_cast<uint16_t *>(p.out) +
+                        ((long long)(job.y + x * T + t) * p.num_q_heads + job.w + g) * D + tpr * 4;
+        *reinterpret_cast<uint2 *>(out) =
+            make_uint2(pack2<BF16>(A[k][0] * inv, A[k][1] * inv), pack2<BF16>(A[k][2] * inv, A[k][3] * inv));
+    }
 }
 
 // ================================================================ host side
@@ -1513,7 +1549,10 @@ namespace {
 // CTAs, G = min(SMs, units * kMaxPiecesPerUnit) so that no unit is cut into
 // more than about kMaxPiecesPerUnit pieces (the last piece's warp combines
 // them all).
-constexpr int kSplitUnitsPerSm = 4, kMaxPiecesPerUnit = 16;
+#ifndef PA_PREFILL_MAX_PIECES
+#define PA_PREFILL_MAX_PIECES 16
+#endif
+constexpr int kSplitUnitsPerSm = 4, kMaxPiecesPerUnit = PA_PREFILL_MAX_PIECES;
 
 struct LaunchPlan {
     int heads_per_cta, head_tiles, rows_per_head, q_pairs;
@@ -1537,10 +1576,28 @@ LaunchPlan plan_launch(int num_seqs, int max_seqlen_q, int num_q_heads, int num_
     if (lp.units > 0 && lp.units <= std::min<long long>(kMaxSplitUnits, (long long)kSplitUnitsPerSm * sms)) {
         lp.split_grid = (int)std::min<long long>(sms, lp.units * kMaxPiecesPerUnit);
         // Per CTA two slots of two 128-row tiles: O rows (head_size fp32)
-        // and (m, l) pairs.
-        lp.split_bytes = (size_t)lp.split_grid * 2 * 2 * kM * ((size_t)head_size * 4 + 8);
+        // and (m, l) pairs; then one job record per CTA.
+        lp.split_bytes = (size_t)lp.split_grid * 2 * 2 * kM * ((size_t)head_size * 4 + 8) + (size_t)lp.split_grid * 16;
     }
     return lp;
+}
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous one in the stream finishes and waits for it with
+// griddepcontrol.wait before reading what it wrote.
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, size_t smem, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // SM count of the current device (cached per device).
@@ -1652,6 +1709,7 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     prm.part_ml = split ? reinterpret_cast<float2 *>(static_cast<float *>(workspace) +
                                                      (size_t)lp.split_grid * 2 * 2 * kM * head_size)
                         : nullptr;
+    prm.jobs = split ? reinterpret_cast<int4 *>(prm.part_ml + (size_t)lp.split_grid * 2 * 2 * kM) : nullptr;
     static std::atomic<unsigned> launches{0};
     prm.sched_slot = (int)(launches.fetch_add(1u) % (unsigned)kSchedSlots);
 
@@ -1702,6 +1760,20 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     e = cudaLaunchKernel(fn, grid, dim3(threads_for(fp8)), args, kSmemBytes, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return set_error(PA_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
+    if (split) {
+        static const void *const merges[4] = {reinterpret_cast<const void *>(&paged_prefill_merge_kernel<false, 128>),
+                                              reinterpret_cast<const void *>(&paged_prefill_merge_kernel<true, 128>),
+                                              reinterpret_cast<const void *>(&paged_prefill_merge_kernel<false, 64>),
+                                              reinterpret_cast<const void *>(&paged_prefill_merge_kernel<true, 64>)};
+        int grid_main = lp.split_grid;
+        const int blocks = kM / ((256 / (head_size / 4)) * kMergeRowsPerThread);  // per 128-row tile
+        const int merge_grid = grid_main * 2 * blocks;
+        void *margs[] = {&prm, &grid_main};
+        e = launch_pdl(merges[(d64 ? 2 : 0) + (bf ? 1 : 0)], dim3(merge_grid), dim3(256), margs, 0,
+                       reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess)
+            return set_error(PA_ERR_CUDA, "%s: merge launch: %s", who, cudaGetErrorString(e));
+    }
     return PA_OK;
 }
 

@@ -4,8 +4,8 @@ the SMs (stream-K) and the pieces merged, through the C ABI.
 A launch with few work units (a few long sequences with short chunks) and a
 workspace deals the units' K/V tiles out to the SMs in equal contiguous
 shares; each piece of a unit stores its partial softmax state (reference
-maximum, row sum, unnormalised output) and the last piece to finish combines
-them, the online-softmax merge of the book's §4.6 over disjoint token
+maximum, row sum, unnormalised output) and a merge kernel combines them in a
+fixed order, the online-softmax merge of the book's §4.6 over disjoint token
 ranges. Bar: the tolerances of the whole-unit prefill (max abs 2e-3 fp16 /
 1e-2 bf16 against the fp64 oracle), NaN padding ignored, results that do not
 depend on the workspace's previous contents or on which piece finishes last
@@ -99,8 +99,9 @@ def test_split_is_deterministic_whatever_the_workspace_held(dev):
 
 
 def test_split_replayed_from_a_cuda_graph_is_bit_identical(dev):
-    """Each launch's arrival counters are cleared by its last CTA, so graph
-    replays interleaved with eager launches give the eager bits."""
+    """A split launch is two kernels (the pieces, then the merge, launched
+    with programmatic dependent launch); replayed from a CUDA graph between
+    eager launches it gives the eager bits."""
     import torch
     c = PrefillCase(dev, workloads.BF16, 16, 2, 16, [8000, 2000], [150, 129], seed=1302, split=True)
     ref = c.gpu()
@@ -130,8 +131,7 @@ def test_split_replayed_from_a_cuda_graph_is_bit_identical(dev):
 def test_split_skips_and_flags_bad_sequences_then_recovers(dev):
     """A sequence whose length is shorter than its chunk gets no tiles: its
     rows stay untouched and PA_DEVERR_SEQ_LEN is set; the other sequence's
-    rows are right, and the next launch (whose counters were cleared) is
-    right too."""
+    rows are right, and so is the next launch."""
     import torch
     c = PrefillCase(dev, workloads.F16, 8, 2, 16, [6000, 3000], [64, 40], seed=1303, split=True)
     good = c.gpu()
@@ -150,15 +150,18 @@ def test_split_skips_and_flags_bad_sequences_then_recovers(dev):
 
 
 def test_split_workspace_rules(dev):
-    """Size query: 0 for a shape with many work units; for few, two slots of
-    two 128-row tiles of (head_size fp32 + 2 fp32) per CTA. A workspace that
-    is too small or misaligned is refused; none at all means whole units."""
+    """Size query: 0 for a shape with many work units; for few, per CTA two
+    slots of two 128-row tiles of (head_size fp32 + 2 fp32) and a 16-byte job
+    record. A workspace that is too small or misaligned is refused; none at
+    all means whole units."""
     import torch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     assert binding.pa_prefill_workspace_size(8, 1024, 40, 40, 128) == 0        # 1280 units
     n = binding.pa_prefill_workspace_size(2, 512, 40, 40, 128)                  # 160 units
-    assert n == min(sms, 160 * 16) * 2 * 2 * 128 * (128 * 4 + 8)
-    assert binding.pa_prefill_workspace_size(1, 8, 16, 1, 64) == min(sms, 16) * 2 * 2 * 128 * (64 * 4 + 8)
+    g = min(sms, 160 * 16)
+    assert n == g * 2 * 2 * 128 * (128 * 4 + 8) + g * 16
+    g = min(sms, 16)
+    assert binding.pa_prefill_workspace_size(1, 8, 16, 1, 64) == g * 2 * 2 * 128 * (64 * 4 + 8) + g * 16
     c = PrefillCase(dev, workloads.F16, 8, 2, 16, [3000, 100], [50, 100], seed=1304)
     c.gpu()
     ws = c.workspace()
