@@ -1083,6 +1083,80 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# (q heads, kv heads, dtype, context of each sequence, chunk of each sequence)
+SPLIT_SWEEP = (
+    [(40, 40, workloads.F16, [8192 + 37 * i for i in range(n)], [512] * n) for n in (1, 2, 3, 4, 6)]
+    + [(32, 8, workloads.BF16, [16384 + 101 * i for i in range(n)], [1024] * n) for n in (1, 2)]
+    + [(32, 8, workloads.BF16, [32768], [64]), (8, 1, workloads.F16, [32768], [256]),
+       (16, 1, workloads.F16, [65536], [16])])
+
+
+def run_split_sweep(args, rank) -> None:
+    """pa_prefill kernel time with each work unit's K/V range whole (no
+    workspace) and split across the SMs (workspace), over shapes from many
+    to very few units (head size 128, 16-token blocks, seeded placement and
+    N(0,1) values): 10 launches replayed from a CUDA graph, median of 7
+    replays. One JSON line per shape."""
+    import torch
+    from paged_kv_cache_120_gb300 import binding, build
+    if rank != 0:
+        return
+    build.build()
+    dev = torch.device("cuda:0")
+    D, B = 128, 16
+
+    def graph_us(call):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                call(s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            for _ in range(10):
+                call(s)
+        ts = []
+        for _ in range(7):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 10 * 1e3)
+        return sorted(ts)[3]
+
+    for k, (hq, hkv, dt, ctx, ql) in enumerate(SPLIT_SWEEP):
+        rng = np.random.default_rng(args.seed + k)
+        nblk = [-(-L // B) for L in ctx]
+        nb = sum(nblk) + 4
+        perm = rng.permutation(nb).astype(np.int32)
+        bt = np.full((len(ctx), max(nblk)), -1, np.int32)
+        o = 0
+        for i, n in enumerate(nblk):
+            bt[i, :n] = perm[o:o + n]
+            o += n
+        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        pool = workloads.normal_values((2, nb, B, hkv, D), dt, args.seed + 100 + k, dev)
+        q = workloads.normal_values((int(cu[-1]), hq, D), dt, args.seed + 200 + k, dev)
+        out = torch.empty_like(q)
+        t = lambda a: torch.from_numpy(a).to(dev)
+        bt_d, cu_d, sl_d = t(bt), t(cu), t(np.array(ctx, np.int32))
+        ws = binding.prefill_workspace(q, pool, len(ctx), max(ql))
+        run = lambda w: (lambda s: binding.pa_prefill(out, q, pool, bt_d, cu_d, sl_d, D ** -0.5, max(ql), w, s))
+        whole = graph_us(run(None))
+        split = graph_us(run(ws)) if ws is not None else None
+        check_device_error("the split sweep")
+        group = hq // hkv
+        hpc = min(group, 16)
+        rows = (128 // hpc) & ~7
+        units = (-(-(-(-max(ql) // rows)) // 2)) * len(ctx) * hkv * (group // hpc)
+        print(json.dumps({"heads": f"{hq}/{hkv}", "contexts": ctx, "chunks": ql, "units": units,
+                          "whole_us": round(whole, 1), "split_us": None if split is None else round(split, 1),
+                          "speedup": None if split is None else round(whole / split, 3)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1107,6 +1181,9 @@ def main():
                     help="decode workloads: pool of this many blocks instead of the workload's (the same "
                          "sequences and lengths, placement drawn from fewer blocks): small profiling cases")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--split-sweep", action="store_true",
+                    help="print pa_prefill kernel times with K/V ranges whole and split over a range of "
+                         "unit counts, then exit")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the main cpu_baseline (0.4x for each other config)")
     args = ap.parse_args()
@@ -1118,7 +1195,9 @@ def main():
         workloads.WORKLOADS[args.workload] = dataclasses.replace(w, num_blocks=args.pool_blocks)
         args.no_configs = True
     rank, local_rank, world = dist_setup()
-    if args.workload == "prefix_cache_prefill":
+    if args.split_sweep:
+        run_split_sweep(args, rank)
+    elif args.workload == "prefix_cache_prefill":
         if args.impl == "reference":
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the prefix-cache wave is host "
