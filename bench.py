@@ -119,12 +119,19 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(tag: str) -> str:
-    """SHA-256 over the CUDA sources a kernel family is built from, in order."""
+    """SHA-256 over the code of the CUDA sources a kernel family is built
+    from, in order, comments and blank lines removed (a comment edit does not
+    change the kernel that an ncu summary measured)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[tag]:
-        with open(os.path.join(ROOT, "paged_kv_cache_120_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_120_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        code = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()
 
 

@@ -17,6 +17,12 @@
 //    per-launch counter (warp 11, which also loads each unit's Q) and hands
 //    them to every role through a small ring; TMA rings and barrier phases
 //    run on across units.
+//  * Few units (a few long sequences with short chunks). With at most four
+//    units per SM and a workspace, the CTAs instead take equal contiguous
+//    shares of all units' K/V tiles (stream-K), so a unit's range may be
+//    cut into pieces on several SMs; a piece stores its partial softmax
+//    state, and paged_prefill_merge_kernel combines the pieces of each unit
+//    with the §4.6 rule in a fixed order.
 //  * Loads. Warp 8 brings the K tiles and warp 10 the V tiles by TMA
 //    (16-token boxes through the block table, 128-byte swizzle) into rings
 //    of two K and three V stages (a V stage is released as soon as its last
