@@ -1381,34 +1381,71 @@ __global__ void __launch_bounds__(threads_for(FP8), 1)
 // Stream-K merge ([book] §4.6: partial softmax states over disjoint token
 // ranges combine exactly). For each split unit (the job record of the CTA
 // holding its first piece) and each valid row of its tiles, the pieces'
-// states (m_c, l_c, O_c) are folded in CTA order with the online rule (M the
-// running maximum, earlier terms rescaled by 2^(M_old - M_new)), so the
-// result does not depend on which piece finished first; out = O / L. A
-// thread takes 4 columns of kMergeRowsPerThread rows (loads of all its rows
-// in flight together); one block per (CTA c, tile, row block). It waits
-// for the main kernel (programmatic dependent launch).
-template <bool BF16, int D>
+// states (m_c, l_c, O_c) are folded with the online rule (M the running
+// maximum, earlier terms rescaled by 2^(M_old - M_new)); out = O / L. A
+// thread takes 4 columns of a row. With Q > 1 "planes", plane q folds the
+// pieces c0 + q, c0 + q + Q, ... in order and the Q partial states are
+// then combined in plane order through shared memory, so that a unit cut
+// into many pieces is merged by many threads; with Q = 1 a thread folds all
+// pieces of kMergeRowsPerThread rows (their loads in flight together).
+// Either way the order is fixed, so the result does not depend on which
+// piece finished first. Blocks go to the jobs in CTA order (block b: the
+// b / (2 * blocks per tile)-th job), found by one warp's scan of the job
+// records. Waits for the main kernel (programmatic dependent launch).
+template <int D, int Q>
+struct MergeGeo {
+    static constexpr int kTpr = D / 4;                      // threads per row (4 columns each)
+    static constexpr int kRows = 256 / (kTpr * Q);          // rows per pass of the block
+    static constexpr int kRpt = Q == 1 ? kMergeRowsPerThread : 1;
+    static constexpr int kBlockRows = kRows * kRpt;
+    static constexpr int kBlocks = kM / kBlockRows;         // blocks per 128-row tile
+};
+
+template <bool BF16, int D, int Q>
 __global__ void __launch_bounds__(256) paged_prefill_merge_kernel(const PrefillParams p, int grid_main)
 {
-    constexpr int kTpr = D / 4;                            // threads per row
-    constexpr int kRows = 256 / kTpr;                      // rows per pass of the block
-    constexpr int kBlockRows = kRows * kMergeRowsPerThread;
-    constexpr int kBlocks = kM / kBlockRows;               // blocks per 128-row tile
-    const int c = blockIdx.x / (2 * kBlocks), x = (blockIdx.x / kBlocks) & 1, rb = blockIdx.x % kBlocks;
-    const int tpr = threadIdx.x % kTpr, rsub = threadIdx.x / kTpr;
+    using Geo = MergeGeo<D, Q>;
+    constexpr int kTpr = Geo::kTpr, kRows = Geo::kRows, kRpt = Geo::kRpt;
+    const int job_k = blockIdx.x / (2 * Geo::kBlocks), x = (blockIdx.x / Geo::kBlocks) & 1,
+              rb = blockIdx.x % Geo::kBlocks;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int tpr = tid % kTpr, q = (tid / kTpr) % Q, rsub = tid / (kTpr * Q);
+    __shared__ int s_c;
+    __shared__ float s_st[Q > 1 ? kRows * Q * kTpr * 6 : 1];
     grid_dependency_wait();
-    if (c >= grid_main)
+    if (tid < 32) {
+        int found = -1, seen = 0;
+        for (int c0 = 0; c0 < grid_main && found < 0; c0 += 32) {
+            const int c = c0 + lane;
+            bool v = false;
+            if (c < grid_main) {
+                const int last = p.jobs[c].x;
+                v = last > c && last < grid_main;
+            }
+            unsigned m = __ballot_sync(0xFFFFFFFFu, v);
+            const int cnt = __popc(m);
+            if (job_k < seen + cnt) {
+                for (int t = job_k - seen; t > 0; --t)
+                    m &= m - 1;
+                found = c0 + __ffs(m) - 1;
+            }
+            seen += cnt;
+        }
+        if (lane == 0)
+            s_c = found;
+    }
+    __syncthreads();
+    const int c = s_c;
+    if (c < 0)
         return;
     const int4 job = p.jobs[c];  // {last CTA, first row of tile A, rows from there, first head}
-    if (job.x <= c || job.x >= grid_main)
-        return;
     const int T = p.rows_per_head;
-    float M[kMergeRowsPerThread], L[kMergeRowsPerThread], A[kMergeRowsPerThread][4];
-    int slot0[kMergeRowsPerThread];
-    bool ok[kMergeRowsPerThread];
+    float M[kRpt], L[kRpt], A[kRpt][4];
+    int slot0[kRpt];
+    bool ok[kRpt];
 #pragma unroll
-    for (int k = 0; k < kMergeRowsPerThread; ++k) {
-        const int r = rb * kBlockRows + k * kRows + rsub;  // row of tile x
+    for (int k = 0; k < kRpt; ++k) {
+        const int r = rb * Geo::kBlockRows + k * kRows + rsub;  // row of tile x
         const int g = r / T, t = r - g * T;
         ok[k] = g < p.heads_per_cta && x * T + t < job.z;
         slot0[k] = x * kM + r;
@@ -1416,42 +1453,64 @@ __global__ void __launch_bounds__(256) paged_prefill_merge_kernel(const PrefillP
         L[k] = 0.f;
         A[k][0] = A[k][1] = A[k][2] = A[k][3] = 0.f;
     }
-    for (int cc = c; cc <= job.x; ++cc) {
+    // Fold one state (m, l, o) into (M, L, A): the online rule.
+    auto fold = [](float &Mk, float &Lk, float *Ak, float m, float l, float o0, float o1, float o2, float o3) {
+        if (m == -INFINITY)
+            return;  // an empty piece (no visible token): weight 0
+        if (m > Mk) {
+            const float alpha = ex2(Mk - m);  // 0 while M is -inf
+            Lk *= alpha;
+            Ak[0] *= alpha;
+            Ak[1] *= alpha;
+            Ak[2] *= alpha;
+            Ak[3] *= alpha;
+            Mk = m;
+        }
+        const float wgt = m == Mk ? 1.f : ex2(m - Mk);
+        Lk += wgt * l;
+        Ak[0] += wgt * o0;
+        Ak[1] += wgt * o1;
+        Ak[2] += wgt * o2;
+        Ak[3] += wgt * o3;
+    };
+    for (int cc = c + q; cc <= job.x; cc += Q) {
         const int base = (cc * 2 + (cc == c ? 1 : 0)) * 2 * kM;  // slot (cc, 1 or 0), tile 0, row 0
-        float2 ml[kMergeRowsPerThread];
-        float4 v[kMergeRowsPerThread];
+        float2 ml[kRpt];
+        float4 v[kRpt];
 #pragma unroll
-        for (int k = 0; k < kMergeRowsPerThread; ++k)
+        for (int k = 0; k < kRpt; ++k)
             if (ok[k]) {
                 ml[k] = __ldcg(&p.part_ml[base + slot0[k]]);
                 v[k] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (size_t)(base + slot0[k]) * D) + tpr);
             }
 #pragma unroll
-        for (int k = 0; k < kMergeRowsPerThread; ++k) {
-            if (!ok[k] || ml[k].x == -INFINITY)
-                continue;  // an empty piece (no visible token): weight 0
-            if (ml[k].x > M[k]) {
-                const float alpha = ex2(M[k] - ml[k].x);  // 0 while M is -inf
-                L[k] *= alpha;
-                A[k][0] *= alpha;
-                A[k][1] *= alpha;
-                A[k][2] *= alpha;
-                A[k][3] *= alpha;
-                M[k] = ml[k].x;
-            }
-            const float wgt = ml[k].x == M[k] ? 1.f : ex2(ml[k].x - M[k]);
-            L[k] += wgt * ml[k].y;
-            A[k][0] += wgt * v[k].x;
-            A[k][1] += wgt * v[k].y;
-            A[k][2] += wgt * v[k].z;
-            A[k][3] += wgt * v[k].w;
+        for (int k = 0; k < kRpt; ++k)
+            if (ok[k])
+                fold(M[k], L[k], A[k], ml[k].x, ml[k].y, v[k].x, v[k].y, v[k].z, v[k].w);
+    }
+    if constexpr (Q > 1) {
+        // Planes 1 .. Q-1 hand their states to plane 0, which folds them in order.
+        float *st = s_st + ((rsub * Q + q) * kTpr + tpr) * 6;
+        st[0] = M[0];
+        st[1] = L[0];
+        st[2] = A[0][0];
+        st[3] = A[0][1];
+        st[4] = A[0][2];
+        st[5] = A[0][3];
+        __syncthreads();
+        if (q != 0)
+            return;
+#pragma unroll 1
+        for (int qq = 1; qq < Q; ++qq) {
+            const float *o = s_st + ((rsub * Q + qq) * kTpr + tpr) * 6;
+            fold(M[0], L[0], A[0], o[0], o[1], o[2], o[3], o[4], o[5]);
         }
     }
 #pragma unroll
-    for (int k = 0; k < kMergeRowsPerThread; ++k) {
+    for (int k = 0; k < kRpt; ++k) {
         if (!ok[k])
             continue;
-        const int r = rb * kBlockRows + k * kRows + rsub;
+        const int r = rb * Geo::kBlockRows + k * kRows + rsub;
         const int g = r / T, t = r - g * T;
         const float inv = L[k] > 0.f ? p.v_scale / L[k] : 0.f;
         uint16_t *out = static_cast<uint16_t *>(p.out) +
@@ -1551,14 +1610,10 @@ namespace {
 // A launch's work units and scheduling. With enough units, each of
 // min(units, SMs) persistent CTAs takes whole units, heaviest first, from a
 // counter. With few (at most kSplitUnitsPerSm per SM, and a workspace), the
-// units' K/V tiles are dealt out in equal contiguous shares (stream-K) to G
-// CTAs, G = min(SMs, units * kMaxPiecesPerUnit) so that no unit is cut into
-// more than about kMaxPiecesPerUnit pieces (the last piece's warp combines
-// them all).
-#ifndef PA_PREFILL_MAX_PIECES
-#define PA_PREFILL_MAX_PIECES 16
-#endif
-constexpr int kSplitUnitsPerSm = 4, kMaxPiecesPerUnit = PA_PREFILL_MAX_PIECES;
+// units' K/V tiles are dealt out in equal contiguous shares (stream-K) to
+// one CTA per SM, however many pieces that cuts a unit into (the merge
+// spreads a unit's pieces over several threads per row).
+constexpr int kSplitUnitsPerSm = 4;
 
 struct LaunchPlan {
     int heads_per_cta, head_tiles, rows_per_head, q_pairs;
@@ -1580,7 +1635,7 @@ LaunchPlan plan_launch(int num_seqs, int max_seqlen_q, int num_q_heads, int num_
     lp.split_grid = 0;
     lp.split_bytes = 0;
     if (lp.units > 0 && lp.units <= std::min<long long>(kMaxSplitUnits, (long long)kSplitUnitsPerSm * sms)) {
-        lp.split_grid = (int)std::min<long long>(sms, lp.units * kMaxPiecesPerUnit);
+        lp.split_grid = sms;
         // Per CTA two slots of two 128-row tiles: O rows (head_size fp32)
         // and (m, l) pairs; then one job record per CTA.
         lp.split_bytes = (size_t)lp.split_grid * 2 * 2 * kM * ((size_t)head_size * 4 + 8) + (size_t)lp.split_grid * 16;
@@ -1767,15 +1822,27 @@ int prefill_impl(const char *who, void *out, const void *query, const void *kv_c
     if (e != cudaSuccess)
         return set_error(PA_ERR_CUDA, "%s: launch: %s", who, cudaGetErrorString(e));
     if (split) {
-        static const void *const merges[4] = {reinterpret_cast<const void *>(&paged_prefill_merge_kernel<false, 128>),
-                                              reinterpret_cast<const void *>(&paged_prefill_merge_kernel<true, 128>),
-                                              reinterpret_cast<const void *>(&paged_prefill_merge_kernel<false, 64>),
-                                              reinterpret_cast<const void *>(&paged_prefill_merge_kernel<true, 64>)};
+        // Merge planes: enough that each thread folds about 8 pieces of a
+        // unit cut into G / units + 1 pieces.
+        const long long pieces = ((long long)lp.split_grid + lp.units - 1) / lp.units + 1;
+        const int qi = pieces <= 8 ? 0 : pieces <= 16 ? 1 : pieces <= 32 ? 2 : 3;
+#define PA_MERGE_INSTANCES(Q)                                                                      \
+    reinterpret_cast<const void *>(&paged_prefill_merge_kernel<false, 128, Q>),                    \
+        reinterpret_cast<const void *>(&paged_prefill_merge_kernel<true, 128, Q>),                 \
+        reinterpret_cast<const void *>(&paged_prefill_merge_kernel<false, 64, Q>),                 \
+        reinterpret_cast<const void *>(&paged_prefill_merge_kernel<true, 64, Q>)
+        static const void *const merges[16] = {PA_MERGE_INSTANCES(1), PA_MERGE_INSTANCES(2), PA_MERGE_INSTANCES(4),
+                                               PA_MERGE_INSTANCES(8)};
+#undef PA_MERGE_INSTANCES
+        static const int blocks128[4] = {MergeGeo<128, 1>::kBlocks, MergeGeo<128, 2>::kBlocks,
+                                         MergeGeo<128, 4>::kBlocks, MergeGeo<128, 8>::kBlocks};
+        static const int blocks64[4] = {MergeGeo<64, 1>::kBlocks, MergeGeo<64, 2>::kBlocks, MergeGeo<64, 4>::kBlocks,
+                                        MergeGeo<64, 8>::kBlocks};
         int grid_main = lp.split_grid;
-        const int blocks = kM / ((256 / (head_size / 4)) * kMergeRowsPerThread);  // per 128-row tile
-        const int merge_grid = grid_main * 2 * blocks;
+        const long long jobs = std::min<long long>(lp.units, grid_main);  // at most one per unit and per CTA
+        const int merge_grid = (int)(jobs * 2 * (d64 ? blocks64[qi] : blocks128[qi]));
         void *margs[] = {&prm, &grid_main};
-        e = launch_pdl(merges[(d64 ? 2 : 0) + (bf ? 1 : 0)], dim3(merge_grid), dim3(256), margs, 0,
+        e = launch_pdl(merges[qi * 4 + (d64 ? 2 : 0) + (bf ? 1 : 0)], dim3(merge_grid), dim3(256), margs, 0,
                        reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess)
             return set_error(PA_ERR_CUDA, "%s: merge launch: %s", who, cudaGetErrorString(e));

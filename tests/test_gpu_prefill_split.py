@@ -51,12 +51,14 @@ def both_modes(c):
 # (q heads, kv heads, dtype, head size, context lengths, chunk lengths):
 # MHA with two long sequences, GQA with a short chunk, one unit cut into
 # pieces by every CTA (16 query heads on one kv head: tiles of 16 heads x 8
-# tokens), head size 64 with a short sequence beside a long one, and the
-# Llama-2-13B head count.
+# tokens; the merge then spreads each row's pieces over 8 threads), the same
+# at head size 64 in bf16, head size 64 with a short sequence beside a long
+# one, and the Llama-2-13B head count.
 LONG = [
     (8, 8, workloads.F16, 128, [6000, 9100], [100, 256]),
     (32, 8, workloads.BF16, 128, [7000, 3000], [300, 64]),
     (16, 1, workloads.F16, 128, [20000], [8]),
+    (16, 1, workloads.BF16, 64, [30000], [8]),
     (8, 2, workloads.BF16, 64, [12000, 40], [77, 40]),
     (40, 40, workloads.F16, 128, [4500, 4100], [256, 129]),
 ]
@@ -75,6 +77,13 @@ def test_split_fp8_long_context_parity(dev):
     c.check(c.gpu())
     c.split = False
     c.check(c.prefill(c.pool, c.bt_d))
+
+
+def test_split_fp8_single_unit(dev):
+    """One work unit over an FP8 cache, cut into a piece per SM: the merge
+    folds each row's pieces on 8 threads and applies the V scale."""
+    c = Fp8PrefillCase(dev, workloads.F16, 16, 1, 16, [20000], [16], seed=1305, poison=True, split=True)
+    c.check(c.gpu())
 
 
 def test_split_is_deterministic_whatever_the_workspace_held(dev):
@@ -158,10 +167,8 @@ def test_split_workspace_rules(dev):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     assert binding.pa_prefill_workspace_size(8, 1024, 40, 40, 128) == 0        # 1280 units
     n = binding.pa_prefill_workspace_size(2, 512, 40, 40, 128)                  # 160 units
-    g = min(sms, 160 * 16)
-    assert n == g * 2 * 2 * 128 * (128 * 4 + 8) + g * 16
-    g = min(sms, 16)
-    assert binding.pa_prefill_workspace_size(1, 8, 16, 1, 64) == g * 2 * 2 * 128 * (64 * 4 + 8) + g * 16
+    assert n == sms * 2 * 2 * 128 * (128 * 4 + 8) + sms * 16
+    assert binding.pa_prefill_workspace_size(1, 8, 16, 1, 64) == sms * 2 * 2 * 128 * (64 * 4 + 8) + sms * 16
     c = PrefillCase(dev, workloads.F16, 8, 2, 16, [3000, 100], [50, 100], seed=1304)
     c.gpu()
     ws = c.workspace()
