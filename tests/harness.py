@@ -104,3 +104,27 @@ def max_abs_err_bf16_large(got, want):
     half-ulp (2^-6) exceeds 1e-2: those elements are compared with the
     oracle rounded to bf16, the rest with the oracle itself."""
     return max_abs_err(got, np.where(np.abs(want) >= 4.0, rne_bf16(want), want))
+
+
+def prefill_tile_samples(plan, w, rng):
+    """(sequence, chunk token, query head) samples covering every query tile
+    of every kv head of a prefill batch: the kernel's work unit is a pair of
+    tiles of (up to 16 query heads of a kv head) x (128 / heads tokens), so
+    one random row per (sequence, tile, kv head) checks both tiles of every
+    unit, and with them every place a split can cut a unit's K/V range. The
+    last row of every chunk is added."""
+    group = w.num_q_heads // w.num_kv_heads
+    hpc = min(group, 16)
+    rows = (128 // hpc) & ~7
+    s_l, i_l, h_l = [], [], []
+    for s in range(len(plan.chunk_lens)):
+        q_len = int(plan.chunk_lens[s])
+        for t0 in range(0, q_len, rows):
+            for h in range(w.num_kv_heads):
+                s_l.append(s)
+                i_l.append(int(rng.integers(t0, min(q_len, t0 + rows))))
+                h_l.append(h * group + int(rng.integers(0, group)))
+        s_l.append(s)
+        i_l.append(q_len - 1)
+        h_l.append(int(rng.integers(0, w.num_q_heads)))
+    return np.array(s_l), np.array(i_l), np.array(h_l, dtype=np.int32)

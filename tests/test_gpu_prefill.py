@@ -14,7 +14,7 @@ import oracle
 from oracle.block_manager import BlockManagerModel
 from paged_kv_cache_120_gb300 import binding, build, workloads
 
-from harness import TOL, max_abs_err, max_abs_err_bf16_large, u16
+from harness import TOL, max_abs_err, max_abs_err_bf16_large, prefill_tile_samples, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -292,9 +292,9 @@ def test_prefill_workload_full_size(dev, name, kv):
     """The prefill step bench.py times (same plan, seed and launch: 8 x
     1024-token chunks after seeded prefixes), run once: the allocator's plan
     against the block-manager model, the chunk's K/V writes bit-exact against
-    the oracle over the whole pool, and 96 sampled (row, head) outputs, the
-    last row of every chunk among them, against the oracle's decode over the
-    row's causal prefix."""
+    the oracle over the whole pool, and a row of every query tile of every
+    kv head (both tiles of every work unit) plus the last row of every chunk
+    against the oracle's decode over the row's causal prefix."""
     import torch
     from paged_kv_cache_120_gb300 import step
     w = workloads.PREFILL_WORKLOADS[name]
@@ -324,12 +324,8 @@ def test_prefill_workload_full_size(dev, name, kv):
         n = oracle.reshape_and_cache(k_bits, v_bits, pool_bits, plan.slot_mapping, *geo)
         assert np.array_equal(u16(st.pool), pool_bits)
     assert n == len(plan.slot_mapping)
-    rng = np.random.default_rng(11)
-    S, m = len(pref), 96
-    s = rng.integers(0, S, size=m)
-    i = rng.integers(0, w.chunk, size=m)
-    s[:S], i[:S] = np.arange(S), w.chunk - 1
-    hq = rng.integers(0, w.num_q_heads, size=m).astype(np.int32)
+    s, i, hq = prefill_tile_samples(plan, w, np.random.default_rng(11))
+    m = len(s)
     rows = plan.cu_seqlens_q[s] + i
     vis = (plan.seq_lens[s] - w.chunk + i + 1).astype(np.int32)
     args = (np.arange(m, dtype=np.int32), hq, q_bits[rows], pool_bits, plan.block_tables[s], vis, w.scale,

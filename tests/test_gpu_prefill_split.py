@@ -17,7 +17,7 @@ import pytest
 import oracle
 from paged_kv_cache_120_gb300 import binding, build, workloads
 
-from harness import TOL, max_abs_err, u16
+from harness import TOL, max_abs_err, prefill_tile_samples, u16
 from test_gpu_prefill import PrefillCase
 from test_gpu_prefill_fp8 import Fp8PrefillCase
 
@@ -186,8 +186,9 @@ def test_split_workspace_rules(dev):
 @pytest.mark.parametrize("name", ["prefill_longctx_llama13b", "prefill_longctx_gqa8b"])
 def test_split_workload_full_size(dev, name):
     """The long-context steps bench.py times (same plan, seed and launch,
-    which splits): the chunk's writes bit-exact, and 64 sampled (row, head)
-    outputs, the last row of every chunk among them, against the oracle's
+    which splits): the chunk's writes bit-exact, and a row of every query
+    tile of every kv head (so both tiles of every work unit, wherever the
+    split cut it) plus the last row of every chunk, against the oracle's
     decode over the row's causal prefix; the split and whole-unit launches
     both."""
     import torch
@@ -210,12 +211,8 @@ def test_split_workload_full_size(dev, name):
     geo = (plan.num_blocks, w.block_size, w.num_kv_heads, w.head_size)
     assert oracle.reshape_and_cache(k_bits, v_bits, pool_bits, plan.slot_mapping, *geo) == len(plan.slot_mapping)
     assert np.array_equal(u16(st.pool), pool_bits)
-    rng = np.random.default_rng(13)
-    S, m = w.num_seqs, 64
-    s = rng.integers(0, S, size=m)
-    i = rng.integers(0, w.chunk, size=m)
-    s[:S], i[:S] = np.arange(S), w.chunk - 1
-    hq = rng.integers(0, w.num_q_heads, size=m).astype(np.int32)
+    s, i, hq = prefill_tile_samples(plan, w, np.random.default_rng(13))
+    m = len(s)
     rows = plan.cu_seqlens_q[s] + i
     vis = (plan.seq_lens[s] - w.chunk + i + 1).astype(np.int32)
     want = oracle.decode_sampled(np.arange(m, dtype=np.int32), hq, q_bits[rows], pool_bits, plan.block_tables[s],
