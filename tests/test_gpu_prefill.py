@@ -140,20 +140,24 @@ def test_prefill_parity_small(dev, dtype, heads, split):
     c.check(c.gpu())
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("B", [32, 64, 48])
-def test_prefill_block_sizes(dev, B):
-    c = PrefillCase(dev, workloads.BF16, 8, 2, B, [33, 300, 129, 64], [33, 100, 129, 1], seed=9 + B)
+def test_prefill_block_sizes(dev, B, split):
+    c = PrefillCase(dev, workloads.BF16, 8, 2, B, [33, 300, 129, 64], [33, 100, 129, 1], seed=9 + B, split=split)
     c.check(c.gpu())
 
 
-def test_prefill_padding_slots_holding_nan_are_ignored(dev):
-    c = PrefillCase(dev, workloads.F16, 8, 8, 16, [3, 18, 140, 77], [3, 5, 140, 20], seed=5, poison=True)
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
+def test_prefill_padding_slots_holding_nan_are_ignored(dev, split):
+    c = PrefillCase(dev, workloads.F16, 8, 8, 16, [3, 18, 140, 77], [3, 5, 140, 20], seed=5, poison=True,
+                    split=split)
     c.check(c.gpu())
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("dtype", [workloads.F16, workloads.BF16])
-def test_prefill_long_context_chunk(dev, dtype):
-    c = PrefillCase(dev, dtype, 8, 1, 16, [5000, 2100], [300, 2100], seed=21)
+def test_prefill_long_context_chunk(dev, dtype, split):
+    c = PrefillCase(dev, dtype, 8, 1, 16, [5000, 2100], [300, 2100], seed=21, split=split)
     c.check(c.gpu())
 
 

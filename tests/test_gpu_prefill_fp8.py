@@ -153,9 +153,10 @@ def test_prefill_fp8_nan_codes_in_padding_change_nothing(dev, dtype, split):
     c.check(c.gpu())
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
 @pytest.mark.parametrize("B", [32, 64])
-def test_prefill_fp8_larger_blocks(dev, B):
-    c = Fp8PrefillCase(dev, workloads.F16, 8, 2, B, [300, 129, 70], [100, 129, 3], seed=43 + B)
+def test_prefill_fp8_larger_blocks(dev, B, split):
+    c = Fp8PrefillCase(dev, workloads.F16, 8, 2, B, [300, 129, 70], [100, 129, 3], seed=43 + B, split=split)
     c.check(c.gpu())
 
 
