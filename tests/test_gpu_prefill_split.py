@@ -71,6 +71,20 @@ def test_split_long_context_parity(dev, case):
     both_modes(c)
 
 
+def test_split_many_short_sequences(dev):
+    """200 sequences (contexts up to 400 tokens, chunks of 0 to 3 tokens,
+    some chunks the whole sequence) over 8/2 heads: 400 units, few enough to
+    split. The plan scans the sequences 32 at a time and walks hundreds of
+    one- and two-tile units, so shares start and end in every kind of place."""
+    rng = np.random.default_rng(1306)
+    ql = rng.integers(0, 4, size=200)
+    ctx = np.maximum(ql, rng.integers(1, 401, size=200))
+    ctx[::17] = ql[::17]  # chunks that are the whole sequence
+    c = PrefillCase(dev, workloads.F16, 8, 2, 16, [int(x) for x in ctx], [int(x) for x in ql], seed=1306,
+                    poison=True, split=True)
+    both_modes(c)
+
+
 def test_split_fp8_long_context_parity(dev):
     c = Fp8PrefillCase(dev, workloads.BF16, 40, 40, 16, [5000, 3000], [200, 128], seed=1300, poison=True,
                        split=True)
